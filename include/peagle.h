@@ -1,0 +1,237 @@
+/*
+ * peagle.h -- C ABI of the P-EAGLE parallel drafting step on one GB300 (sm_103a).
+ *
+ * One drafting step turns the verified target batch into all K draft tokens
+ * of every request in a single drafter pass:
+ *
+ *   pe_expand_batch   -> expanded rows [token, MASK, ..., MASK] + metadata
+ *                        + expanded target hidden states (h_shared in MASK rows)
+ *   pe_draft_forward  -> N LLaMA-style drafter layers over the expanded rows,
+ *                        paged-KV causal attention, final RMSNorm of the
+ *                        B*K rows that get sampled
+ *   pe_lmhead_argmax  -> LM head and argmax: one draft token per sampled row
+ *
+ * Sources (web pages on P-EAGLE), cited by title and section:
+ *   [paper] "P-EAGLE: Parallel-Drafting EAGLE with Scalable Training",
+ *           section 2 (architecture) and Figure 2.
+ *   [blog]  "P-EAGLE: Faster LLM Inference with Parallel Speculative Decoding
+ *           in vLLM": the input formula (Input_i = emb(new) (+) h_context for
+ *           i = 1, emb(mask) (+) h_shared for 2 <= i <= K), prompt-position
+ *           handling (position i carries the hidden state of i-1), and the
+ *           engineering section (fused expansion kernel, hidden-state
+ *           management, KV-cache slot mapping with -1 for rejected tokens).
+ *
+ * Conventions shared by every entry point
+ *   - All tensors are caller-owned DEVICE memory on the current device unless
+ *     a parameter says "host".  The library never frees caller memory.  The
+ *     handle owns only its workspace, allocated in pe_create.
+ *   - Every compute call is asynchronous on the given stream (cudaStream_t
+ *     passed as void*; NULL = legacy default stream).  Calls on one handle
+ *     must not overlap in time (they share the workspace).
+ *   - Host-checkable errors are returned synchronously and launch nothing:
+ *     PE_ERR_INVALID_ARGUMENT (bad size, null pointer, misaligned pointer),
+ *     PE_ERR_UNSUPPORTED (a shape the kernels do not implement),
+ *     PE_ERR_CUDA (a CUDA runtime call or launch failed).
+ *   - Data-dependent violations found by the kernels (an accepted count
+ *     outside the window, a block id outside [0, num_blocks), a position past
+ *     the block table, a token id outside the vocabulary, a wait that timed
+ *     out) never trap: the kernel records a code, skips the offending write,
+ *     and pe_get_device_error reports it.
+ *   - Matrices are row-major [out, in].  bf16 tensors are IEEE bfloat16.
+ *   - No C++ exception crosses this ABI and the library keeps no global state
+ *     besides the per-device tensor-map encoder entry point.
+ */
+#ifndef PEAGLE_H_
+#define PEAGLE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t pe_status;
+enum {
+  PE_OK = 0,
+  PE_ERR_INVALID_ARGUMENT = 1,
+  PE_ERR_UNSUPPORTED = 2,
+  PE_ERR_CUDA = 3,
+  PE_ERR_OUT_OF_MEMORY = 4,
+  PE_ERR_DEVICE = 5 /* a kernel recorded a data-dependent violation */
+};
+
+/* Device-side error codes reported by pe_get_device_error (first one wins). */
+enum {
+  PE_DEV_OK = 0,
+  PE_DEV_BAD_ACCEPTED = 1,    /* num_accepted[r] outside [0, n_r - 1] */
+  PE_DEV_BAD_BLOCK = 2,       /* block id outside [0, num_blocks) */
+  PE_DEV_BAD_POSITION = 3,    /* position beyond bt_stride * page_size */
+  PE_DEV_BAD_TOKEN = 4,       /* token id outside [0, vocab) */
+  PE_DEV_TIMEOUT = 5,         /* a bounded wait inside a kernel gave up */
+  PE_DEV_BAD_ROW = 6          /* a row index outside the expanded batch */
+};
+
+typedef enum { PE_DTYPE_BF16 = 0, PE_DTYPE_F32 = 1 } pe_dtype;
+
+/* Drafter shape ([paper] section 2: N LLaMA 3 decoder layers with RoPE). */
+typedef struct {
+  int32_t d;             /* drafter hidden width */
+  int32_t n_layers;      /* N */
+  int32_t n_heads;       /* query heads Hq */
+  int32_t n_kv_heads;    /* key/value heads Hkv (Hq % Hkv == 0) */
+  int32_t head_dim;      /* dh: 64 or 128 */
+  int32_t ffn;           /* SwiGLU inner width F */
+  int32_t vocab;         /* V */
+  int32_t hidden3;       /* width of the target hidden states = 3d ([paper] Fig. 2) */
+  int32_t page_size;     /* KV page size: must be 16 */
+  int32_t mask_token_id; /* the MASK token id ([blog] fused-kernel bullet) */
+  float rope_theta;      /* rotate-half RoPE base */
+  float rms_eps;         /* RMSNorm epsilon */
+  int32_t dtype;         /* pe_dtype of weights, hidden states, KV cache */
+} pe_model_desc;
+
+/* One decoder layer's weights (borrowed device pointers, dtype of the model).
+ * qkv [(Hq + 2 Hkv) dh, d_in] with rows ordered q heads, k heads, v heads;
+ * d_in = 2d for layer 0 (input = [RMSNorm_e(emb) ; RMSNorm_h(fc h)]) and d
+ * for later layers.  o [d, Hq dh]; gate, up [F, d]; down [d, F].
+ * Norm gains are [d]: norm_e and norm_h for layer 0, norm_in for later
+ * layers (NULL where not used), norm_post for every layer. */
+typedef struct {
+  const void* qkv;
+  const void* o;
+  const void* gate;
+  const void* up;
+  const void* down;
+  const void* norm_e;
+  const void* norm_h;
+  const void* norm_in;
+  const void* norm_post;
+} pe_layer_weights;
+
+/* Drafter weights (borrowed device pointers; must outlive the handle).
+ * emb [V, d] (its MASK row is the learned emb(mask)); fc [d, hidden3];
+ * h_shared [hidden3] ([blog] hidden-state management; [paper] section 2);
+ * norm_final [d]; lm_head [V, d]; layers: HOST array of n_layers entries
+ * (copied by pe_create). */
+typedef struct {
+  const void* emb;
+  const void* fc;
+  const void* h_shared;
+  const void* norm_final;
+  const void* lm_head;
+  const pe_layer_weights* layers;
+} pe_weights;
+
+/* The expanded drafting batch.  Device pointers are caller-owned buffers
+ * sized for T' = T + B (K - 1) rows; pe_expand_batch fills them and records
+ * B, K, T and T_out (host fields) for pe_draft_forward.
+ * Layout of request r: rows cu_out[r] .. cu_out[r] + n_r - 1 come from the
+ * target window (row j carries the target hidden state of window row j and
+ * sits one position after it), rows cu_out[r] + n_r .. + n_r + K - 2 are the
+ * K - 1 MASK rows. */
+typedef struct {
+  int32_t* ids;          /* [T'] token ids */
+  int32_t* pos;          /* [T'] positions */
+  int32_t* slot;         /* [T'] KV slot = block * 16 + pos % 16; -1 if rejected */
+  uint8_t* is_rejected;  /* [T'] 1 for window rows after the accepted prefix */
+  uint8_t* is_masked;    /* [T'] 1 for MASK rows */
+  int32_t* new_idx;      /* [B*K] rows that are sampled: next-token row, then MASK rows */
+  int32_t* hidden_map;   /* [T] target row t -> expanded row */
+  int32_t* cu_out;       /* [B+1] first expanded row of each request */
+  int32_t* seq_lens;     /* [B] drafter sequence length after this step */
+  void* hidden;          /* [T', hidden3] expanded target hidden states */
+  int32_t B, K, T, T_out;  /* host fields written by pe_expand_batch */
+} pe_expanded;
+
+typedef struct pe_handle pe_handle;
+
+/* Create a handle: validates the shape, copies the layer-pointer array,
+ * builds the TMA descriptors of the weights and allocates the workspace for
+ * up to max_tokens expanded rows and max_reqs requests.  Weights are
+ * borrowed.  Returns PE_ERR_UNSUPPORTED for shapes the kernels do not cover
+ * (d, F, hidden3 and Hq*dh must be multiples of 64; dh in {64, 128};
+ * page_size 16). */
+pe_status pe_create(const pe_model_desc* desc, const pe_weights* weights,
+                    int32_t max_tokens, int32_t max_reqs, pe_handle** out);
+
+/* Free the handle's workspace (synchronises the device first). */
+pe_status pe_destroy(pe_handle* h);
+
+/* Batch expansion + hidden-state broadcast ([blog] engineering section:
+ * fused expansion kernel and hidden-state management; KV-cache bullet).
+ *
+ * Inputs (device): target_ids/target_pos [T] int32, the verify window of
+ * every request back to back; cu_in [B+1] int32 window offsets (n_r =
+ * cu_in[r+1] - cu_in[r] >= 1); num_accepted [B] int32 (a_r in [0, n_r-1]);
+ * sampled_ids [B] int32 (the target's sampled token per request);
+ * block_table [B, bt_stride] int32 physical page ids; target_hidden
+ * [T, hidden3] (model dtype).  B, K, T, bt_stride, num_blocks are host ints.
+ * Rules per request r (a = a_r, s = sampled, q_j = target_pos of window
+ * row j): row j < n_r gets position q_j + 1 and token target_ids[j+1] (s for
+ * the last row), then row a gets s; rows j > a are rejected (slot -1);
+ * MASK rows k = 1..K-1 get the MASK id at position q_a + 1 + k;
+ * new_idx = [row a, MASK rows]; seq_lens = q_a + K + 1;
+ * hidden[hidden_map[t]] = target_hidden[t], then MASK rows = h_shared.
+ * Writes every field of *out (which the caller fills with buffer pointers).
+ * Requires 1 <= K <= 16 and n_r + K - 1 <= 32. */
+pe_status pe_expand_batch(pe_handle* h, int32_t B, int32_t K, int32_t T,
+                          const int32_t* target_ids, const int32_t* target_pos,
+                          const int32_t* cu_in, const int32_t* num_accepted,
+                          const int32_t* sampled_ids, const int32_t* block_table,
+                          int32_t bt_stride, int32_t num_blocks,
+                          const void* target_hidden, pe_expanded* out,
+                          void* stream);
+
+/* The drafter pass over the expanded batch ([paper] section 2: all rows go
+ * through the N layers at once; [blog] "parallel prediction").
+ *
+ * Per row: e = emb[id], h = fc x hidden; layer 0 input [RMSNorm_e(e) ;
+ * RMSNorm_h(h)], residual h; each layer: QKV projection, rotate-half RoPE at
+ * the row's position, K/V written to the paged cache at slot (rows with
+ * slot -1 write nothing), causal attention of every non-rejected row over
+ * positions 0..pos of its request (GQA), O projection + residual, RMSNorm,
+ * SwiGLU MLP + residual.  Finally the rows new_idx are gathered and
+ * RMSNorm'ed with norm_final into out_hidden [B*K, d] (model dtype).
+ * k_cache/v_cache: HOST arrays of n_layers device pointers, each a pool
+ * [num_blocks, Hkv, 16, dh] (model dtype); block_table as in
+ * pe_expand_batch.  B and K must match the values recorded in *ex. */
+pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B,
+                           int32_t K, const int32_t* block_table,
+                           int32_t bt_stride, void* const* k_cache,
+                           void* const* v_cache, int32_t num_blocks,
+                           void* out_hidden, void* stream);
+
+/* LM head + argmax ([paper] section 2: LM head after the N layers).
+ * hidden [M, d] (model dtype, already final-normed), M <= max_tokens.
+ * out_tokens [M] int32: argmax over the vocabulary of hidden x lm_head^T,
+ * lowest index on ties.  out_logits: NULL, or [M, V] fp32 logits. */
+pe_status pe_lmhead_argmax(pe_handle* h, const void* hidden, int32_t M,
+                           int32_t* out_tokens, float* out_logits,
+                           void* stream);
+
+/* Synchronise the stream, return the first device-side error code recorded
+ * since the last call (PE_DEV_*), and clear it. */
+pe_status pe_get_device_error(pe_handle* h, int32_t* code, void* stream);
+
+/* Optional diagnostics: when residual_trace is non-NULL, every later
+ * pe_draft_forward copies the fp32 residual stream [T', d] after each layer
+ * into residual_trace + layer * max_tokens * d (caller-owned device buffer of
+ * n_layers * max_tokens * d floats).  NULL turns it off. */
+pe_status pe_set_trace(pe_handle* h, float* residual_trace);
+
+/* y[M, N] = x[M, K] . w[N, K]^T with the library's GEMM for the model dtype
+ * (tcgen05 tensor cores for bf16, FFMA for f32); y is fp32.  A diagnostic
+ * entry point for checking the projection kernels in isolation; K % 64 == 0
+ * for bf16. */
+pe_status pe_linear(pe_handle* h, const void* x, const void* w, float* y,
+                    int32_t M, int32_t N, int32_t K, void* stream);
+
+/* Static description of a status code. */
+const char* pe_status_string(pe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PEAGLE_H_ */

@@ -1,0 +1,266 @@
+"""ctypes binding of libpeagle.so (include/peagle.h): argument marshalling only.
+
+Every step of the drafting path runs in the library's CUDA kernels; PyTorch
+is used here for device memory and streams.  Importing this module does not
+need a GPU, but calling into the library does; if the library has not been
+built the import fails loudly (there is no fallback path).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libpeagle.so")
+
+PE_OK = 0
+PE_ERR_INVALID_ARGUMENT = 1
+PE_ERR_UNSUPPORTED = 2
+PE_ERR_CUDA = 3
+PE_ERR_OUT_OF_MEMORY = 4
+PE_ERR_DEVICE = 5
+PE_DTYPE_BF16 = 0
+PE_DTYPE_F32 = 1
+
+EXPORTED = ("pe_create", "pe_destroy", "pe_expand_batch", "pe_draft_forward",
+            "pe_lmhead_argmax", "pe_get_device_error", "pe_set_trace", "pe_linear",
+            "pe_status_string")
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+
+
+class pe_model_desc(ctypes.Structure):
+    _fields_ = [("d", _i32), ("n_layers", _i32), ("n_heads", _i32), ("n_kv_heads", _i32),
+                ("head_dim", _i32), ("ffn", _i32), ("vocab", _i32), ("hidden3", _i32),
+                ("page_size", _i32), ("mask_token_id", _i32), ("rope_theta", ctypes.c_float),
+                ("rms_eps", ctypes.c_float), ("dtype", _i32)]
+
+
+class pe_layer_weights(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in ("qkv", "o", "gate", "up", "down", "norm_e", "norm_h",
+                                   "norm_in", "norm_post")]
+
+
+class pe_weights(ctypes.Structure):
+    _fields_ = [("emb", _vp), ("fc", _vp), ("h_shared", _vp), ("norm_final", _vp),
+                ("lm_head", _vp), ("layers", ctypes.POINTER(pe_layer_weights))]
+
+
+class pe_expanded(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in ("ids", "pos", "slot", "is_rejected", "is_masked",
+                                   "new_idx", "hidden_map", "cu_out", "seq_lens", "hidden")] + \
+               [("B", _i32), ("K", _i32), ("T", _i32), ("T_out", _i32)]
+
+
+class PeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+        self.status = status
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with "
+                          "speculative_drafting_expand_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER
+    lib.pe_create.argtypes = [P(pe_model_desc), P(pe_weights), _i32, _i32, P(_vp)]
+    lib.pe_destroy.argtypes = [_vp]
+    lib.pe_expand_batch.argtypes = [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                    _i32, _vp, P(pe_expanded), _vp]
+    lib.pe_draft_forward.argtypes = [_vp, P(pe_expanded), _i32, _i32, _vp, _i32, P(_vp), P(_vp),
+                                     _i32, _vp, _vp]
+    lib.pe_lmhead_argmax.argtypes = [_vp, _vp, _i32, _vp, _vp, _vp]
+    lib.pe_get_device_error.argtypes = [_vp, P(_i32), _vp]
+    lib.pe_set_trace.argtypes = [_vp, _vp]
+    lib.pe_linear.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp]
+    lib.pe_status_string.argtypes = [_i32]
+    lib.pe_status_string.restype = ctypes.c_char_p
+    for name in EXPORTED[:-1]:
+        getattr(lib, name).restype = _i32
+    return lib
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    global _LIB
+    if _LIB is None:
+        _LIB = load_library()
+    return _LIB
+
+
+def status_string(s: int) -> str:
+    return lib().pe_status_string(s).decode()
+
+
+def _check(fn: str, s: int):
+    if s != PE_OK:
+        raise PeError(fn, s)
+
+
+# ---------------------------------------------------------------------------
+# tensors
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def stream_ptr(stream=None) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def to_device(a: np.ndarray, dtype: str, device="cuda"):
+    """Host array (bf16 bits as uint16, or float32 / int32 / uint8) -> tensor."""
+    torch = _torch()
+    if dtype == "bf16" and a.dtype == np.uint16:
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(a))
+    return t.to(device)
+
+
+def to_host(t) -> np.ndarray:
+    """Tensor -> host array (bf16 as uint16 bits)."""
+    torch = _torch()
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def model_desc(shape) -> pe_model_desc:
+    return pe_model_desc(shape.d, shape.n_layers, shape.n_heads, shape.n_kv_heads,
+                         shape.head_dim, shape.ffn, shape.vocab, shape.hidden3,
+                         shape.page_size, shape.mask_token_id, shape.rope_theta,
+                         shape.rms_eps, PE_DTYPE_BF16 if shape.dtype == "bf16" else PE_DTYPE_F32)
+
+
+class Drafter:
+    """Owns the device copies of the weights and a pe_handle."""
+
+    def __init__(self, shape, host_weights: Dict, max_tokens: int, max_reqs: int,
+                 device="cuda"):
+        self.shape = shape
+        self.device = device
+        dt = shape.dtype
+        W = host_weights
+        self.w = {k: to_device(W[k], dt, device) for k in
+                  ("emb", "fc", "h_shared", "norm_final", "lm_head")}
+        self.layers = [{k: to_device(v, dt, device) for k, v in lw.items()}
+                       for lw in W["layers"]]
+        arr = (pe_layer_weights * shape.n_layers)()
+        for l, lw in enumerate(self.layers):
+            arr[l] = pe_layer_weights(*(ptr(lw.get(f[0])) for f in pe_layer_weights._fields_))
+        self._layer_arr = arr
+        self._weights = pe_weights(ptr(self.w["emb"]), ptr(self.w["fc"]),
+                                   ptr(self.w["h_shared"]), ptr(self.w["norm_final"]),
+                                   ptr(self.w["lm_head"]), arr)
+        self._desc = model_desc(shape)
+        h = _vp()
+        _check("pe_create", lib().pe_create(ctypes.byref(self._desc), ctypes.byref(self._weights),
+                                            max_tokens, max_reqs, ctypes.byref(h)))
+        self.handle = h
+        self.max_tokens = max_tokens
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib().pe_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ---------------------------------------------------------------------------
+# the entry points, same names as the C ABI
+# ---------------------------------------------------------------------------
+
+class Expanded:
+    """Caller-owned device buffers of one expanded batch (pe_expanded)."""
+
+    def __init__(self, T_out: int, T: int, B: int, K: int, hidden3: int, dtype: str,
+                 device="cuda"):
+        torch = _torch()
+        i32 = dict(dtype=torch.int32, device=device)
+        self.ids = torch.empty(T_out, **i32)
+        self.pos = torch.empty(T_out, **i32)
+        self.slot = torch.empty(T_out, **i32)
+        self.is_rejected = torch.empty(T_out, dtype=torch.uint8, device=device)
+        self.is_masked = torch.empty(T_out, dtype=torch.uint8, device=device)
+        self.new_idx = torch.empty(B * K, **i32)
+        self.hidden_map = torch.empty(T, **i32)
+        self.cu_out = torch.empty(B + 1, **i32)
+        self.seq_lens = torch.empty(B, **i32)
+        tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+        self.hidden = torch.empty(T_out, hidden3, dtype=tdt, device=device)
+        self.struct = pe_expanded(*(ptr(getattr(self, f)) for f in
+                                    ("ids", "pos", "slot", "is_rejected", "is_masked",
+                                     "new_idx", "hidden_map", "cu_out", "seq_lens", "hidden")),
+                                  0, 0, 0, 0)
+
+
+def pe_expand_batch(dr: Drafter, K: int, target_ids, target_pos, cu_in, num_accepted,
+                    sampled_ids, block_table, num_blocks: int, target_hidden,
+                    out: Expanded, stream=None):
+    B = num_accepted.shape[0]
+    T = target_ids.shape[0]
+    _check("pe_expand_batch", lib().pe_expand_batch(
+        dr.handle, B, K, T, ptr(target_ids), ptr(target_pos), ptr(cu_in), ptr(num_accepted),
+        ptr(sampled_ids), ptr(block_table), block_table.shape[1], num_blocks,
+        ptr(target_hidden), ctypes.byref(out.struct), stream_ptr(stream)))
+    return out
+
+
+def pe_draft_forward(dr: Drafter, ex: Expanded, block_table, k_cache: Sequence,
+                     v_cache: Sequence, num_blocks: int, out_hidden, stream=None):
+    L = len(k_cache)
+    kc = (_vp * L)(*[ptr(t) for t in k_cache])
+    vc = (_vp * L)(*[ptr(t) for t in v_cache])
+    _check("pe_draft_forward", lib().pe_draft_forward(
+        dr.handle, ctypes.byref(ex.struct), ex.struct.B, ex.struct.K, ptr(block_table),
+        block_table.shape[1], kc, vc, num_blocks, ptr(out_hidden), stream_ptr(stream)))
+    return out_hidden
+
+
+def pe_lmhead_argmax(dr: Drafter, hidden, out_tokens, out_logits=None, stream=None):
+    _check("pe_lmhead_argmax", lib().pe_lmhead_argmax(
+        dr.handle, ptr(hidden), hidden.shape[0], ptr(out_tokens), ptr(out_logits),
+        stream_ptr(stream)))
+    return out_tokens
+
+
+def pe_get_device_error(dr: Drafter, stream=None) -> int:
+    code = _i32(0)
+    _check("pe_get_device_error", lib().pe_get_device_error(dr.handle, ctypes.byref(code),
+                                                            stream_ptr(stream)))
+    return code.value
+
+
+def pe_set_trace(dr: Drafter, trace) -> None:
+    _check("pe_set_trace", lib().pe_set_trace(dr.handle, ptr(trace)))
+
+
+def pe_linear(dr: Drafter, x, w, y, stream=None):
+    M, K = x.shape
+    N = w.shape[0]
+    _check("pe_linear", lib().pe_linear(dr.handle, ptr(x), ptr(w), ptr(y), M, N, K,
+                                        stream_ptr(stream)))
+    return y

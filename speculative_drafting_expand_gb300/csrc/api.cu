@@ -1,0 +1,505 @@
+// api.cu -- the C ABI declared in include/peagle.h: handle and workspace,
+// host-side validation, and the order of kernels in one drafting step.
+#include <algorithm>
+#include <cmath>
+#include <map>
+#include <new>
+#include <tuple>
+#include <vector>
+
+#include "pe_common.cuh"
+#include "pe_kernels.h"
+
+namespace pe {
+cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
+                                const CUtensorMap& xb, bool dual, int M, int N, int K,
+                                const EpiArgs& epi, const TcGemmWorkspace& ws, int* err,
+                                cudaStream_t s);
+int tc_pick_bn(int M);
+size_t tc_partial_floats(int grid, int bn, bool dual);
+cudaError_t launch_attention_tc(const AttnArgs& a, float* partials, int* counters,
+                                cudaStream_t s);
+size_t attention_tc_partial_floats(const AttnArgs& a);
+}  // namespace pe
+
+using namespace pe;
+
+struct pe_handle {
+  pe_model_desc desc;
+  pe_weights w;
+  std::vector<pe_layer_weights> layers;
+  int device = 0;
+  int sm_count = 0;
+  int max_tokens = 0, max_reqs = 0;
+  size_t esize = 2;  // bytes per element of the model dtype
+
+  int* err = nullptr;
+  float* resid = nullptr;   // [max_tokens, d] fp32 residual stream
+  void* x_in = nullptr;     // [max_tokens, 2d] QKV input
+  void* qkv = nullptr;      // [max_tokens, (Hq + 2Hkv) dh]
+  void* q = nullptr;        // [max_tokens, Hq dh] rotated queries
+  void* attn = nullptr;     // [max_tokens, Hq dh]
+  void* xn = nullptr;       // [max_tokens, d] MLP input
+  void* act = nullptr;      // [max_tokens, F]
+  unsigned long long* keys = nullptr;  // [max_tokens] argmax keys (kept zero)
+  double* inv_freq64 = nullptr;        // [dh / 2]
+  float* gemm_partials = nullptr;
+  size_t gemm_partial_floats = 0;
+  int* tile_counters = nullptr;
+  int max_tiles = 0;
+  int* done_counter = nullptr;
+  float* attn_partials = nullptr;
+  size_t attn_partial_floats = 0;
+  int* attn_counters = nullptr;
+  float* trace = nullptr;
+
+  std::map<std::tuple<const void*, uint64_t, uint64_t, uint64_t, uint32_t>, CUtensorMap> maps;
+  std::vector<void*> allocations;
+};
+
+namespace {
+
+pe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PE_OK : PE_ERR_CUDA; }
+
+template <typename T>
+cudaError_t dev_alloc(pe_handle* h, T** p, size_t count) {
+  void* raw = nullptr;
+  cudaError_t e = cudaMalloc(&raw, std::max<size_t>(count, 1) * sizeof(T));
+  if (e != cudaSuccess) return e;
+  h->allocations.push_back(raw);
+  *p = static_cast<T*>(raw);
+  return cudaMemset(raw, 0, std::max<size_t>(count, 1) * sizeof(T));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+const CUtensorMap* get_map(pe_handle* h, const void* ptr, uint64_t rows, uint64_t cols,
+                           uint64_t ld, uint32_t box_rows) {
+  auto key = std::make_tuple(ptr, rows, cols, ld, box_rows);
+  auto it = h->maps.find(key);
+  if (it != h->maps.end()) return &it->second;
+  CUtensorMap m;
+  if (!tensor_map_2d_bf16(&m, ptr, rows, cols, ld, 64, box_rows)) return nullptr;
+  return &h->maps.emplace(key, m).first->second;
+}
+
+TcGemmWorkspace tc_ws(pe_handle* h) {
+  TcGemmWorkspace ws;
+  ws.partials = h->gemm_partials;
+  ws.partial_floats = h->gemm_partial_floats;
+  ws.tile_counters = h->tile_counters;
+  ws.max_tiles = h->max_tiles;
+  ws.done_counter = h->done_counter;
+  ws.sm_count = h->sm_count;
+  return ws;
+}
+
+// y = x . w^T (+ epilogue) with the GEMM of the model dtype.
+cudaError_t linear(pe_handle* h, const void* x, int ldx, const void* w, const void* w2, int M,
+                   int N, int K, const EpiArgs& epi, cudaStream_t s) {
+  if (h->desc.dtype == PE_DTYPE_F32)
+    return launch_gemm_simt(static_cast<const float*>(x), ldx, static_cast<const float*>(w),
+                            static_cast<const float*>(w2), M, N, K, epi, h->err, s);
+  const CUtensorMap* wa = get_map(h, w, N, K, K, 128);
+  const CUtensorMap* wa2 = w2 ? get_map(h, w2, N, K, K, 128) : wa;
+  const CUtensorMap* xb = get_map(h, x, M, K, ldx, tc_pick_bn(M));
+  if (!wa || !wa2 || !xb) return cudaErrorInvalidValue;
+  return launch_gemm_tc_maps(*wa, *wa2, *xb, w2 != nullptr, M, N, K, epi, tc_ws(h), h->err, s);
+}
+
+EpiArgs epi_none() {
+  EpiArgs e = {};
+  return e;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pe_status_string(pe_status s) {
+  switch (s) {
+    case PE_OK: return "ok";
+    case PE_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case PE_ERR_UNSUPPORTED: return "unsupported shape";
+    case PE_ERR_CUDA: return "CUDA runtime error";
+    case PE_ERR_OUT_OF_MEMORY: return "out of device memory";
+    case PE_ERR_DEVICE: return "device-side violation recorded";
+  }
+  return "unknown status";
+}
+
+pe_status pe_destroy(pe_handle* h) {
+  if (!h) return PE_ERR_INVALID_ARGUMENT;
+  cudaDeviceSynchronize();
+  for (void* p : h->allocations) cudaFree(p);
+  delete h;
+  return PE_OK;
+}
+
+pe_status pe_create(const pe_model_desc* desc, const pe_weights* weights, int32_t max_tokens,
+                    int32_t max_reqs, pe_handle** out) {
+  if (!desc || !weights || !out || max_tokens < 1 || max_reqs < 1) return PE_ERR_INVALID_ARGUMENT;
+  *out = nullptr;
+  const pe_model_desc& d = *desc;
+  if (d.d < 1 || d.n_layers < 1 || d.n_heads < 1 || d.n_kv_heads < 1 || d.ffn < 1 ||
+      d.vocab < 2 || d.hidden3 < 1 || d.head_dim < 1 || d.n_heads % d.n_kv_heads != 0 ||
+      d.mask_token_id < 0 || d.mask_token_id >= d.vocab || !(d.rms_eps >= 0.f) ||
+      !(d.rope_theta > 0.f))
+    return PE_ERR_INVALID_ARGUMENT;
+  if (d.dtype != PE_DTYPE_BF16 && d.dtype != PE_DTYPE_F32) return PE_ERR_INVALID_ARGUMENT;
+  if (d.page_size != 16 || (d.head_dim != 64 && d.head_dim != 128)) return PE_ERR_UNSUPPORTED;
+  const size_t es = d.dtype == PE_DTYPE_BF16 ? 2 : 4;
+  if ((d.hidden3 * es) % 16 != 0) return PE_ERR_UNSUPPORTED;
+  if (d.dtype == PE_DTYPE_BF16 &&
+      (d.d % 8 || d.ffn % 8 || d.hidden3 % 8 || (d.n_heads * d.head_dim) % 8))
+    return PE_ERR_UNSUPPORTED;
+  const pe_weights& w = *weights;
+  if (!w.emb || !w.fc || !w.h_shared || !w.norm_final || !w.lm_head || !w.layers)
+    return PE_ERR_INVALID_ARGUMENT;
+  for (int l = 0; l < d.n_layers; ++l) {
+    const pe_layer_weights& L = w.layers[l];
+    if (!L.qkv || !L.o || !L.gate || !L.up || !L.down || !L.norm_post) return PE_ERR_INVALID_ARGUMENT;
+    if (l == 0 ? (!L.norm_e || !L.norm_h) : !L.norm_in) return PE_ERR_INVALID_ARGUMENT;
+    if (d.dtype == PE_DTYPE_BF16 &&
+        !(aligned16(L.qkv) && aligned16(L.o) && aligned16(L.gate) && aligned16(L.up) &&
+          aligned16(L.down)))
+      return PE_ERR_INVALID_ARGUMENT;
+  }
+  if (d.dtype == PE_DTYPE_BF16 && !(aligned16(w.fc) && aligned16(w.lm_head)))
+    return PE_ERR_INVALID_ARGUMENT;
+  if (!aligned16(w.h_shared)) return PE_ERR_INVALID_ARGUMENT;
+
+  pe_handle* h = new (std::nothrow) pe_handle();
+  if (!h) return PE_ERR_OUT_OF_MEMORY;
+  h->desc = d;
+  h->w = w;
+  h->layers.assign(w.layers, w.layers + d.n_layers);
+  h->w.layers = h->layers.data();
+  h->max_tokens = max_tokens;
+  h->max_reqs = max_reqs;
+  h->esize = es;
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device);
+  const size_t T = max_tokens;
+  const int qkv_rows = (d.n_heads + 2 * d.n_kv_heads) * d.head_dim;
+  const int qd = d.n_heads * d.head_dim;
+  auto alloc_bytes = [&](void** p, size_t bytes) {
+    unsigned char* q = nullptr;
+    cudaError_t r = dev_alloc(h, &q, bytes);
+    *p = q;
+    return r;
+  };
+  if (e == cudaSuccess) e = dev_alloc(h, &h->err, 1);
+  if (e == cudaSuccess) e = dev_alloc(h, &h->resid, T * d.d);
+  if (e == cudaSuccess) e = alloc_bytes(&h->x_in, T * 2 * d.d * es);
+  if (e == cudaSuccess) e = alloc_bytes(&h->qkv, T * qkv_rows * es);
+  if (e == cudaSuccess) e = alloc_bytes(&h->q, T * qd * es);
+  if (e == cudaSuccess) e = alloc_bytes(&h->attn, T * qd * es);
+  if (e == cudaSuccess) e = alloc_bytes(&h->xn, T * d.d * es);
+  if (e == cudaSuccess) e = alloc_bytes(&h->act, T * d.ffn * es);
+  if (e == cudaSuccess) e = dev_alloc(h, &h->keys, T);
+  if (e == cudaSuccess) e = dev_alloc(h, &h->inv_freq64, d.head_dim / 2);
+  if (e == cudaSuccess) {
+    std::vector<double> inv(d.head_dim / 2);
+    for (int i = 0; i < d.head_dim / 2; ++i)
+      inv[i] = std::pow(static_cast<double>(d.rope_theta), -2.0 * i / d.head_dim);
+    e = cudaMemcpy(h->inv_freq64, inv.data(), inv.size() * sizeof(double), cudaMemcpyHostToDevice);
+  }
+  if (e == cudaSuccess && d.dtype == PE_DTYPE_BF16) {
+    const int bn = tc_pick_bn(max_tokens);
+    h->gemm_partial_floats = tc_partial_floats(h->sm_count, bn, true);
+    e = dev_alloc(h, &h->gemm_partials, h->gemm_partial_floats);
+    const int widest = std::max({d.vocab, qkv_rows, d.ffn, d.d, qd});
+    h->max_tiles = ((widest + 127) / 128) * ((max_tokens + 15) / 16);
+    if (e == cudaSuccess) e = dev_alloc(h, &h->tile_counters, h->max_tiles);
+    if (e == cudaSuccess) e = dev_alloc(h, &h->done_counter, 1);
+  }
+  if (e != cudaSuccess) {
+    pe_destroy(h);
+    return e == cudaErrorMemoryAllocation ? PE_ERR_OUT_OF_MEMORY : PE_ERR_CUDA;
+  }
+  *out = h;
+  return PE_OK;
+}
+
+pe_status pe_set_trace(pe_handle* h, float* residual_trace) {
+  if (!h) return PE_ERR_INVALID_ARGUMENT;
+  h->trace = residual_trace;
+  return PE_OK;
+}
+
+pe_status pe_get_device_error(pe_handle* h, int32_t* code, void* stream) {
+  if (!h || !code) return PE_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, h->err, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->err, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  *code = v;
+  return cuda_status(e);
+}
+
+pe_status pe_expand_batch(pe_handle* h, int32_t B, int32_t K, int32_t T, const int32_t* target_ids,
+                          const int32_t* target_pos, const int32_t* cu_in,
+                          const int32_t* num_accepted, const int32_t* sampled_ids,
+                          const int32_t* block_table, int32_t bt_stride, int32_t num_blocks,
+                          const void* target_hidden, pe_expanded* out, void* stream) {
+  if (!h || !out || B < 1 || B > h->max_reqs || K < 1 || K > 64 || T < B || bt_stride < 1 ||
+      num_blocks < 1)
+    return PE_ERR_INVALID_ARGUMENT;
+  const long long T_out = static_cast<long long>(T) + static_cast<long long>(B) * (K - 1);
+  if (T_out > h->max_tokens) return PE_ERR_INVALID_ARGUMENT;
+  if (!target_ids || !target_pos || !cu_in || !num_accepted || !sampled_ids || !block_table ||
+      !target_hidden || !out->ids || !out->pos || !out->slot || !out->is_rejected ||
+      !out->is_masked || !out->new_idx || !out->hidden_map || !out->cu_out || !out->seq_lens ||
+      !out->hidden)
+    return PE_ERR_INVALID_ARGUMENT;
+  if (!aligned16(target_hidden) || !aligned16(out->hidden)) return PE_ERR_INVALID_ARGUMENT;
+  ExpandArgs a;
+  a.B = B;
+  a.K = K;
+  a.T = T;
+  a.T_out = static_cast<int>(T_out);
+  a.target_ids = target_ids;
+  a.target_pos = target_pos;
+  a.cu_in = cu_in;
+  a.num_accepted = num_accepted;
+  a.sampled_ids = sampled_ids;
+  a.block_table = block_table;
+  a.bt_stride = bt_stride;
+  a.num_blocks = num_blocks;
+  a.page_size = h->desc.page_size;
+  a.mask_token_id = h->desc.mask_token_id;
+  a.target_hidden = target_hidden;
+  a.h_shared = h->w.h_shared;
+  a.row_bytes = static_cast<int>(h->desc.hidden3 * h->esize);
+  a.ids = out->ids;
+  a.pos = out->pos;
+  a.slot = out->slot;
+  a.is_rejected = out->is_rejected;
+  a.is_masked = out->is_masked;
+  a.new_idx = out->new_idx;
+  a.hidden_map = out->hidden_map;
+  a.cu_out = out->cu_out;
+  a.seq_lens = out->seq_lens;
+  a.hidden = out->hidden;
+  a.err = h->err;
+  cudaError_t e = launch_expand(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return PE_ERR_CUDA;
+  out->B = B;
+  out->K = K;
+  out->T = T;
+  out->T_out = a.T_out;
+  return PE_OK;
+}
+
+pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32_t K,
+                           const int32_t* block_table, int32_t bt_stride, void* const* k_cache,
+                           void* const* v_cache, int32_t num_blocks, void* out_hidden,
+                           void* stream) {
+  if (!h || !ex || !block_table || !k_cache || !v_cache || !out_hidden || bt_stride < 1 ||
+      num_blocks < 1)
+    return PE_ERR_INVALID_ARGUMENT;
+  if (ex->B != B || ex->K != K || ex->T_out < 1 || ex->T_out > h->max_tokens ||
+      ex->T_out != ex->T + B * (K - 1))
+    return PE_ERR_INVALID_ARGUMENT;
+  const pe_model_desc& d = h->desc;
+  for (int l = 0; l < d.n_layers; ++l)
+    if (!k_cache[l] || !v_cache[l]) return PE_ERR_INVALID_ARGUMENT;
+  if (static_cast<long long>(B) * K > h->max_tokens) return PE_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int rows = ex->T_out;
+  const int dt = d.dtype;
+  const int qkv_rows = (d.n_heads + 2 * d.n_kv_heads) * d.head_dim;
+  const int qd = d.n_heads * d.head_dim;
+  cudaError_t e;
+
+  // fc: projected target hidden state -> residual stream (fp32)
+  EpiArgs ep = epi_none();
+  ep.kind = EPI_STORE;
+  ep.M = rows;
+  ep.N = d.d;
+  ep.out = h->resid;
+  ep.ldo = d.d;
+  ep.out_f32 = 1;
+  if ((e = linear(h, ex->hidden, d.hidden3, h->w.fc, nullptr, rows, d.d, d.hidden3, ep, s)))
+    return PE_ERR_CUDA;
+  // layer-0 input: [RMSNorm_e(emb[id]) ; RMSNorm_h(fc h)]
+  EmbedConcatArgs ec;
+  ec.rows = rows;
+  ec.d = d.d;
+  ec.vocab = d.vocab;
+  ec.ids = ex->ids;
+  ec.emb = h->w.emb;
+  ec.h = h->resid;
+  ec.g_e = h->layers[0].norm_e;
+  ec.g_h = h->layers[0].norm_h;
+  ec.eps = d.rms_eps;
+  ec.x = h->x_in;
+  ec.err = h->err;
+  if ((e = launch_embed_concat(dt, ec, s))) return PE_ERR_CUDA;
+
+  for (int l = 0; l < d.n_layers; ++l) {
+    const pe_layer_weights& L = h->layers[l];
+    const int d_in = l == 0 ? 2 * d.d : d.d;
+    if (l > 0) {
+      RmsNormArgs rn = {};
+      rn.rows = rows;
+      rn.d = d.d;
+      rn.x = h->resid;
+      rn.rows_in = rows;
+      rn.g = L.norm_in;
+      rn.eps = d.rms_eps;
+      rn.y = h->x_in;
+      rn.err = h->err;
+      if ((e = launch_rmsnorm(dt, rn, s))) return PE_ERR_CUDA;
+    }
+    // QKV projection
+    ep = epi_none();
+    ep.kind = EPI_STORE;
+    ep.M = rows;
+    ep.N = qkv_rows;
+    ep.out = h->qkv;
+    ep.ldo = qkv_rows;
+    ep.out_f32 = dt == PE_DTYPE_F32 ? 1 : 0;
+    if ((e = linear(h, h->x_in, d_in, L.qkv, nullptr, rows, qkv_rows, d_in, ep, s)))
+      return PE_ERR_CUDA;
+    // RoPE + paged KV write (slot -1: nothing written)
+    RopeKvArgs rk;
+    rk.rows = rows;
+    rk.Hq = d.n_heads;
+    rk.Hkv = d.n_kv_heads;
+    rk.dh = d.head_dim;
+    rk.num_blocks = num_blocks;
+    rk.qkv = h->qkv;
+    rk.pos = ex->pos;
+    rk.slot = ex->slot;
+    rk.inv_freq = nullptr;
+    rk.inv_freq64 = h->inv_freq64;
+    rk.q_out = h->q;
+    rk.k_cache = k_cache[l];
+    rk.v_cache = v_cache[l];
+    rk.err = h->err;
+    if ((e = launch_rope_kv(dt, rk, s))) return PE_ERR_CUDA;
+    // paged causal attention
+    AttnArgs at;
+    at.rows = rows;
+    at.B = B;
+    at.Hq = d.n_heads;
+    at.Hkv = d.n_kv_heads;
+    at.dh = d.head_dim;
+    at.bt_stride = bt_stride;
+    at.num_blocks = num_blocks;
+    at.max_seq = bt_stride * d.page_size;
+    at.q = h->q;
+    at.k_cache = k_cache[l];
+    at.v_cache = v_cache[l];
+    at.pos = ex->pos;
+    at.is_rejected = ex->is_rejected;
+    at.cu_out = ex->cu_out;
+    at.block_table = block_table;
+    at.out = h->attn;
+    at.scale = 1.0f / std::sqrt(static_cast<float>(d.head_dim));
+    at.err = h->err;
+    if ((e = launch_attention_simt(dt, at, s))) return PE_ERR_CUDA;
+    // O projection + residual
+    ep = epi_none();
+    ep.kind = EPI_ADD;
+    ep.M = rows;
+    ep.N = d.d;
+    ep.resid = h->resid;
+    ep.ldr = d.d;
+    if ((e = linear(h, h->attn, qd, L.o, nullptr, rows, d.d, qd, ep, s))) return PE_ERR_CUDA;
+    // MLP
+    RmsNormArgs rn = {};
+    rn.rows = rows;
+    rn.d = d.d;
+    rn.x = h->resid;
+    rn.rows_in = rows;
+    rn.g = L.norm_post;
+    rn.eps = d.rms_eps;
+    rn.y = h->xn;
+    rn.err = h->err;
+    if ((e = launch_rmsnorm(dt, rn, s))) return PE_ERR_CUDA;
+    ep = epi_none();
+    ep.kind = EPI_SILU_MUL;
+    ep.M = rows;
+    ep.N = d.ffn;
+    ep.out = h->act;
+    ep.ldo = d.ffn;
+    ep.out_f32 = dt == PE_DTYPE_F32 ? 1 : 0;
+    if ((e = linear(h, h->xn, d.d, L.gate, L.up, rows, d.ffn, d.d, ep, s))) return PE_ERR_CUDA;
+    ep = epi_none();
+    ep.kind = EPI_ADD;
+    ep.M = rows;
+    ep.N = d.d;
+    ep.resid = h->resid;
+    ep.ldr = d.d;
+    if ((e = linear(h, h->act, d.ffn, L.down, nullptr, rows, d.d, d.ffn, ep, s)))
+      return PE_ERR_CUDA;
+    if (h->trace) {
+      e = cudaMemcpyAsync(h->trace + static_cast<size_t>(l) * h->max_tokens * d.d, h->resid,
+                          static_cast<size_t>(rows) * d.d * sizeof(float),
+                          cudaMemcpyDeviceToDevice, s);
+      if (e) return PE_ERR_CUDA;
+    }
+  }
+  // final norm of the B*K sampled rows
+  RmsNormArgs rn = {};
+  rn.rows = B * K;
+  rn.d = d.d;
+  rn.x = h->resid;
+  rn.row_index = ex->new_idx;
+  rn.rows_in = rows;
+  rn.g = h->w.norm_final;
+  rn.eps = d.rms_eps;
+  rn.y = out_hidden;
+  rn.err = h->err;
+  if ((e = launch_rmsnorm(dt, rn, s))) return PE_ERR_CUDA;
+  return PE_OK;
+}
+
+pe_status pe_lmhead_argmax(pe_handle* h, const void* hidden, int32_t M, int32_t* out_tokens,
+                           float* out_logits, void* stream) {
+  if (!h || !hidden || !out_tokens || M < 1 || M > h->max_tokens) return PE_ERR_INVALID_ARGUMENT;
+  const pe_model_desc& d = h->desc;
+  if (d.dtype == PE_DTYPE_BF16 && !aligned16(hidden)) return PE_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  EpiArgs ep = epi_none();
+  ep.kind = EPI_ARGMAX;
+  ep.M = M;
+  ep.N = d.vocab;
+  ep.logits = out_logits;
+  ep.ldl = d.vocab;
+  ep.keys = h->keys;
+  ep.tokens = out_tokens;
+  cudaError_t e = linear(h, hidden, d.d, h->w.lm_head, nullptr, M, d.vocab, d.d, ep, s);
+  if (e == cudaSuccess && d.dtype == PE_DTYPE_F32)
+    e = launch_argmax_finalize(M, h->keys, out_tokens, s);
+  return cuda_status(e);
+}
+
+pe_status pe_linear(pe_handle* h, const void* x, const void* w, float* y, int32_t M, int32_t N,
+                    int32_t K, void* stream) {
+  if (!h || !x || !w || !y || M < 1 || N < 1 || K < 1 || M > h->max_tokens)
+    return PE_ERR_INVALID_ARGUMENT;
+  if (h->desc.dtype == PE_DTYPE_BF16 && (K % 8 || !aligned16(x) || !aligned16(w)))
+    return PE_ERR_INVALID_ARGUMENT;
+  if (h->desc.dtype == PE_DTYPE_BF16) {
+    const int bn = tc_pick_bn(M);
+    const long long tiles = static_cast<long long>((N + 127) / 128) * ((M + bn - 1) / bn);
+    if (tiles > h->max_tiles) return PE_ERR_INVALID_ARGUMENT;
+  }
+  EpiArgs ep = epi_none();
+  ep.kind = EPI_STORE;
+  ep.M = M;
+  ep.N = N;
+  ep.out = y;
+  ep.ldo = N;
+  ep.out_f32 = 1;
+  return cuda_status(linear(h, x, K, w, nullptr, M, N, K, ep, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,475 @@
+// gemm_tc.cu -- the drafter's dense projections on 5th-generation tensor
+// cores: y[t, o] = sum_k x[t, k] w[o, k] with bf16 operands and fp32
+// accumulators in tensor memory (fc, QKV, O, gate/up, down, LM head; paper
+// summary "P-EAGLE: Parallel-Drafting EAGLE with Scalable Training",
+// section 2: embedding + projected hidden state, N LLaMA layers, LM head).
+//
+// Layout: the weight rows are the MMA's M side (128 output features per
+// tile) and the tokens its N side (16..256 per tile), so a batch of a few
+// rows still fills the 128-lane accumulator.  Both operands are K-major and
+// arrive by TMA in 128-byte-swizzled 64-wide k-blocks.
+//
+// Work split: persistent, one CTA per SM.  The (feature tile, token tile,
+// k-block) units are dealt out in equal contiguous ranges ("stream-K"), so
+// a 5120 x 2880 projection at batch 1 keeps all SMs streaming weights.  A
+// tile split between CTAs is summed by its last-arriving CTA from fp32
+// partials in a fixed order (deterministic, no float atomics, no waiting).
+//
+// Warp roles: warps 0-3 epilogue (TMEM lanes 0-127), warp 4 TMA producer,
+// warp 5 MMA issuer and TMEM owner.  The producer loads the first weight
+// tiles before waiting on the previous kernel (programmatic dependent
+// launch), so weight streaming overlaps the previous kernel's tail.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "pe_common.cuh"
+#include "pe_kernels.h"
+
+namespace pe {
+
+template <int BN, bool DUAL>
+struct TcCfg {
+  static constexpr int BM = 128, BK = 64;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int NA = DUAL ? 2 : 1;
+  static constexpr int STAGE_BYTES = A_BYTES * NA + B_BYTES;
+  static constexpr int ACC_COLS = BN * NA;
+  static constexpr int NUM_ACC = (2 * ACC_COLS <= 512) ? 2 : 1;
+  static constexpr int TMEM_RAW = ACC_COLS * NUM_ACC;
+  static constexpr int TMEM_COLS = TMEM_RAW <= 32    ? 32
+                                   : TMEM_RAW <= 64  ? 64
+                                   : TMEM_RAW <= 128 ? 128
+                                   : TMEM_RAW <= 256 ? 256
+                                                     : 512;
+  static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+  static_assert(2 * STAGES + 5 <= BAR_BYTES / 8, "barrier space");
+};
+
+struct TcParams {
+  int M, N, K, kb, tiles_m;
+  long long units;
+  EpiArgs epi;
+  float* ws;
+  int* counters;
+  int* done;
+  int* err;
+};
+
+__device__ __forceinline__ long long unit_lo(int c, long long U, int G) {
+  return static_cast<long long>(c) * U / G;
+}
+// The CTA whose unit range contains unit u.
+__device__ __forceinline__ int cta_of_unit(long long u, long long U, int G) {
+  int c = static_cast<int>((u * G) / U);
+  if (c > G - 1) c = G - 1;
+  while (c > 0 && unit_lo(c, U, G) > u) --c;
+  while (c + 1 < G && unit_lo(c + 1, U, G) <= u) ++c;
+  return c;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Apply the epilogue to 16 token columns [t0, t0 + 16) of output feature o.
+// Called by all 32 lanes of a warp together (the argmax reduces across them).
+template <bool DUAL>
+__device__ __forceinline__ void epi_chunk(const EpiArgs& e, int o, int t0, const float* v,
+                                          const float* v2, int lane) {
+  const bool of = o < e.N;
+  switch (e.kind) {
+    case EPI_STORE:
+      if (e.out_f32) {
+        float* out = static_cast<float*>(e.out);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (of && t0 + j < e.M) out[static_cast<size_t>(t0 + j) * e.ldo + o] = v[j];
+      } else {
+        bf16* out = static_cast<bf16*>(e.out);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (of && t0 + j < e.M)
+            out[static_cast<size_t>(t0 + j) * e.ldo + o] = __float2bfloat16_rn(v[j]);
+      }
+      break;
+    case EPI_ADD:
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (of && t0 + j < e.M) e.resid[static_cast<size_t>(t0 + j) * e.ldr + o] += v[j];
+      break;
+    case EPI_SILU_MUL: {
+      bf16* out = static_cast<bf16*>(e.out);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (of && t0 + j < e.M)
+          out[static_cast<size_t>(t0 + j) * e.ldo + o] =
+              __float2bfloat16_rn(silu_f(v[j]) * (DUAL ? v2[j] : 1.f));
+      break;
+    }
+    case EPI_ARGMAX:
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int t = t0 + j;
+        const bool ok = of && t < e.M;
+        if (ok && e.logits) e.logits[static_cast<size_t>(t) * e.ldl + o] = v[j];
+        unsigned long long key = ok ? argmax_key(v[j], o) : 0ull;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, off);
+          key = other > key ? other : key;
+        }
+        if (lane == 0 && key != 0ull) atomicMax(e.keys + t, key);
+      }
+      break;
+  }
+}
+
+template <int BN, bool DUAL>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                   const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+  using C = TcCfg<BN, DUAL>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;  // [2]
+  uint64_t* acc_empty = acc_full + 2;      // [2]
+  uint64_t* drain = acc_empty + 2;         // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* flag = reinterpret_cast<volatile int*>(tmem_slot + 1);     // reducer election
+  volatile int* epi_ok = reinterpret_cast<volatile int*>(tmem_slot + 2);   // epilogue wait result
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 128);
+    }
+    mbar_init(drain, 1);
+    mbar_fence_init();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if (DUAL) tma_prefetch_desc(&tmA2);
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // TMEM is held before dependents may start, so their allocation can only
+  // wait for this grid to finish, never the other way round.
+  grid_dep_launch();
+
+  const long long U = p.units;
+  const int G = gridDim.x, cta = blockIdx.x, kb = p.kb;
+  const long long lo = unit_lo(cta, U, G), hi = unit_lo(cta + 1, U, G);
+
+  if (warp == 4) {
+    if (lane == 0) {
+      const uint64_t pol_a = p.tiles_m == 1 ? l2_policy_evict_first() : l2_policy_evict_last();
+      const uint64_t pol_b = l2_policy_evict_last();
+      const long long n = hi - lo;
+      const int npre = static_cast<int>(n < C::STAGES ? n : C::STAGES);
+      // weight tiles of the first stages do not depend on earlier kernels
+      for (int i = 0; i < npre; ++i) {
+        const long long u = lo + i;
+        const int tile = static_cast<int>(u / kb), kk = static_cast<int>(u % kb);
+        const int f = tile / p.tiles_m;
+        uint8_t* st = smem + i * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
+        tma_load_2d(st, &tmA, &full[i], kk * 64, f * 128, pol_a);
+        if (DUAL) tma_load_2d(st + C::A_BYTES, &tmA2, &full[i], kk * 64, f * 128, pol_a);
+      }
+      grid_dep_wait();
+      for (int i = 0; i < npre; ++i) {
+        const long long u = lo + i;
+        const int tile = static_cast<int>(u / kb), kk = static_cast<int>(u % kb);
+        const int m = tile % p.tiles_m;
+        tma_load_2d(smem + i * C::STAGE_BYTES + C::NA * C::A_BYTES, &tmB, &full[i], kk * 64,
+                    m * BN, pol_b);
+      }
+      long long issued = npre;
+      for (long long i = npre; i < n; ++i) {
+        const int stage = static_cast<int>(i % C::STAGES);
+        const uint32_t round = static_cast<uint32_t>(i / C::STAGES);
+        if (!mbar_wait(&empty[stage], (round - 1) & 1, p.err)) break;
+        const long long u = lo + i;
+        const int tile = static_cast<int>(u / kb), kk = static_cast<int>(u % kb);
+        const int f = tile / p.tiles_m, m = tile % p.tiles_m;
+        uint8_t* st = smem + stage * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+        tma_load_2d(st, &tmA, &full[stage], kk * 64, f * 128, pol_a);
+        if (DUAL) tma_load_2d(st + C::A_BYTES, &tmA2, &full[stage], kk * 64, f * 128, pol_a);
+        tma_load_2d(st + C::NA * C::A_BYTES, &tmB, &full[stage], kk * 64, m * BN, pol_b);
+        issued = i + 1;
+      }
+      // drain: every copy this thread issued has landed before the CTA exits
+      for (long long i = issued - 1; i >= 0 && i >= issued - C::STAGES; --i) {
+        const int stage = static_cast<int>(i % C::STAGES);
+        mbar_wait(&full[stage], static_cast<uint32_t>(i / C::STAGES) & 1, p.err);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      long long i = 0;
+      int seg = 0;
+      bool ok = true;
+      for (long long u = lo; u < hi && ok;) {
+        const int tile = static_cast<int>(u / kb);
+        const int k_lo = static_cast<int>(u - static_cast<long long>(tile) * kb);
+        const int k_hi = static_cast<int>(std::min<long long>(kb, k_lo + (hi - u)));
+        const int acc = seg % C::NUM_ACC;
+        const uint32_t around = static_cast<uint32_t>(seg / C::NUM_ACC);
+        if (around > 0 && !mbar_wait(&acc_empty[acc], (around - 1) & 1, p.err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * C::ACC_COLS;
+        for (int kk = k_lo; kk < k_hi; ++kk, ++i) {
+          const int stage = static_cast<int>(i % C::STAGES);
+          if (!mbar_wait(&full[stage], static_cast<uint32_t>(i / C::STAGES) & 1, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t b_addr = a_addr + C::NA * C::A_BYTES;
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const uint64_t bdesc = sw128_kmajor_desc(b_addr + k4 * 32);
+            const uint32_t accum = (kk > k_lo || k4 > 0) ? 1u : 0u;
+            umma_bf16(d, sw128_kmajor_desc(a_addr + k4 * 32), bdesc, C::IDESC, accum);
+            if (DUAL)
+              umma_bf16(d + BN, sw128_kmajor_desc(a_addr + C::A_BYTES + k4 * 32), bdesc,
+                        C::IDESC, accum);
+          }
+          umma_commit(&empty[stage]);
+        }
+        if (!ok) break;
+        umma_commit(&acc_full[acc]);
+        u += k_hi - k_lo;
+        ++seg;
+      }
+      // drain: all MMAs of this thread are complete before TMEM is freed
+      umma_commit(drain);
+      mbar_wait(drain, 0, p.err);
+    }
+  } else {
+    grid_dep_wait();
+    int seg = 0;
+    const int row = warp * 32 + lane;
+    for (long long u = lo; u < hi;) {
+      const int tile = static_cast<int>(u / kb);
+      const int k_lo = static_cast<int>(u - static_cast<long long>(tile) * kb);
+      const int k_hi = static_cast<int>(std::min<long long>(kb, k_lo + (hi - u)));
+      const int acc = seg % C::NUM_ACC;
+      const uint32_t around = static_cast<uint32_t>(seg / C::NUM_ACC);
+      // one thread waits (bounded) and the outcome is shared, so the four
+      // epilogue warps always take the same path through the barriers below
+      if (threadIdx.x == 0) *epi_ok = mbar_wait(&acc_full[acc], around & 1, p.err) ? 1 : 0;
+      named_bar_sync(1, 128);
+      if (!*epi_ok) break;
+      tc_fence_after();
+      const int f = tile / p.tiles_m, m = tile % p.tiles_m;
+      const int o = f * 128 + row;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * C::ACC_COLS;
+      if (k_lo == 0 && k_hi == kb) {
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          float v[16], v2[16];
+          tmem_ld16(taddr + c0, v);
+          if (DUAL) tmem_ld16(taddr + BN + c0, v2);
+          tmem_ld_wait();
+          epi_chunk<DUAL>(p.epi, o, m * BN + c0, v, v2, lane);
+        }
+        tc_fence_before();
+        mbar_arrive(&acc_empty[acc]);
+      } else {
+        const int slot = (u == lo) ? 0 : 1;
+        float* wsp = p.ws + (static_cast<size_t>(cta) * 2 + slot) * (128 * C::ACC_COLS);
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          float v[16], v2[16];
+          tmem_ld16(taddr + c0, v);
+          if (DUAL) tmem_ld16(taddr + BN + c0, v2);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            wsp[(c0 + j) * 128 + row] = v[j];
+            if (DUAL) wsp[(BN + c0 + j) * 128 + row] = v2[j];
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&acc_empty[acc]);
+        __threadfence();
+        named_bar_sync(1, 128);
+        const int c_first = cta_of_unit(static_cast<long long>(tile) * kb, U, G);
+        const int c_last = cta_of_unit(static_cast<long long>(tile + 1) * kb - 1, U, G);
+        if (threadIdx.x == 0) {
+          const int old = atomicAdd(p.counters + tile, 1);
+          *flag = (old == c_last - c_first) ? 1 : 0;
+        }
+        named_bar_sync(1, 128);
+        if (*flag) {
+          __threadfence();
+          for (int c0 = 0; c0 < BN; c0 += 16) {
+            float v[16], v2[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = v2[j] = 0.f;
+            for (int c = c_first; c <= c_last; ++c) {
+              const int cs = unit_lo(c, U, G) >= static_cast<long long>(tile) * kb ? 0 : 1;
+              const float* src = p.ws + (static_cast<size_t>(c) * 2 + cs) * (128 * C::ACC_COLS);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                v[j] += __ldcg(src + (c0 + j) * 128 + row);
+                if (DUAL) v2[j] += __ldcg(src + (BN + c0 + j) * 128 + row);
+              }
+            }
+            epi_chunk<DUAL>(p.epi, o, m * BN + c0, v, v2, lane);
+          }
+          if (threadIdx.x == 0) p.counters[tile] = 0;
+        }
+      }
+      u += k_hi - k_lo;
+      ++seg;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+  if (p.epi.kind == EPI_ARGMAX) {
+    // the last CTA turns the packed (value, index) keys into token ids
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const int old = atomicAdd(p.done, 1);
+      *flag = (old == G - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (*flag) {
+      __threadfence();
+      for (int t = threadIdx.x; t < p.epi.M; t += blockDim.x) {
+        const unsigned long long k = atomicExch(p.epi.keys + t, 0ull);
+        p.epi.tokens[t] = k ? argmax_key_index(k) : -1;
+      }
+      if (threadIdx.x == 0) *p.done = 0;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+bool tensor_map_2d_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
+                        uint64_t ld_elems, uint32_t box_cols, uint32_t box_rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) != 0 || (ld_elems * 2) % 16 != 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld_elems * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, bool DUAL>
+static cudaError_t run_tc(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
+                          const TcParams& p, int grid, cudaStream_t s) {
+  using C = TcCfg<BN, DUAL>;
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, DUAL>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(gemm_tc_kernel<BN, DUAL>, dim3(grid), dim3(192), C::SMEM, s, a, a2, b, p);
+}
+
+int tc_pick_bn(int M) {
+  if (M <= 16) return 16;
+  if (M <= 32) return 32;
+  if (M <= 64) return 64;
+  if (M <= 128) return 128;
+  return 256;
+}
+
+size_t tc_partial_floats(int grid, int bn, bool dual) {
+  return static_cast<size_t>(grid) * 2 * 128 * bn * (dual ? 2 : 1);
+}
+
+cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
+                                const CUtensorMap& xb, bool dual, int M, int N, int K,
+                                const EpiArgs& epi, const TcGemmWorkspace& ws, int* err,
+                                cudaStream_t s) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  const int bn = tc_pick_bn(M);
+  TcParams p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.kb = (K + 63) / 64;
+  p.tiles_m = (M + bn - 1) / bn;
+  const int tiles_n = (N + 127) / 128;
+  p.units = static_cast<long long>(tiles_n) * p.tiles_m * p.kb;
+  p.epi = epi;
+  p.ws = ws.partials;
+  p.counters = ws.tile_counters;
+  p.done = ws.done_counter;
+  p.err = err;
+  const int grid = static_cast<int>(std::min<long long>(ws.sm_count, p.units));
+  if (tiles_n * p.tiles_m > ws.max_tiles || tc_partial_floats(grid, bn, dual) > ws.partial_floats)
+    return cudaErrorInvalidValue;
+#define PE_TC_CASE(BNV)                                                  \
+  case BNV:                                                              \
+    return dual ? run_tc<BNV, true>(wa, wa2, xb, p, grid, s)             \
+                : run_tc<BNV, false>(wa, wa2, xb, p, grid, s);
+  switch (bn) {
+    PE_TC_CASE(16)
+    PE_TC_CASE(32)
+    PE_TC_CASE(64)
+    PE_TC_CASE(128)
+    PE_TC_CASE(256)
+  }
+#undef PE_TC_CASE
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_tc(const void* x, int ldx, const void* w, const void* w2, int M, int N,
+                           int K, const EpiArgs& epi, const TcGemmWorkspace& ws, int* err,
+                           cudaStream_t s) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  CUtensorMap wa, wa2, xb;
+  if (!tensor_map_2d_bf16(&wa, w, N, K, K, 64, 128)) return cudaErrorInvalidValue;
+  wa2 = wa;
+  if (w2 && !tensor_map_2d_bf16(&wa2, w2, N, K, K, 64, 128)) return cudaErrorInvalidValue;
+  if (!tensor_map_2d_bf16(&xb, x, M, K, ldx, 64, tc_pick_bn(M))) return cudaErrorInvalidValue;
+  return launch_gemm_tc_maps(wa, wa2, xb, w2 != nullptr, M, N, K, epi, ws, err, s);
+}
+
+}  // namespace pe

@@ -1,0 +1,153 @@
+// pe_kernels.h -- launchers of the sm_103a kernels (host side, internal).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pe {
+
+// Launch with programmatic stream serialization so a kernel's prologue
+// (barrier setup, TMEM allocation, weight prefetch) overlaps the tail of the
+// kernel before it.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// ---------------------------------------------------------------- expansion
+struct ExpandArgs {
+  int B, K, T, T_out;
+  const int32_t* target_ids;
+  const int32_t* target_pos;
+  const int32_t* cu_in;
+  const int32_t* num_accepted;
+  const int32_t* sampled_ids;
+  const int32_t* block_table;
+  int bt_stride, num_blocks, page_size, mask_token_id;
+  const void* target_hidden;
+  const void* h_shared;
+  int row_bytes;  // hidden3 * element size (multiple of 16)
+  int32_t* ids;
+  int32_t* pos;
+  int32_t* slot;
+  uint8_t* is_rejected;
+  uint8_t* is_masked;
+  int32_t* new_idx;
+  int32_t* hidden_map;
+  int32_t* cu_out;
+  int32_t* seq_lens;
+  void* hidden;
+  int* err;
+};
+cudaError_t launch_expand(const ExpandArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------- row ops
+// dtype tag: 0 = bf16, 1 = f32 (activations, weights, caches share it)
+struct EmbedConcatArgs {
+  int rows, d, vocab;
+  const int32_t* ids;
+  const void* emb;      // [V, d]
+  const float* h;       // [rows, d] fp32 fc output (the residual)
+  const void* g_e;      // [d]
+  const void* g_h;      // [d]
+  float eps;
+  void* x;              // [rows, 2d] activations
+  int* err;
+};
+cudaError_t launch_embed_concat(int dtype, const EmbedConcatArgs& a, cudaStream_t s);
+
+struct RmsNormArgs {
+  int rows, d;
+  const float* x;       // [*, d] fp32 residual
+  const int32_t* row_index;  // optional gather: out row i reads x[row_index[i]]
+  int rows_in;          // bound for row_index values
+  const void* g;        // [d]
+  float eps;
+  void* y;              // [rows, d] activations
+  int* err;
+};
+cudaError_t launch_rmsnorm(int dtype, const RmsNormArgs& a, cudaStream_t s);
+
+struct RopeKvArgs {
+  int rows, Hq, Hkv, dh, num_blocks;
+  const void* qkv;          // [rows, (Hq + 2 Hkv) dh]
+  const int32_t* pos;       // [rows]
+  const int32_t* slot;      // [rows], -1 = no KV write
+  const float* inv_freq;    // [dh / 2] (fp32 copy of fp64 table, unused)
+  const double* inv_freq64; // [dh / 2]
+  void* q_out;              // [rows, Hq dh]
+  void* k_cache;            // [num_blocks, Hkv, 16, dh]
+  void* v_cache;
+  int* err;
+};
+cudaError_t launch_rope_kv(int dtype, const RopeKvArgs& a, cudaStream_t s);
+
+struct AttnArgs {
+  int rows, B, Hq, Hkv, dh, bt_stride, num_blocks, max_seq;
+  const void* q;             // [rows, Hq dh] (roped)
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* pos;        // [rows]
+  const uint8_t* is_rejected;
+  const int32_t* cu_out;     // [B+1]
+  const int32_t* block_table;
+  void* out;                 // [rows, Hq dh]
+  float scale;
+  int* err;
+};
+cudaError_t launch_attention_simt(int dtype, const AttnArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------- GEMM
+enum EpiKind { EPI_STORE = 0, EPI_ADD = 1, EPI_SILU_MUL = 2, EPI_ARGMAX = 3 };
+
+struct EpiArgs {
+  int kind;
+  int M, N;                 // valid tokens, valid output features
+  void* out;                // STORE / SILU_MUL destination [M, ldo]
+  int ldo;
+  int out_f32;              // 1: fp32 output, 0: bf16 (or model dtype)
+  float* resid;             // ADD: resid[M, ldr] += acc
+  int ldr;
+  float* logits;            // ARGMAX: optional fp32 [M, ldl]
+  int ldl;
+  unsigned long long* keys; // ARGMAX: [M] packed (value, index), zero on entry
+  int32_t* tokens;          // ARGMAX: [M] result
+};
+
+// y = x . w^T (+ epilogue) with tcgen05 tensor cores (bf16 in, fp32 accumulate).
+// x [M, K] row stride ldx, w [N, K] (w2 the second matrix for SILU_MUL).
+struct TcGemmWorkspace {
+  float* partials;          // split-K partial tiles
+  size_t partial_floats;
+  int* tile_counters;       // zero on entry, left zero on exit
+  int max_tiles;
+  int* done_counter;        // zero on entry, left zero on exit
+  int sm_count;
+};
+cudaError_t launch_gemm_tc(const void* x, int ldx, const void* w, const void* w2, int M, int N,
+                           int K, const EpiArgs& epi, const TcGemmWorkspace& ws, int* err,
+                           cudaStream_t s);
+
+// The same contraction with FFMA for the fp32 path.
+cudaError_t launch_gemm_simt(const float* x, int ldx, const float* w, const float* w2, int M,
+                             int N, int K, const EpiArgs& epi, int* err, cudaStream_t s);
+cudaError_t launch_argmax_finalize(int M, unsigned long long* keys, int32_t* tokens,
+                                   cudaStream_t s);
+
+// tensor-map encoder (fetched once through cudart)
+bool tensor_map_2d_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
+                        uint64_t ld_elems, uint32_t box_cols, uint32_t box_rows);
+
+}  // namespace pe

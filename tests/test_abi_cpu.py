@@ -1,0 +1,99 @@
+"""The C ABI without a GPU: the library builds, loads, exports every function
+include/peagle.h declares, its structs match the binding's layout, and host
+validation rejects bad arguments before touching the device."""
+
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "peagle.h")
+
+
+@pytest.fixture(scope="module")
+def B():
+    from speculative_drafting_expand_gb300 import binding, build
+    if not os.path.exists(binding.LIB_PATH):
+        build.build()
+    binding.lib()
+    return binding
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^(?:pe_status|const char\*)\s+(pe_\w+)\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    fns = declared_functions()
+    for name in ("pe_create", "pe_destroy", "pe_expand_batch", "pe_draft_forward",
+                 "pe_lmhead_argmax", "pe_get_device_error", "pe_status_string"):
+        assert name in fns
+
+
+def test_library_exports_every_declared_symbol(B):
+    lib = B.lib()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) == set(B.EXPORTED)
+
+
+def test_struct_layouts_match_the_header(B):
+    src = r"""
+    #include <stdio.h>
+    #include <stddef.h>
+    #include "peagle.h"
+    int main(void) {
+      printf("%zu %zu %zu %zu %zu %zu\n", sizeof(pe_model_desc), sizeof(pe_layer_weights),
+             sizeof(pe_weights), sizeof(pe_expanded), offsetof(pe_expanded, T_out),
+             offsetof(pe_model_desc, dtype));
+      return 0;
+    }
+    """
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "l.c")
+        exe = os.path.join(d, "l")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
+        got = [int(v) for v in subprocess.run([exe], capture_output=True, text=True,
+                                              check=True).stdout.split()]
+    want = [ctypes.sizeof(B.pe_model_desc), ctypes.sizeof(B.pe_layer_weights),
+            ctypes.sizeof(B.pe_weights), ctypes.sizeof(B.pe_expanded),
+            B.pe_expanded.T_out.offset, B.pe_model_desc.dtype.offset]
+    assert got == want
+
+
+def test_status_strings(B):
+    assert B.status_string(0) == "ok"
+    assert B.status_string(1) == "invalid argument"
+    assert B.status_string(2) == "unsupported shape"
+    assert B.status_string(99) == "unknown status"
+
+
+def test_host_validation_rejects_bad_arguments_without_a_device(B):
+    lib = B.lib()
+    h = ctypes.c_void_p()
+    w = B.pe_weights()
+    desc = B.pe_model_desc(64, 1, 2, 1, 64, 64, 100, 192, 16, 99, 1e4, 1e-5, 0)
+    # null weights
+    assert lib.pe_create(ctypes.byref(desc), ctypes.byref(w), 16, 1, ctypes.byref(h)) == 1
+    # bad page size / head dim are unsupported shapes
+    desc.page_size = 32
+    assert lib.pe_create(ctypes.byref(desc), ctypes.byref(w), 16, 1, ctypes.byref(h)) == 2
+    desc.page_size, desc.head_dim = 16, 96
+    assert lib.pe_create(ctypes.byref(desc), ctypes.byref(w), 16, 1, ctypes.byref(h)) == 2
+    # heads not divisible by kv heads
+    desc.head_dim, desc.n_heads, desc.n_kv_heads = 64, 3, 2
+    assert lib.pe_create(ctypes.byref(desc), ctypes.byref(w), 16, 1, ctypes.byref(h)) == 1
+    # null handles
+    ex = B.pe_expanded()
+    assert lib.pe_expand_batch(None, 1, 1, 1, None, None, None, None, None, None, 1, 1, None,
+                               ctypes.byref(ex), None) == 1
+    assert lib.pe_draft_forward(None, ctypes.byref(ex), 1, 1, None, 1, None, None, 1, None,
+                                None) == 1
+    assert lib.pe_lmhead_argmax(None, None, 1, None, None, None) == 1
+    assert lib.pe_destroy(None) == 1

@@ -1,0 +1,68 @@
+"""GPU check of the tensor-core projection kernel through pe_linear.
+
+y = x w^T with bf16 operands and fp32 accumulation (tcgen05, TMEM) against
+an fp64 product of the same bf16 values.  The shapes cover one tile, many
+tiles, ragged token/feature/k tails, every token-tile width (16..256) and
+stream-K splits of a tile across CTAs (the deterministic fix-up path).
+"""
+
+import numpy as np
+import pytest
+
+import oracle as O
+from synthetic import workloads as W
+from tests import gpu_helpers as G
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    (1, 128, 64),       # one unit
+    (14, 5120, 2880),   # GPT-OSS QKV at batch 1 (split across CTAs)
+    (16, 300, 200),     # ragged features and k (k % 64 != 0)
+    (7, 2880, 8640),    # fc-shaped, long k
+    (40, 1000, 512),    # token tile 64
+    (100, 640, 1024),   # token tile 128
+    (300, 384, 256),    # token tile 256, two token tiles, ragged
+    (896, 2880, 2880),  # batch-64 shape
+]
+
+
+def _handle(max_tokens):
+    shape = W.small_shape("lin", d=64, n_layers=1, n_heads=1, n_kv_heads=1, head_dim=64,
+                          ffn=64, vocab=8192)
+    z = np.zeros(64, np.uint16)
+    w = {k: z for k in ("emb", "fc", "norm_final", "lm_head", "h_shared")}
+    w["h_shared"] = np.zeros(shape.hidden3, np.uint16)
+    w["layers"] = [dict(qkv=z, o=z, gate=z, up=z, down=z, norm_e=z, norm_h=z, norm_post=z)]
+    return G.make_drafter(shape, w, max_tokens, 1)
+
+
+@pytest.mark.parametrize("M,N,K", CASES)
+def test_linear_matches_fp64(M, N, K):
+    B = G.library()
+    torch = G.torch_mod()
+    dr = _handle(max(M, 16))
+    x = W.normal(7, "x", (M, K), 1.0, "bf16", M, N)
+    w = W.normal(7, "w", (N, K), 0.05, "bf16", M, N)
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    B.pe_linear(dr, B.to_device(x, "bf16"), B.to_device(w, "bf16"), y)
+    torch.cuda.synchronize()
+    got = y.cpu().numpy().astype(np.float64)
+    want = O.to_f64(x, "bf16") @ O.to_f64(w, "bf16").T
+    err = np.abs(got - want).max()
+    assert np.isfinite(got).all()
+    assert err <= 2e-5 * np.sqrt(K) * max(1.0, np.abs(want).max()), err
+
+
+def test_linear_is_deterministic():
+    B = G.library()
+    torch = G.torch_mod()
+    dr = _handle(16)
+    x = B.to_device(W.normal(8, "x", (14, 2880), 1.0, "bf16"), "bf16")
+    w = B.to_device(W.normal(8, "w", (5120, 2880), 0.05, "bf16"), "bf16")
+    y1 = torch.empty(14, 5120, device="cuda")
+    y2 = torch.empty(14, 5120, device="cuda")
+    B.pe_linear(dr, x, w, y1)
+    B.pe_linear(dr, x, w, y2)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)

@@ -1,0 +1,67 @@
+"""GPU parity of the whole drafting step (pe_expand_batch -> pe_draft_forward
+-> pe_lmhead_argmax) against the CPU oracle.
+
+Bar: metadata bit-exact; final hidden states and logits within
+max-abs <= tol x max|value| (1e-4 for the fp32 path, 2e-2 for bf16); draft
+tokens identical wherever the oracle's top-2 logit margin exceeds 1e-2;
+KV writes at exactly the non-rejected slots, every other slot untouched.
+"""
+
+import numpy as np
+import pytest
+
+from synthetic import workloads as W
+from tests import gpu_helpers as G
+
+pytestmark = pytest.mark.gpu
+
+TOL_F32 = 1e-4
+TOL_BF16 = 2e-2
+
+
+def test_tiny_fp32_config():
+    """Tiny fp32 drafter: d=256, 2 layers, 4x64 heads, ctx 64, K=4."""
+    G.full_parity(W.tiny_fp32(), TOL_F32)
+
+
+def test_tiny_fp32_with_rejections_and_random_gains():
+    wl = W.custom("tiny-rej", 61, W.TINY, 5, [40, 17, 90], [6, 6, 3], [2, 5, 0],
+                  gains="random")
+    G.full_parity(wl, TOL_F32)
+
+
+SMALL = W.small_shape("small-bf16", d=512, n_layers=2, n_heads=8, n_kv_heads=2,
+                      head_dim=64, ffn=1024, vocab=4096)
+
+
+@pytest.mark.parametrize("B,K", [(1, 7), (4, 5), (16, 8)])
+def test_small_bf16_batches(B, K):
+    rng = np.random.default_rng(B * 10 + K)
+    ctx = rng.integers(1, 600, size=B)
+    win = np.full(B, K + 1)
+    acc = rng.integers(0, K + 1, size=B)
+    wl = W.custom(f"small-b{B}", 70 + B, SMALL, K, ctx, win, acc, gains="random")
+    G.full_parity(wl, TOL_BF16)
+
+
+def test_small_bf16_head_dim_128():
+    sh = W.small_shape("small-dh128", d=512, n_layers=2, n_heads=4, n_kv_heads=2,
+                       head_dim=128, ffn=768, vocab=2048)
+    wl = W.custom("dh128", 80, sh, 4, [33, 250], [5, 5], [4, 1], gains="random")
+    G.full_parity(wl, TOL_BF16)
+
+
+def test_k1_is_one_autoregressive_step_on_gpu():
+    import oracle as O
+    wl = W.custom("k1", 81, SMALL, 1, [100, 7, 300], [2, 3, 1], [1, 2, 0], gains="random")
+    res, ref, dr, st = G.full_parity(wl, TOL_BF16)
+    kc, vc = W.make_kv_cache(wl, st.inp)   # the pools as they were before the step
+    logits, tokens = O.ar_eagle_step(SMALL, W.make_weights(SMALL, 81, gains="random"),
+                                     st.inp, kc, vc)
+    B = G.library()
+    G.margin_ok_tokens(logits, tokens, B.to_host(res["tokens"]))
+
+
+def test_gpt_oss_b1_full_size():
+    """GPT-OSS-20B-shaped drafter, bf16, one request, K=7, context 4096."""
+    G.full_parity(W.gpt_oss_b1(), TOL_BF16)
