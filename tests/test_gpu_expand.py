@@ -21,7 +21,7 @@ def _expand_drafter(shape, max_tokens, max_reqs):
     z = np.zeros(64, np.uint16 if dt == "bf16" else np.float32)
     w = {k: z for k in ("emb", "fc", "norm_final", "lm_head")}
     w["h_shared"] = W.normal(77, "h_shared", (shape.hidden3,), 0.02, dt)
-    w["layers"] = [dict(qkv=z, o=z, gate=z, up=z, down=z, norm_e=z, norm_h=z, norm_post=z)
+    w["layers"] = [dict(qkv=z, o=z, gate=z, up=z, down=z, norm_e=z, norm_h=z, norm_in=z, norm_post=z)
                    for _ in range(shape.n_layers)]
     return G.make_drafter(shape, w, max_tokens, max_reqs), w["h_shared"]
 

@@ -33,7 +33,7 @@ def _handle(max_tokens):
     z = np.zeros(64, np.uint16)
     w = {k: z for k in ("emb", "fc", "norm_final", "lm_head", "h_shared")}
     w["h_shared"] = np.zeros(shape.hidden3, np.uint16)
-    w["layers"] = [dict(qkv=z, o=z, gate=z, up=z, down=z, norm_e=z, norm_h=z, norm_post=z)]
+    w["layers"] = [dict(qkv=z, o=z, gate=z, up=z, down=z, norm_e=z, norm_h=z, norm_in=z, norm_post=z)]
     return G.make_drafter(shape, w, max_tokens, 1)
 
 
