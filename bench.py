@@ -1,0 +1,459 @@
+"""Benchmark of the P-EAGLE parallel drafting step on GB300.
+
+One step = pe_expand_batch + pe_draft_forward + pe_lmhead_argmax over one
+batch of seeded synthetic input (all K draft tokens of every request from one
+drafter pass).  Default workload: the GPT-OSS-20B-shaped drafter (bf16,
+d=2880, 4 layers, 64x64 q heads, 8 kv heads, FFN 7680, vocab 201088), one
+request, K=7, context 4096 in a paged KV cache.
+
+`value` is device-timed throughput (draft steps/s, whole job) of the step
+replayed as a CUDA graph with inputs resident in HBM; `e2e` is the same
+metric through the public calls with pinned host inputs copied in and draft
+tokens copied out inside the timed region.  Each rank of a multi-GPU run
+drafts its own batch (requests are independent: weak scaling, no
+collective on the data path).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload b1|b64|qwen-k<K>|expand]
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synthetic import workloads as W  # noqa: E402
+
+L2_BYTES = 129 * 2 ** 20
+METRIC = "P-EAGLE draft steps/s & drafted tok/s at K=7, 1 GB300; % of HBM/tensor roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def workload(name: str):
+    if name == "b1":
+        return W.gpt_oss_b1()
+    if name == "b64":
+        return W.gpt_oss_b64()
+    if name.startswith("qwen-k"):
+        return W.qwen_b16(int(name[len("qwen-k"):]))
+    if name == "expand":
+        return W.expand_b256()
+    raise SystemExit(f"unknown workload {name}")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work of one step (bytes that must move, flops that must run)
+# ---------------------------------------------------------------------------
+
+def step_work(wl, inp):
+    sh = wl.shape
+    es = 2 if sh.dtype == "bf16" else 4
+    d, F, V = sh.d, sh.ffn, sh.vocab
+    qd = sh.n_heads * sh.head_dim
+    layer_params = [sh.qkv_rows * (2 * d if l == 0 else d) + d * qd + 3 * F * d
+                    for l in range(sh.n_layers)]
+    params = d * sh.hidden3 + sum(layer_params) + V * d
+    rows = wl.T_out
+    valid = int(sum(int(a) + wl.K for a in wl.accepted))
+    seq = [int(inp.target_pos[int(inp.cu_in[r]) + int(wl.accepted[r])]) + wl.K + 1
+           for r in range(wl.B)]
+    kv_bytes = sh.n_layers * 2 * sum(seq) * sh.n_kv_heads * sh.head_dim * es
+    weight_bytes = params * es
+    act_bytes = rows * sh.hidden3 * es + wl.B * wl.K * 4
+    gemm_flops = 2.0 * valid * (params - V * d) + 2.0 * wl.B * wl.K * V * d
+    attn_flops = 0.0
+    for r in range(wl.B):
+        a = int(wl.accepted[r])
+        C = seq[r] - (a + wl.K)
+        for j in range(a + wl.K):
+            attn_flops += 4.0 * sh.n_heads * sh.head_dim * (C + j + 1) * sh.n_layers
+    lm_bytes = V * d * es + wl.B * wl.K * d * es + wl.B * wl.K * 4
+    return dict(weight_bytes=weight_bytes, kv_bytes=kv_bytes, act_bytes=act_bytes,
+                bytes=weight_bytes + kv_bytes + act_bytes, gemm_flops=gemm_flops,
+                attn_flops=attn_flops, lm_head_bytes=lm_bytes,
+                lm_head_flops=2.0 * wl.B * wl.K * V * d, valid_rows=valid, rows=rows)
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled while the timed region runs
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; barrier + max over ranks)
+# ---------------------------------------------------------------------------
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("num_threads")]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def time_oracle(wl, inp, w, kc, vc, budget_s: float, max_steps: int):
+    import oracle as O
+    n, t0 = 0, time.perf_counter()
+    while n < max_steps:
+        O.draft_step(wl.shape, w, wl.K, inp, kc, vc)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return n / dt, n, dt
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    wl = workload(args.workload)
+    inp = W.make_step_inputs(wl)
+    w = W.make_weights(wl.shape, wl.config_id, gains=wl.gains)
+    kc, vc = W.make_kv_cache(wl, inp)
+    budget = float(os.environ.get("PE_REF_BUDGET_S", "120"))
+    import oracle as O
+    for _ in range(min(args.warmup, 1)):
+        O.draft_step(wl.shape, w, wl.K, inp, kc, vc)
+    sps, n, dt = time_oracle(wl, inp, w, kc, vc, budget, args.steps)
+    cores = oracle_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": sps, "unit": "steps/s",
+        "n_gpus": world, "steps": n, "warmup": args.warmup, "ms_per_step": 1e3 * dt / n,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "drafted_tok_per_s": sps * wl.B * wl.K,
+        "config": config_of(wl, args),
+        "cpu_baseline": {"value": sps, "unit": "steps/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} full oracle steps of the workload "
+                                   f"(of {args.steps} requested; time budget {budget:.0f} s)"},
+        "e2e": {"value": sps, "unit": "steps/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(wl, args):
+    sh = wl.shape
+    return {"workload": wl.name, "drafter": sh.name, "B": wl.B, "K": wl.K,
+            "window": int(wl.window[0]), "contexts_mean": float(np.mean(wl.contexts)),
+            "d": sh.d, "layers": sh.n_layers, "heads": f"{sh.n_heads}x{sh.head_dim}",
+            "kv_heads": sh.n_kv_heads, "ffn": sh.ffn, "vocab": sh.vocab,
+            "page_size": sh.page_size, "parallelism": f"replicas x{args.gpus}",
+            "l2": "weights stream from HBM every step (working set > 129 MB L2)",
+            "graph": "step replayed as one CUDA graph"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+class DeviceInputs:
+    """One step's inputs and the paged KV pools, resident in HBM."""
+
+    def __init__(self, wl, inp, kc, vc, B, torch):
+        dt = wl.shape.dtype
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).cuda()
+        self.target_ids = i32(inp.target_ids)
+        self.target_pos = i32(inp.target_pos)
+        self.cu_in = i32(inp.cu_in)
+        self.num_accepted = i32(inp.num_accepted)
+        self.sampled_ids = i32(inp.sampled_ids)
+        self.block_table = i32(inp.block_table)
+        self.target_hidden = B.to_device(inp.target_hidden, dt)
+        self.kc = [B.to_device(k, dt) for k in kc]
+        self.vc = [B.to_device(v, dt) for v in vc]
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    from speculative_drafting_expand_gb300 import binding as B
+
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    wl = workload(args.workload)
+    sh = wl.shape
+    inp = W.make_step_inputs(wl)
+    w = W.make_weights(sh, wl.config_id, gains=wl.gains)
+    kc, vc = W.make_kv_cache(wl, inp)
+    dr = B.Drafter(sh, w, max(wl.T_out, wl.B * wl.K), wl.B)
+    st = DeviceInputs(wl, inp, kc, vc, B, torch)
+    ex = B.Expanded(wl.T_out, wl.T, wl.B, wl.K, sh.hidden3, sh.dtype)
+    tdt = torch.bfloat16 if sh.dtype == "bf16" else torch.float32
+    out_hidden = torch.empty(wl.B * wl.K, sh.d, dtype=tdt, device="cuda")
+    tokens = torch.empty(wl.B * wl.K, dtype=torch.int32, device="cuda")
+
+    def step():
+        B.pe_expand_batch(dr, wl.K, st.target_ids, st.target_pos, st.cu_in, st.num_accepted,
+                          st.sampled_ids, st.block_table, inp.num_blocks, st.target_hidden, ex)
+        B.pe_draft_forward(dr, ex, st.block_table, st.kc, st.vc, inp.num_blocks, out_hidden)
+        B.pe_lmhead_argmax(dr, out_hidden, tokens)
+
+    # eager warm-up, then capture the step as one CUDA graph
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    assert B.pe_get_device_error(dr) == 0
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    n0 = B.pe_get_launch_count(dr)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            step()
+    launches_per_step = B.pe_get_launch_count(dr) - n0
+    torch.cuda.synchronize()
+    for _ in range(max(3, args.warmup)):
+        g.replay()
+    torch.cuda.synchronize()
+
+    # ---- device-timed region: K graph replays ------------------------------
+    clocks = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    clocks.start()
+    t_pre = time.time()
+    while time.time() - t_pre < 0.4:          # load the GPU while the sampler starts
+        g.replay()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    elapsed_ms = max_over_ranks(world, e0.elapsed_time(e1))
+    clocks.stop()
+    ms_per_step = elapsed_ms / args.steps
+    value = world * args.steps / (elapsed_ms / 1e3)
+    assert B.pe_get_device_error(dr) == 0
+
+    # ---- dominant kernel: the LM-head GEMM + argmax, timed on its stream ----
+    work = step_work(wl, inp)
+    stream = torch.cuda.current_stream()
+    n_lm = max(20, min(args.steps, 200))
+    lm_ms = []
+    for _ in range(n_lm):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        B.pe_lmhead_argmax(dr, out_hidden, tokens)
+        b.record(stream)
+        lm_ms.append((a, b))
+    torch.cuda.synchronize()
+    lm_avg_s = statistics.mean(a.elapsed_time(b) for a, b in lm_ms) / 1e3
+    pk, pk_kind = peaks()
+    hbm = float(pk["hbm_gbs"])
+    achieved = work["lm_head_bytes"] / lm_avg_s / 1e9
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "lm_head_traffic.json")
+    if os.path.exists(prof):
+        t = json.load(open(prof))
+        if t.get("workload") == wl.name:
+            traffic = t.get("traffic_bytes_per_launch")
+
+    # ---- end to end through the public calls with host buffers -------------
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    h_ids, h_pos, h_cu = pin(inp.target_ids), pin(inp.target_pos), pin(inp.cu_in)
+    h_acc, h_samp, h_bt = pin(inp.num_accepted), pin(inp.sampled_ids), pin(inp.block_table)
+    h_hid = B.to_device(inp.target_hidden, sh.dtype, device="cpu").pin_memory()
+    h_tok = torch.empty(wl.B * wl.K, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_ids, h_pos, h_cu, h_acc, h_samp, h_bt, h_hid))
+    d2h = h_tok.numel() * h_tok.element_size()
+
+    def e2e_step():
+        st.target_ids.copy_(h_ids, non_blocking=True)
+        st.target_pos.copy_(h_pos, non_blocking=True)
+        st.cu_in.copy_(h_cu, non_blocking=True)
+        st.num_accepted.copy_(h_acc, non_blocking=True)
+        st.sampled_ids.copy_(h_samp, non_blocking=True)
+        st.block_table.copy_(h_bt, non_blocking=True)
+        st.target_hidden.copy_(h_hid, non_blocking=True)
+        step()
+        h_tok.copy_(tokens, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    n_e2e = max(10, min(args.steps, 500))
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(world, time.perf_counter() - t0)
+    e2e_value = world * n_e2e / e2e_s
+    assert B.pe_get_device_error(dr) == 0
+
+    # ---- CPU oracle baseline (rank 0, one GPU only) -------------------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        budget = float(os.environ.get("PE_CPU_BUDGET_S", "15"))
+        sps, n, dt = time_oracle(wl, inp, w, kc, vc, budget, 1000)
+        cpu = {"value": sps, "unit": "steps/s", "cores": oracle_threads(), "kind": "oracle",
+               "sample": f"{n} full oracle steps of the same workload in {dt:.1f} s"}
+
+    if rank == 0:
+        bound = "hbm"
+        step_floor_s = work["bytes"] / (hbm * 1e9)
+        line = {
+            "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": sh.dtype, "data": "synthetic (seeded random-init weights and inputs)",
+            "config": config_of(wl, args),
+            "drafted_tok_per_s": value * wl.B * wl.K,
+            "roofline": {"bound": bound, "kernel": "gemm_tc_kernel (LM head + argmax)",
+                         "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": traffic,
+                         "peak_source": f"{pk_kind} hbm_gbs",
+                         "bytes_per_launch": work["lm_head_bytes"],
+                         "launch_us": lm_avg_s * 1e6},
+            "step_roofline": {"bytes": work["bytes"], "floor_us": step_floor_s * 1e6,
+                              "frac": step_floor_s / (ms_per_step / 1e3),
+                              "gemm_flops": work["gemm_flops"],
+                              "attn_flops": work["attn_flops"]},
+            "e2e": {"value": e2e_value, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "launches_per_step": launches_per_step,
+            "clocks": clocks.summary(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    dr.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="b1")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -194,8 +194,14 @@ pe_status pe_expand_batch(pe_handle* h, int32_t B, int32_t K, int32_t T,
  * SwiGLU MLP + residual.  Finally the rows new_idx are gathered and
  * RMSNorm'ed with norm_final into out_hidden [B*K, d] (model dtype).
  * k_cache/v_cache: HOST arrays of n_layers device pointers, each a pool
- * [num_blocks, Hkv, 16, dh] (model dtype); block_table as in
- * pe_expand_batch.  B and K must match the values recorded in *ex. */
+ * [num_blocks, Hkv, 16, dh] (model dtype, 16-byte aligned); block_table as
+ * in pe_expand_batch.  B and K must match the values recorded in *ex.
+ * Each request's verify window is expected to hold at most K + 1 rows (the
+ * previous step's drafts plus one); a request with more rows than that is
+ * reported as PE_DEV_BAD_ROW.  The bf16 path keeps a split-KV workspace
+ * sized by B and bt_stride: the first call with a larger batch or block
+ * table grows it with cudaMalloc, so make that call before capturing the
+ * step into a CUDA graph. */
 pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B,
                            int32_t K, const int32_t* block_table,
                            int32_t bt_stride, void* const* k_cache,
@@ -226,6 +232,11 @@ pe_status pe_set_trace(pe_handle* h, float* residual_trace);
  * for bf16. */
 pe_status pe_linear(pe_handle* h, const void* x, const void* w, float* y,
                     int32_t M, int32_t N, int32_t K, void* stream);
+
+/* Number of kernels this handle has launched since pe_create (host-side
+ * count, incremented per launch, including launches captured into a CUDA
+ * graph).  A diagnostic for counting the kernels of one step. */
+pe_status pe_get_launch_count(pe_handle* h, int64_t* count);
 
 /* Static description of a status code. */
 const char* pe_status_string(pe_status s);

@@ -28,7 +28,7 @@ PE_DTYPE_F32 = 1
 
 EXPORTED = ("pe_create", "pe_destroy", "pe_expand_batch", "pe_draft_forward",
             "pe_lmhead_argmax", "pe_get_device_error", "pe_set_trace", "pe_linear",
-            "pe_status_string")
+            "pe_get_launch_count", "pe_status_string")
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -79,6 +79,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pe_get_device_error.argtypes = [_vp, P(_i32), _vp]
     lib.pe_set_trace.argtypes = [_vp, _vp]
     lib.pe_linear.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp]
+    lib.pe_get_launch_count.argtypes = [_vp, P(ctypes.c_int64)]
     lib.pe_status_string.argtypes = [_i32]
     lib.pe_status_string.restype = ctypes.c_char_p
     for name in EXPORTED[:-1]:
@@ -256,6 +257,12 @@ def pe_get_device_error(dr: Drafter, stream=None) -> int:
 
 def pe_set_trace(dr: Drafter, trace) -> None:
     _check("pe_set_trace", lib().pe_set_trace(dr.handle, ptr(trace)))
+
+
+def pe_get_launch_count(dr: Drafter) -> int:
+    n = ctypes.c_int64(0)
+    _check("pe_get_launch_count", lib().pe_get_launch_count(dr.handle, ctypes.byref(n)))
+    return n.value
 
 
 def pe_linear(dr: Drafter, x, w, y, stream=None):

@@ -16,10 +16,15 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
                                 const EpiArgs& epi, const TcGemmWorkspace& ws, int* err,
                                 cudaStream_t s);
 int tc_pick_bn(int M);
+cudaError_t init_gemm_tc();
 size_t tc_partial_floats(int grid, int bn, bool dual);
-cudaError_t launch_attention_tc(const AttnArgs& a, float* partials, int* counters,
-                                cudaStream_t s);
-size_t attention_tc_partial_floats(const AttnArgs& a);
+cudaError_t init_attention_tc();
+size_t attention_tc_partial_floats(const AttnArgs& a, int max_rows_per_req, int sm_count);
+size_t attention_tc_counters(const AttnArgs& a, int max_rows_per_req, int sm_count);
+cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                const int32_t* seq_lens, int max_rows_per_req, int sm_count,
+                                float* part, size_t part_floats, int* counters,
+                                size_t n_counters, cudaStream_t s);
 }  // namespace pe
 
 using namespace pe;
@@ -51,7 +56,9 @@ struct pe_handle {
   float* attn_partials = nullptr;
   size_t attn_partial_floats = 0;
   int* attn_counters = nullptr;
+  size_t attn_n_counters = 0;
   float* trace = nullptr;
+  long long launches = 0;
 
   std::map<std::tuple<const void*, uint64_t, uint64_t, uint64_t, uint32_t>, CUtensorMap> maps;
   std::vector<void*> allocations;
@@ -60,6 +67,12 @@ struct pe_handle {
 namespace {
 
 pe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PE_OK : PE_ERR_CUDA; }
+
+// Count one kernel launch of the handle when it was issued successfully.
+cudaError_t counted(pe_handle* h, cudaError_t e) {
+  if (e == cudaSuccess) ++h->launches;
+  return e;
+}
 
 template <typename T>
 cudaError_t dev_alloc(pe_handle* h, T** p, size_t count) {
@@ -98,13 +111,15 @@ TcGemmWorkspace tc_ws(pe_handle* h) {
 cudaError_t linear(pe_handle* h, const void* x, int ldx, const void* w, const void* w2, int M,
                    int N, int K, const EpiArgs& epi, cudaStream_t s) {
   if (h->desc.dtype == PE_DTYPE_F32)
-    return launch_gemm_simt(static_cast<const float*>(x), ldx, static_cast<const float*>(w),
-                            static_cast<const float*>(w2), M, N, K, epi, h->err, s);
+    return counted(h, launch_gemm_simt(static_cast<const float*>(x), ldx,
+                                       static_cast<const float*>(w),
+                                       static_cast<const float*>(w2), M, N, K, epi, h->err, s));
   const CUtensorMap* wa = get_map(h, w, N, K, K, 128);
   const CUtensorMap* wa2 = w2 ? get_map(h, w2, N, K, K, 128) : wa;
   const CUtensorMap* xb = get_map(h, x, M, K, ldx, tc_pick_bn(M));
   if (!wa || !wa2 || !xb) return cudaErrorInvalidValue;
-  return launch_gemm_tc_maps(*wa, *wa2, *xb, w2 != nullptr, M, N, K, epi, tc_ws(h), h->err, s);
+  return counted(h, launch_gemm_tc_maps(*wa, *wa2, *xb, w2 != nullptr, M, N, K, epi, tc_ws(h),
+                                        h->err, s));
 }
 
 EpiArgs epi_none() {
@@ -206,6 +221,8 @@ pe_status pe_create(const pe_model_desc* desc, const pe_weights* weights, int32_
       inv[i] = std::pow(static_cast<double>(d.rope_theta), -2.0 * i / d.head_dim);
     e = cudaMemcpy(h->inv_freq64, inv.data(), inv.size() * sizeof(double), cudaMemcpyHostToDevice);
   }
+  if (e == cudaSuccess && d.dtype == PE_DTYPE_BF16) e = init_gemm_tc();
+  if (e == cudaSuccess && d.dtype == PE_DTYPE_BF16) e = init_attention_tc();
   if (e == cudaSuccess && d.dtype == PE_DTYPE_BF16) {
     const int bn = tc_pick_bn(max_tokens);
     h->gemm_partial_floats = tc_partial_floats(h->sm_count, bn, true);
@@ -220,6 +237,12 @@ pe_status pe_create(const pe_model_desc* desc, const pe_weights* weights, int32_
     return e == cudaErrorMemoryAllocation ? PE_ERR_OUT_OF_MEMORY : PE_ERR_CUDA;
   }
   *out = h;
+  return PE_OK;
+}
+
+pe_status pe_get_launch_count(pe_handle* h, int64_t* count) {
+  if (!h || !count) return PE_ERR_INVALID_ARGUMENT;
+  *count = h->launches;
   return PE_OK;
 }
 
@@ -286,7 +309,7 @@ pe_status pe_expand_batch(pe_handle* h, int32_t B, int32_t K, int32_t T, const i
   a.seq_lens = out->seq_lens;
   a.hidden = out->hidden;
   a.err = h->err;
-  cudaError_t e = launch_expand(a, static_cast<cudaStream_t>(stream));
+  cudaError_t e = counted(h, launch_expand(a, static_cast<cudaStream_t>(stream)));
   if (e != cudaSuccess) return PE_ERR_CUDA;
   out->B = B;
   out->K = K;
@@ -314,7 +337,35 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
   const int dt = d.dtype;
   const int qkv_rows = (d.n_heads + 2 * d.n_kv_heads) * d.head_dim;
   const int qd = d.n_heads * d.head_dim;
+  const uint64_t cache_rows = static_cast<uint64_t>(num_blocks) * d.n_kv_heads * 16;
+  // rows of one request: its verify window (at most K + 1 rows, and at most
+  // what the batch leaves it) plus the K - 1 MASK rows
+  const int max_rows_per_req = std::min(ex->T - B + 1, K + 1) + K - 1;
   cudaError_t e;
+  if (dt == PE_DTYPE_BF16) {
+    if (d.head_dim % 64 || (d.n_heads / d.n_kv_heads) > 128) return PE_ERR_UNSUPPORTED;
+    for (int l = 0; l < d.n_layers; ++l)
+      if (!aligned16(k_cache[l]) || !aligned16(v_cache[l])) return PE_ERR_INVALID_ARGUMENT;
+    // the split-KV workspace depends on the batch and the block table; the
+    // first call that needs more grows it (make that call before capturing
+    // the step into a CUDA graph)
+    AttnArgs probe = {};
+    probe.B = B;
+    probe.Hq = d.n_heads;
+    probe.Hkv = d.n_kv_heads;
+    probe.dh = d.head_dim;
+    probe.bt_stride = bt_stride;
+    const size_t need = attention_tc_partial_floats(probe, max_rows_per_req, h->sm_count);
+    const size_t need_c = attention_tc_counters(probe, max_rows_per_req, h->sm_count);
+    if (need > h->attn_partial_floats) {
+      if ((e = dev_alloc(h, &h->attn_partials, need))) return PE_ERR_OUT_OF_MEMORY;
+      h->attn_partial_floats = need;
+    }
+    if (need_c > h->attn_n_counters) {
+      if ((e = dev_alloc(h, &h->attn_counters, need_c))) return PE_ERR_OUT_OF_MEMORY;
+      h->attn_n_counters = need_c;
+    }
+  }
 
   // fc: projected target hidden state -> residual stream (fp32)
   EpiArgs ep = epi_none();
@@ -339,7 +390,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
   ec.eps = d.rms_eps;
   ec.x = h->x_in;
   ec.err = h->err;
-  if ((e = launch_embed_concat(dt, ec, s))) return PE_ERR_CUDA;
+  if ((e = counted(h, launch_embed_concat(dt, ec, s)))) return PE_ERR_CUDA;
 
   for (int l = 0; l < d.n_layers; ++l) {
     const pe_layer_weights& L = h->layers[l];
@@ -354,7 +405,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
       rn.eps = d.rms_eps;
       rn.y = h->x_in;
       rn.err = h->err;
-      if ((e = launch_rmsnorm(dt, rn, s))) return PE_ERR_CUDA;
+      if ((e = counted(h, launch_rmsnorm(dt, rn, s)))) return PE_ERR_CUDA;
     }
     // QKV projection
     ep = epi_none();
@@ -382,7 +433,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     rk.k_cache = k_cache[l];
     rk.v_cache = v_cache[l];
     rk.err = h->err;
-    if ((e = launch_rope_kv(dt, rk, s))) return PE_ERR_CUDA;
+    if ((e = counted(h, launch_rope_kv(dt, rk, s)))) return PE_ERR_CUDA;
     // paged causal attention
     AttnArgs at;
     at.rows = rows;
@@ -403,7 +454,17 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     at.out = h->attn;
     at.scale = 1.0f / std::sqrt(static_cast<float>(d.head_dim));
     at.err = h->err;
-    if ((e = launch_attention_simt(dt, at, s))) return PE_ERR_CUDA;
+    if (dt == PE_DTYPE_F32) {
+      if ((e = counted(h, launch_attention_simt(dt, at, s)))) return PE_ERR_CUDA;
+    } else {
+      const CUtensorMap* tk = get_map(h, k_cache[l], cache_rows, d.head_dim, d.head_dim, 16);
+      const CUtensorMap* tv = get_map(h, v_cache[l], cache_rows, d.head_dim, d.head_dim, 16);
+      if (!tk || !tv) return PE_ERR_INVALID_ARGUMENT;
+      e = counted(h, launch_attention_tc(at, *tk, *tv, ex->seq_lens, max_rows_per_req,
+                                         h->sm_count, h->attn_partials, h->attn_partial_floats,
+                                         h->attn_counters, h->attn_n_counters, s));
+      if (e) return PE_ERR_CUDA;
+    }
     // O projection + residual
     ep = epi_none();
     ep.kind = EPI_ADD;
@@ -422,7 +483,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     rn.eps = d.rms_eps;
     rn.y = h->xn;
     rn.err = h->err;
-    if ((e = launch_rmsnorm(dt, rn, s))) return PE_ERR_CUDA;
+    if ((e = counted(h, launch_rmsnorm(dt, rn, s)))) return PE_ERR_CUDA;
     ep = epi_none();
     ep.kind = EPI_SILU_MUL;
     ep.M = rows;
@@ -457,7 +518,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
   rn.eps = d.rms_eps;
   rn.y = out_hidden;
   rn.err = h->err;
-  if ((e = launch_rmsnorm(dt, rn, s))) return PE_ERR_CUDA;
+  if ((e = counted(h, launch_rmsnorm(dt, rn, s)))) return PE_ERR_CUDA;
   return PE_OK;
 }
 
@@ -477,7 +538,7 @@ pe_status pe_lmhead_argmax(pe_handle* h, const void* hidden, int32_t M, int32_t*
   ep.tokens = out_tokens;
   cudaError_t e = linear(h, hidden, d.d, h->w.lm_head, nullptr, M, d.vocab, d.d, ep, s);
   if (e == cudaSuccess && d.dtype == PE_DTYPE_F32)
-    e = launch_argmax_finalize(M, h->keys, out_tokens, s);
+    e = counted(h, launch_argmax_finalize(M, h->keys, out_tokens, s));
   return cuda_status(e);
 }
 

@@ -1,0 +1,488 @@
+// attention_tc.cu -- paged causal attention of the drafting rows on 5th-gen
+// tensor cores (bf16 operands, fp32 scores and accumulators in TMEM).
+//
+// Semantics (what the oracle states): each non-rejected row at position P
+// attends key positions 0..P of its request through the block table; query
+// head h reads kv head h / (Hq / Hkv); softmax of q.k / sqrt(dh); rejected
+// rows (vLLM blog summary "P-EAGLE: Faster LLM Inference with Parallel
+// Speculative Decoding in vLLM", KV-cache bullet) produce zeros.  The rows of
+// one request are [accepted window rows, next-token row, MASK rows], so a
+// shorter request's mask is the top-left block of a longer one's (paper
+// summary "P-EAGLE: Parallel-Drafting EAGLE with Scalable Training", Fig. 3).
+//
+// Work unit (one CTA): request r, kv head g, a tile of up to 128 query rows
+// (the request's rows x the g-th group of q heads -- GQA packs the group
+// into the MMA's M side), and one split of the key range.  Per 128-key chunk:
+//   S = Q K^T      (tcgen05, M=128 queries, N=128 keys, K=dh)
+//   P = softmax    (4 warps, one query row per thread; max kept lazily and
+//                   O rescaled in TMEM only when the running max grows by
+//                   more than 2^8)
+//   O += P V       (tcgen05, M=128, N=64 per half of dh, K=128 keys)
+// K and V pages come by TMA (16 keys x 64 dims per copy, 128-byte swizzle)
+// into a 2-stage ring.  Splits of one (r, g, tile) are merged by the CTA that
+// finishes last, in split order (deterministic).
+#include "pe_common.cuh"
+#include "pe_kernels.h"
+
+namespace pe {
+
+struct AttnTcParams {
+  AttnArgs a;
+  const int32_t* seq_lens;
+  int G;             // q heads per kv head
+  int rows_per_qt;   // request rows per query tile (128 / G)
+  int qtiles;        // query tiles per request
+  int split_keys;    // keys per split (multiple of 128)
+  int max_splits;
+  float* part;       // [B, Hkv, qtiles, max_splits, 128, dh + 2]
+  int* counters;     // [B, Hkv, qtiles]
+};
+
+template <int DH>
+struct AttnCfg {
+  static constexpr int NH = DH / 64;          // 64-wide halves of the head dim
+  static constexpr int KEYS = 128;            // keys per chunk
+  static constexpr int TILE_BYTES = 128 * 128;  // 128 rows x 128 B
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = Q_OFF + NH * TILE_BYTES;          // [2 stages][NH]
+  static constexpr int V_OFF = K_OFF + 2 * NH * TILE_BYTES;      // [2 stages][NH]
+  static constexpr int P_OFF = V_OFF + 2 * NH * TILE_BYTES;      // [2 key halves]
+  static constexpr int BAR_OFF = P_OFF + 2 * TILE_BYTES;
+  static constexpr int SMEM = 1024 + BAR_OFF + 256;
+  static constexpr int TMEM_COLS = 256;       // S: 0..127, O: 128..128+DH
+  static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128);
+  static constexpr uint32_t IDESC_PV = idesc_bf16_f32_bmn(128, 64);
+};
+
+template <int DH>
+__global__ void __launch_bounds__(192, 1)
+    attention_tc_kernel(const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const AttnTcParams p) {
+  using C = AttnCfg<DH>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* kv_full = bars;        // [2]
+  uint64_t* kv_empty = bars + 2;   // [2]
+  uint64_t* q_ready = bars + 4;
+  uint64_t* s_full = bars + 5;
+  uint64_t* s_free = bars + 6;
+  uint64_t* p_full = bars + 7;
+  uint64_t* pv_done = bars + 8;
+  uint64_t* drain = bars + 9;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  volatile int* flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* ok_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+
+  const AttnArgs& a = p.a;
+  const int split = blockIdx.x;
+  const int g = blockIdx.y % a.Hkv;
+  const int qt = blockIdx.y / a.Hkv;
+  const int r = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- which rows and keys this CTA covers (uniform across the CTA) ------
+  grid_dep_wait();
+  const int row0 = a.cu_out[r];
+  const int nrows = a.cu_out[r + 1] - row0;
+  const int tile_row0 = qt * p.rows_per_qt;
+  const int tile_rows = min(p.rows_per_qt, nrows - tile_row0);
+  if (qt == p.qtiles - 1 && split == 0 && g == 0 && threadIdx.x == 0 &&
+      nrows > p.qtiles * p.rows_per_qt)
+    record_error(a.err, PE_DEV_BAD_ROW);
+  const int seq = p.seq_lens[r];
+  const int key0 = split * p.split_keys;
+  const int nsplits = (seq + p.split_keys - 1) / p.split_keys;
+  if (tile_rows <= 0 || key0 >= seq || seq > a.bt_stride * 16) {
+    if (threadIdx.x == 0 && seq > a.bt_stride * 16 && split == 0 && g == 0 && qt == 0)
+      record_error(a.err, PE_DEV_BAD_POSITION);
+    grid_dep_launch();
+    return;
+  }
+  const int key1 = min(seq, key0 + p.split_keys);
+  const int nchunks = (key1 - key0 + C::KEYS - 1) / C::KEYS;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    mbar_init(q_ready, 1);
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 128);
+    mbar_init(p_full, 128);
+    mbar_init(pv_done, 1);
+    mbar_init(drain, 1);
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  grid_dep_launch();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const uint64_t pol = l2_policy_evict_first();
+      const int32_t* bt = a.block_table + static_cast<size_t>(r) * a.bt_stride;
+      for (int c = 0; c < nchunks; ++c) {
+        const int st = c & 1;
+        if (c >= 2 && !mbar_wait(&kv_empty[st], ((c >> 1) - 1) & 1, a.err)) break;
+        const int t0 = key0 + c * C::KEYS;
+        int blks[8];
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int pg = 0; pg < 8; ++pg) {
+          const int t = t0 + pg * 16;
+          blks[pg] = -1;
+          if (t < key1) {
+            const int b = bt[t >> 4];
+            if (b < 0 || b >= a.num_blocks) record_error(a.err, PE_DEV_BAD_BLOCK);
+            else {
+              blks[pg] = b;
+              bytes += 2u * C::NH * 2048u;
+            }
+          }
+        }
+        mbar_arrive_expect_tx(&kv_full[st], bytes);
+#pragma unroll
+        for (int pg = 0; pg < 8; ++pg) {
+          if (blks[pg] < 0) continue;
+          const int row = (blks[pg] * a.Hkv + g) * 16;
+#pragma unroll
+          for (int h = 0; h < C::NH; ++h) {
+            uint8_t* kd = smem + C::K_OFF + (st * C::NH + h) * C::TILE_BYTES + pg * 2048;
+            uint8_t* vd = smem + C::V_OFF + (st * C::NH + h) * C::TILE_BYTES + pg * 2048;
+            tma_load_2d(kd, &tmK, &kv_full[st], h * 64, row, pol);
+            tma_load_2d(vd, &tmV, &kv_full[st], h * 64, row, pol);
+          }
+        }
+      }
+      // drain: the copies of the last stages have landed before exit
+      for (int c = max(0, nchunks - 2); c < nchunks; ++c)
+        mbar_wait(&kv_full[c & 1], (c >> 1) & 1, a.err);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t s_tm = tmem, o_tm = tmem + 128;
+      bool ok = mbar_wait(q_ready, 0, a.err);
+      const uint32_t q_addr = smem_u32(smem + C::Q_OFF);
+      const uint32_t p_addr = smem_u32(smem + C::P_OFF);
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int st = c & 1;
+        if (!mbar_wait(&kv_full[st], (c >> 1) & 1, a.err)) break;
+        if (c > 0 && !mbar_wait(s_free, (c - 1) & 1, a.err)) break;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(smem + C::K_OFF + st * C::NH * C::TILE_BYTES);
+#pragma unroll
+        for (int h = 0; h < C::NH; ++h)
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4)
+            umma_bf16(s_tm, sw128_kmajor_desc(q_addr + h * C::TILE_BYTES + k4 * 32),
+                      sw128_kmajor_desc(k_addr + h * C::TILE_BYTES + k4 * 32), C::IDESC_S,
+                      (h | k4) != 0);
+        umma_commit(s_full);
+        if (!mbar_wait(p_full, c & 1, a.err)) break;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(smem + C::V_OFF + st * C::NH * C::TILE_BYTES);
+#pragma unroll
+        for (int kh = 0; kh < 2; ++kh)      // 64-key halves of the chunk
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const uint64_t adesc = sw128_kmajor_desc(p_addr + kh * C::TILE_BYTES + k4 * 32);
+#pragma unroll
+            for (int h = 0; h < C::NH; ++h)
+              umma_bf16(o_tm + h * 64,  adesc,
+                        sw128_mnmajor_desc(v_addr + h * C::TILE_BYTES + (kh * 64 + k4 * 16) * 128),
+                        C::IDESC_PV, (c > 0 || kh > 0 || k4 > 0) ? 1u : 0u);
+          }
+        umma_commit(&kv_empty[st]);
+        umma_commit(pv_done);
+      }
+      umma_commit(drain);
+      mbar_wait(drain, 0, a.err);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int qrow = 32 * (warp & 3) + lane;        // TMEM lane of this thread
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const int lr = qrow / p.G, hl = qrow % p.G;
+    const bool in_tile = lr < tile_rows;
+    const int row = row0 + tile_row0 + lr;          // expanded row
+    const int head = g * p.G + hl;
+    bool valid = false;
+    int P = -1;
+    if (in_tile) {
+      valid = a.is_rejected[row] == 0;
+      if (valid) P = a.pos[row];
+    }
+    // Q row -> shared memory (128-byte swizzle, zero for padding / rejected)
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          static_cast<const bf16*>(a.q) + (static_cast<size_t>(row) * a.Hq + head) * DH);
+#pragma unroll
+      for (int h = 0; h < C::NH; ++h)
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (valid) v = src[h * 8 + ch];
+          *reinterpret_cast<uint4*>(smem + C::Q_OFF + h * C::TILE_BYTES + qrow * 128 +
+                                    ((ch ^ (qrow & 7)) * 16)) = v;
+        }
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1, 128);
+    if (threadIdx.x == 64) mbar_arrive(q_ready);
+
+    const float sc = a.scale * 1.4426950408889634f;   // log2(e) / sqrt(dh)
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int c = 0; c < nchunks; ++c) {
+      if (threadIdx.x == 64) *ok_flag = mbar_wait(s_full, c & 1, a.err) ? 1 : 0;
+      named_bar_sync(1, 128);
+      if (!*ok_flag) { ok = false; break; }
+      tc_fence_after();
+      const int t0 = key0 + c * C::KEYS;
+      // pass 1: masked maximum of the scaled scores
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c0 = 0; c0 < C::KEYS; c0 += 16) {
+        float s[16];
+        tmem_ld16(tmem + lane_off + c0, s);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (t0 + c0 + j <= P) mx = fmaxf(mx, s[j] * sc);
+      }
+      // lazy rescale: keep the old reference unless the max grew past 2^8
+      float m_new = m_used, factor = 1.f;
+      if (mx > -INFINITY) {
+        if (m_used == -INFINITY) m_new = mx;
+        else if (mx > m_used + 8.f) {
+          m_new = mx;
+          factor = exp2f(m_used - mx);
+        }
+      }
+      // pass 2: probabilities as bf16 (kept in registers until P is free)
+      uint32_t pk[64];
+      float psum = 0.f;
+#pragma unroll
+      for (int c0 = 0; c0 < C::KEYS; c0 += 16) {
+        float s[16];
+        tmem_ld16(tmem + lane_off + c0, s);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+          const float p0 = (t0 + c0 + j <= P) ? exp2f(s[j] * sc - m_new) : 0.f;
+          const float p1 = (t0 + c0 + j + 1 <= P) ? exp2f(s[j + 1] * sc - m_new) : 0.f;
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+          psum += __low2float(b2) + __high2float(b2);
+          pk[(c0 + j) / 2] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(s_free);                         // S may be overwritten now
+      l = l * factor + psum;
+      m_used = m_new;
+      // wait until the previous P.V finished (P buffer and O are ours)
+      if (c > 0) {
+        if (threadIdx.x == 64) *ok_flag = mbar_wait(pv_done, (c - 1) & 1, a.err) ? 1 : 0;
+        named_bar_sync(1, 128);
+        if (!*ok_flag) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, factor != 1.f)) {
+#pragma unroll
+          for (int c0 = 0; c0 < DH; c0 += 16) {
+            float o[16];
+            tmem_ld16(tmem + lane_off + 128 + c0, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) o[j] *= factor;
+            tmem_st16(tmem + lane_off + 128 + c0, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      // P row -> shared memory: keys 0..63 in the first tile, 64..127 in the second
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        const int kh = ch >> 3, cc = ch & 7;
+        *reinterpret_cast<uint4*>(smem + C::P_OFF + kh * C::TILE_BYTES + qrow * 128 +
+                                  ((cc ^ (qrow & 7)) * 16)) =
+            make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+      }
+      // keys past the sequence end: zero their V rows so 0 * garbage cannot
+      // reach O (the pool may hold anything there)
+      if (t0 + C::KEYS > key1 && t0 + qrow >= key1) {
+        const int st = c & 1;
+#pragma unroll
+        for (int h = 0; h < C::NH; ++h) {
+          uint4* vr = reinterpret_cast<uint4*>(smem + C::V_OFF + (st * C::NH + h) * C::TILE_BYTES +
+                                               qrow * 128);
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) vr[ch] = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok) {
+      if (threadIdx.x == 64) *ok_flag = mbar_wait(pv_done, (nchunks - 1) & 1, a.err) ? 1 : 0;
+      named_bar_sync(1, 128);
+      ok = *ok_flag != 0;
+    }
+    if (ok) {
+      tc_fence_after();
+      float o[DH];
+#pragma unroll
+      for (int c0 = 0; c0 < DH; c0 += 16) {
+        float t[16];
+        tmem_ld16(tmem + lane_off + 128 + c0, t);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) o[c0 + j] = t[j];
+      }
+      bf16* out = static_cast<bf16*>(a.out) + (static_cast<size_t>(row) * a.Hq + head) * DH;
+      if (nsplits == 1) {
+        if (in_tile) {
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+          for (int j = 0; j < DH; j += 2)
+            *reinterpret_cast<__nv_bfloat162*>(out + j) =
+                __floats2bfloat162_rn(o[j] * inv, o[j + 1] * inv);
+        }
+      } else {
+        const size_t unit = (static_cast<size_t>(r) * a.Hkv + g) * p.qtiles + qt;
+        const size_t stride = static_cast<size_t>(128) * (DH + 2);
+        float* mine = p.part + (unit * p.max_splits + split) * stride + qrow * (DH + 2);
+#pragma unroll
+        for (int j = 0; j < DH; ++j) mine[j] = o[j];
+        mine[DH] = m_used;
+        mine[DH + 1] = l;
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (threadIdx.x == 64) {
+          const int old = atomicAdd(p.counters + unit, 1);
+          *flag = (old == nsplits - 1) ? 1 : 0;
+        }
+        named_bar_sync(1, 128);
+        if (*flag) {
+          __threadfence();
+          float M = -INFINITY;
+          for (int s = 0; s < nsplits; ++s) {
+            const float* src = p.part + (unit * p.max_splits + s) * stride + qrow * (DH + 2);
+            if (__ldcg(src + DH + 1) > 0.f) M = fmaxf(M, __ldcg(src + DH));
+          }
+          float acc[DH];
+#pragma unroll
+          for (int j = 0; j < DH; ++j) acc[j] = 0.f;
+          float L = 0.f;
+          for (int s = 0; s < nsplits; ++s) {
+            const float* src = p.part + (unit * p.max_splits + s) * stride + qrow * (DH + 2);
+            const float ls = __ldcg(src + DH + 1);
+            if (!(ls > 0.f)) continue;
+            const float w = exp2f(__ldcg(src + DH) - M);
+            L += w * ls;
+#pragma unroll
+            for (int j = 0; j < DH; ++j) acc[j] += w * __ldcg(src + j);
+          }
+          if (in_tile) {
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+            for (int j = 0; j < DH; j += 2)
+              *reinterpret_cast<__nv_bfloat162*>(out + j) =
+                  __floats2bfloat162_rn(acc[j] * inv, acc[j + 1] * inv);
+          }
+          if (threadIdx.x == 64) p.counters[unit] = 0;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+struct AttnPlan {
+  int G, rows_per_qt, qtiles, split_keys, max_splits;
+};
+
+static AttnPlan plan_attention(const AttnArgs& a, int max_rows_per_req, int sm_count) {
+  AttnPlan pl;
+  pl.G = a.Hq / a.Hkv;
+  pl.rows_per_qt = 128 / pl.G;
+  pl.qtiles = (max_rows_per_req + pl.rows_per_qt - 1) / pl.rows_per_qt;
+  const int max_seq = a.bt_stride * 16;
+  const int chunks_max = (max_seq + 127) / 128;
+  const long long pairs = static_cast<long long>(a.B) * a.Hkv * pl.qtiles;
+  const int want = static_cast<int>(std::max<long long>(1, (sm_count + pairs - 1) / pairs));
+  int cps = (chunks_max + want - 1) / want;
+  cps = std::max(2, std::min(16, cps));
+  pl.split_keys = cps * 128;
+  pl.max_splits = (max_seq + pl.split_keys - 1) / pl.split_keys;
+  return pl;
+}
+
+size_t attention_tc_partial_floats(const AttnArgs& a, int max_rows_per_req, int sm_count) {
+  const AttnPlan pl = plan_attention(a, max_rows_per_req, sm_count);
+  return static_cast<size_t>(a.B) * a.Hkv * pl.qtiles * pl.max_splits * 128 * (a.dh + 2);
+}
+
+size_t attention_tc_counters(const AttnArgs& a, int max_rows_per_req, int sm_count) {
+  const AttnPlan pl = plan_attention(a, max_rows_per_req, sm_count);
+  return static_cast<size_t>(a.B) * a.Hkv * pl.qtiles;
+}
+
+cudaError_t init_attention_tc() {
+  cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel<64>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       AttnCfg<64>::SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attention_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             AttnCfg<128>::SMEM);
+  return e;
+}
+
+cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                const int32_t* seq_lens, int max_rows_per_req, int sm_count,
+                                float* part, size_t part_floats, int* counters,
+                                size_t n_counters, cudaStream_t s) {
+  if (a.rows <= 0) return cudaSuccess;
+  const AttnPlan pl = plan_attention(a, max_rows_per_req, sm_count);
+  AttnTcParams p;
+  p.a = a;
+  p.seq_lens = seq_lens;
+  p.G = pl.G;
+  p.rows_per_qt = pl.rows_per_qt;
+  p.qtiles = pl.qtiles;
+  p.split_keys = pl.split_keys;
+  p.max_splits = pl.max_splits;
+  p.part = part;
+  p.counters = counters;
+  const size_t need = static_cast<size_t>(a.B) * a.Hkv * pl.qtiles * pl.max_splits * 128 * (a.dh + 2);
+  if (need > part_floats || static_cast<size_t>(a.B) * a.Hkv * pl.qtiles > n_counters)
+    return cudaErrorInvalidValue;
+  dim3 grid(pl.max_splits, a.Hkv * pl.qtiles, a.B);
+  if (a.dh == 64)
+    return launch_pdl(attention_tc_kernel<64>, grid, dim3(192), AttnCfg<64>::SMEM, s, tmK, tmV, p);
+  return launch_pdl(attention_tc_kernel<128>, grid, dim3(192), AttnCfg<128>::SMEM, s, tmK, tmV, p);
+}
+
+}  // namespace pe

@@ -74,10 +74,6 @@ __device__ __forceinline__ int cta_of_unit(long long u, long long U, int G) {
   return c;
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 // Apply the epilogue to 16 token columns [t0, t0 + 16) of output feature o.
 // Called by all 32 lanes of a warp together (the argmax reduces across them).
 template <bool DUAL>
@@ -402,12 +398,31 @@ bool tensor_map_2d_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t
 }
 
 template <int BN, bool DUAL>
+static cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(gemm_tc_kernel<BN, DUAL>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<BN, DUAL>::SMEM);
+}
+
+// Opt every instantiation into its dynamic shared memory (once per process
+// and device, before any launch or stream capture).
+cudaError_t init_gemm_tc() {
+  cudaError_t e = cudaSuccess;
+#define PE_TC_ATTR(BNV)                                            \
+  if (e == cudaSuccess) e = set_smem_attr<BNV, false>();           \
+  if (e == cudaSuccess) e = set_smem_attr<BNV, true>();
+  PE_TC_ATTR(16)
+  PE_TC_ATTR(32)
+  PE_TC_ATTR(64)
+  PE_TC_ATTR(128)
+  PE_TC_ATTR(256)
+#undef PE_TC_ATTR
+  return e;
+}
+
+template <int BN, bool DUAL>
 static cudaError_t run_tc(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
                           const TcParams& p, int grid, cudaStream_t s) {
   using C = TcCfg<BN, DUAL>;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, DUAL>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  if (e != cudaSuccess) return e;
   return launch_pdl(gemm_tc_kernel<BN, DUAL>, dim3(grid), dim3(192), C::SMEM, s, a, a2, b, p);
 }
 

@@ -65,3 +65,32 @@ def test_k1_is_one_autoregressive_step_on_gpu():
 def test_gpt_oss_b1_full_size():
     """GPT-OSS-20B-shaped drafter, bf16, one request, K=7, context 4096."""
     G.full_parity(W.gpt_oss_b1(), TOL_BF16)
+
+
+def _sample_requests(wl, n=3):
+    """The longest context, a request with everything rejected (if any), and
+    one more: requests are independent, so the oracle checks a sample."""
+    order = np.argsort(-wl.contexts)
+    pick = [int(order[0])]
+    zero = [i for i in range(wl.B) if wl.accepted[i] == 0 and i not in pick]
+    if zero:
+        pick.append(zero[0])
+    for i in range(wl.B):
+        if len(pick) >= n:
+            break
+        if i not in pick:
+            pick.append(i)
+    return sorted(pick)
+
+
+def test_gpt_oss_b64_full_size_sampled_requests():
+    """GPT-OSS-20B-shaped drafter at batch 64, K=7, lognormal contexts."""
+    wl = W.gpt_oss_b64()
+    G.full_parity(wl, TOL_BF16, requests=_sample_requests(wl))
+
+
+@pytest.mark.parametrize("K", [1, 4, 8])
+def test_qwen_b16_full_size_sampled_requests(K):
+    """Qwen3-Coder-30B-shaped drafter (head_dim 128), batch 16, K sweep."""
+    wl = W.qwen_b16(K)
+    G.full_parity(wl, TOL_BF16, requests=_sample_requests(wl, 2))
