@@ -223,8 +223,11 @@ pe_status pe_get_device_error(pe_handle* h, int32_t* code, void* stream);
 /* Optional diagnostics: when residual_trace is non-NULL, every later
  * pe_draft_forward copies the fp32 residual stream [T', d] after each layer
  * into residual_trace + layer * max_tokens * d (caller-owned device buffer of
- * n_layers * max_tokens * d floats).  NULL turns it off. */
-pe_status pe_set_trace(pe_handle* h, float* residual_trace);
+ * n_layers * max_tokens * d floats).  When attn_trace is non-NULL, it copies
+ * each layer's attention output [T', Hq * dh] (model dtype) into
+ * attn_trace + layer * max_tokens * Hq * dh elements.  NULL turns a trace
+ * off. */
+pe_status pe_set_trace(pe_handle* h, float* residual_trace, void* attn_trace);
 
 /* y[M, N] = x[M, K] . w[N, K]^T with the library's GEMM for the model dtype
  * (tcgen05 tensor cores for bf16, FFMA for f32); y is fp32.  A diagnostic

@@ -251,6 +251,7 @@ class DrafterOut:
     residual: np.ndarray                 # [R, d] fp64 after the last layer
     kv_writes: List[Dict[str, np.ndarray]]  # per layer: slot, k, v
     layer_residuals: List[np.ndarray]
+    layer_attn: List[np.ndarray]         # per layer: attention output [R, Hq, dh]
 
 
 def gather_request_cache(cache_layer: np.ndarray, block_table_row,
@@ -285,7 +286,7 @@ def drafter_forward_rows(shape, weights, rows: DrafterRows, block_table,
     e = to_f64(W["emb"][rows.tokens], dt)                       # [R, d]
     h = linear(to_f64(rows.hidden3, dt), W["fc"], dt)           # [R, d]
     residual = h
-    kv_writes, layer_res = [], []
+    kv_writes, layer_res, layer_attn = [], [], []
     requests = sorted(set(int(r) for r in rows.request))
     for l, lw in enumerate(W["layers"]):
         if l == 0:
@@ -316,13 +317,14 @@ def drafter_forward_rows(shape, weights, rows: DrafterRows, block_table,
             for i in sel:                     # ... then attention
                 attn[i] = attention_one_row(q[i], kd, vd, int(rows.positions[i]))
         kv_writes.append({"slot": slots, "k": k, "v": v})
+        layer_attn.append(attn)
 
         residual = residual + linear(attn.reshape(R, Hq * dh), lw["o"], dt)
         n = rms_norm(residual, to_f64(lw["norm_post"], dt), eps)
         act = silu(linear(n, lw["gate"], dt)) * linear(n, lw["up"], dt)
         residual = residual + linear(act, lw["down"], dt)
         layer_res.append(residual)
-    return DrafterOut(residual, kv_writes, layer_res)
+    return DrafterOut(residual, kv_writes, layer_res, layer_attn)
 
 
 # ---------------------------------------------------------------------------

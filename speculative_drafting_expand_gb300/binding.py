@@ -77,7 +77,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                      _i32, _vp, _vp]
     lib.pe_lmhead_argmax.argtypes = [_vp, _vp, _i32, _vp, _vp, _vp]
     lib.pe_get_device_error.argtypes = [_vp, P(_i32), _vp]
-    lib.pe_set_trace.argtypes = [_vp, _vp]
+    lib.pe_set_trace.argtypes = [_vp, _vp, _vp]
     lib.pe_linear.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp]
     lib.pe_get_launch_count.argtypes = [_vp, P(ctypes.c_int64)]
     lib.pe_status_string.argtypes = [_i32]
@@ -255,8 +255,8 @@ def pe_get_device_error(dr: Drafter, stream=None) -> int:
     return code.value
 
 
-def pe_set_trace(dr: Drafter, trace) -> None:
-    _check("pe_set_trace", lib().pe_set_trace(dr.handle, ptr(trace)))
+def pe_set_trace(dr: Drafter, residual_trace=None, attn_trace=None) -> None:
+    _check("pe_set_trace", lib().pe_set_trace(dr.handle, ptr(residual_trace), ptr(attn_trace)))
 
 
 def pe_get_launch_count(dr: Drafter) -> int:

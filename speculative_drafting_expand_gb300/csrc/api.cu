@@ -58,6 +58,7 @@ struct pe_handle {
   int* attn_counters = nullptr;
   size_t attn_n_counters = 0;
   float* trace = nullptr;
+  void* attn_trace = nullptr;
   long long launches = 0;
 
   std::map<std::tuple<const void*, uint64_t, uint64_t, uint64_t, uint32_t>, CUtensorMap> maps;
@@ -246,9 +247,10 @@ pe_status pe_get_launch_count(pe_handle* h, int64_t* count) {
   return PE_OK;
 }
 
-pe_status pe_set_trace(pe_handle* h, float* residual_trace) {
+pe_status pe_set_trace(pe_handle* h, float* residual_trace, void* attn_trace) {
   if (!h) return PE_ERR_INVALID_ARGUMENT;
   h->trace = residual_trace;
+  h->attn_trace = attn_trace;
   return PE_OK;
 }
 
@@ -463,6 +465,12 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
       e = counted(h, launch_attention_tc(at, *tk, *tv, ex->seq_lens, max_rows_per_req,
                                          h->sm_count, h->attn_partials, h->attn_partial_floats,
                                          h->attn_counters, h->attn_n_counters, s));
+      if (e) return PE_ERR_CUDA;
+    }
+    if (h->attn_trace) {
+      const size_t per = static_cast<size_t>(qd) * h->esize;
+      e = cudaMemcpyAsync(static_cast<char*>(h->attn_trace) + l * h->max_tokens * per, h->attn,
+                          rows * per, cudaMemcpyDeviceToDevice, s);
       if (e) return PE_ERR_CUDA;
     }
     // O projection + residual

@@ -133,14 +133,33 @@ def full_parity(wl, tol, gains=None, requests=None, check_cache=True):
     inp = W.make_step_inputs(wl)
     w = W.make_weights(sh, wl.config_id, gains=gains or wl.gains)
     kc, vc = W.make_kv_cache(wl, inp)
-    dr = make_drafter(sh, w, max(wl.T_out, wl.B * wl.K), wl.B)
+    max_tokens = max(wl.T_out, wl.B * wl.K)
+    dr = make_drafter(sh, w, max_tokens, wl.B)
     st = DeviceStep(wl, inp, kc, vc)
     remember_host_caches(st, kc, vc)
+    torch = torch_mod()
+    B = library()
+    tdt = torch.bfloat16 if sh.dtype == "bf16" else torch.float32
+    qd = sh.n_heads * sh.head_dim
+    attn_trace = torch.zeros(sh.n_layers, max_tokens, qd, dtype=tdt, device="cuda")
+    B.pe_set_trace(dr, None, attn_trace)
     res = run_step(dr, st, want_logits=True)
     assert res["err"] == 0, res["err"]
     ref = O.draft_step(sh, w, wl.K, inp, kc, vc, requests=requests)
     check_expand(res["ex"], ref.expanded, wl.T)
-    B = library()
+    # attention output of every row the oracle computed, layer by layer
+    at = B.to_host(attn_trace)
+    for l in range(sh.n_layers):
+        got_a = f64(at[l][ref.row_index], sh.dtype)
+        want_a = ref.drafter.layer_attn[l].reshape(len(ref.row_index), qd)
+        scale = np.abs(want_a).max()
+        err = np.abs(got_a - want_a).max()
+        assert err <= 1.5 * tol * scale, ("attention", l, err / scale)
+    ex = ref.expanded
+    dead = [i for i in range(len(ex.ids)) if ex.is_rejected[i]
+            and int(ex.request_of_row[i]) in set(ref.requests)]
+    for l in range(sh.n_layers):
+        assert not np.any(f64(at[l][dead], sh.dtype)), ("rejected rows attend", l)
     rows = np.concatenate([np.arange(r * wl.K, (r + 1) * wl.K) for r in ref.requests])
     got_h = f64(B.to_host(res["out_hidden"]), sh.dtype)[rows]
     hs = np.abs(ref.out_hidden).max()
