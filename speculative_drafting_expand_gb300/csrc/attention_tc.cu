@@ -362,13 +362,15 @@ __global__ void __launch_bounds__(192, 1)
                 __floats2bfloat162_rn(o[j] * inv, o[j + 1] * inv);
         }
       } else {
+        // partial [split][column][query row]: a warp's stores and loads of
+        // one column are contiguous
         const size_t unit = (static_cast<size_t>(r) * a.Hkv + g) * p.qtiles + qt;
         const size_t stride = static_cast<size_t>(128) * (DH + 2);
-        float* mine = p.part + (unit * p.max_splits + split) * stride + qrow * (DH + 2);
+        float* mine = p.part + (unit * p.max_splits + split) * stride + qrow;
 #pragma unroll
-        for (int j = 0; j < DH; ++j) mine[j] = o[j];
-        mine[DH] = m_used;
-        mine[DH + 1] = l;
+        for (int j = 0; j < DH; ++j) mine[j * 128] = o[j];
+        mine[DH * 128] = m_used;
+        mine[(DH + 1) * 128] = l;
         __threadfence();
         named_bar_sync(1, 128);
         if (threadIdx.x == 64) {
@@ -378,23 +380,32 @@ __global__ void __launch_bounds__(192, 1)
         named_bar_sync(1, 128);
         if (*flag) {
           __threadfence();
+          const float* base = p.part + unit * p.max_splits * stride + qrow;
           float M = -INFINITY;
-          for (int s = 0; s < nsplits; ++s) {
-            const float* src = p.part + (unit * p.max_splits + s) * stride + qrow * (DH + 2);
-            if (__ldcg(src + DH + 1) > 0.f) M = fmaxf(M, __ldcg(src + DH));
+          for (int s0 = 0; s0 < nsplits; s0 += 8) {
+            float ms[8], ls[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const bool in = s0 + q < nsplits;
+              ms[q] = in ? __ldcg(base + (s0 + q) * stride + DH * 128) : -INFINITY;
+              ls[q] = in ? __ldcg(base + (s0 + q) * stride + (DH + 1) * 128) : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if (ls[q] > 0.f) M = fmaxf(M, ms[q]);
           }
           float acc[DH];
 #pragma unroll
           for (int j = 0; j < DH; ++j) acc[j] = 0.f;
           float L = 0.f;
           for (int s = 0; s < nsplits; ++s) {
-            const float* src = p.part + (unit * p.max_splits + s) * stride + qrow * (DH + 2);
-            const float ls = __ldcg(src + DH + 1);
+            const float* src = base + s * stride;
+            const float ls = __ldcg(src + (DH + 1) * 128);
             if (!(ls > 0.f)) continue;
-            const float w = exp2f(__ldcg(src + DH) - M);
+            const float w = exp2f(__ldcg(src + DH * 128) - M);
             L += w * ls;
 #pragma unroll
-            for (int j = 0; j < DH; ++j) acc[j] += w * __ldcg(src + j);
+            for (int j = 0; j < DH; ++j) acc[j] += w * __ldcg(src + j * 128);
           }
           if (in_tile) {
             const float inv = L > 0.f ? 1.f / L : 0.f;

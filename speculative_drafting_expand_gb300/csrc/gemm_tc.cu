@@ -43,7 +43,11 @@ struct TcCfg {
                                    : TMEM_RAW <= 128 ? 128
                                    : TMEM_RAW <= 256 ? 256
                                                      : 512;
-  static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
+  // Narrow token tiles (a few rows, weight streaming) keep the CTA near
+  // 100 KB of shared memory so that the next projection's CTA fits on the
+  // same SM and prefetches its weights while this one drains.
+  static constexpr int SMEM_BUDGET = BN <= 32 ? 104 * 1024 : 200 * 1024;
+  static constexpr int STAGES_RAW = SMEM_BUDGET / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
@@ -326,13 +330,29 @@ __global__ void __launch_bounds__(192, 1)
             float v[16], v2[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = v2[j] = 0.f;
-            for (int c = c_first; c <= c_last; ++c) {
-              const int cs = unit_lo(c, U, G) >= static_cast<long long>(tile) * kb ? 0 : 1;
-              const float* src = p.ws + (static_cast<size_t>(c) * 2 + cs) * (128 * C::ACC_COLS);
+            // contributors in order; four at a time so their loads overlap
+            for (int c = c_first; c <= c_last; c += 4) {
+              float t[4][16], t2[4][DUAL ? 16 : 1];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                v[j] += __ldcg(src + (c0 + j) * 128 + row);
-                if (DUAL) v2[j] += __ldcg(src + (BN + c0 + j) * 128 + row);
+              for (int q = 0; q < 4; ++q) {
+                if (c + q > c_last) break;
+                const int cq = c + q;
+                const int cs = unit_lo(cq, U, G) >= static_cast<long long>(tile) * kb ? 0 : 1;
+                const float* src = p.ws + (static_cast<size_t>(cq) * 2 + cs) * (128 * C::ACC_COLS);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  t[q][j] = __ldcg(src + (c0 + j) * 128 + row);
+                  if (DUAL) t2[q][j] = __ldcg(src + (BN + c0 + j) * 128 + row);
+                }
+              }
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                if (c + q > c_last) break;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  v[j] += t[q][j];
+                  if (DUAL) v2[j] += t2[q][j];
+                }
               }
             }
             epi_chunk<DUAL>(p.epi, o, m * BN + c0, v, v2, lane);

@@ -27,7 +27,10 @@ __device__ __forceinline__ void record_error(int* err, int code) {
 // ---------------------------------------------------------------------------
 // programmatic dependent launch.  Every kernel calls grid_dep_wait() before it
 // touches data written by earlier kernels (and in any case before it exits),
-// so completion stays transitive along the stream.
+// so completion stays transitive along the stream.  Kernels without tensor
+// memory trigger their dependents first thing; kernels that allocate tensor
+// memory trigger only after the allocation, so a dependent that holds TMEM
+// can never be waiting for a predecessor that still has to allocate.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void grid_dep_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
