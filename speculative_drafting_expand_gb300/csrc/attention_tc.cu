@@ -55,7 +55,7 @@ struct AttnCfg {
 };
 
 template <int DH>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(192, DH == 64 ? 2 : 1)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const AttnTcParams p) {
   using C = AttnCfg<DH>;

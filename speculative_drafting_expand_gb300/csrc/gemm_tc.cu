@@ -131,8 +131,10 @@ __device__ __forceinline__ void epi_chunk(const EpiArgs& e, int o, int t0, const
   }
 }
 
+// Two CTAs per SM (at most 170 registers a thread): the next kernel's CTA
+// can start on an SM while this one drains.
 template <int BN, bool DUAL>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(192, 2)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                    const __grid_constant__ CUtensorMap tmB, const TcParams p) {
   using C = TcCfg<BN, DUAL>;
@@ -331,10 +333,11 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = v2[j] = 0.f;
             // contributors in order; four at a time so their loads overlap
-            for (int c = c_first; c <= c_last; c += 4) {
-              float t[4][16], t2[4][DUAL ? 16 : 1];
+            constexpr int UNR = DUAL ? 2 : 4;
+            for (int c = c_first; c <= c_last; c += UNR) {
+              float t[UNR][16], t2[UNR][DUAL ? 16 : 1];
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
+              for (int q = 0; q < UNR; ++q) {
                 if (c + q > c_last) break;
                 const int cq = c + q;
                 const int cs = unit_lo(cq, U, G) >= static_cast<long long>(tile) * kb ? 0 : 1;
@@ -346,7 +349,7 @@ __global__ void __launch_bounds__(192, 1)
                 }
               }
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
+              for (int q = 0; q < UNR; ++q) {
                 if (c + q > c_last) break;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
