@@ -236,6 +236,24 @@ pe_status pe_set_trace(pe_handle* h, float* residual_trace, void* attn_trace);
 pe_status pe_linear(pe_handle* h, const void* x, const void* w, float* y,
                     int32_t M, int32_t N, int32_t K, void* stream);
 
+/* y[M, N] = x[M, K] . w[N, K]^T in bf16 on the tensor cores (fp32 out),
+ * without a handle and without allocating anything.  The P-EAGLE pages have
+ * no counterpart: this is for callers that may not call cudaMalloc -- code
+ * running inside an allocator or memory-pool callback, under a framework
+ * that owns every byte of device memory, or on a path that must never enter
+ * the driver's allocator.  x [M, K] and w [N, K] are 16-byte-aligned bf16,
+ * y [M, N] fp32, all caller-owned device memory; K % 8 == 0.
+ * The split-K scratch is one static device array of about 4 MiB, reserved
+ * on every GPU that loads the library until the process exits; it bounds
+ * M <= 32 and N <= 4096 * 128, and larger sizes return PE_ERR_UNSUPPORTED
+ * before launching anything.  The first call on a device looks up the
+ * array's device address and prepares the kernels for that device; make
+ * that first call before any stream capture.  All calls share the array,
+ * so calls that overlap on the GPU race on it and must be serialised by the
+ * caller.  Asynchronous on `stream`. */
+pe_status pe_linear_static(const void* x, const void* w, float* y, int32_t M,
+                           int32_t N, int32_t K, void* stream);
+
 /* Number of kernels this handle has launched since pe_create (host-side
  * count, incremented per launch, including launches captured into a CUDA
  * graph).  A diagnostic for counting the kernels of one step. */

@@ -28,7 +28,7 @@ PE_DTYPE_F32 = 1
 
 EXPORTED = ("pe_create", "pe_destroy", "pe_expand_batch", "pe_draft_forward",
             "pe_lmhead_argmax", "pe_get_device_error", "pe_set_trace", "pe_linear",
-            "pe_get_launch_count", "pe_status_string")
+            "pe_get_launch_count", "pe_linear_static", "pe_status_string")
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -80,6 +80,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pe_set_trace.argtypes = [_vp, _vp, _vp]
     lib.pe_linear.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp]
     lib.pe_get_launch_count.argtypes = [_vp, P(ctypes.c_int64)]
+    lib.pe_linear_static.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _vp]
     lib.pe_status_string.argtypes = [_i32]
     lib.pe_status_string.restype = ctypes.c_char_p
     for name in EXPORTED[:-1]:
@@ -270,4 +271,14 @@ def pe_linear(dr: Drafter, x, w, y, stream=None):
     N = w.shape[0]
     _check("pe_linear", lib().pe_linear(dr.handle, ptr(x), ptr(w), ptr(y), M, N, K,
                                         stream_ptr(stream)))
+    return y
+
+
+def pe_linear_static(x, w, y, stream=None):
+    """y = x w^T (bf16 in, fp32 out) through the entry point that allocates
+    nothing: its scratch is a static device array inside the library."""
+    M, K = x.shape
+    N = w.shape[0]
+    _check("pe_linear_static", lib().pe_linear_static(ptr(x), ptr(w), ptr(y), M, N, K,
+                                                      stream_ptr(stream)))
     return y
