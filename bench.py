@@ -94,6 +94,31 @@ def step_work(wl, inp):
                 lm_head_flops=2.0 * wl.B * wl.K * V * d, valid_rows=valid, rows=rows)
 
 
+def kernel_source_hash() -> str:
+    """Hash of the GEMM kernel's sources: a recorded DRAM-traffic figure is
+    only reported while the kernel it was measured on is unchanged."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("gemm_tc.cu", "pe_common.cuh"):
+        with open(os.path.join(ROOT, "speculative_drafting_expand_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload_name: str):
+    """dram bytes read + written per launch from profiles/traffic.txt
+    (lines: kernel workload source-hash bytes), or None."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = kernel_source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) == 4 and parts[0] == kernel and parts[1] == workload_name and parts[2] == src:
+            return float(parts[3])
+    return None
+
+
 # ---------------------------------------------------------------------------
 # clocks sampled while the timed region runs
 # ---------------------------------------------------------------------------
@@ -355,12 +380,7 @@ def run_ours(args, world, rank, local):
     pk, pk_kind = peaks()
     hbm = float(pk["hbm_gbs"])
     achieved = work["lm_head_bytes"] / lm_avg_s / 1e9
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "lm_head_traffic.json")
-    if os.path.exists(prof):
-        t = json.load(open(prof))
-        if t.get("workload") == wl.name:
-            traffic = t.get("traffic_bytes_per_launch")
+    traffic = measured_traffic("gemm_tc_kernel", wl.name)
 
     # ---- end to end through the public calls with host buffers -------------
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
