@@ -14,13 +14,16 @@
 // (the request's rows x the g-th group of q heads -- GQA packs the group
 // into the MMA's M side), and one split of the key range.  Per 128-key chunk:
 //   S = Q K^T      (tcgen05, M=128 queries, N=128 keys, K=dh)
-//   P = softmax    (4 warps, one query row per thread; max kept lazily and
-//                   O rescaled in TMEM only when the running max grows by
-//                   more than 2^8)
-//   O += P V       (tcgen05, M=128, N=64 per half of dh, K=128 keys)
-// K and V pages come by TMA (16 keys x 64 dims per copy, 128-byte swizzle)
-// into a 2-stage ring.  Splits of one (r, g, tile) are merged by the CTA that
-// finishes last, in split order (deterministic).
+//   P = softmax    (8 warps: each query row is served by two threads, one per
+//                   64-key half of the chunk; each half keeps its own running
+//                   max (rescaling its O in TMEM only when the max grows past
+//                   2^8), its own sum and its own O, combined once at the end)
+//   O_h += P_h V_h (tcgen05, M=128, N=64 per half of dh, K=64 keys)
+// S of the next chunk is computed while this chunk's softmax runs; P is
+// double-buffered.  K and V pages come by TMA (16 keys x 64 dims per copy,
+// 128-byte swizzle) into a 3-stage ring (2 for dh=128).  Splits of one
+// (r, g, tile) are merged by the CTA that finishes last, in split order
+// (deterministic).
 #include "pe_common.cuh"
 #include "pe_kernels.h"
 
@@ -40,22 +43,29 @@ struct AttnTcParams {
 
 template <int DH>
 struct AttnCfg {
-  static constexpr int NH = DH / 64;          // 64-wide halves of the head dim
-  static constexpr int KEYS = 128;            // keys per chunk
-  static constexpr int TILE_BYTES = 128 * 128;  // 128 rows x 128 B
+  static constexpr int NH = DH / 64;            // 64-wide halves of the head dim
+  static constexpr int KEYS = 128;              // keys per chunk (two 64-key halves)
+  static constexpr int TILE = 128 * 128;        // 128 rows x 128 B
+  static constexpr int KV_STAGES = DH == 64 ? 3 : 2;
   static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + NH * TILE_BYTES;          // [2 stages][NH]
-  static constexpr int V_OFF = K_OFF + 2 * NH * TILE_BYTES;      // [2 stages][NH]
-  static constexpr int P_OFF = V_OFF + 2 * NH * TILE_BYTES;      // [2 key halves]
-  static constexpr int BAR_OFF = P_OFF + 2 * TILE_BYTES;
+  static constexpr int K_OFF = Q_OFF + NH * TILE;                 // [stage][NH]
+  static constexpr int V_OFF = K_OFF + KV_STAGES * NH * TILE;     // [stage][NH]
+  static constexpr int P_OFF = V_OFF + KV_STAGES * NH * TILE;     // [buffer][key half]
+  // float[4][128] for combining the two halves; used only after the last
+  // P.V has finished reading P, so it shares P's space
+  static constexpr int RED_OFF = P_OFF;
+  static constexpr int BAR_OFF = P_OFF + 4 * TILE;
   static constexpr int SMEM = 1024 + BAR_OFF + 256;
-  static constexpr int TMEM_COLS = 256;       // S: 0..127, O: 128..128+DH
+  // TMEM: S at columns 0..127; O of key half h at 128 + h * DH
+  static constexpr int TMEM_COLS = 128 + 2 * DH <= 256 ? 256 : 512;
+  static constexpr int THREADS = 320;           // producer, MMA, 8 softmax warps
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128);
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32_bmn(128, 64);
+  static_assert(SMEM <= 232448, "shared memory");
 };
 
 template <int DH>
-__global__ void __launch_bounds__(192, DH == 64 ? 2 : 1)
+__global__ void __launch_bounds__(320, 1)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const AttnTcParams p) {
   using C = AttnCfg<DH>;
@@ -63,17 +73,18 @@ __global__ void __launch_bounds__(192, DH == 64 ? 2 : 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-  uint64_t* kv_full = bars;        // [2]
-  uint64_t* kv_empty = bars + 2;   // [2]
-  uint64_t* q_ready = bars + 4;
-  uint64_t* s_full = bars + 5;
-  uint64_t* s_free = bars + 6;
-  uint64_t* p_full = bars + 7;
-  uint64_t* pv_done = bars + 8;
-  uint64_t* drain = bars + 9;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  uint64_t* kv_full = bars;                       // [KV_STAGES]
+  uint64_t* kv_empty = bars + C::KV_STAGES;       // [KV_STAGES]
+  uint64_t* q_ready = bars + 2 * C::KV_STAGES;
+  uint64_t* s_full = q_ready + 1;
+  uint64_t* s_free = q_ready + 2;
+  uint64_t* p_full = q_ready + 3;
+  uint64_t* pv_done = q_ready + 4;                // [2]: one per P buffer
+  uint64_t* drain = q_ready + 6;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 7);
   volatile int* flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* ok_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
 
   const AttnArgs& a = p.a;
   const int split = blockIdx.x;
@@ -104,16 +115,18 @@ __global__ void __launch_bounds__(192, DH == 64 ? 2 : 1)
   const int nchunks = (key1 - key0 + C::KEYS - 1) / C::KEYS;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::KV_STAGES; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
     mbar_init(q_ready, 1);
     mbar_init(s_full, 1);
-    mbar_init(s_free, 128);
-    mbar_init(p_full, 128);
-    mbar_init(pv_done, 1);
+    mbar_init(s_free, 256);
+    mbar_init(p_full, 256);
+    mbar_init(&pv_done[0], 1);
+    mbar_init(&pv_done[1], 1);
     mbar_init(drain, 1);
+    *abort_flag = 0;
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -134,8 +147,9 @@ __global__ void __launch_bounds__(192, DH == 64 ? 2 : 1)
       const uint64_t pol = l2_policy_evict_first();
       const int32_t* bt = a.block_table + static_cast<size_t>(r) * a.bt_stride;
       for (int c = 0; c < nchunks; ++c) {
-        const int st = c & 1;
-        if (c >= 2 && !mbar_wait(&kv_empty[st], ((c >> 1) - 1) & 1, a.err)) break;
+        const int st = c % C::KV_STAGES;
+        const int round = c / C::KV_STAGES;
+        if (round > 0 && !mbar_wait(&kv_empty[st], (round - 1) & 1, a.err)) break;
         const int t0 = key0 + c * C::KEYS;
         int blks[8];
         uint32_t bytes = 0;
@@ -159,110 +173,124 @@ __global__ void __launch_bounds__(192, DH == 64 ? 2 : 1)
           const int row = (blks[pg] * a.Hkv + g) * 16;
 #pragma unroll
           for (int h = 0; h < C::NH; ++h) {
-            uint8_t* kd = smem + C::K_OFF + (st * C::NH + h) * C::TILE_BYTES + pg * 2048;
-            uint8_t* vd = smem + C::V_OFF + (st * C::NH + h) * C::TILE_BYTES + pg * 2048;
+            uint8_t* kd = smem + C::K_OFF + (st * C::NH + h) * C::TILE + pg * 2048;
+            uint8_t* vd = smem + C::V_OFF + (st * C::NH + h) * C::TILE + pg * 2048;
             tma_load_2d(kd, &tmK, &kv_full[st], h * 64, row, pol);
             tma_load_2d(vd, &tmV, &kv_full[st], h * 64, row, pol);
           }
         }
       }
       // drain: the copies of the last stages have landed before exit
-      for (int c = max(0, nchunks - 2); c < nchunks; ++c)
-        mbar_wait(&kv_full[c & 1], (c >> 1) & 1, a.err);
+      for (int c = max(0, nchunks - C::KV_STAGES); c < nchunks; ++c)
+        mbar_wait(&kv_full[c % C::KV_STAGES], (c / C::KV_STAGES) & 1, a.err);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t s_tm = tmem, o_tm = tmem + 128;
-      bool ok = mbar_wait(q_ready, 0, a.err);
       const uint32_t q_addr = smem_u32(smem + C::Q_OFF);
-      const uint32_t p_addr = smem_u32(smem + C::P_OFF);
-      for (int c = 0; c < nchunks && ok; ++c) {
-        const int st = c & 1;
-        if (!mbar_wait(&kv_full[st], (c >> 1) & 1, a.err)) break;
-        if (c > 0 && !mbar_wait(s_free, (c - 1) & 1, a.err)) break;
+      // S(c) = Q K(c)^T into TMEM columns 0..127
+      auto issue_s = [&](int c) -> bool {
+        const int st = c % C::KV_STAGES;
+        if (!mbar_wait(&kv_full[st], (c / C::KV_STAGES) & 1, a.err)) return false;
+        if (c > 0 && !mbar_wait(s_free, (c - 1) & 1, a.err)) return false;
         tc_fence_after();
-        const uint32_t k_addr = smem_u32(smem + C::K_OFF + st * C::NH * C::TILE_BYTES);
+        const uint32_t k_addr = smem_u32(smem + C::K_OFF + st * C::NH * C::TILE);
 #pragma unroll
         for (int h = 0; h < C::NH; ++h)
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4)
-            umma_bf16(s_tm, sw128_kmajor_desc(q_addr + h * C::TILE_BYTES + k4 * 32),
-                      sw128_kmajor_desc(k_addr + h * C::TILE_BYTES + k4 * 32), C::IDESC_S,
+            umma_bf16(tmem, sw128_kmajor_desc(q_addr + h * C::TILE + k4 * 32),
+                      sw128_kmajor_desc(k_addr + h * C::TILE + k4 * 32), C::IDESC_S,
                       (h | k4) != 0);
         umma_commit(s_full);
+        return true;
+      };
+      bool ok = mbar_wait(q_ready, 0, a.err) && issue_s(0);
+      for (int c = 0; c < nchunks && ok; ++c) {
+        // the next chunk's scores are computed while this chunk's softmax runs
+        if (c + 1 < nchunks && !issue_s(c + 1)) break;
         if (!mbar_wait(p_full, c & 1, a.err)) break;
         tc_fence_after();
-        const uint32_t v_addr = smem_u32(smem + C::V_OFF + st * C::NH * C::TILE_BYTES);
+        const int st = c % C::KV_STAGES;
+        const uint32_t v_addr = smem_u32(smem + C::V_OFF + st * C::NH * C::TILE);
+        const uint32_t p_addr = smem_u32(smem + C::P_OFF + (c & 1) * 2 * C::TILE);
+        // O_h += P(keys of half h) V(keys of half h), per 64-wide half of dh
 #pragma unroll
-        for (int kh = 0; kh < 2; ++kh)      // 64-key halves of the chunk
+        for (int kh = 0; kh < 2; ++kh)
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
-            const uint64_t adesc = sw128_kmajor_desc(p_addr + kh * C::TILE_BYTES + k4 * 32);
+            const uint64_t adesc = sw128_kmajor_desc(p_addr + kh * C::TILE + k4 * 32);
 #pragma unroll
-            for (int h = 0; h < C::NH; ++h)
-              umma_bf16(o_tm + h * 64,  adesc,
-                        sw128_mnmajor_desc(v_addr + h * C::TILE_BYTES + (kh * 64 + k4 * 16) * 128),
-                        C::IDESC_PV, (c > 0 || kh > 0 || k4 > 0) ? 1u : 0u);
+            for (int j = 0; j < C::NH; ++j)
+              umma_bf16(tmem + 128 + kh * DH + j * 64, adesc,
+                        sw128_mnmajor_desc(v_addr + j * C::TILE + (kh * 64 + k4 * 16) * 128),
+                        C::IDESC_PV, (c > 0 || k4 > 0) ? 1u : 0u);
           }
         umma_commit(&kv_empty[st]);
-        umma_commit(pv_done);
+        umma_commit(&pv_done[c & 1]);
       }
       umma_commit(drain);
       mbar_wait(drain, 0, a.err);
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int qrow = 32 * (warp & 3) + lane;        // TMEM lane of this thread
+    // two warps per TMEM lane quarter: half h takes keys h*64..h*64+63 of
+    // every chunk and runs its own online softmax into its own O
+    const int qrow = 32 * (warp & 3) + lane;
+    const int h = (warp - 2) >> 2;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const int lr = qrow / p.G, hl = qrow % p.G;
     const bool in_tile = lr < tile_rows;
     const int row = row0 + tile_row0 + lr;          // expanded row
     const int head = g * p.G + hl;
-    bool valid = false;
-    int P = -1;
-    if (in_tile) {
-      valid = a.is_rejected[row] == 0;
-      if (valid) P = a.pos[row];
-    }
-    // Q row -> shared memory (128-byte swizzle, zero for padding / rejected)
+    int P = -1;                                     // last key this row reads
+    if (in_tile && a.is_rejected[row] == 0) P = a.pos[row];
+    // Q -> shared memory (128-byte swizzle; zero for padding / rejected rows)
     {
       const uint4* src = reinterpret_cast<const uint4*>(
           static_cast<const bf16*>(a.q) + (static_cast<size_t>(row) * a.Hq + head) * DH);
 #pragma unroll
-      for (int h = 0; h < C::NH; ++h)
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (valid) v = src[h * 8 + ch];
-          *reinterpret_cast<uint4*>(smem + C::Q_OFF + h * C::TILE_BYTES + qrow * 128 +
-                                    ((ch ^ (qrow & 7)) * 16)) = v;
-        }
+      for (int i = 0; i < 4 * C::NH; ++i) {
+        const int ch = h * 4 * C::NH + i;
+        const int tl = ch >> 3, cc = ch & 7;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (P >= 0) v = src[ch];
+        *reinterpret_cast<uint4*>(smem + C::Q_OFF + tl * C::TILE + qrow * 128 +
+                                  ((cc ^ (qrow & 7)) * 16)) = v;
+      }
     }
     fence_proxy_async_smem();
-    named_bar_sync(1, 128);
+    named_bar_sync(1, 256);
     if (threadIdx.x == 64) mbar_arrive(q_ready);
 
     const float sc = a.scale * 1.4426950408889634f;   // log2(e) / sqrt(dh)
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
+    const uint32_t o_col = 128 + h * DH;
     for (int c = 0; c < nchunks; ++c) {
-      if (threadIdx.x == 64) *ok_flag = mbar_wait(s_full, c & 1, a.err) ? 1 : 0;
-      named_bar_sync(1, 128);
-      if (!*ok_flag) { ok = false; break; }
+      if (!mbar_wait(s_full, c & 1, a.err)) { ok = false; break; }
       tc_fence_after();
-      const int t0 = key0 + c * C::KEYS;
-      // pass 1: masked maximum of the scaled scores
+      float sv[4][16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + h * 64 + q * 16, sv[q]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) reg_fence16(sv[q]);
+      const float* s = &sv[0][0];
+      tc_fence_before();
+      mbar_arrive(s_free);                          // S may be overwritten now
+      const int tb = key0 + c * C::KEYS + h * 64;   // first key of this half
+      const bool whole = tb + 63 <= P;              // no masking inside
       float mx = -INFINITY;
+      if (whole) {
 #pragma unroll
-      for (int c0 = 0; c0 < C::KEYS; c0 += 16) {
-        float s[16];
-        tmem_ld16(tmem + lane_off + c0, s);
-        tmem_ld_wait();
+        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, s[j]);
+      } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (t0 + c0 + j <= P) mx = fmaxf(mx, s[j] * sc);
+        for (int j = 0; j < 64; ++j)
+          if (tb + j <= P) mx = fmaxf(mx, s[j]);
       }
+      mx = mx * sc;                                 // sc > 0: scaling keeps the max
       // lazy rescale: keep the old reference unless the max grew past 2^8
       float m_new = m_used, factor = 1.f;
       if (mx > -INFINITY) {
@@ -272,116 +300,120 @@ __global__ void __launch_bounds__(192, DH == 64 ? 2 : 1)
           factor = exp2f(m_used - mx);
         }
       }
-      // pass 2: probabilities as bf16 (kept in registers until P is free)
-      uint32_t pk[64];
+      uint32_t pk[32];
       float psum = 0.f;
 #pragma unroll
-      for (int c0 = 0; c0 < C::KEYS; c0 += 16) {
-        float s[16];
-        tmem_ld16(tmem + lane_off + c0, s);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; j += 2) {
-          const float p0 = (t0 + c0 + j <= P) ? exp2f(s[j] * sc - m_new) : 0.f;
-          const float p1 = (t0 + c0 + j + 1 <= P) ? exp2f(s[j + 1] * sc - m_new) : 0.f;
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-          psum += __low2float(b2) + __high2float(b2);
-          pk[(c0 + j) / 2] = *reinterpret_cast<const uint32_t*>(&b2);
-        }
+      for (int j = 0; j < 64; j += 2) {
+        float p0 = 0.f, p1 = 0.f;
+        if (whole || tb + j <= P) p0 = exp2f(fmaf(s[j], sc, -m_new));
+        if (whole || tb + j + 1 <= P) p1 = exp2f(fmaf(s[j + 1], sc, -m_new));
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+        psum += __low2float(b2) + __high2float(b2);
+        pk[j / 2] = *reinterpret_cast<const uint32_t*>(&b2);
       }
-      tc_fence_before();
-      mbar_arrive(s_free);                         // S may be overwritten now
       l = l * factor + psum;
       m_used = m_new;
-      // wait until the previous P.V finished (P buffer and O are ours)
-      if (c > 0) {
-        if (threadIdx.x == 64) *ok_flag = mbar_wait(pv_done, (c - 1) & 1, a.err) ? 1 : 0;
-        named_bar_sync(1, 128);
-        if (!*ok_flag) { ok = false; break; }
+      // the P buffer of this chunk was last read by P.V two chunks ago
+      if (c >= 2 && !mbar_wait(&pv_done[c & 1], ((c - 2) >> 1) & 1, a.err)) { ok = false; break; }
+      // O must hold every earlier chunk before it is rescaled
+      if (c >= 1 && __any_sync(0xffffffffu, factor != 1.f)) {
+        if (!mbar_wait(&pv_done[(c - 1) & 1], ((c - 1) >> 1) & 1, a.err)) { ok = false; break; }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, factor != 1.f)) {
 #pragma unroll
-          for (int c0 = 0; c0 < DH; c0 += 16) {
-            float o[16];
-            tmem_ld16(tmem + lane_off + 128 + c0, o);
-            tmem_ld_wait();
+        for (int c0 = 0; c0 < DH; c0 += 16) {
+          float o[16];
+          tmem_ld16(tmem + lane_off + o_col + c0, o);
+          tmem_ld_wait();
+          reg_fence16(o);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) o[j] *= factor;
-            tmem_st16(tmem + lane_off + 128 + c0, o);
-          }
-          tmem_st_wait();
+          for (int j = 0; j < 16; ++j) o[j] *= factor;
+          tmem_st16(tmem + lane_off + o_col + c0, o);
         }
+        tmem_st_wait();
       }
-      // P row -> shared memory: keys 0..63 in the first tile, 64..127 in the second
+      // P row of this half -> its 64-key tile of the chunk's P buffer
+      uint8_t* pt = smem + C::P_OFF + ((c & 1) * 2 + h) * C::TILE + qrow * 128;
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        const int kh = ch >> 3, cc = ch & 7;
-        *reinterpret_cast<uint4*>(smem + C::P_OFF + kh * C::TILE_BYTES + qrow * 128 +
-                                  ((cc ^ (qrow & 7)) * 16)) =
-            make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-      }
+      for (int cc = 0; cc < 8; ++cc)
+        *reinterpret_cast<uint4*>(pt + ((cc ^ (qrow & 7)) * 16)) =
+            make_uint4(pk[cc * 4], pk[cc * 4 + 1], pk[cc * 4 + 2], pk[cc * 4 + 3]);
       // keys past the sequence end: zero their V rows so 0 * garbage cannot
       // reach O (the pool may hold anything there)
-      if (t0 + C::KEYS > key1 && t0 + qrow >= key1) {
-        const int st = c & 1;
+      const int t0 = key0 + c * C::KEYS;
+      if (h == 0 && t0 + C::KEYS > key1 && t0 + qrow >= key1) {
+        const int st = c % C::KV_STAGES;
 #pragma unroll
-        for (int h = 0; h < C::NH; ++h) {
-          uint4* vr = reinterpret_cast<uint4*>(smem + C::V_OFF + (st * C::NH + h) * C::TILE_BYTES +
+        for (int j = 0; j < C::NH; ++j) {
+          uint4* vr = reinterpret_cast<uint4*>(smem + C::V_OFF + (st * C::NH + j) * C::TILE +
                                                qrow * 128);
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) vr[ch] = make_uint4(0, 0, 0, 0);
+          for (int cc = 0; cc < 8; ++cc) vr[cc] = make_uint4(0, 0, 0, 0);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(p_full);
     }
-    if (ok) {
-      if (threadIdx.x == 64) *ok_flag = mbar_wait(pv_done, (nchunks - 1) & 1, a.err) ? 1 : 0;
-      named_bar_sync(1, 128);
-      ok = *ok_flag != 0;
-    }
-    if (ok) {
+    if (ok && !mbar_wait(&pv_done[(nchunks - 1) & 1], ((nchunks - 1) >> 1) & 1, a.err)) ok = false;
+    if (!ok) *abort_flag = 1;
+    // combine the two halves: (m, l) through shared memory
+    red[h * 128 + qrow] = m_used;
+    red[(2 + h) * 128 + qrow] = l;
+    named_bar_sync(1, 256);
+    if (!*abort_flag) {
       tc_fence_after();
-      float o[DH];
+      const float m0 = red[qrow], m1 = red[128 + qrow];
+      const float l0 = red[256 + qrow], l1 = red[384 + qrow];
+      const float M = fmaxf(m0, m1);
+      const float w0 = m0 > -INFINITY ? exp2f(m0 - M) : 0.f;
+      const float w1 = m1 > -INFINITY ? exp2f(m1 - M) : 0.f;
+      const float L = l0 * w0 + l1 * w1;
+      // this thread finishes columns h*DH/2 .. h*DH/2 + DH/2 of its row
+      constexpr int HC = DH / 2;
+      float o[HC];
 #pragma unroll
-      for (int c0 = 0; c0 < DH; c0 += 16) {
-        float t[16];
-        tmem_ld16(tmem + lane_off + 128 + c0, t);
+      for (int c0 = 0; c0 < HC; c0 += 16) {
+        float x0[16], x1[16];
+        tmem_ld16(tmem + lane_off + 128 + h * HC + c0, x0);
+        tmem_ld16(tmem + lane_off + 128 + DH + h * HC + c0, x1);
         tmem_ld_wait();
+        reg_fence16(x0);
+        reg_fence16(x1);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) o[c0 + j] = t[j];
+        for (int j = 0; j < 16; ++j) o[c0 + j] = x0[j] * w0 + x1[j] * w1;
       }
-      bf16* out = static_cast<bf16*>(a.out) + (static_cast<size_t>(row) * a.Hq + head) * DH;
+      bf16* out = static_cast<bf16*>(a.out) + (static_cast<size_t>(row) * a.Hq + head) * DH + h * HC;
       if (nsplits == 1) {
         if (in_tile) {
-          const float inv = l > 0.f ? 1.f / l : 0.f;
+          const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-          for (int j = 0; j < DH; j += 2)
+          for (int j = 0; j < HC; j += 2)
             *reinterpret_cast<__nv_bfloat162*>(out + j) =
                 __floats2bfloat162_rn(o[j] * inv, o[j + 1] * inv);
         }
       } else {
-        // partial [split][column][query row]: a warp's stores and loads of
-        // one column are contiguous
+        // partial [split][column][query row]: a warp's accesses of one column
+        // are contiguous
         const size_t unit = (static_cast<size_t>(r) * a.Hkv + g) * p.qtiles + qt;
         const size_t stride = static_cast<size_t>(128) * (DH + 2);
         float* mine = p.part + (unit * p.max_splits + split) * stride + qrow;
 #pragma unroll
-        for (int j = 0; j < DH; ++j) mine[j * 128] = o[j];
-        mine[DH * 128] = m_used;
-        mine[(DH + 1) * 128] = l;
+        for (int j = 0; j < HC; ++j) mine[(h * HC + j) * 128] = o[j];
+        if (h == 0) {
+          mine[DH * 128] = M;
+          mine[(DH + 1) * 128] = L;
+        }
         __threadfence();
-        named_bar_sync(1, 128);
+        named_bar_sync(1, 256);
         if (threadIdx.x == 64) {
           const int old = atomicAdd(p.counters + unit, 1);
           *flag = (old == nsplits - 1) ? 1 : 0;
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, 256);
         if (*flag) {
           __threadfence();
           const float* base = p.part + unit * p.max_splits * stride + qrow;
-          float M = -INFINITY;
+          float Mx = -INFINITY;
           for (int s0 = 0; s0 < nsplits; s0 += 8) {
             float ms[8], ls[8];
 #pragma unroll
@@ -392,25 +424,25 @@ __global__ void __launch_bounds__(192, DH == 64 ? 2 : 1)
             }
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-              if (ls[q] > 0.f) M = fmaxf(M, ms[q]);
+              if (ls[q] > 0.f) Mx = fmaxf(Mx, ms[q]);
           }
-          float acc[DH];
+          float acc[HC];
 #pragma unroll
-          for (int j = 0; j < DH; ++j) acc[j] = 0.f;
-          float L = 0.f;
-          for (int s = 0; s < nsplits; ++s) {
-            const float* src = base + s * stride;
+          for (int j = 0; j < HC; ++j) acc[j] = 0.f;
+          float Ls = 0.f;
+          for (int s2 = 0; s2 < nsplits; ++s2) {
+            const float* src = base + s2 * stride;
             const float ls = __ldcg(src + (DH + 1) * 128);
             if (!(ls > 0.f)) continue;
-            const float w = exp2f(__ldcg(src + DH * 128) - M);
-            L += w * ls;
+            const float w = exp2f(__ldcg(src + DH * 128) - Mx);
+            Ls += w * ls;
 #pragma unroll
-            for (int j = 0; j < DH; ++j) acc[j] += w * __ldcg(src + j * 128);
+            for (int j = 0; j < HC; ++j) acc[j] += w * __ldcg(src + (h * HC + j) * 128);
           }
           if (in_tile) {
-            const float inv = L > 0.f ? 1.f / L : 0.f;
+            const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
 #pragma unroll
-            for (int j = 0; j < DH; j += 2)
+            for (int j = 0; j < HC; j += 2)
               *reinterpret_cast<__nv_bfloat162*>(out + j) =
                   __floats2bfloat162_rn(acc[j] * inv, acc[j + 1] * inv);
           }
@@ -492,8 +524,10 @@ cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const
     return cudaErrorInvalidValue;
   dim3 grid(pl.max_splits, a.Hkv * pl.qtiles, a.B);
   if (a.dh == 64)
-    return launch_pdl(attention_tc_kernel<64>, grid, dim3(192), AttnCfg<64>::SMEM, s, tmK, tmV, p);
-  return launch_pdl(attention_tc_kernel<128>, grid, dim3(192), AttnCfg<128>::SMEM, s, tmK, tmV, p);
+    return launch_pdl(attention_tc_kernel<64>, grid, dim3(AttnCfg<64>::THREADS),
+                      AttnCfg<64>::SMEM, s, tmK, tmV, p);
+  return launch_pdl(attention_tc_kernel<128>, grid, dim3(AttnCfg<128>::THREADS),
+                    AttnCfg<128>::SMEM, s, tmK, tmV, p);
 }
 
 }  // namespace pe

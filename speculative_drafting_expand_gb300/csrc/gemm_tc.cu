@@ -297,6 +297,8 @@ __global__ void __launch_bounds__(192, 2)
           tmem_ld16(taddr + c0, v);
           if (DUAL) tmem_ld16(taddr + BN + c0, v2);
           tmem_ld_wait();
+          reg_fence16(v);
+          if (DUAL) reg_fence16(v2);
           epi_chunk<DUAL>(p.epi, o, m * BN + c0, v, v2, lane);
         }
         tc_fence_before();
@@ -309,6 +311,8 @@ __global__ void __launch_bounds__(192, 2)
           tmem_ld16(taddr + c0, v);
           if (DUAL) tmem_ld16(taddr + BN + c0, v2);
           tmem_ld_wait();
+          reg_fence16(v);
+          if (DUAL) reg_fence16(v2);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             wsp[(c0 + j) * 128 + row] = v[j];
