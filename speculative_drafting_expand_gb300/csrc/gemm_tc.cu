@@ -64,6 +64,7 @@ struct TcParams {
   int* counters;
   int* done;
   int* err;
+  int split_s;  // 0: stream-K over all units; >= 1: S CTAs (one cluster) per tile
 };
 
 __device__ __forceinline__ long long unit_lo(int c, long long U, int G) {
@@ -182,7 +183,17 @@ __global__ void __launch_bounds__(192, 2)
 
   const long long U = p.units;
   const int G = gridDim.x, cta = blockIdx.x, kb = p.kb;
-  const long long lo = unit_lo(cta, U, G), hi = unit_lo(cta + 1, U, G);
+  long long lo, hi;
+  if (p.split_s >= 1) {
+    // cluster split: CTA s of the tile's cluster takes k-blocks
+    // [s kb / S, (s + 1) kb / S) of that one tile
+    const int S = p.split_s, tile = cta / S, sr = cta % S;
+    lo = static_cast<long long>(tile) * kb + (static_cast<long long>(sr) * kb) / S;
+    hi = static_cast<long long>(tile) * kb + (static_cast<long long>(sr + 1) * kb) / S;
+  } else {
+    lo = unit_lo(cta, U, G);
+    hi = unit_lo(cta + 1, U, G);
+  }
 
   if (warp == 4) {
     if (lane == 0) {
@@ -303,6 +314,26 @@ __global__ void __launch_bounds__(192, 2)
         }
         tc_fence_before();
         mbar_arrive(&acc_empty[acc]);
+      } else if (p.split_s >= 2) {
+        // cluster split: the partial goes to this CTA's own shared memory
+        // (the operand stages are all consumed); rank 0 sums the cluster's
+        // partials after the cluster barrier below
+        float* part = reinterpret_cast<float*>(smem);
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          float v[16], v2[16];
+          tmem_ld16(taddr + c0, v);
+          if (DUAL) tmem_ld16(taddr + BN + c0, v2);
+          tmem_ld_wait();
+          reg_fence16(v);
+          if (DUAL) reg_fence16(v2);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            part[(c0 + j) * 128 + row] = v[j];
+            if (DUAL) part[(BN + c0 + j) * 128 + row] = v2[j];
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&acc_empty[acc]);
       } else {
         const int slot = (u == lo) ? 0 : 1;
         float* wsp = p.ws + (static_cast<size_t>(cta) * 2 + slot) * (128 * C::ACC_COLS);
@@ -378,6 +409,33 @@ __global__ void __launch_bounds__(192, 2)
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
+  if (p.split_s >= 2) {
+    // every CTA of the cluster has its partial in shared memory; rank 0
+    // adds them in rank order (deterministic) and applies the epilogue
+    cluster_sync_all();
+    if (cluster_ctarank() == 0 && warp < 4) {
+      const int S = p.split_s, tile = cta / S;
+      const int f = tile / p.tiles_m, m = tile % p.tiles_m;
+      const int row = warp * 32 + lane;
+      const uint32_t base = smem_u32(smem);
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float v[16], v2[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = v2[j] = 0.f;
+        for (int rk = 0; rk < S; ++rk) {
+          const uint32_t rb = cluster_map_shared(base, rk);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            v[j] += ld_shared_cluster_f32(rb + ((c0 + j) * 128 + row) * 4);
+            if (DUAL) v2[j] += ld_shared_cluster_f32(rb + ((BN + c0 + j) * 128 + row) * 4);
+          }
+        }
+        epi_chunk<DUAL>(p.epi, f * 128 + row, m * BN + c0, v, v2, lane);
+      }
+    }
+    // peers keep their shared memory until rank 0 has read it
+    cluster_sync_all();
+  }
   if (p.epi.kind == EPI_ARGMAX) {
     // the last CTA turns the packed (value, index) keys into token ids
     if (threadIdx.x == 0) {
@@ -446,10 +504,33 @@ cudaError_t init_gemm_tc() {
   return e;
 }
 
+size_t tc_partial_floats(int grid, int bn, bool dual);
+
 template <int BN, bool DUAL>
 static cudaError_t run_tc(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
-                          const TcParams& p, int grid, cudaStream_t s) {
+                          TcParams p, int tiles, long long units, int sm_count,
+                          size_t partial_floats, cudaStream_t s) {
   using C = TcCfg<BN, DUAL>;
+  // Fewer tiles than SMs: split k across a cluster of S CTAs per tile and
+  // reduce through distributed shared memory.  Otherwise stream-K.
+  const bool fits = static_cast<size_t>(C::ACC_COLS) * 128 * 4 <=
+                    static_cast<size_t>(C::STAGES) * C::STAGE_BYTES;
+  // The whole grid must fit in one wave: two CTAs an SM when the stages fit
+  // in about half of the shared memory, otherwise one.
+  const int per_sm = C::SMEM <= 113 * 1024 ? 2 : 1;
+  int S = per_sm == 2 ? (sm_count + tiles / 2) / tiles : sm_count / std::max(1, tiles);
+  S = std::min(S, std::min(8, p.kb));
+  if (tiles < sm_count && fits && (S >= 2 || per_sm == 2) && S >= 1 &&
+      tiles * S <= per_sm * sm_count) {
+    p.split_s = S;
+    if (S == 1)
+      return launch_pdl(gemm_tc_kernel<BN, DUAL>, dim3(tiles), dim3(192), C::SMEM, s, a, a2, b, p);
+    return launch_pdl_cluster(gemm_tc_kernel<BN, DUAL>, dim3(tiles * S), dim3(192), C::SMEM, s, S,
+                              a, a2, b, p);
+  }
+  p.split_s = 0;
+  const int grid = static_cast<int>(std::min<long long>(sm_count, units));
+  if (tc_partial_floats(grid, BN, DUAL) > partial_floats) return cudaErrorInvalidValue;
   return launch_pdl(gemm_tc_kernel<BN, DUAL>, dim3(grid), dim3(192), C::SMEM, s, a, a2, b, p);
 }
 
@@ -484,13 +565,14 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
   p.counters = ws.tile_counters;
   p.done = ws.done_counter;
   p.err = err;
-  const int grid = static_cast<int>(std::min<long long>(ws.sm_count, p.units));
-  if (tiles_n * p.tiles_m > ws.max_tiles || tc_partial_floats(grid, bn, dual) > ws.partial_floats)
-    return cudaErrorInvalidValue;
-#define PE_TC_CASE(BNV)                                                  \
-  case BNV:                                                              \
-    return dual ? run_tc<BNV, true>(wa, wa2, xb, p, grid, s)             \
-                : run_tc<BNV, false>(wa, wa2, xb, p, grid, s);
+  const int tiles = tiles_n * p.tiles_m;
+  if (tiles > ws.max_tiles) return cudaErrorInvalidValue;
+#define PE_TC_CASE(BNV)                                                                       \
+  case BNV:                                                                                   \
+    return dual ? run_tc<BNV, true>(wa, wa2, xb, p, tiles, p.units, ws.sm_count,              \
+                                    ws.partial_floats, s)                                     \
+                : run_tc<BNV, false>(wa, wa2, xb, p, tiles, p.units, ws.sm_count,             \
+                                     ws.partial_floats, s);
   switch (bn) {
     PE_TC_CASE(16)
     PE_TC_CASE(32)

@@ -168,7 +168,17 @@ def full_parity(wl, tol, gains=None, requests=None, check_cache=True):
     ls = np.abs(ref.logits).max()
     assert np.abs(got_l - ref.logits).max() <= tol * ls, np.abs(got_l - ref.logits).max() / ls
     got_t = B.to_host(res["tokens"])[rows]
-    margin_ok_tokens(ref.logits, ref.tokens, got_t)
+    # End to end the logits may differ from the fp64 statement by up to
+    # tol x max|logit|, so a token is pinned wherever the oracle's top-2
+    # margin is more than twice that (for fp32 the stated 1e-2 margin).
+    margin_ok_tokens(ref.logits, ref.tokens, got_t, margin=max(1e-2, 2 * tol * ls))
+    # The argmax decision itself, taken in the same precision on both sides:
+    # the oracle's LM head on the GPU's own final hidden rows.  Logits agree
+    # to the GEMM's fp32 accumulation and tokens wherever the margin > 1e-3.
+    lm_logits, lm_tokens = O.lm_head_argmax(sh, w, f64(B.to_host(res["out_hidden"]), sh.dtype)[rows])
+    lm_err = np.abs(got_l - lm_logits).max()
+    assert lm_err <= 1e-4 * np.abs(lm_logits).max(), lm_err
+    margin_ok_tokens(lm_logits, lm_tokens, got_t, margin=1e-3)
     if check_cache and requests is None:
         check_kv(st, ref, sh, tol * 2)
     return res, ref, dr, st

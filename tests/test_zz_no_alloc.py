@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 
 def _reference_handle(max_tokens):
     shape = W.small_shape("static-ref", d=64, n_layers=1, n_heads=1, n_kv_heads=1,
-                          head_dim=64, ffn=64, vocab=8192)
+                          head_dim=64, ffn=64, vocab=32768)
     z = np.zeros(64, np.uint16)
     w = {k: z for k in ("emb", "fc", "norm_final", "lm_head")}
     w["h_shared"] = np.zeros(shape.hidden3, np.uint16)
@@ -30,7 +30,8 @@ def _reference_handle(max_tokens):
     return G.make_drafter(shape, w, max_tokens, 1)
 
 
-@pytest.mark.parametrize("M,N,K", [(14, 5120, 2880), (7, 2880, 8640), (32, 300, 200)])
+@pytest.mark.parametrize("M,N,K", [(14, 5120, 2880), (7, 2880, 8640), (32, 300, 200),
+                                   (7, 20480, 2880)])
 def test_static_entry_point_matches_pe_linear_twice(M, N, K):
     B = G.library()
     torch = G.torch_mod()
