@@ -14,7 +14,7 @@ drafts its own batch (requests are independent: weak scaling, no
 collective on the data path).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload b1|b64|qwen-k<K>|expand]
+                  [--workload b1|b16|b64|qwen-k<K>|expand]
 """
 
 from __future__ import annotations
@@ -46,6 +46,8 @@ def workload(name: str):
         return W.gpt_oss_b1()
     if name == "b64":
         return W.gpt_oss_b64()
+    if name == "b16":
+        return W.gpt_oss_b64(16)
     if name.startswith("qwen-k"):
         return W.qwen_b16(int(name[len("qwen-k"):]))
     if name == "expand":
@@ -283,6 +285,12 @@ def config_of(wl, args):
 # our arm
 # ---------------------------------------------------------------------------
 
+def check_device(B, dr):
+    code = B.pe_get_device_error(dr)
+    if code != 0:
+        raise SystemExit(f"device-side error code {code} recorded by the drafting kernels")
+
+
 class DeviceInputs:
     """One step's inputs and the paged KV pools, resident in HBM."""
 
@@ -329,7 +337,7 @@ def run_ours(args, world, rank, local):
     for _ in range(2):
         step()
     torch.cuda.synchronize()
-    assert B.pe_get_device_error(dr) == 0
+    check_device(B, dr)
     cap = torch.cuda.Stream()
     cap.wait_stream(torch.cuda.current_stream())
     g = torch.cuda.CUDAGraph()
@@ -362,7 +370,7 @@ def run_ours(args, world, rank, local):
     clocks.stop()
     ms_per_step = elapsed_ms / args.steps
     value = world * args.steps / (elapsed_ms / 1e3)
-    assert B.pe_get_device_error(dr) == 0
+    check_device(B, dr)
 
     # ---- dominant kernel: the LM-head GEMM + argmax, timed on its stream ----
     work = step_work(wl, inp)
@@ -414,7 +422,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(world, time.perf_counter() - t0)
     e2e_value = world * n_e2e / e2e_s
-    assert B.pe_get_device_error(dr) == 0
+    check_device(B, dr)
 
     # ---- CPU oracle baseline (rank 0, one GPU only) -------------------------
     cpu = None

@@ -12,8 +12,8 @@ namespace pe {
 
 template <typename T, int DH>
 __global__ void __launch_bounds__(128) attention_simt_kernel(const AttnArgs a) {
-  grid_dep_launch();
   grid_dep_wait();
+  grid_dep_launch();
   constexpr int E = DH / 32;  // elements per lane
   const int i = blockIdx.x;
   const int h = blockIdx.y * 4 + (threadIdx.x >> 5);

@@ -39,6 +39,7 @@ struct AttnTcParams {
   int max_splits;
   float* part;       // [B, Hkv, qtiles, max_splits, 128, dh + 2]
   int* counters;     // [B, Hkv, qtiles]
+  int cluster;       // 1: the splits of a unit are one cluster, merged through DSMEM
 };
 
 template <int DH>
@@ -78,10 +79,18 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* q_ready = bars + 2 * C::KV_STAGES;
   uint64_t* s_full = q_ready + 1;
   uint64_t* s_free = q_ready + 2;
+  // [2]: one per P buffer.  The softmax warps are only loosely coupled: a
+  // warp may finish chunk c + 1 while another still computes chunk c, so
+  // the arrivals of consecutive chunks must land on different barriers (on
+  // one shared barrier they would complete chunk c's phase early).  A warp
+  // reaches chunk c + 2 only after every warp has read S(c + 1), so two
+  // barriers suffice.
   uint64_t* p_full = q_ready + 3;
-  uint64_t* pv_done = q_ready + 4;                // [2]: one per P buffer
-  uint64_t* drain = q_ready + 6;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 7);
+  uint64_t* pv_done = q_ready + 5;                // [2]: one per P buffer
+  uint64_t* drain = q_ready + 7;
+  uint64_t* merge_ready = q_ready + 8;            // rank 0: one arrive per active peer
+  uint64_t* merge_done = q_ready + 9;             // peers: rank 0 has read their partial
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 10);
   volatile int* flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
   float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
@@ -122,10 +131,13 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(q_ready, 1);
     mbar_init(s_full, 1);
     mbar_init(s_free, 256);
-    mbar_init(p_full, 256);
+    mbar_init(&p_full[0], 256);
+    mbar_init(&p_full[1], 256);
     mbar_init(&pv_done[0], 1);
     mbar_init(&pv_done[1], 1);
     mbar_init(drain, 1);
+    mbar_init(merge_ready, nsplits > 1 ? nsplits - 1 : 1);
+    mbar_init(merge_done, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -209,7 +221,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int c = 0; c < nchunks && ok; ++c) {
         // the next chunk's scores are computed while this chunk's softmax runs
         if (c + 1 < nchunks && !issue_s(c + 1)) break;
-        if (!mbar_wait(p_full, c & 1, a.err)) break;
+        if (!mbar_wait(&p_full[c & 1], (c >> 1) & 1, a.err)) break;
         tc_fence_after();
         const int st = c % C::KV_STAGES;
         const uint32_t v_addr = smem_u32(smem + C::V_OFF + st * C::NH * C::TILE);
@@ -281,36 +293,53 @@ __global__ void __launch_bounds__(320, 1)
       mbar_arrive(s_free);                          // S may be overwritten now
       const int tb = key0 + c * C::KEYS + h * 64;   // first key of this half
       const bool whole = tb + 63 <= P;              // no masking inside
-      float mx = -INFINITY;
+      // masked maximum (four independent chains)
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (whole) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, s[j]);
+        for (int j = 0; j < 64; ++j) m4[j & 3] = fmaxf(m4[j & 3], s[j]);
       } else {
 #pragma unroll
         for (int j = 0; j < 64; ++j)
-          if (tb + j <= P) mx = fmaxf(mx, s[j]);
+          if (tb + j <= P) m4[j & 3] = fmaxf(m4[j & 3], s[j]);
       }
-      mx = mx * sc;                                 // sc > 0: scaling keeps the max
+      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sc;  // sc > 0
       // lazy rescale: keep the old reference unless the max grew past 2^8
       float m_new = m_used, factor = 1.f;
       if (mx > -INFINITY) {
         if (m_used == -INFINITY) m_new = mx;
         else if (mx > m_used + 8.f) {
           m_new = mx;
-          factor = exp2f(m_used - mx);
+          factor = fast_exp2(m_used - mx);
         }
       }
+      // probabilities: one FFMA and one MUFU.EX2 a score; the row sum is
+      // kept in fp32 (two chains), P goes to the MMA as bf16 pairs
       uint32_t pk[32];
-      float psum = 0.f;
+      float ps0 = 0.f, ps1 = 0.f;
+      const float nm = -m_new;
+      if (whole) {
 #pragma unroll
-      for (int j = 0; j < 64; j += 2) {
-        float p0 = 0.f, p1 = 0.f;
-        if (whole || tb + j <= P) p0 = exp2f(fmaf(s[j], sc, -m_new));
-        if (whole || tb + j + 1 <= P) p1 = exp2f(fmaf(s[j + 1], sc, -m_new));
-        const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-        psum += __low2float(b2) + __high2float(b2);
-        pk[j / 2] = *reinterpret_cast<const uint32_t*>(&b2);
+        for (int j = 0; j < 64; j += 2) {
+          const float p0 = fast_exp2(fmaf(s[j], sc, nm));
+          const float p1 = fast_exp2(fmaf(s[j + 1], sc, nm));
+          ps0 += p0;
+          ps1 += p1;
+          pk[j / 2] = pack_bf16x2(p0, p1);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 64; j += 2) {
+          const float e0 = fast_exp2(fmaf(s[j], sc, nm));
+          const float e1 = fast_exp2(fmaf(s[j + 1], sc, nm));
+          const float p0 = (tb + j <= P) ? e0 : 0.f;
+          const float p1 = (tb + j + 1 <= P) ? e1 : 0.f;
+          ps0 += p0;
+          ps1 += p1;
+          pk[j / 2] = pack_bf16x2(p0, p1);
+        }
       }
+      const float psum = ps0 + ps1;
       l = l * factor + psum;
       m_used = m_new;
       // the P buffer of this chunk was last read by P.V two chunks ago
@@ -352,7 +381,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[c & 1]);
     }
     if (ok && !mbar_wait(&pv_done[(nchunks - 1) & 1], ((nchunks - 1) >> 1) & 1, a.err)) ok = false;
     if (!ok) *abort_flag = 1;
@@ -390,6 +419,73 @@ __global__ void __launch_bounds__(320, 1)
           for (int j = 0; j < HC; j += 2)
             *reinterpret_cast<__nv_bfloat162*>(out + j) =
                 __floats2bfloat162_rn(o[j] * inv, o[j + 1] * inv);
+        }
+      } else if (p.cluster) {
+        // partial -> this CTA's shared memory (the K/V ring is drained);
+        // layout [column][query row], then (m, l)
+        float* mine = reinterpret_cast<float*>(smem + C::K_OFF);
+#pragma unroll
+        for (int j = 0; j < HC; ++j) mine[(h * HC + j) * 128 + qrow] = o[j];
+        if (h == 0) {
+          mine[DH * 128 + qrow] = M;
+          mine[(DH + 1) * 128 + qrow] = L;
+        }
+        named_bar_sync(1, 256);
+        if (split != 0) {
+          // hand the partial to rank 0, keep it until rank 0 has read it
+          if (threadIdx.x == 64) {
+            asm volatile("fence.acq_rel.cluster;" ::: "memory");
+            mbar_arrive_remote(cluster_map_shared(smem_u32(merge_ready), 0));
+            mbar_wait(merge_done, 0, a.err);
+          }
+          named_bar_sync(1, 256);
+        } else {
+          if (threadIdx.x == 64) *flag = mbar_wait_cluster(merge_ready, 0, a.err) ? 1 : 0;
+          named_bar_sync(1, 256);
+          if (*flag) {
+            // merge the splits in split order through distributed shared memory
+            const uint32_t base = smem_u32(smem + C::K_OFF);
+            float ms[8], ls[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              ms[q] = -INFINITY;
+              ls[q] = 0.f;
+              if (q < nsplits) {
+                const uint32_t rb = cluster_map_shared(base, q);
+                ms[q] = ld_shared_cluster_f32(rb + (DH * 128 + qrow) * 4);
+                ls[q] = ld_shared_cluster_f32(rb + ((DH + 1) * 128 + qrow) * 4);
+              }
+            }
+            float Mx = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if (ls[q] > 0.f) Mx = fmaxf(Mx, ms[q]);
+            float acc[HC];
+#pragma unroll
+            for (int j = 0; j < HC; ++j) acc[j] = 0.f;
+            float Ls = 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              if (q >= nsplits || !(ls[q] > 0.f)) continue;
+              const float w = exp2f(ms[q] - Mx);
+              Ls += w * ls[q];
+              const uint32_t rb = cluster_map_shared(base, q);
+#pragma unroll
+              for (int j = 0; j < HC; ++j)
+                acc[j] += w * ld_shared_cluster_f32(rb + ((h * HC + j) * 128 + qrow) * 4);
+            }
+            if (in_tile) {
+              const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll
+              for (int j = 0; j < HC; j += 2)
+                *reinterpret_cast<__nv_bfloat162*>(out + j) =
+                    __floats2bfloat162_rn(acc[j] * inv, acc[j + 1] * inv);
+            }
+          }
+          named_bar_sync(1, 256);
+          // release the peers
+          if (threadIdx.x >= 64 && threadIdx.x < 64 + nsplits - 1)
+            mbar_arrive_remote(cluster_map_shared(smem_u32(merge_done), threadIdx.x - 63));
         }
       } else {
         // partial [split][column][query row]: a warp's accesses of one column
@@ -430,14 +526,28 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int j = 0; j < HC; ++j) acc[j] = 0.f;
           float Ls = 0.f;
-          for (int s2 = 0; s2 < nsplits; ++s2) {
-            const float* src = base + s2 * stride;
-            const float ls = __ldcg(src + (DH + 1) * 128);
-            if (!(ls > 0.f)) continue;
-            const float w = exp2f(__ldcg(src + DH * 128) - Mx);
-            Ls += w * ls;
+          // QN splits at a time: their weights and columns are all loaded
+          // before any of them is added (in split order)
+          constexpr int QN = DH == 64 ? 2 : 1;   // splits loaded together
+          for (int s2 = 0; s2 < nsplits; s2 += QN) {
+            float wq[QN], lq[QN], col[QN][HC];
 #pragma unroll
-            for (int j = 0; j < HC; ++j) acc[j] += w * __ldcg(src + (h * HC + j) * 128);
+            for (int q = 0; q < QN; ++q) {
+              const bool in = s2 + q < nsplits;
+              const float* src = base + (s2 + q) * stride;
+              lq[q] = in ? __ldcg(src + (DH + 1) * 128) : 0.f;
+              wq[q] = in ? __ldcg(src + DH * 128) : -INFINITY;
+#pragma unroll
+              for (int j = 0; j < HC; ++j) col[q][j] = in ? __ldcg(src + (h * HC + j) * 128) : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < QN; ++q) {
+              if (!(lq[q] > 0.f)) continue;
+              const float w = exp2f(wq[q] - Mx);
+              Ls += w * lq[q];
+#pragma unroll
+              for (int j = 0; j < HC; ++j) acc[j] += w * col[q][j];
+            }
           }
           if (in_tile) {
             const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
@@ -464,7 +574,7 @@ __global__ void __launch_bounds__(320, 1)
 // ---------------------------------------------------------------------------
 
 struct AttnPlan {
-  int G, rows_per_qt, qtiles, split_keys, max_splits;
+  int G, rows_per_qt, qtiles, split_keys, max_splits, cluster;
 };
 
 static AttnPlan plan_attention(const AttnArgs& a, int max_rows_per_req, int sm_count) {
@@ -476,10 +586,21 @@ static AttnPlan plan_attention(const AttnArgs& a, int max_rows_per_req, int sm_c
   const int chunks_max = (max_seq + 127) / 128;
   const long long pairs = static_cast<long long>(a.B) * a.Hkv * pl.qtiles;
   const int want = static_cast<int>(std::max<long long>(1, (sm_count + pairs - 1) / pairs));
-  int cps = (chunks_max + want - 1) / want;
-  cps = std::max(2, std::min(16, cps));
-  pl.split_keys = cps * 128;
+  if (pairs < sm_count) {
+    // latency regime: at most 8 splits, one cluster per unit, DSMEM merge
+    pl.cluster = 1;
+    (void)want;
+    int cps = (chunks_max + 7) / 8;
+    cps = std::max(2, cps);
+    pl.split_keys = cps * 128;
+  } else {
+    pl.cluster = 0;
+    int cps = (chunks_max + want - 1) / want;
+    cps = std::max(2, std::min(16, cps));
+    pl.split_keys = cps * 128;
+  }
   pl.max_splits = (max_seq + pl.split_keys - 1) / pl.split_keys;
+  if (pl.max_splits < 2) pl.cluster = 0;
   return pl;
 }
 
@@ -519,10 +640,18 @@ cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const
   p.max_splits = pl.max_splits;
   p.part = part;
   p.counters = counters;
+  p.cluster = pl.cluster;
   const size_t need = static_cast<size_t>(a.B) * a.Hkv * pl.qtiles * pl.max_splits * 128 * (a.dh + 2);
   if (need > part_floats || static_cast<size_t>(a.B) * a.Hkv * pl.qtiles > n_counters)
     return cudaErrorInvalidValue;
   dim3 grid(pl.max_splits, a.Hkv * pl.qtiles, a.B);
+  if (pl.cluster) {
+    if (a.dh == 64)
+      return launch_pdl_cluster(attention_tc_kernel<64>, grid, dim3(AttnCfg<64>::THREADS),
+                                AttnCfg<64>::SMEM, s, pl.max_splits, tmK, tmV, p);
+    return launch_pdl_cluster(attention_tc_kernel<128>, grid, dim3(AttnCfg<128>::THREADS),
+                              AttnCfg<128>::SMEM, s, pl.max_splits, tmK, tmV, p);
+  }
   if (a.dh == 64)
     return launch_pdl(attention_tc_kernel<64>, grid, dim3(AttnCfg<64>::THREADS),
                       AttnCfg<64>::SMEM, s, tmK, tmV, p);

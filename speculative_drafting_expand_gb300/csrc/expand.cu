@@ -23,8 +23,8 @@
 namespace pe {
 
 __global__ void __launch_bounds__(128) expand_kernel(const ExpandArgs a) {
-  grid_dep_launch();
   grid_dep_wait();
+  grid_dep_launch();
   const int i = blockIdx.x;  // expanded row
   __shared__ int s_src;      // source hidden row (-1: h_shared)
 

@@ -16,8 +16,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const float* __restrict_
   __shared__ float sw[SBF][SBK + 1];
   __shared__ float sw2[DUAL ? SBF : 1][SBK + 1];
   __shared__ float sx[SBT][SBK + 1];
-  grid_dep_launch();
   grid_dep_wait();
+  grid_dep_launch();
   const int f0 = blockIdx.x * SBF, t0 = blockIdx.y * SBT;
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
   float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
@@ -70,8 +70,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const float* __restrict_
 }
 
 __global__ void argmax_finalize_kernel(int M, unsigned long long* keys, int32_t* tokens) {
-  grid_dep_launch();
   grid_dep_wait();
+  grid_dep_launch();
   for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < M; t += gridDim.x * blockDim.x) {
     const unsigned long long k = keys[t];
     tokens[t] = k ? argmax_key_index(k) : -1;

@@ -177,9 +177,6 @@ __global__ void __launch_bounds__(192, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // TMEM is held before dependents may start, so their allocation can only
-  // wait for this grid to finish, never the other way round.
-  grid_dep_launch();
 
   const long long U = p.units;
   const int G = gridDim.x, cta = blockIdx.x, kb = p.kb;
@@ -212,6 +209,10 @@ __global__ void __launch_bounds__(192, 2)
         if (DUAL) tma_load_2d(st + C::A_BYTES, &tmA2, &full[i], kk * 64, f * 128, pol_a);
       }
       grid_dep_wait();
+      // Dependents may launch once this CTA has waited for its own inputs;
+      // TMEM is already held, so their allocation can only wait for this
+      // grid to finish, never the other way round.
+      grid_dep_launch();
       for (int i = 0; i < npre; ++i) {
         const long long u = lo + i;
         const int tile = static_cast<int>(u / kb), kk = static_cast<int>(u % kb);

@@ -32,8 +32,8 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads) embed_concat_kernel(const EmbedConcatArgs a) {
   __shared__ float red[32];
-  grid_dep_launch();
   grid_dep_wait();
+  grid_dep_launch();
   const int i = blockIdx.x;
   int id = a.ids[i];
   if (id < 0 || id >= a.vocab) {
@@ -65,8 +65,8 @@ __global__ void __launch_bounds__(kRowThreads) embed_concat_kernel(const EmbedCo
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads) rmsnorm_kernel(const RmsNormArgs a) {
   __shared__ float red[32];
-  grid_dep_launch();
   grid_dep_wait();
+  grid_dep_launch();
   const int i = blockIdx.x;
   int src = a.row_index ? a.row_index[i] : i;
   T* y = static_cast<T*>(a.y) + static_cast<size_t>(i) * a.d;
@@ -87,8 +87,8 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_kernel(const RmsNormArgs 
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads) rope_kv_kernel(const RopeKvArgs a) {
   __shared__ float cs[64], sn[64];
-  grid_dep_launch();
   grid_dep_wait();
+  grid_dep_launch();
   const int i = blockIdx.x;
   const int half = a.dh / 2;
   const int p = a.pos[i];
