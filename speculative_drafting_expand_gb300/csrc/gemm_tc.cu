@@ -100,11 +100,20 @@ __device__ __forceinline__ void epi_chunk(const EpiArgs& e, int o, int t0, const
             out[static_cast<size_t>(t0 + j) * e.ldo + o] = __float2bfloat16_rn(v[j]);
       }
       break;
-    case EPI_ADD:
+    case EPI_ADD: {
+      // all 16 reads are issued before any write: written as `+=` in one
+      // loop, each read would wait for the previous write (the compiler
+      // cannot tell that the rows differ), one memory round trip per token
+      float* r = e.resid + static_cast<size_t>(t0) * e.ldr + o;
+      float old[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        if (of && t0 + j < e.M) e.resid[static_cast<size_t>(t0 + j) * e.ldr + o] += v[j];
+        old[j] = (of && t0 + j < e.M) ? r[static_cast<size_t>(j) * e.ldr] : 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (of && t0 + j < e.M) r[static_cast<size_t>(j) * e.ldr] = old[j] + v[j];
       break;
+    }
     case EPI_SILU_MUL: {
       bf16* out = static_cast<bf16*>(e.out);
 #pragma unroll
