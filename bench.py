@@ -72,28 +72,35 @@ def step_work(wl, inp):
     es = 2 if sh.dtype == "bf16" else 4
     d, F, V = sh.d, sh.ffn, sh.vocab
     qd = sh.n_heads * sh.head_dim
-    layer_params = [sh.qkv_rows * (2 * d if l == 0 else d) + d * qd + 3 * F * d
-                    for l in range(sh.n_layers)]
-    params = d * sh.hidden3 + sum(layer_params) + V * d
     rows = wl.T_out
     valid = int(sum(int(a) + wl.K for a in wl.accepted))
     seq = [int(inp.target_pos[int(inp.cu_in[r]) + int(wl.accepted[r])]) + wl.K + 1
            for r in range(wl.B)]
+    # projections: (weight elements, rows that carry a result); flops count
+    # the valid rows only (accepted window rows and the K draft rows)
+    proj = [(d * sh.hidden3, valid)]
+    for l in range(sh.n_layers):
+        proj += [(sh.qkv_rows * (2 * d if l == 0 else d), valid), (d * qd, valid),
+                 (2 * F * d, valid), (F * d, valid)]
+    lm = (V * d, wl.B * wl.K)
+    parts = [(n * es, 2.0 * m * n) for n, m in proj + [lm]]
     kv_bytes = sh.n_layers * 2 * sum(seq) * sh.n_kv_heads * sh.head_dim * es
-    weight_bytes = params * es
-    act_bytes = rows * sh.hidden3 * es + wl.B * wl.K * 4
-    gemm_flops = 2.0 * valid * (params - V * d) + 2.0 * wl.B * wl.K * V * d
     attn_flops = 0.0
     for r in range(wl.B):
         a = int(wl.accepted[r])
         C = seq[r] - (a + wl.K)
         for j in range(a + wl.K):
             attn_flops += 4.0 * sh.n_heads * sh.head_dim * (C + j + 1) * sh.n_layers
+    parts.append((kv_bytes, attn_flops))
+    weight_bytes = sum(n for n, _ in proj + [lm]) * es
+    act_bytes = rows * sh.hidden3 * es + wl.B * wl.K * 4
+    gemm_flops = sum(f for _, f in parts[:-1])
     lm_bytes = V * d * es + wl.B * wl.K * d * es + wl.B * wl.K * 4
     return dict(weight_bytes=weight_bytes, kv_bytes=kv_bytes, act_bytes=act_bytes,
                 bytes=weight_bytes + kv_bytes + act_bytes, gemm_flops=gemm_flops,
-                attn_flops=attn_flops, lm_head_bytes=lm_bytes,
-                lm_head_flops=2.0 * wl.B * wl.K * V * d, valid_rows=valid, rows=rows)
+                attn_flops=attn_flops, flops=gemm_flops + attn_flops, parts=parts,
+                lm_head_bytes=lm_bytes, lm_head_flops=2.0 * wl.B * wl.K * V * d,
+                valid_rows=valid, rows=rows)
 
 
 def kernel_source_hash() -> str:
@@ -101,7 +108,7 @@ def kernel_source_hash() -> str:
     only reported while the kernel it was measured on is unchanged."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("gemm_tc.cu", "pe_common.cuh"):
+    for f in ("gemm_tc.cu", "gemm_tc.cuh", "gemm_mc.cu", "pe_common.cuh"):
         with open(os.path.join(ROOT, "speculative_drafting_expand_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -387,8 +394,18 @@ def run_ours(args, world, rank, local):
     lm_avg_s = statistics.mean(a.elapsed_time(b) for a, b in lm_ms) / 1e3
     pk, pk_kind = peaks()
     hbm = float(pk["hbm_gbs"])
-    achieved = work["lm_head_bytes"] / lm_avg_s / 1e9
-    traffic = measured_traffic("gemm_tc_kernel", wl.name)
+    tflops = float(pk["bf16_tflops"])                      # burst: timed alone
+    tflops_sus = float(pk.get("bf16_tflops_sustained", tflops))  # inside the step
+    traffic = measured_traffic("lm_head", wl.name)
+    # the LM head's bound: its flops per byte against the ridge point
+    lm_intensity = work["lm_head_flops"] / work["lm_head_bytes"]
+    if lm_intensity > tflops * 1e12 / (hbm * 1e9):
+        lm_roof = {"bound": "tensor", "achieved": work["lm_head_flops"] / lm_avg_s / 1e12,
+                   "peak": tflops, "unit": "TFLOP/s", "peak_source": f"{pk_kind} bf16_tflops"}
+    else:
+        lm_roof = {"bound": "hbm", "achieved": work["lm_head_bytes"] / lm_avg_s / 1e9,
+                   "peak": hbm, "unit": "GB/s", "peak_source": f"{pk_kind} hbm_gbs"}
+    lm_roof["frac"] = lm_roof["achieved"] / lm_roof["peak"]
 
     # ---- end to end through the public calls with host buffers -------------
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
@@ -433,8 +450,11 @@ def run_ours(args, world, rank, local):
                "sample": f"{n} full oracle steps of the same workload in {dt:.1f} s"}
 
     if rank == 0:
-        bound = "hbm"
-        step_floor_s = work["bytes"] / (hbm * 1e9)
+        # each projection and the attention at the slower of its bytes and
+        # its flops (sustained tensor peak: they run inside a long step)
+        step_floor_s = sum(max(b / (hbm * 1e9), f / (tflops_sus * 1e12))
+                           for b, f in work["parts"])
+        step_s = ms_per_step / 1e3
         line = {
             "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -442,14 +462,16 @@ def run_ours(args, world, rank, local):
             "dtype": sh.dtype, "data": "synthetic (seeded random-init weights and inputs)",
             "config": config_of(wl, args),
             "drafted_tok_per_s": value * wl.B * wl.K,
-            "roofline": {"bound": bound, "kernel": "gemm_tc_kernel (LM head + argmax)",
-                         "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                         "frac": achieved / hbm, "traffic": traffic,
-                         "peak_source": f"{pk_kind} hbm_gbs",
-                         "bytes_per_launch": work["lm_head_bytes"],
-                         "launch_us": lm_avg_s * 1e6},
-            "step_roofline": {"bytes": work["bytes"], "floor_us": step_floor_s * 1e6,
-                              "frac": step_floor_s / (ms_per_step / 1e3),
+            "roofline": dict(lm_roof, kernel="LM-head GEMM + fused argmax",
+                             traffic=traffic, bytes_per_launch=work["lm_head_bytes"],
+                             flops_per_launch=work["lm_head_flops"],
+                             launch_us=lm_avg_s * 1e6),
+            "step_roofline": {"bytes": work["bytes"], "flops": work["flops"],
+                              "floor_us": step_floor_s * 1e6,
+                              "frac": step_floor_s / step_s,
+                              "hbm_frac": work["bytes"] / step_s / (hbm * 1e9),
+                              "tensor_frac": work["flops"] / step_s / (tflops_sus * 1e12),
+                              "tensor_peak": tflops_sus, "hbm_peak": hbm,
                               "gemm_flops": work["gemm_flops"],
                               "attn_flops": work["attn_flops"]},
             "e2e": {"value": e2e_value, "unit": "steps/s", "h2d_bytes_per_step": h2d,

@@ -16,6 +16,7 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
                                 const EpiArgs& epi, const TcGemmWorkspace& ws, int* err,
                                 cudaStream_t s);
 int tc_pick_bn(int M);
+int tc_b_box_rows(int M, int N, int sm_count);
 cudaError_t init_gemm_tc();
 size_t tc_partial_floats(int grid, int bn, bool dual);
 cudaError_t init_attention_tc();
@@ -117,7 +118,7 @@ cudaError_t linear(pe_handle* h, const void* x, int ldx, const void* w, const vo
                                        static_cast<const float*>(w2), M, N, K, epi, h->err, s));
   const CUtensorMap* wa = get_map(h, w, N, K, K, 128);
   const CUtensorMap* wa2 = w2 ? get_map(h, w2, N, K, K, 128) : wa;
-  const CUtensorMap* xb = get_map(h, x, M, K, ldx, tc_pick_bn(M));
+  const CUtensorMap* xb = get_map(h, x, M, K, ldx, tc_b_box_rows(M, N, h->sm_count));
   if (!wa || !wa2 || !xb) return cudaErrorInvalidValue;
   return counted(h, launch_gemm_tc_maps(*wa, *wa2, *xb, w2 != nullptr, M, N, K, epi, tc_ws(h),
                                         h->err, s));

@@ -23,123 +23,9 @@
 
 #include <algorithm>
 
-#include "pe_common.cuh"
-#include "pe_kernels.h"
+#include "gemm_tc.cuh"
 
 namespace pe {
-
-template <int BN, bool DUAL>
-struct TcCfg {
-  static constexpr int BM = 128, BK = 64;
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int NA = DUAL ? 2 : 1;
-  static constexpr int STAGE_BYTES = A_BYTES * NA + B_BYTES;
-  static constexpr int ACC_COLS = BN * NA;
-  static constexpr int NUM_ACC = (2 * ACC_COLS <= 512) ? 2 : 1;
-  static constexpr int TMEM_RAW = ACC_COLS * NUM_ACC;
-  static constexpr int TMEM_COLS = TMEM_RAW <= 32    ? 32
-                                   : TMEM_RAW <= 64  ? 64
-                                   : TMEM_RAW <= 128 ? 128
-                                   : TMEM_RAW <= 256 ? 256
-                                                     : 512;
-  // Narrow token tiles (a few rows, weight streaming) keep the CTA near
-  // 100 KB of shared memory so that the next projection's CTA fits on the
-  // same SM and prefetches its weights while this one drains.
-  static constexpr int SMEM_BUDGET = BN <= 32 ? 104 * 1024 : 200 * 1024;
-  static constexpr int STAGES_RAW = SMEM_BUDGET / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
-  static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
-  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
-  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
-  static_assert(2 * STAGES + 5 <= BAR_BYTES / 8, "barrier space");
-};
-
-struct TcParams {
-  int M, N, K, kb, tiles_m;
-  long long units;
-  EpiArgs epi;
-  float* ws;
-  int* counters;
-  int* done;
-  int* err;
-  int split_s;  // 0: stream-K over all units; >= 1: S CTAs (one cluster) per tile
-};
-
-__device__ __forceinline__ long long unit_lo(int c, long long U, int G) {
-  return static_cast<long long>(c) * U / G;
-}
-// The CTA whose unit range contains unit u.
-__device__ __forceinline__ int cta_of_unit(long long u, long long U, int G) {
-  int c = static_cast<int>((u * G) / U);
-  if (c > G - 1) c = G - 1;
-  while (c > 0 && unit_lo(c, U, G) > u) --c;
-  while (c + 1 < G && unit_lo(c + 1, U, G) <= u) ++c;
-  return c;
-}
-
-// Apply the epilogue to 16 token columns [t0, t0 + 16) of output feature o.
-// Called by all 32 lanes of a warp together (the argmax reduces across them).
-template <bool DUAL>
-__device__ __forceinline__ void epi_chunk(const EpiArgs& e, int o, int t0, const float* v,
-                                          const float* v2, int lane) {
-  const bool of = o < e.N;
-  switch (e.kind) {
-    case EPI_STORE:
-      if (e.out_f32) {
-        float* out = static_cast<float*>(e.out);
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (of && t0 + j < e.M) out[static_cast<size_t>(t0 + j) * e.ldo + o] = v[j];
-      } else {
-        bf16* out = static_cast<bf16*>(e.out);
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (of && t0 + j < e.M)
-            out[static_cast<size_t>(t0 + j) * e.ldo + o] = __float2bfloat16_rn(v[j]);
-      }
-      break;
-    case EPI_ADD: {
-      // all 16 reads are issued before any write: written as `+=` in one
-      // loop, each read would wait for the previous write (the compiler
-      // cannot tell that the rows differ), one memory round trip per token
-      float* r = e.resid + static_cast<size_t>(t0) * e.ldr + o;
-      float old[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        old[j] = (of && t0 + j < e.M) ? r[static_cast<size_t>(j) * e.ldr] : 0.f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (of && t0 + j < e.M) r[static_cast<size_t>(j) * e.ldr] = old[j] + v[j];
-      break;
-    }
-    case EPI_SILU_MUL: {
-      bf16* out = static_cast<bf16*>(e.out);
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (of && t0 + j < e.M)
-          out[static_cast<size_t>(t0 + j) * e.ldo + o] =
-              __float2bfloat16_rn(silu_f(v[j]) * (DUAL ? v2[j] : 1.f));
-      break;
-    }
-    case EPI_ARGMAX:
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int t = t0 + j;
-        const bool ok = of && t < e.M;
-        if (ok && e.logits) e.logits[static_cast<size_t>(t) * e.ldl + o] = v[j];
-        unsigned long long key = ok ? argmax_key(v[j], o) : 0ull;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, off);
-          key = other > key ? other : key;
-        }
-        if (lane == 0 && key != 0ull) atomicMax(e.keys + t, key);
-      }
-      break;
-  }
-}
 
 // Two CTAs per SM (at most 170 registers a thread): the next kernel's CTA
 // can start on an SM while this one drains.
@@ -511,6 +397,7 @@ cudaError_t init_gemm_tc() {
   PE_TC_ATTR(128)
   PE_TC_ATTR(256)
 #undef PE_TC_ATTR
+  if (e == cudaSuccess) e = init_gemm_mc();
   return e;
 }
 
@@ -552,6 +439,15 @@ int tc_pick_bn(int M) {
   return 256;
 }
 
+// Rows of the token box in the x tensor map that launch_gemm_tc_maps
+// expects for an M x N projection: the token tile, or its slice when the
+// multicast kernel takes the projection.
+int tc_b_box_rows(int M, int N, int sm_count) {
+  const int bn = tc_pick_bn(M);
+  const long long tiles = static_cast<long long>((N + 127) / 128) * ((M + bn - 1) / bn);
+  return bn / gemm_mc_cluster(bn, false, tiles, sm_count);
+}
+
 size_t tc_partial_floats(int grid, int bn, bool dual) {
   return static_cast<size_t>(grid) * 2 * 128 * bn * (dual ? 2 : 1);
 }
@@ -576,6 +472,9 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
   p.done = ws.done_counter;
   p.err = err;
   const int tiles = tiles_n * p.tiles_m;
+  p.split_s = 0;
+  const int cs = gemm_mc_cluster(bn, dual, tiles, ws.sm_count);
+  if (cs > 1) return launch_gemm_mc(wa, wa2, xb, dual, bn, cs, p, s);
   if (tiles > ws.max_tiles) return cudaErrorInvalidValue;
 #define PE_TC_CASE(BNV)                                                                       \
   case BNV:                                                                                   \
@@ -602,7 +501,8 @@ cudaError_t launch_gemm_tc(const void* x, int ldx, const void* w, const void* w2
   if (!tensor_map_2d_bf16(&wa, w, N, K, K, 64, 128)) return cudaErrorInvalidValue;
   wa2 = wa;
   if (w2 && !tensor_map_2d_bf16(&wa2, w2, N, K, K, 64, 128)) return cudaErrorInvalidValue;
-  if (!tensor_map_2d_bf16(&xb, x, M, K, ldx, 64, tc_pick_bn(M))) return cudaErrorInvalidValue;
+  if (!tensor_map_2d_bf16(&xb, x, M, K, ldx, 64, tc_b_box_rows(M, N, ws.sm_count)))
+    return cudaErrorInvalidValue;
   return launch_gemm_tc_maps(wa, wa2, xb, w2 != nullptr, M, N, K, epi, ws, err, s);
 }
 

@@ -26,7 +26,7 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
                                 const CUtensorMap& xb, bool dual, int M, int N, int K,
                                 const EpiArgs& epi, const TcGemmWorkspace& ws, int* err,
                                 cudaStream_t s);
-int tc_pick_bn(int M);
+int tc_b_box_rows(int M, int N, int sm_count);
 }  // namespace pe
 
 namespace {
@@ -97,9 +97,10 @@ extern "C" pe_status pe_linear_static(const void* x, const void* w, float* y, in
   // the tile counters must start at zero; clear them (and the error word)
   if (cudaMemsetAsync(counters, 0, (kMaxTiles + 1) * sizeof(int), s) != cudaSuccess)
     return PE_ERR_CUDA;
+  const int sms = slot->sm_count < kMaxCtas ? slot->sm_count : kMaxCtas;
   CUtensorMap wa, xb;
   if (!tensor_map_2d_bf16(&wa, w, N, K, K, 64, 128) ||
-      !tensor_map_2d_bf16(&xb, x, M, K, K, 64, tc_pick_bn(M)))
+      !tensor_map_2d_bf16(&xb, x, M, K, K, 64, tc_b_box_rows(M, N, sms)))
     return PE_ERR_INVALID_ARGUMENT;
   TcGemmWorkspace ws;
   ws.partials = partials;
@@ -107,7 +108,7 @@ extern "C" pe_status pe_linear_static(const void* x, const void* w, float* y, in
   ws.tile_counters = counters;
   ws.max_tiles = kMaxTiles;
   ws.done_counter = nullptr;  // only the argmax epilogue uses it
-  ws.sm_count = slot->sm_count < kMaxCtas ? slot->sm_count : kMaxCtas;
+  ws.sm_count = sms;
   EpiArgs ep = {};
   ep.kind = EPI_STORE;
   ep.M = M;

@@ -3,7 +3,8 @@
 y = x w^T with bf16 operands and fp32 accumulation (tcgen05, TMEM) against
 an fp64 product of the same bf16 values.  The shapes cover one tile, many
 tiles, ragged token/feature/k tails, every token-tile width (16..256) and
-stream-K splits of a tile across CTAs (the deterministic fix-up path).
+stream-K splits of a tile across CTAs (the deterministic fix-up path) and
+clusters that share one token tile by TMA multicast (many tiles per SM).
 """
 
 import numpy as np
@@ -24,12 +25,17 @@ CASES = [
     (100, 640, 1024),   # token tile 128
     (300, 384, 256),    # token tile 256, two token tiles, ragged
     (896, 2880, 2880),  # batch-64 shape
+    # at least four tiles per SM with 128- or 256-token tiles: clusters of
+    # CTAs sharing the token tile by multicast; ragged tokens, features, k
+    (300, 40000, 200),
+    (100, 80000, 256),
 ]
 
 
-def _handle(max_tokens):
+def _handle(max_tokens, widest=8192):
+    # the handle's tile capacity follows its vocabulary and token count
     shape = W.small_shape("lin", d=64, n_layers=1, n_heads=1, n_kv_heads=1, head_dim=64,
-                          ffn=64, vocab=8192)
+                          ffn=64, vocab=max(8192, widest))
     z = np.zeros(64, np.uint16)
     w = {k: z for k in ("emb", "fc", "norm_final", "lm_head", "h_shared")}
     w["h_shared"] = np.zeros(shape.hidden3, np.uint16)
@@ -41,7 +47,7 @@ def _handle(max_tokens):
 def test_linear_matches_fp64(M, N, K):
     B = G.library()
     torch = G.torch_mod()
-    dr = _handle(max(M, 16))
+    dr = _handle(max(M, 16), N)
     x = W.normal(7, "x", (M, K), 1.0, "bf16", M, N)
     w = W.normal(7, "w", (N, K), 0.05, "bf16", M, N)
     y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
