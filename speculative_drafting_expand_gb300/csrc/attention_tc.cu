@@ -56,7 +56,11 @@ struct AttnCfg {
   // P.V has finished reading P, so it shares P's space
   static constexpr int RED_OFF = P_OFF;
   static constexpr int BAR_OFF = P_OFF + 4 * TILE;
-  static constexpr int SMEM = 1024 + BAR_OFF + 256;
+  // block ids of the CTA's pages, read once: a split covers at most
+  // BT_ENTRIES pages of 16 keys (32 chunks)
+  static constexpr int BT_ENTRIES = 256;
+  static constexpr int BT_OFF = BAR_OFF + 256;
+  static constexpr int SMEM = 1024 + BT_OFF + BT_ENTRIES * 4;
   // TMEM: S at columns 0..127; O of key half h at 128 + h * DH
   static constexpr int TMEM_COLS = 128 + 2 * DH <= 256 ? 256 : 512;
   static constexpr int THREADS = 320;           // producer, MMA, 8 softmax warps
@@ -137,7 +141,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(&pv_done[1], 1);
     mbar_init(drain, 1);
     mbar_init(merge_ready, nsplits > 1 ? nsplits - 1 : 1);
-    mbar_init(merge_done, 1);
+    mbar_init(merge_done, nsplits > 1 ? nsplits - 1 : 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -153,11 +157,37 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // The block ids of all pages of [key0, key1), read by the whole warp in
+    // one round trip (not one per chunk on the loads' critical path) and
+    // checked here; -1 marks a bad id (recorded, its page not loaded).
+    int* bt_s = reinterpret_cast<int*>(smem + C::BT_OFF);
+    {
+      const int32_t* bt = a.block_table + static_cast<size_t>(r) * a.bt_stride + (key0 >> 4);
+      const int npages = (key1 - key0 + 15) >> 4;  // <= BT_ENTRIES (split size on the host)
+      int v[C::BT_ENTRIES / 32];
+#pragma unroll
+      for (int k = 0; k < C::BT_ENTRIES / 32; ++k) {
+        const int i = lane + 32 * k;
+        v[k] = i < npages ? bt[i] : 0;
+      }
+#pragma unroll
+      for (int k = 0; k < C::BT_ENTRIES / 32; ++k) {
+        const int i = lane + 32 * k;
+        if (i < npages) {
+          int b = v[k];
+          if (b < 0 || b >= a.num_blocks) {
+            record_error(a.err, PE_DEV_BAD_BLOCK);
+            b = -1;
+          }
+          bt_s[i] = b;
+        }
+      }
+      __syncwarp();
+    }
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       const uint64_t pol = l2_policy_evict_first();
-      const int32_t* bt = a.block_table + static_cast<size_t>(r) * a.bt_stride;
       for (int c = 0; c < nchunks; ++c) {
         const int st = c % C::KV_STAGES;
         const int round = c / C::KV_STAGES;
@@ -168,15 +198,8 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int pg = 0; pg < 8; ++pg) {
           const int t = t0 + pg * 16;
-          blks[pg] = -1;
-          if (t < key1) {
-            const int b = bt[t >> 4];
-            if (b < 0 || b >= a.num_blocks) record_error(a.err, PE_DEV_BAD_BLOCK);
-            else {
-              blks[pg] = b;
-              bytes += 2u * C::NH * 2048u;
-            }
-          }
+          blks[pg] = t < key1 ? bt_s[c * 8 + pg] : -1;
+          if (blks[pg] >= 0) bytes += 2u * C::NH * 2048u;
         }
         mbar_arrive_expect_tx(&kv_full[st], bytes);
 #pragma unroll
@@ -431,62 +454,75 @@ __global__ void __launch_bounds__(320, 1)
           mine[(DH + 1) * 128 + qrow] = L;
         }
         named_bar_sync(1, 256);
-        if (split != 0) {
-          // hand the partial to rank 0, keep it until rank 0 has read it
-          if (threadIdx.x == 64) {
-            asm volatile("fence.acq_rel.cluster;" ::: "memory");
-            mbar_arrive_remote(cluster_map_shared(smem_u32(merge_ready), 0));
-            mbar_wait(merge_done, 0, a.err);
-          }
-          named_bar_sync(1, 256);
-        } else {
-          if (threadIdx.x == 64) *flag = mbar_wait_cluster(merge_ready, 0, a.err) ? 1 : 0;
-          named_bar_sync(1, 256);
-          if (*flag) {
-            // merge the splits in split order through distributed shared memory
-            const uint32_t base = smem_u32(smem + C::K_OFF);
-            float ms[8], ls[8];
+        // Every split tells every other that its partial is ready, then
+        // merges its share of the columns (8-column groups dealt round-robin
+        // to the splits) from all partials at once, in split order
+        // (deterministic), and tells the others it has read them; a split
+        // leaves only when all others have read its partial.
+        if (threadIdx.x == 64) {
+          asm volatile("fence.acq_rel.cluster;" ::: "memory");
+          for (int q = 0; q < nsplits; ++q)
+            if (q != split) mbar_arrive_remote(cluster_map_shared(smem_u32(merge_ready), q));
+          *flag = mbar_wait_cluster(merge_ready, 0, a.err) ? 1 : 0;
+        }
+        named_bar_sync(1, 256);
+        if (*flag) {
+          const uint32_t base = smem_u32(smem + C::K_OFF);
+          float ms[8], ls[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              ms[q] = -INFINITY;
-              ls[q] = 0.f;
-              if (q < nsplits) {
-                const uint32_t rb = cluster_map_shared(base, q);
-                ms[q] = ld_shared_cluster_f32(rb + (DH * 128 + qrow) * 4);
-                ls[q] = ld_shared_cluster_f32(rb + ((DH + 1) * 128 + qrow) * 4);
-              }
+          for (int q = 0; q < 8; ++q) {
+            ms[q] = -INFINITY;
+            ls[q] = 0.f;
+            if (q < nsplits) {
+              const uint32_t rb = cluster_map_shared(base, q);
+              ms[q] = ld_shared_cluster_f32(rb + (DH * 128 + qrow) * 4);
+              ls[q] = ld_shared_cluster_f32(rb + ((DH + 1) * 128 + qrow) * 4);
             }
-            float Mx = -INFINITY;
+          }
+          float Mx = -INFINITY;
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (ls[q] > 0.f) Mx = fmaxf(Mx, ms[q]);
+          float wq[8], Ls = 0.f;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            wq[q] = (q < nsplits && ls[q] > 0.f) ? exp2f(ms[q] - Mx) : 0.f;
+            Ls += wq[q] * ls[q];
+          }
+          const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+          bf16* orow = static_cast<bf16*>(a.out) + (static_cast<size_t>(row) * a.Hq + head) * DH;
+          // this thread: 4 columns (half h) of each of its split's groups
+          for (int grp = split; grp < DH / 8; grp += nsplits) {
+            const int c0 = grp * 8 + h * 4;
+            float t[8][4];
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-              if (ls[q] > 0.f) Mx = fmaxf(Mx, ms[q]);
-            float acc[HC];
+              if (q < nsplits) {
+                const uint32_t rb = cluster_map_shared(base, q) + (c0 * 128 + qrow) * 4;
 #pragma unroll
-            for (int j = 0; j < HC; ++j) acc[j] = 0.f;
-            float Ls = 0.f;
+                for (int j = 0; j < 4; ++j) t[q][j] = ld_shared_cluster_f32(rb + j * 128 * 4);
+              }
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              if (q >= nsplits || !(ls[q] > 0.f)) continue;
-              const float w = exp2f(ms[q] - Mx);
-              Ls += w * ls[q];
-              const uint32_t rb = cluster_map_shared(base, q);
+            for (int q = 0; q < 8; ++q)
+              if (q < nsplits && wq[q] > 0.f)
 #pragma unroll
-              for (int j = 0; j < HC; ++j)
-                acc[j] += w * ld_shared_cluster_f32(rb + ((h * HC + j) * 128 + qrow) * 4);
-            }
+                for (int j = 0; j < 4; ++j) acc[j] += wq[q] * t[q][j];
             if (in_tile) {
-              const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-#pragma unroll
-              for (int j = 0; j < HC; j += 2)
-                *reinterpret_cast<__nv_bfloat162*>(out + j) =
-                    __floats2bfloat162_rn(acc[j] * inv, acc[j + 1] * inv);
+              *reinterpret_cast<__nv_bfloat162*>(orow + c0) =
+                  __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+              *reinterpret_cast<__nv_bfloat162*>(orow + c0 + 2) =
+                  __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
             }
           }
-          named_bar_sync(1, 256);
-          // release the peers
-          if (threadIdx.x >= 64 && threadIdx.x < 64 + nsplits - 1)
-            mbar_arrive_remote(cluster_map_shared(smem_u32(merge_done), threadIdx.x - 63));
         }
+        named_bar_sync(1, 256);
+        if (threadIdx.x == 64) {
+          for (int q = 0; q < nsplits; ++q)
+            if (q != split) mbar_arrive_remote(cluster_map_shared(smem_u32(merge_done), q));
+          mbar_wait_cluster(merge_done, 0, a.err);
+        }
+        named_bar_sync(1, 256);
       } else {
         // partial [split][column][query row]: a warp's accesses of one column
         // are contiguous
@@ -586,17 +622,26 @@ static AttnPlan plan_attention(const AttnArgs& a, int max_rows_per_req, int sm_c
   const int chunks_max = (max_seq + 127) / 128;
   const long long pairs = static_cast<long long>(a.B) * a.Hkv * pl.qtiles;
   const int want = static_cast<int>(std::max<long long>(1, (sm_count + pairs - 1) / pairs));
+  // a split is at most 32 chunks (its block ids fit the CTA's table)
+  constexpr int kMaxCps = 32;
   if (pairs < sm_count) {
-    // latency regime: at most 8 splits, one cluster per unit, DSMEM merge
+    // latency regime: at most 8 splits, one cluster per unit, DSMEM merge;
+    // beyond 8 x 32 chunks, more splits merged through global memory
     pl.cluster = 1;
     (void)want;
     int cps = (chunks_max + 7) / 8;
     cps = std::max(2, cps);
+    if (cps > kMaxCps) {
+      cps = kMaxCps;
+      pl.cluster = 0;
+    }
     pl.split_keys = cps * 128;
   } else {
+    // throughput regime: splits of up to 32 chunks (measured at batch 64:
+    // 32 beats 16 and 64), merged through global memory
     pl.cluster = 0;
     int cps = (chunks_max + want - 1) / want;
-    cps = std::max(2, std::min(16, cps));
+    cps = std::max(2, std::min(kMaxCps, cps));
     pl.split_keys = cps * 128;
   }
   pl.max_splits = (max_seq + pl.split_keys - 1) / pl.split_keys;
@@ -641,6 +686,8 @@ cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const
   p.part = part;
   p.counters = counters;
   p.cluster = pl.cluster;
+  if (pl.split_keys / 16 > AttnCfg<64>::BT_ENTRIES || pl.split_keys / 16 > AttnCfg<128>::BT_ENTRIES)
+    return cudaErrorInvalidValue;
   const size_t need = static_cast<size_t>(a.B) * a.Hkv * pl.qtiles * pl.max_splits * 128 * (a.dh + 2);
   if (need > part_floats || static_cast<size_t>(a.B) * a.Hkv * pl.qtiles > n_counters)
     return cudaErrorInvalidValue;

@@ -306,30 +306,49 @@ __global__ void __launch_bounds__(192, 2)
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
   if (p.split_s >= 2) {
-    // every CTA of the cluster has its partial in shared memory; rank 0
-    // adds them in rank order (deterministic) and applies the epilogue
+    // Every CTA of the cluster has its partial in shared memory.  The sum
+    // is scattered over the cluster: the tile's (32-row group, 16-column
+    // chunk) items go round-robin to the S CTAs, and the warp of that row
+    // group reads its item from all S partials with the loads of 8 columns
+    // in flight together (one DSMEM round trip per 8 columns, not one per
+    // CTA), adds them in rank order (deterministic) and applies the
+    // epilogue.
     cluster_sync_all();
-    if (cluster_ctarank() == 0 && warp < 4) {
-      const int S = p.split_s, tile = cta / S;
+    const int S = p.split_s, tile = cta / S;
+    const int rk = static_cast<int>(cluster_ctarank());
+    if (warp < 4) {
       const int f = tile / p.tiles_m, m = tile % p.tiles_m;
       const int row = warp * 32 + lane;
       const uint32_t base = smem_u32(smem);
+      constexpr int kMaxS = 8;  // cluster split sizes are at most 8
       for (int c0 = 0; c0 < BN; c0 += 16) {
+        if (((c0 / 16) * 4 + warp) % S != rk) continue;
         float v[16], v2[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = v2[j] = 0.f;
-        for (int rk = 0; rk < S; ++rk) {
-          const uint32_t rb = cluster_map_shared(base, rk);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            v[j] += ld_shared_cluster_f32(rb + ((c0 + j) * 128 + row) * 4);
-            if (DUAL) v2[j] += ld_shared_cluster_f32(rb + ((BN + c0 + j) * 128 + row) * 4);
+        for (int part = 0; part < (DUAL ? 4 : 2); ++part) {
+          const int col = (part & 2 ? BN : 0) + c0 + (part & 1) * 8;
+          float t[kMaxS][8];
+#pragma unroll
+          for (int q = 0; q < kMaxS; ++q) {
+            if (q < S) {
+              const uint32_t rb = cluster_map_shared(base, q) + (col * 128 + row) * 4;
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) t[q][jj] = ld_shared_cluster_f32(rb + jj * 128 * 4);
+            }
           }
+          float* dst = (part & 2 ? v2 : v) + (part & 1) * 8;
+#pragma unroll
+          for (int q = 0; q < kMaxS; ++q)
+            if (q < S)
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) dst[jj] += t[q][jj];
         }
         epi_chunk<DUAL>(p.epi, f * 128 + row, m * BN + c0, v, v2, lane);
       }
     }
-    // peers keep their shared memory until rank 0 has read it
+    // every CTA keeps its shared memory until all of the cluster has read it
     cluster_sync_all();
   }
   if (p.epi.kind == EPI_ARGMAX) {
