@@ -39,7 +39,6 @@ struct AttnTcParams {
   int max_splits;
   float* part;       // [B, Hkv, qtiles, max_splits, 128, dh + 2]
   int* counters;     // [B, Hkv, qtiles]
-  int cluster;       // 1: the splits of a unit are one cluster, merged through DSMEM
 };
 
 template <int DH>
@@ -92,9 +91,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* p_full = q_ready + 3;
   uint64_t* pv_done = q_ready + 5;                // [2]: one per P buffer
   uint64_t* drain = q_ready + 7;
-  uint64_t* merge_ready = q_ready + 8;            // rank 0: one arrive per active peer
-  uint64_t* merge_done = q_ready + 9;             // peers: rank 0 has read their partial
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 10);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 8);
   volatile int* flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
   float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
@@ -140,8 +137,6 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(&pv_done[0], 1);
     mbar_init(&pv_done[1], 1);
     mbar_init(drain, 1);
-    mbar_init(merge_ready, nsplits > 1 ? nsplits - 1 : 1);
-    mbar_init(merge_done, nsplits > 1 ? nsplits - 1 : 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -443,86 +438,6 @@ __global__ void __launch_bounds__(320, 1)
             *reinterpret_cast<__nv_bfloat162*>(out + j) =
                 __floats2bfloat162_rn(o[j] * inv, o[j + 1] * inv);
         }
-      } else if (p.cluster) {
-        // partial -> this CTA's shared memory (the K/V ring is drained);
-        // layout [column][query row], then (m, l)
-        float* mine = reinterpret_cast<float*>(smem + C::K_OFF);
-#pragma unroll
-        for (int j = 0; j < HC; ++j) mine[(h * HC + j) * 128 + qrow] = o[j];
-        if (h == 0) {
-          mine[DH * 128 + qrow] = M;
-          mine[(DH + 1) * 128 + qrow] = L;
-        }
-        named_bar_sync(1, 256);
-        // Every split tells every other that its partial is ready, then
-        // merges its share of the columns (8-column groups dealt round-robin
-        // to the splits) from all partials at once, in split order
-        // (deterministic), and tells the others it has read them; a split
-        // leaves only when all others have read its partial.
-        if (threadIdx.x == 64) {
-          asm volatile("fence.acq_rel.cluster;" ::: "memory");
-          for (int q = 0; q < nsplits; ++q)
-            if (q != split) mbar_arrive_remote(cluster_map_shared(smem_u32(merge_ready), q));
-          *flag = mbar_wait_cluster(merge_ready, 0, a.err) ? 1 : 0;
-        }
-        named_bar_sync(1, 256);
-        if (*flag) {
-          const uint32_t base = smem_u32(smem + C::K_OFF);
-          float ms[8], ls[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            ms[q] = -INFINITY;
-            ls[q] = 0.f;
-            if (q < nsplits) {
-              const uint32_t rb = cluster_map_shared(base, q);
-              ms[q] = ld_shared_cluster_f32(rb + (DH * 128 + qrow) * 4);
-              ls[q] = ld_shared_cluster_f32(rb + ((DH + 1) * 128 + qrow) * 4);
-            }
-          }
-          float Mx = -INFINITY;
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            if (ls[q] > 0.f) Mx = fmaxf(Mx, ms[q]);
-          float wq[8], Ls = 0.f;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            wq[q] = (q < nsplits && ls[q] > 0.f) ? exp2f(ms[q] - Mx) : 0.f;
-            Ls += wq[q] * ls[q];
-          }
-          const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-          bf16* orow = static_cast<bf16*>(a.out) + (static_cast<size_t>(row) * a.Hq + head) * DH;
-          // this thread: 4 columns (half h) of each of its split's groups
-          for (int grp = split; grp < DH / 8; grp += nsplits) {
-            const int c0 = grp * 8 + h * 4;
-            float t[8][4];
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              if (q < nsplits) {
-                const uint32_t rb = cluster_map_shared(base, q) + (c0 * 128 + qrow) * 4;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) t[q][j] = ld_shared_cluster_f32(rb + j * 128 * 4);
-              }
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              if (q < nsplits && wq[q] > 0.f)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[j] += wq[q] * t[q][j];
-            if (in_tile) {
-              *reinterpret_cast<__nv_bfloat162*>(orow + c0) =
-                  __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
-              *reinterpret_cast<__nv_bfloat162*>(orow + c0 + 2) =
-                  __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
-            }
-          }
-        }
-        named_bar_sync(1, 256);
-        if (threadIdx.x == 64) {
-          for (int q = 0; q < nsplits; ++q)
-            if (q != split) mbar_arrive_remote(cluster_map_shared(smem_u32(merge_done), q));
-          mbar_wait_cluster(merge_done, 0, a.err);
-        }
-        named_bar_sync(1, 256);
       } else {
         // partial [split][column][query row]: a warp's accesses of one column
         // are contiguous
@@ -610,7 +525,7 @@ __global__ void __launch_bounds__(320, 1)
 // ---------------------------------------------------------------------------
 
 struct AttnPlan {
-  int G, rows_per_qt, qtiles, split_keys, max_splits, cluster;
+  int G, rows_per_qt, qtiles, split_keys, max_splits;
 };
 
 static AttnPlan plan_attention(const AttnArgs& a, int max_rows_per_req, int sm_count) {
@@ -622,30 +537,19 @@ static AttnPlan plan_attention(const AttnArgs& a, int max_rows_per_req, int sm_c
   const int chunks_max = (max_seq + 127) / 128;
   const long long pairs = static_cast<long long>(a.B) * a.Hkv * pl.qtiles;
   const int want = static_cast<int>(std::max<long long>(1, (sm_count + pairs - 1) / pairs));
-  // a split is at most 32 chunks (its block ids fit the CTA's table)
+  // A split is at most 32 chunks (its block ids fit the CTA's table).
+  // Fewer units than SMs: about 8 splits per unit; otherwise enough splits
+  // to give every SM a unit, 2 to 32 chunks each (32 measured best at
+  // batch 64).  The splits of a unit are merged through global memory by
+  // the last one to finish: at batch 16 that beat merging the splits of a
+  // thread-block cluster through distributed shared memory by a sixth of
+  // the step (8-CTA clusters of one-CTA-per-SM kernels leave SMs idle), and
+  // tied with it at batch 1.
   constexpr int kMaxCps = 32;
-  if (pairs < sm_count) {
-    // latency regime: at most 8 splits, one cluster per unit, DSMEM merge;
-    // beyond 8 x 32 chunks, more splits merged through global memory
-    pl.cluster = 1;
-    (void)want;
-    int cps = (chunks_max + 7) / 8;
-    cps = std::max(2, cps);
-    if (cps > kMaxCps) {
-      cps = kMaxCps;
-      pl.cluster = 0;
-    }
-    pl.split_keys = cps * 128;
-  } else {
-    // throughput regime: splits of up to 32 chunks (measured at batch 64:
-    // 32 beats 16 and 64), merged through global memory
-    pl.cluster = 0;
-    int cps = (chunks_max + want - 1) / want;
-    cps = std::max(2, std::min(kMaxCps, cps));
-    pl.split_keys = cps * 128;
-  }
+  int cps = pairs < sm_count ? (chunks_max + 7) / 8 : (chunks_max + want - 1) / want;
+  cps = std::max(2, std::min(kMaxCps, cps));
+  pl.split_keys = cps * 128;
   pl.max_splits = (max_seq + pl.split_keys - 1) / pl.split_keys;
-  if (pl.max_splits < 2) pl.cluster = 0;
   return pl;
 }
 
@@ -685,20 +589,12 @@ cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const
   p.max_splits = pl.max_splits;
   p.part = part;
   p.counters = counters;
-  p.cluster = pl.cluster;
   if (pl.split_keys / 16 > AttnCfg<64>::BT_ENTRIES || pl.split_keys / 16 > AttnCfg<128>::BT_ENTRIES)
     return cudaErrorInvalidValue;
   const size_t need = static_cast<size_t>(a.B) * a.Hkv * pl.qtiles * pl.max_splits * 128 * (a.dh + 2);
   if (need > part_floats || static_cast<size_t>(a.B) * a.Hkv * pl.qtiles > n_counters)
     return cudaErrorInvalidValue;
   dim3 grid(pl.max_splits, a.Hkv * pl.qtiles, a.B);
-  if (pl.cluster) {
-    if (a.dh == 64)
-      return launch_pdl_cluster(attention_tc_kernel<64>, grid, dim3(AttnCfg<64>::THREADS),
-                                AttnCfg<64>::SMEM, s, pl.max_splits, tmK, tmV, p);
-    return launch_pdl_cluster(attention_tc_kernel<128>, grid, dim3(AttnCfg<128>::THREADS),
-                              AttnCfg<128>::SMEM, s, pl.max_splits, tmK, tmV, p);
-  }
   if (a.dh == 64)
     return launch_pdl(attention_tc_kernel<64>, grid, dim3(AttnCfg<64>::THREADS),
                       AttnCfg<64>::SMEM, s, tmK, tmV, p);

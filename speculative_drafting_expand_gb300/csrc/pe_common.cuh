@@ -28,11 +28,10 @@ __device__ __forceinline__ void record_error(int* err, int code) {
 // programmatic dependent launch.  Every kernel calls grid_dep_wait() before it
 // touches data written by earlier kernels (and in any case before it exits),
 // so completion stays transitive along the stream, and triggers its
-// dependents (grid_dep_launch) only after that wait.  (Triggering before the
-// wait was measured to let a cluster-launched dependent read rows that the
-// kernel had not written yet.)  Kernels that allocate tensor memory trigger
-// only after the allocation, so a dependent that holds TMEM can never be
-// waiting for a predecessor that still has to allocate.
+// dependents (grid_dep_launch) only after that wait, so that at most two
+// kernels of the stream have CTAs resident at a time.  Kernels that allocate
+// tensor memory trigger only after the allocation, so a dependent that holds
+// TMEM can never be waiting for a predecessor that still has to allocate.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void grid_dep_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -98,37 +97,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   }
 }
 
-// Cluster-scope variants: arrive on an mbarrier in another CTA of the
-// cluster (release), and wait with cluster-scope acquire so that the peer's
-// shared-memory writes before its arrive are visible.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int* err) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const unsigned long long t0 = global_timer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
-      record_error(err, PE_DEV_TIMEOUT);
-      return false;
-    }
-  }
-}
 
 // ---------------------------------------------------------------------------
 // TMA (tiled tensor copies global -> shared, completion on an mbarrier)
