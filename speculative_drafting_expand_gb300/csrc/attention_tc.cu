@@ -19,8 +19,10 @@
 //                   max (rescaling its O in TMEM only when the max grows past
 //                   2^8), its own sum and its own O, combined once at the end)
 //   O_h += P_h V_h (tcgen05, M=128, N=64 per half of dh, K=64 keys)
-// S of the next chunk is computed while this chunk's softmax runs; P is
-// double-buffered.  K and V pages come by TMA (16 keys x 64 dims per copy,
+// S and P are double-buffered (S in TMEM, P in shared memory): S of the next
+// chunk is computed while this chunk's softmax runs, and it needs only that
+// every softmax warp has read the S two chunks back, so a slow warp never
+// waits for the scores of its next chunk.  K and V pages come by TMA (16 keys x 64 dims per copy,
 // 128-byte swizzle) into a 3-stage ring (2 for dh=128).  Splits of one
 // (r, g, tile) are merged by the CTA that finishes last, in split order
 // (deterministic).
@@ -51,7 +53,13 @@ struct AttnCfg {
   static constexpr int K_OFF = Q_OFF + NH * TILE;                 // [stage][NH]
   static constexpr int V_OFF = K_OFF + KV_STAGES * NH * TILE;     // [stage][NH]
   static constexpr int P_OFF = V_OFF + KV_STAGES * NH * TILE;     // [buffer][key half]
-  // float[4][128] for combining the two halves; used only after the last
+  // Key slices of a chunk: each query row is served by NQ softmax threads,
+  // one per KPW-key slice, each with its own running max, sum and O.  Two
+  // slices (8 softmax warps); four (16 warps) measured no faster at dh 64.
+  static constexpr int NQ = 2;
+  static constexpr int KPW = KEYS / NQ;
+  static constexpr int SOFT = 128 * NQ;          // softmax threads
+  // float[2 NQ][128] for combining the slices; used only after the last
   // P.V has finished reading P, so it shares P's space
   static constexpr int RED_OFF = P_OFF;
   static constexpr int BAR_OFF = P_OFF + 4 * TILE;
@@ -60,16 +68,19 @@ struct AttnCfg {
   static constexpr int BT_ENTRIES = 256;
   static constexpr int BT_OFF = BAR_OFF + 256;
   static constexpr int SMEM = 1024 + BT_OFF + BT_ENTRIES * 4;
-  // TMEM: S at columns 0..127; O of key half h at 128 + h * DH
-  static constexpr int TMEM_COLS = 128 + 2 * DH <= 256 ? 256 : 512;
-  static constexpr int THREADS = 320;           // producer, MMA, 8 softmax warps
+  // TMEM: two S buffers at columns 0..255 (S of chunk c in buffer c % 2);
+  // O of key slice h at 256 + h * DH
+  static constexpr int O_COL = 256;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int THREADS = 64 + SOFT;     // producer, MMA, softmax warps
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128);
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32_bmn(128, 64);
   static_assert(SMEM <= 232448, "shared memory");
+  static_assert(O_COL + NQ * DH <= TMEM_COLS && KPW % 16 == 0, "slices");
 };
 
 template <int DH>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(AttnCfg<DH>::THREADS, 1)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const AttnTcParams p) {
   using C = AttnCfg<DH>;
@@ -80,8 +91,11 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* kv_full = bars;                       // [KV_STAGES]
   uint64_t* kv_empty = bars + C::KV_STAGES;       // [KV_STAGES]
   uint64_t* q_ready = bars + 2 * C::KV_STAGES;
-  uint64_t* s_full = q_ready + 1;
-  uint64_t* s_free = q_ready + 2;
+  // [2] each: one per S buffer.  S(c + 2) reuses the buffer of S(c), so it
+  // waits only until every softmax warp has read S(c): the next chunk's
+  // scores are ready when the slowest warp gets to them.
+  uint64_t* s_full = q_ready + 8;
+  uint64_t* s_free = q_ready + 10;
   // [2]: one per P buffer.  The softmax warps are only loosely coupled: a
   // warp may finish chunk c + 1 while another still computes chunk c, so
   // the arrivals of consecutive chunks must land on different barriers (on
@@ -91,7 +105,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* p_full = q_ready + 3;
   uint64_t* pv_done = q_ready + 5;                // [2]: one per P buffer
   uint64_t* drain = q_ready + 7;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 12);
   volatile int* flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
   float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
@@ -130,10 +144,12 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&kv_empty[i], 1);
     }
     mbar_init(q_ready, 1);
-    mbar_init(s_full, 1);
-    mbar_init(s_free, 256);
-    mbar_init(&p_full[0], 256);
-    mbar_init(&p_full[1], 256);
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
+    mbar_init(&s_free[0], C::SOFT);
+    mbar_init(&s_free[1], C::SOFT);
+    mbar_init(&p_full[0], C::SOFT);
+    mbar_init(&p_full[1], C::SOFT);
     mbar_init(&pv_done[0], 1);
     mbar_init(&pv_done[1], 1);
     mbar_init(drain, 1);
@@ -222,17 +238,17 @@ __global__ void __launch_bounds__(320, 1)
       auto issue_s = [&](int c) -> bool {
         const int st = c % C::KV_STAGES;
         if (!mbar_wait(&kv_full[st], (c / C::KV_STAGES) & 1, a.err)) return false;
-        if (c > 0 && !mbar_wait(s_free, (c - 1) & 1, a.err)) return false;
+        if (c >= 2 && !mbar_wait(&s_free[c & 1], ((c - 2) >> 1) & 1, a.err)) return false;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(smem + C::K_OFF + st * C::NH * C::TILE);
 #pragma unroll
         for (int h = 0; h < C::NH; ++h)
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4)
-            umma_bf16(tmem, sw128_kmajor_desc(q_addr + h * C::TILE + k4 * 32),
+            umma_bf16(tmem + (c & 1) * 128, sw128_kmajor_desc(q_addr + h * C::TILE + k4 * 32),
                       sw128_kmajor_desc(k_addr + h * C::TILE + k4 * 32), C::IDESC_S,
                       (h | k4) != 0);
-        umma_commit(s_full);
+        umma_commit(&s_full[c & 1]);
         return true;
       };
       bool ok = mbar_wait(q_ready, 0, a.err) && issue_s(0);
@@ -244,17 +260,20 @@ __global__ void __launch_bounds__(320, 1)
         const int st = c % C::KV_STAGES;
         const uint32_t v_addr = smem_u32(smem + C::V_OFF + st * C::NH * C::TILE);
         const uint32_t p_addr = smem_u32(smem + C::P_OFF + (c & 1) * 2 * C::TILE);
-        // O_h += P(keys of half h) V(keys of half h), per 64-wide half of dh
+        // O_h += P(keys of slice h) V(keys of slice h), per 64-wide part of
+        // dh; P is stored as two 64-key half tiles
 #pragma unroll
-        for (int kh = 0; kh < 2; ++kh)
+        for (int sl = 0; sl < C::NQ; ++sl)
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const uint64_t adesc = sw128_kmajor_desc(p_addr + kh * C::TILE + k4 * 32);
+          for (int k = 0; k < C::KPW / 16; ++k) {
+            const int kk = sl * C::KPW + k * 16;     // first key of this step
+            const uint64_t adesc =
+                sw128_kmajor_desc(p_addr + (kk / 64) * C::TILE + ((kk % 64) / 16) * 32);
 #pragma unroll
             for (int j = 0; j < C::NH; ++j)
-              umma_bf16(tmem + 128 + kh * DH + j * 64, adesc,
-                        sw128_mnmajor_desc(v_addr + j * C::TILE + (kh * 64 + k4 * 16) * 128),
-                        C::IDESC_PV, (c > 0 || k4 > 0) ? 1u : 0u);
+              umma_bf16(tmem + C::O_COL + sl * DH + j * 64, adesc,
+                        sw128_mnmajor_desc(v_addr + j * C::TILE + kk * 128), C::IDESC_PV,
+                        (c > 0 || k > 0) ? 1u : 0u);
           }
         umma_commit(&kv_empty[st]);
         umma_commit(&pv_done[c & 1]);
@@ -264,8 +283,8 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    // two warps per TMEM lane quarter: half h takes keys h*64..h*64+63 of
-    // every chunk and runs its own online softmax into its own O
+    // NQ warps per TMEM lane quarter: slice h takes keys h*KPW..h*KPW+KPW-1
+    // of every chunk and runs its own online softmax into its own O
     const int qrow = 32 * (warp & 3) + lane;
     const int h = (warp - 2) >> 2;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
@@ -280,8 +299,8 @@ __global__ void __launch_bounds__(320, 1)
       const uint4* src = reinterpret_cast<const uint4*>(
           static_cast<const bf16*>(a.q) + (static_cast<size_t>(row) * a.Hq + head) * DH);
 #pragma unroll
-      for (int i = 0; i < 4 * C::NH; ++i) {
-        const int ch = h * 4 * C::NH + i;
+      for (int i = 0; i < 8 * C::NH / C::NQ; ++i) {
+        const int ch = h * (8 * C::NH / C::NQ) + i;
         const int tl = ch >> 3, cc = ch & 7;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (P >= 0) v = src[ch];
@@ -290,35 +309,37 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
     fence_proxy_async_smem();
-    named_bar_sync(1, 256);
+    named_bar_sync(1, C::SOFT);
     if (threadIdx.x == 64) mbar_arrive(q_ready);
 
     const float sc = a.scale * 1.4426950408889634f;   // log2(e) / sqrt(dh)
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    const uint32_t o_col = 128 + h * DH;
+    const uint32_t o_col = C::O_COL + h * DH;
     for (int c = 0; c < nchunks; ++c) {
-      if (!mbar_wait(s_full, c & 1, a.err)) { ok = false; break; }
+      if (!mbar_wait(&s_full[c & 1], (c >> 1) & 1, a.err)) { ok = false; break; }
       tc_fence_after();
-      float sv[4][16];
+      constexpr int KPW = C::KPW;
+      float sv[KPW / 16][16];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) tmem_ld16(tmem + lane_off + h * 64 + q * 16, sv[q]);
+      for (int q = 0; q < KPW / 16; ++q)
+        tmem_ld16(tmem + lane_off + (c & 1) * 128 + h * KPW + q * 16, sv[q]);
       tmem_ld_wait();
 #pragma unroll
-      for (int q = 0; q < 4; ++q) reg_fence16(sv[q]);
+      for (int q = 0; q < KPW / 16; ++q) reg_fence16(sv[q]);
       const float* s = &sv[0][0];
       tc_fence_before();
-      mbar_arrive(s_free);                          // S may be overwritten now
-      const int tb = key0 + c * C::KEYS + h * 64;   // first key of this half
-      const bool whole = tb + 63 <= P;              // no masking inside
+      mbar_arrive(&s_free[c & 1]);                  // this S buffer may be reused
+      const int tb = key0 + c * C::KEYS + h * KPW;  // first key of this slice
+      const bool whole = tb + KPW - 1 <= P;         // no masking inside
       // masked maximum (four independent chains)
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (whole) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) m4[j & 3] = fmaxf(m4[j & 3], s[j]);
+        for (int j = 0; j < KPW; ++j) m4[j & 3] = fmaxf(m4[j & 3], s[j]);
       } else {
 #pragma unroll
-        for (int j = 0; j < 64; ++j)
+        for (int j = 0; j < KPW; ++j)
           if (tb + j <= P) m4[j & 3] = fmaxf(m4[j & 3], s[j]);
       }
       const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sc;  // sc > 0
@@ -333,12 +354,12 @@ __global__ void __launch_bounds__(320, 1)
       }
       // probabilities: one FFMA and one MUFU.EX2 a score; the row sum is
       // kept in fp32 (two chains), P goes to the MMA as bf16 pairs
-      uint32_t pk[32];
+      uint32_t pk[KPW / 2];
       float ps0 = 0.f, ps1 = 0.f;
       const float nm = -m_new;
       if (whole) {
 #pragma unroll
-        for (int j = 0; j < 64; j += 2) {
+        for (int j = 0; j < KPW; j += 2) {
           const float p0 = fast_exp2(fmaf(s[j], sc, nm));
           const float p1 = fast_exp2(fmaf(s[j + 1], sc, nm));
           ps0 += p0;
@@ -347,7 +368,7 @@ __global__ void __launch_bounds__(320, 1)
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < 64; j += 2) {
+        for (int j = 0; j < KPW; j += 2) {
           const float e0 = fast_exp2(fmaf(s[j], sc, nm));
           const float e1 = fast_exp2(fmaf(s[j + 1], sc, nm));
           const float p0 = (tb + j <= P) ? e0 : 0.f;
@@ -378,12 +399,16 @@ __global__ void __launch_bounds__(320, 1)
         }
         tmem_st_wait();
       }
-      // P row of this half -> its 64-key tile of the chunk's P buffer
-      uint8_t* pt = smem + C::P_OFF + ((c & 1) * 2 + h) * C::TILE + qrow * 128;
+      // P row of this slice -> its 16-byte chunks of the 64-key half tile
+      // of the chunk's P buffer that holds it (128-byte swizzle)
+      {
+        uint8_t* pt = smem + C::P_OFF + ((c & 1) * 2 + (h * KPW) / 64) * C::TILE + qrow * 128;
+        const int cb = ((h * KPW) % 64) / 8;
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc)
-        *reinterpret_cast<uint4*>(pt + ((cc ^ (qrow & 7)) * 16)) =
-            make_uint4(pk[cc * 4], pk[cc * 4 + 1], pk[cc * 4 + 2], pk[cc * 4 + 3]);
+        for (int cc = 0; cc < KPW / 8; ++cc)
+          *reinterpret_cast<uint4*>(pt + (((cb + cc) ^ (qrow & 7)) * 16)) =
+              make_uint4(pk[cc * 4], pk[cc * 4 + 1], pk[cc * 4 + 2], pk[cc * 4 + 3]);
+      }
       // keys past the sequence end: zero their V rows so 0 * garbage cannot
       // reach O (the pool may hold anything there)
       const int t0 = key0 + c * C::KEYS;
@@ -403,31 +428,44 @@ __global__ void __launch_bounds__(320, 1)
     }
     if (ok && !mbar_wait(&pv_done[(nchunks - 1) & 1], ((nchunks - 1) >> 1) & 1, a.err)) ok = false;
     if (!ok) *abort_flag = 1;
-    // combine the two halves: (m, l) through shared memory
+    // combine the slices: (m, l) through shared memory
     red[h * 128 + qrow] = m_used;
-    red[(2 + h) * 128 + qrow] = l;
-    named_bar_sync(1, 256);
+    red[(C::NQ + h) * 128 + qrow] = l;
+    named_bar_sync(1, C::SOFT);
     if (!*abort_flag) {
       tc_fence_after();
-      const float m0 = red[qrow], m1 = red[128 + qrow];
-      const float l0 = red[256 + qrow], l1 = red[384 + qrow];
-      const float M = fmaxf(m0, m1);
-      const float w0 = m0 > -INFINITY ? exp2f(m0 - M) : 0.f;
-      const float w1 = m1 > -INFINITY ? exp2f(m1 - M) : 0.f;
-      const float L = l0 * w0 + l1 * w1;
-      // this thread finishes columns h*DH/2 .. h*DH/2 + DH/2 of its row
-      constexpr int HC = DH / 2;
+      float mi[C::NQ], wi[C::NQ];
+      float M = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < C::NQ; ++i) {
+        mi[i] = red[i * 128 + qrow];
+        M = fmaxf(M, mi[i]);
+      }
+      float L = 0.f;
+#pragma unroll
+      for (int i = 0; i < C::NQ; ++i) {
+        wi[i] = mi[i] > -INFINITY ? exp2f(mi[i] - M) : 0.f;
+        L += red[(C::NQ + i) * 128 + qrow] * wi[i];
+      }
+      // this thread finishes columns h*HC .. h*HC + HC - 1 of its row
+      constexpr int HC = DH / C::NQ;
       float o[HC];
 #pragma unroll
       for (int c0 = 0; c0 < HC; c0 += 16) {
-        float x0[16], x1[16];
-        tmem_ld16(tmem + lane_off + 128 + h * HC + c0, x0);
-        tmem_ld16(tmem + lane_off + 128 + DH + h * HC + c0, x1);
-        tmem_ld_wait();
-        reg_fence16(x0);
-        reg_fence16(x1);
+        float x[C::NQ][16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) o[c0 + j] = x0[j] * w0 + x1[j] * w1;
+        for (int i = 0; i < C::NQ; ++i)
+          tmem_ld16(tmem + lane_off + C::O_COL + i * DH + h * HC + c0, x[i]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < C::NQ; ++i) reg_fence16(x[i]);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float acc = 0.f;
+#pragma unroll
+          for (int i = 0; i < C::NQ; ++i) acc += x[i][j] * wi[i];
+          o[c0 + j] = acc;
+        }
       }
       bf16* out = static_cast<bf16*>(a.out) + (static_cast<size_t>(row) * a.Hq + head) * DH + h * HC;
       if (nsplits == 1) {
@@ -451,12 +489,12 @@ __global__ void __launch_bounds__(320, 1)
           mine[(DH + 1) * 128] = L;
         }
         __threadfence();
-        named_bar_sync(1, 256);
+        named_bar_sync(1, C::SOFT);
         if (threadIdx.x == 64) {
           const int old = atomicAdd(p.counters + unit, 1);
           *flag = (old == nsplits - 1) ? 1 : 0;
         }
-        named_bar_sync(1, 256);
+        named_bar_sync(1, C::SOFT);
         if (*flag) {
           __threadfence();
           const float* base = p.part + unit * p.max_splits * stride + qrow;
