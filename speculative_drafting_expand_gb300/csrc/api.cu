@@ -15,8 +15,8 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
                                 const CUtensorMap& xb, bool dual, int M, int N, int K,
                                 const EpiArgs& epi, const TcGemmWorkspace& ws, int* err,
                                 cudaStream_t s);
-int tc_pick_bn(int M);
-int tc_b_box_rows(int M, int N, int sm_count);
+int tc_pick_bn(int M, bool dual);
+int tc_b_box_rows(int M, int N, int sm_count, bool dual);
 cudaError_t init_gemm_tc();
 size_t tc_partial_floats(int grid, int bn, bool dual);
 cudaError_t init_attention_tc();
@@ -118,7 +118,7 @@ cudaError_t linear(pe_handle* h, const void* x, int ldx, const void* w, const vo
                                        static_cast<const float*>(w2), M, N, K, epi, h->err, s));
   const CUtensorMap* wa = get_map(h, w, N, K, K, 128);
   const CUtensorMap* wa2 = w2 ? get_map(h, w2, N, K, K, 128) : wa;
-  const CUtensorMap* xb = get_map(h, x, M, K, ldx, tc_b_box_rows(M, N, h->sm_count));
+  const CUtensorMap* xb = get_map(h, x, M, K, ldx, tc_b_box_rows(M, N, h->sm_count, w2 != nullptr));
   if (!wa || !wa2 || !xb) return cudaErrorInvalidValue;
   return counted(h, launch_gemm_tc_maps(*wa, *wa2, *xb, w2 != nullptr, M, N, K, epi, tc_ws(h),
                                         h->err, s));
@@ -226,7 +226,7 @@ pe_status pe_create(const pe_model_desc* desc, const pe_weights* weights, int32_
   if (e == cudaSuccess && d.dtype == PE_DTYPE_BF16) e = init_gemm_tc();
   if (e == cudaSuccess && d.dtype == PE_DTYPE_BF16) e = init_attention_tc();
   if (e == cudaSuccess && d.dtype == PE_DTYPE_BF16) {
-    const int bn = tc_pick_bn(max_tokens);
+    const int bn = tc_pick_bn(max_tokens, false);
     h->gemm_partial_floats = tc_partial_floats(h->sm_count, bn, true);
     e = dev_alloc(h, &h->gemm_partials, h->gemm_partial_floats);
     const int widest = std::max({d.vocab, qkv_rows, d.ffn, d.d, qd});
@@ -558,7 +558,7 @@ pe_status pe_linear(pe_handle* h, const void* x, const void* w, float* y, int32_
   if (h->desc.dtype == PE_DTYPE_BF16 && (K % 8 || !aligned16(x) || !aligned16(w)))
     return PE_ERR_INVALID_ARGUMENT;
   if (h->desc.dtype == PE_DTYPE_BF16) {
-    const int bn = tc_pick_bn(M);
+    const int bn = tc_pick_bn(M, false);
     const long long tiles = static_cast<long long>((N + 127) / 128) * ((M + bn - 1) / bn);
     if (tiles > h->max_tiles) return PE_ERR_INVALID_ARGUMENT;
   }

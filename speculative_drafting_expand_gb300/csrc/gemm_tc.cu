@@ -27,10 +27,11 @@
 
 namespace pe {
 
-// Two CTAs per SM (at most 170 registers a thread): the next kernel's CTA
-// can start on an SM while this one drains.
+// Narrow token tiles: two CTAs per SM (at most 170 registers a thread), so
+// the next kernel's CTA can start on an SM while this one drains.  From 64
+// tokens on the stages fill the shared memory and one CTA runs per SM.
 template <int BN, bool DUAL>
-__global__ void __launch_bounds__(192, 2)
+__global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                    const __grid_constant__ CUtensorMap tmB, const TcParams p) {
   using C = TcCfg<BN, DUAL>;
@@ -199,15 +200,9 @@ __global__ void __launch_bounds__(192, 2)
       const int o = f * 128 + row;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * C::ACC_COLS;
       if (k_lo == 0 && k_hi == kb) {
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-          float v[16], v2[16];
-          tmem_ld16(taddr + c0, v);
-          if (DUAL) tmem_ld16(taddr + BN + c0, v2);
-          tmem_ld_wait();
-          reg_fence16(v);
-          if (DUAL) reg_fence16(v2);
+        tmem_walk<BN, DUAL>(taddr, [&](int c0, const float* v, const float* v2) {
           epi_chunk<DUAL>(p.epi, o, m * BN + c0, v, v2, lane);
-        }
+        });
         tc_fence_before();
         mbar_arrive(&acc_empty[acc]);
       } else if (p.split_s >= 2) {
@@ -215,37 +210,25 @@ __global__ void __launch_bounds__(192, 2)
         // (the operand stages are all consumed); rank 0 sums the cluster's
         // partials after the cluster barrier below
         float* part = reinterpret_cast<float*>(smem);
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-          float v[16], v2[16];
-          tmem_ld16(taddr + c0, v);
-          if (DUAL) tmem_ld16(taddr + BN + c0, v2);
-          tmem_ld_wait();
-          reg_fence16(v);
-          if (DUAL) reg_fence16(v2);
+        tmem_walk<BN, DUAL>(taddr, [&](int c0, const float* v, const float* v2) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             part[(c0 + j) * 128 + row] = v[j];
             if (DUAL) part[(BN + c0 + j) * 128 + row] = v2[j];
           }
-        }
+        });
         tc_fence_before();
         mbar_arrive(&acc_empty[acc]);
       } else {
         const int slot = (u == lo) ? 0 : 1;
         float* wsp = p.ws + (static_cast<size_t>(cta) * 2 + slot) * (128 * C::ACC_COLS);
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-          float v[16], v2[16];
-          tmem_ld16(taddr + c0, v);
-          if (DUAL) tmem_ld16(taddr + BN + c0, v2);
-          tmem_ld_wait();
-          reg_fence16(v);
-          if (DUAL) reg_fence16(v2);
+        tmem_walk<BN, DUAL>(taddr, [&](int c0, const float* v, const float* v2) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             wsp[(c0 + j) * 128 + row] = v[j];
             if (DUAL) wsp[(BN + c0 + j) * 128 + row] = v2[j];
           }
-        }
+        });
         tc_fence_before();
         mbar_arrive(&acc_empty[acc]);
         __threadfence();
@@ -257,7 +240,63 @@ __global__ void __launch_bounds__(192, 2)
           *flag = (old == c_last - c_first) ? 1 : 0;
         }
         named_bar_sync(1, 128);
-        if (*flag) {
+        // contributors the pipelined path holds in registers: a tile spans at
+        // most three CTAs at the wide-tile shapes of the drafter (k-blocks
+        // per tile below twice the k-blocks per CTA), two at the others
+        // (none for the gate/up pair at 32 tokens or fewer: its registers
+        // are capped by two CTAs an SM, and it splits by clusters there)
+        constexpr int NCM = (DUAL && BN <= 32) ? 0 : (DUAL || BN <= 64) ? 2 : 3;
+        if (NCM > 0 && *flag && c_last - c_first < NCM) {
+          // up to NCM contributors (the usual split): the loads of the next
+          // chunk's partials are in flight while this chunk is summed (in
+          // contributor order) and stored
+          __threadfence();
+          const int nc = c_last - c_first + 1;
+          constexpr int NCA = NCM > 0 ? NCM : 1;
+          const float* src[NCA];
+#pragma unroll
+          for (int q = 0; q < NCA; ++q) {
+            const int cq = min(c_first + q, c_last);
+            const int cs = unit_lo(cq, U, G) >= static_cast<long long>(tile) * kb ? 0 : 1;
+            src[q] = p.ws + (static_cast<size_t>(cq) * 2 + cs) * (128 * C::ACC_COLS) + row;
+          }
+          constexpr int W = DUAL ? 32 : 16;  // values per contributor and chunk
+          float xa[NCA][W], xb[NCA][W];
+          auto load = [&](int c0, float (&x)[NCA][W]) {
+#pragma unroll
+            for (int q = 0; q < NCA; ++q)
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                x[q][j] = q < nc ? __ldcg(src[q] + (c0 + j) * 128) : 0.f;
+                if (DUAL) x[q][16 + j] = q < nc ? __ldcg(src[q] + (BN + c0 + j) * 128) : 0.f;
+              }
+          };
+          auto finish = [&](int c0, const float (&x)[NCA][W]) {
+            float v[16], v2[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = v2[j] = 0.f;
+#pragma unroll
+            for (int q = 0; q < NCA; ++q)
+              if (q < nc)
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  v[j] += x[q][j];
+                  if (DUAL) v2[j] += x[q][16 + j];
+                }
+            epi_chunk<DUAL>(p.epi, o, m * BN + c0, v, v2, lane);
+          };
+          load(0, xa);
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN; c0 += 32) {
+            if (c0 + 16 < BN) load(c0 + 16, xb);
+            finish(c0, xa);
+            if (c0 + 16 < BN) {
+              if (c0 + 32 < BN) load(c0 + 32, xa);
+              finish(c0 + 16, xb);
+            }
+          }
+          if (threadIdx.x == 0) p.counters[tile] = 0;
+        } else if (*flag) {
           __threadfence();
           for (int c0 = 0; c0 < BN; c0 += 16) {
             float v[16], v2[16];
@@ -397,10 +436,45 @@ bool tensor_map_2d_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Clusters of S CTAs (2..8) that can be resident at once, per
+// instantiation and device, queried at init (0 when unknown).
+constexpr int kMaxDev = 64;
+template <int BN, bool DUAL>
+int g_tc_clusters[kMaxDev][9];
+
+template <int BN, bool DUAL>
+int tc_max_clusters(int S) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  return g_tc_clusters<BN, DUAL>[dev][S];
+}
+
 template <int BN, bool DUAL>
 static cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(gemm_tc_kernel<BN, DUAL>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<BN, DUAL>::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, DUAL>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       TcCfg<BN, DUAL>::SMEM);
+  int dev = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  for (int S = 2; S <= 8 && e == cudaSuccess; ++S) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S * 32);
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = TcCfg<BN, DUAL>::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, DUAL>, &cfg);
+    g_tc_clusters<BN, DUAL>[dev][S] = n;
+  }
+  return e;
 }
 
 // Opt every instantiation into its dynamic shared memory (once per process
@@ -431,11 +505,20 @@ static cudaError_t run_tc(const CUtensorMap& a, const CUtensorMap& a2, const CUt
   // reduce through distributed shared memory.  Otherwise stream-K.
   const bool fits = static_cast<size_t>(C::ACC_COLS) * 128 * 4 <=
                     static_cast<size_t>(C::STAGES) * C::STAGE_BYTES;
-  // The whole grid must fit in one wave: two CTAs an SM when the stages fit
-  // in about half of the shared memory, otherwise one.
+  // S CTAs a tile, about one CTA per SM in all (measured best in the
+  // drafting step: with two CTAs an SM resident, the next kernel's CTAs
+  // start beside these), at most 8 a tile and one k-block each; the whole
+  // grid fits one wave (two CTAs an SM when the stages fit in about half
+  // of the shared memory, otherwise one).
   const int per_sm = C::SMEM <= 113 * 1024 ? 2 : 1;
-  int S = per_sm == 2 ? (sm_count + tiles / 2) / tiles : sm_count / std::max(1, tiles);
+  int S = per_sm == 2 ? (sm_count + tiles / 2) / std::max(1, tiles) : sm_count / std::max(1, tiles);
   S = std::min(S, std::min(8, p.kb));
+  // One CTA an SM: clusters are placed whole within a GPC, so no more than
+  // the resident-cluster count the runtime reports (a cluster left for a
+  // second wave doubles the time; measured on 256-row projections).  With
+  // two an SM that count measured too low, and the one-per-SM total fits.
+  if (per_sm == 1)
+    while (S >= 2 && tiles > tc_max_clusters<BN, DUAL>(S)) --S;
   if (tiles < sm_count && fits && (S >= 2 || per_sm == 2) && S >= 1 &&
       tiles * S <= per_sm * sm_count) {
     p.split_s = S;
@@ -450,21 +533,25 @@ static cudaError_t run_tc(const CUtensorMap& a, const CUtensorMap& a2, const CUt
   return launch_pdl(gemm_tc_kernel<BN, DUAL>, dim3(grid), dim3(192), C::SMEM, s, a, a2, b, p);
 }
 
-int tc_pick_bn(int M) {
+// Token-tile width for M rows.  The gate/up pair (dual) stays at 128 from
+// there on: at 256 its two accumulators fill the tensor memory (no overlap
+// of the epilogue with the next tile) and its 64 KB stages leave room for
+// three (measured 136 us against about 90 us at 128 on 896 x 15360 x 2880).
+int tc_pick_bn(int M, bool dual) {
   if (M <= 16) return 16;
   if (M <= 32) return 32;
   if (M <= 64) return 64;
-  if (M <= 128) return 128;
+  if (M <= 128 || dual) return 128;
   return 256;
 }
 
 // Rows of the token box in the x tensor map that launch_gemm_tc_maps
 // expects for an M x N projection: the token tile, or its slice when the
 // multicast kernel takes the projection.
-int tc_b_box_rows(int M, int N, int sm_count) {
-  const int bn = tc_pick_bn(M);
+int tc_b_box_rows(int M, int N, int sm_count, bool dual) {
+  const int bn = tc_pick_bn(M, dual);
   const long long tiles = static_cast<long long>((N + 127) / 128) * ((M + bn - 1) / bn);
-  return bn / gemm_mc_cluster(bn, false, tiles, sm_count);
+  return bn / gemm_mc_cluster(bn, dual, tiles, sm_count);
 }
 
 size_t tc_partial_floats(int grid, int bn, bool dual) {
@@ -476,7 +563,7 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
                                 const EpiArgs& epi, const TcGemmWorkspace& ws, int* err,
                                 cudaStream_t s) {
   if (M <= 0 || N <= 0) return cudaSuccess;
-  const int bn = tc_pick_bn(M);
+  const int bn = tc_pick_bn(M, dual);
   TcParams p;
   p.M = M;
   p.N = N;
@@ -520,7 +607,7 @@ cudaError_t launch_gemm_tc(const void* x, int ldx, const void* w, const void* w2
   if (!tensor_map_2d_bf16(&wa, w, N, K, K, 64, 128)) return cudaErrorInvalidValue;
   wa2 = wa;
   if (w2 && !tensor_map_2d_bf16(&wa2, w2, N, K, K, 64, 128)) return cudaErrorInvalidValue;
-  if (!tensor_map_2d_bf16(&xb, x, M, K, ldx, 64, tc_b_box_rows(M, N, ws.sm_count)))
+  if (!tensor_map_2d_bf16(&xb, x, M, K, ldx, 64, tc_b_box_rows(M, N, ws.sm_count, w2 != nullptr)))
     return cudaErrorInvalidValue;
   return launch_gemm_tc_maps(wa, wa2, xb, w2 != nullptr, M, N, K, epi, ws, err, s);
 }

@@ -140,6 +140,44 @@ __device__ __forceinline__ void epi_chunk(const EpiArgs& e, int o, int t0, const
   }
 }
 
+// Walk the BN accumulator columns of a TMEM lane quarter in 16-column
+// chunks with the load of the next chunk in flight while fn(c0, v, v2)
+// consumes the current one (the load latency is paid once, not per chunk).
+template <int BN, bool DUAL, typename F>
+__device__ __forceinline__ void tmem_walk(uint32_t taddr, F&& fn) {
+  float a[16], a2[16], b[16], b2[16];
+  tmem_ld16(taddr, a);
+  if (DUAL) tmem_ld16(taddr + BN, a2);
+  tmem_ld_wait();
+  reg_fence16(a);
+  if (DUAL) reg_fence16(a2);
+#pragma unroll 1
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    const bool nb = c0 + 16 < BN;
+    if (nb) {
+      tmem_ld16(taddr + c0 + 16, b);
+      if (DUAL) tmem_ld16(taddr + BN + c0 + 16, b2);
+    }
+    fn(c0, a, a2);
+    if (nb) {
+      tmem_ld_wait();
+      reg_fence16(b);
+      if (DUAL) reg_fence16(b2);
+      const bool na = c0 + 32 < BN;
+      if (na) {
+        tmem_ld16(taddr + c0 + 32, a);
+        if (DUAL) tmem_ld16(taddr + BN + c0 + 32, a2);
+      }
+      fn(c0 + 16, b, b2);
+      if (na) {
+        tmem_ld_wait();
+        reg_fence16(a);
+        if (DUAL) reg_fence16(a2);
+      }
+    }
+  }
+}
+
 // The multicast-cluster kernel (gemm_mc.cu).
 cudaError_t init_gemm_mc();
 // Cluster size for a projection of `tiles` 128 x bn tiles: 1 = gemm_tc.cu.
