@@ -226,7 +226,8 @@ pe_status pe_create(const pe_model_desc* desc, const pe_weights* weights, int32_
   if (e == cudaSuccess && d.dtype == PE_DTYPE_BF16) e = init_gemm_tc();
   if (e == cudaSuccess && d.dtype == PE_DTYPE_BF16) e = init_attention_tc();
   if (e == cudaSuccess && d.dtype == PE_DTYPE_BF16) {
-    const int bn = tc_pick_bn(max_tokens, false);
+    // the widest token tile any row count up to max_tokens can take
+    const int bn = max_tokens > 128 ? 256 : tc_pick_bn(max_tokens, false);
     h->gemm_partial_floats = tc_partial_floats(h->sm_count, bn, true);
     e = dev_alloc(h, &h->gemm_partials, h->gemm_partial_floats);
     const int widest = std::max({d.vocab, qkv_rows, d.ffn, d.d, qd});

@@ -11,7 +11,7 @@
 // token slice goes by one TMA multicast into the same stage of every CTA of
 // the cluster, so L2 delivers 16 KB of weights plus 32/CS KB of tokens per
 // k-block and CTA.  On the LM head at 448-896 tokens, pairs are about 5%
-// faster than one CTA per tile (gemm_tc.cu).
+// faster than one CTA per tile (gemm_tc.cu).  Token tiles of 224 or 256.
 //
 // Pipeline per CTA (warp roles as in gemm_tc.cu: warps 0-3 epilogue, warp 4
 // TMA producer, warp 5 MMA issuer and TMEM owner):
@@ -236,7 +236,8 @@ namespace {
 
 constexpr int kMaxDev = 64;
 // clusters of each instantiation that can be resident at once, per device
-int g_max_clusters[kMaxDev];  // [device], for the one instantiation below
+int g_max_clusters[kMaxDev][2];  // [device][token tile 224 / 256]
+int bn_slot(int bn) { return bn == 224 ? 0 : 1; }
 
 template <int BN, bool DUAL, int CS>
 cudaError_t init_one(int dev) {
@@ -258,7 +259,7 @@ cudaError_t init_one(int dev) {
   int n = 0;
   e = cudaOccupancyMaxActiveClusters(&n, gemm_mc_kernel<BN, DUAL, CS>, &cfg);
   if (e != cudaSuccess) return e;
-  g_max_clusters[dev] = n;
+  g_max_clusters[dev][bn_slot(BN)] = n;
   return cudaSuccess;
 }
 
@@ -268,7 +269,7 @@ cudaError_t run_mc(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMa
   using C = TcCfg<BN, DUAL>;
   const int tiles_f = (p.N + 127) / 128;
   const long long groups = static_cast<long long>((tiles_f + CS - 1) / CS) * p.tiles_m;
-  const int most = g_max_clusters[dev];
+  const int most = g_max_clusters[dev][bn_slot(BN)];
   const int ncl = static_cast<int>(std::min<long long>(groups, most));
   if (ncl < 1) return cudaErrorInvalidValue;
   return launch_pdl_cluster(gemm_mc_kernel<BN, DUAL, CS>, dim3(ncl * CS), dim3(192), C::SMEM, s,
@@ -284,6 +285,7 @@ cudaError_t init_gemm_mc() {
   if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
 #define PE_MC_INIT(BNV, DV, CSV) \
   if (e == cudaSuccess) e = init_one<BNV, DV, CSV>(dev);
+  PE_MC_INIT(224, false, 2)
   PE_MC_INIT(256, false, 2)
 #undef PE_MC_INIT
   return e;
@@ -292,10 +294,11 @@ cudaError_t init_gemm_mc() {
 // Measured on the LM head (d 2880, vocab 201088): pairs sharing 256-token
 // tiles gain about 5% at 448 and 896 tokens over one CTA per tile; clusters
 // of 4 leave 8 SMs idle (36 resident clusters) and lose; for 128-token
-// tiles the one-CTA kernel is faster.  So: pairs, for 256-token tiles, with
-// at least four tiles per SM; the gate/up pair (dual) keeps gemm_tc.cu.
+// tiles the one-CTA kernel is faster.  So: pairs, for 224- and 256-token
+// tiles, with at least four tiles per SM; the gate/up pair (dual) keeps
+// gemm_tc.cu.
 int gemm_mc_cluster(int bn, bool dual, long long tiles, int sm_count) {
-  if (bn != 256 || dual) return 1;
+  if ((bn != 224 && bn != 256) || dual) return 1;
   return tiles >= 4LL * sm_count ? 2 : 1;
 }
 
@@ -308,6 +311,7 @@ cudaError_t launch_gemm_mc(const CUtensorMap& a, const CUtensorMap& a2, const CU
   if (dual) return cudaErrorInvalidValue;
 #define PE_MC_CASE(BNV, CSV) \
   if (bn == BNV && cs == CSV) return run_mc<BNV, false, CSV>(a, a2, b, p, dev, s);
+  PE_MC_CASE(224, 2)
   PE_MC_CASE(256, 2)
 #undef PE_MC_CASE
   return cudaErrorInvalidValue;

@@ -488,6 +488,7 @@ cudaError_t init_gemm_tc() {
   PE_TC_ATTR(32)
   PE_TC_ATTR(64)
   PE_TC_ATTR(128)
+  PE_TC_ATTR(224)
   PE_TC_ATTR(256)
 #undef PE_TC_ATTR
   if (e == cudaSuccess) e = init_gemm_mc();
@@ -537,12 +538,15 @@ static cudaError_t run_tc(const CUtensorMap& a, const CUtensorMap& a2, const CUt
 // there on: at 256 its two accumulators fill the tensor memory (no overlap
 // of the epilogue with the next tile) and its 64 KB stages leave room for
 // three (measured 136 us against about 90 us at 128 on 896 x 15360 x 2880).
+// Above 128 rows the others take ceil(M / 256) tiles of 224 tokens when
+// they cover M (448 and 896 rows: no padded columns) and of 256 otherwise.
 int tc_pick_bn(int M, bool dual) {
   if (M <= 16) return 16;
   if (M <= 32) return 32;
   if (M <= 64) return 64;
   if (M <= 128 || dual) return 128;
-  return 256;
+  const int tm = (M + 255) / 256;
+  return (M + tm - 1) / tm <= 224 ? 224 : 256;
 }
 
 // Rows of the token box in the x tensor map that launch_gemm_tc_maps
@@ -593,6 +597,7 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
     PE_TC_CASE(32)
     PE_TC_CASE(64)
     PE_TC_CASE(128)
+    PE_TC_CASE(224)
     PE_TC_CASE(256)
   }
 #undef PE_TC_CASE

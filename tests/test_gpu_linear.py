@@ -2,7 +2,7 @@
 
 y = x w^T with bf16 operands and fp32 accumulation (tcgen05, TMEM) against
 an fp64 product of the same bf16 values.  The shapes cover one tile, many
-tiles, ragged token/feature/k tails, every token-tile width (16..256) and
+tiles, ragged token/feature/k tails, every token-tile width (16..224, 256) and
 stream-K splits of a tile across CTAs (the deterministic fix-up path) and
 clusters that share one token tile by TMA multicast (many tiles per SM).
 """
@@ -27,7 +27,8 @@ CASES = [
     (896, 2880, 2880),  # batch-64 shape
     # at least four tiles per SM with 128- or 256-token tiles: clusters of
     # CTAs sharing the token tile by multicast; ragged tokens, features, k
-    (300, 40000, 200),
+    (300, 40000, 200),   # two 224-token tiles, ragged
+    (500, 40000, 200),   # two 256-token tiles, ragged
     (100, 80000, 256),
 ]
 
