@@ -14,7 +14,7 @@ drafts its own batch (requests are independent: weak scaling, no
 collective on the data path).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload b1|b16|b64|qwen-k<K>|expand]
+                  [--workload b1|b16|b64|qwen-k<K>|expand|ar-<workload>]
 """
 
 from __future__ import annotations
@@ -315,6 +315,102 @@ class DeviceInputs:
         self.vc = [B.to_device(v, dt) for v in vc]
 
 
+def run_ar(args, world, rank, local):
+    """Autoregressive drafting of the same K tokens on the same kernels: K
+    sequential passes of the K = 1 step (the pages' baseline, whose cost
+    grows with K).  Pass 0 takes the verify window and drafts the first token;
+    pass i takes one row per request at the next position, whose token is
+    the previous pass's draft (copied on the device), and drafts the next.
+    A reported step is all K passes (K draft tokens per request)."""
+    import torch
+
+    from speculative_drafting_expand_gb300 import binding as B
+
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    wl = workload(args.workload[len("ar-"):])
+    sh, K = wl.shape, wl.K
+    inp = W.make_step_inputs(wl)
+    w = W.make_weights(sh, wl.config_id, gains=wl.gains)
+    kc, vc = W.make_kv_cache(wl, inp)
+    dr = B.Drafter(sh, w, max(wl.T, wl.B), wl.B)
+    st = DeviceInputs(wl, inp, kc, vc, B, torch)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).cuda()
+    tdt = torch.bfloat16 if sh.dtype == "bf16" else torch.float32
+    Bn = wl.B
+    # pass 0: the window, K = 1
+    passes = [dict(ids=st.target_ids, pos=st.target_pos, cu=st.cu_in, acc=st.num_accepted,
+                   samp=st.sampled_ids, hid=st.target_hidden, T=wl.T)]
+    # position of the sampled token's row in pass 0, per request
+    p0 = np.array([int(inp.target_pos[int(inp.cu_in[r]) + int(wl.accepted[r])]) + 1
+                   for r in range(Bn)], np.int64)
+    last_rows = [int(inp.cu_in[r]) + int(wl.accepted[r]) for r in range(Bn)]
+    hid1 = np.ascontiguousarray(inp.target_hidden[last_rows])
+    for i in range(1, K):
+        passes.append(dict(ids=i32(np.zeros(Bn)), pos=i32(p0 + i - 1), cu=i32(np.arange(Bn + 1)),
+                           acc=i32(np.zeros(Bn)), samp=torch.zeros(Bn, dtype=torch.int32, device="cuda"),
+                           hid=B.to_device(hid1, sh.dtype), T=Bn))
+    exs = [B.Expanded(q["T"], q["T"], Bn, 1, sh.hidden3, sh.dtype) for q in passes]
+    outs = [torch.empty(Bn, sh.d, dtype=tdt, device="cuda") for _ in passes]
+    toks = [torch.empty(Bn, dtype=torch.int32, device="cuda") for _ in passes]
+
+    def step():
+        for i, q in enumerate(passes):
+            if i > 0:
+                q["samp"].copy_(toks[i - 1])
+            B.pe_expand_batch(dr, 1, q["ids"], q["pos"], q["cu"], q["acc"], q["samp"],
+                              st.block_table, inp.num_blocks, q["hid"], exs[i])
+            B.pe_draft_forward(dr, exs[i], st.block_table, st.kc, st.vc, inp.num_blocks, outs[i])
+            B.pe_lmhead_argmax(dr, outs[i], toks[i])
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    check_device(B, dr)
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    n0 = B.pe_get_launch_count(dr)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            step()
+    launches_per_step = B.pe_get_launch_count(dr) - n0
+    torch.cuda.synchronize()
+    for _ in range(max(3, args.warmup)):
+        g.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    elapsed_ms = max_over_ranks(world, e0.elapsed_time(e1))
+    clocks.stop()
+    check_device(B, dr)
+    if rank == 0:
+        ms = elapsed_ms / args.steps
+        value = world * args.steps / (elapsed_ms / 1e3)
+        cfg = config_of(wl, args)
+        cfg["workload"] = wl.name + "-autoregressive"
+        cfg["drafting"] = f"autoregressive: {K} sequential passes of the K=1 step per draft step"
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": sh.dtype, "data": "synthetic (seeded random-init weights and inputs)",
+            "config": cfg, "drafted_tok_per_s": value * Bn * K, "mode": "autoregressive",
+            "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,
+            "clocks": clocks.summary()}), flush=True)
+    dr.close()
+    return 0
+
+
 def run_ours(args, world, rank, local):
     import torch
 
@@ -502,6 +598,8 @@ def main():
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.workload.startswith("ar-"):
+        return run_ar(args, world, rank, local)
     return run_ours(args, world, rank, local)
 
 
