@@ -228,7 +228,8 @@ pe_status pe_create(const pe_model_desc* desc, const pe_weights* weights, int32_
   if (e == cudaSuccess && d.dtype == PE_DTYPE_BF16) {
     // the widest token tile any row count up to max_tokens can take
     const int bn = max_tokens > 128 ? 256 : tc_pick_bn(max_tokens, false);
-    h->gemm_partial_floats = tc_partial_floats(h->sm_count, bn, true);
+    // stream-K runs two CTAs an SM for token tiles up to 32 wide
+    h->gemm_partial_floats = tc_partial_floats((bn <= 32 ? 2 : 1) * h->sm_count, bn, true);
     e = dev_alloc(h, &h->gemm_partials, h->gemm_partial_floats);
     const int widest = std::max({d.vocab, qkv_rows, d.ffn, d.d, qd});
     h->max_tiles = ((widest + 127) / 128) * ((max_tokens + 15) / 16);

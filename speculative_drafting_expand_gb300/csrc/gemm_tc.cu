@@ -529,8 +529,12 @@ static cudaError_t run_tc(const CUtensorMap& a, const CUtensorMap& a2, const CUt
                               a, a2, b, p);
   }
   p.split_s = 0;
-  const int grid = static_cast<int>(std::min<long long>(sm_count, units));
-  if (tc_partial_floats(grid, BN, DUAL) > partial_floats) return cudaErrorInvalidValue;
+  // as many CTAs as the SMs hold (two an SM for narrow token tiles: twice
+  // the weight bytes in flight), within the caller's partial workspace
+  const long long ws_ctas = static_cast<long long>(partial_floats / tc_partial_floats(1, BN, DUAL));
+  const int grid = static_cast<int>(
+      std::min<long long>(std::min<long long>(per_sm * sm_count, units), ws_ctas));
+  if (grid < 1) return cudaErrorInvalidValue;
   return launch_pdl(gemm_tc_kernel<BN, DUAL>, dim3(grid), dim3(192), C::SMEM, s, a, a2, b, p);
 }
 
