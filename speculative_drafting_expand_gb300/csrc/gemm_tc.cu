@@ -513,6 +513,12 @@ static cudaError_t run_tc(const CUtensorMap& a, const CUtensorMap& a2, const CUt
   // of the shared memory, otherwise one).
   const int per_sm = C::SMEM <= 113 * 1024 ? 2 : 1;
   int S = per_sm == 2 ? (sm_count + tiles / 2) / std::max(1, tiles) : sm_count / std::max(1, tiles);
+  if (per_sm == 2) {
+    // the next power of two, if the grid still fits two CTAs an SM
+    int S2 = 1;
+    while (S2 < S) S2 *= 2;
+    if (tiles * S2 <= per_sm * sm_count) S = S2;
+  }
   S = std::min(S, std::min(8, p.kb));
   // One CTA an SM: clusters are placed whole within a GPC, so no more than
   // the resident-cluster count the runtime reports (a cluster left for a
