@@ -335,8 +335,14 @@ __global__ void __launch_bounds__(AttnCfg<DH>::THREADS, 1)
       // masked maximum (four independent chains)
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (whole) {
+        // two scores per instruction in each of the four chains
 #pragma unroll
-        for (int j = 0; j < KPW; ++j) m4[j & 3] = fmaxf(m4[j & 3], s[j]);
+        for (int j = 0; j < KPW; j += 8) {
+          m4[0] = fmax3(m4[0], s[j], s[j + 1]);
+          m4[1] = fmax3(m4[1], s[j + 2], s[j + 3]);
+          m4[2] = fmax3(m4[2], s[j + 4], s[j + 5]);
+          m4[3] = fmax3(m4[3], s[j + 6], s[j + 7]);
+        }
       } else {
 #pragma unroll
         for (int j = 0; j < KPW; ++j)

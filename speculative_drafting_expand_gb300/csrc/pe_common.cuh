@@ -331,6 +331,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 // Two floats -> packed bf16 pair (round to nearest even), lo in the low half.
+// Three-input maximum (one instruction on sm_100 and later; a NaN operand
+// loses to a number, as with fmaxf).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&b);
