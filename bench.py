@@ -14,7 +14,7 @@ drafts its own batch (requests are independent: weak scaling, no
 collective on the data path).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload b1|b16|b64|qwen-k<K>|expand|ar-<workload>]
+                  [--workload b1|b16|b64|qwen-k<K>|expand|ar-<workload>|lmhead-<rows>]
 """
 
 from __future__ import annotations
@@ -315,6 +315,48 @@ class DeviceInputs:
         self.vc = [B.to_device(v, dt) for v in vc]
 
 
+def run_lmhead(args, local):
+    """The LM-head GEMM + argmax alone on the GPT-OSS LM-head shape (d 2880,
+    vocab 201088) for M rows (--workload lmhead-<M>): the launch the bench
+    reports as its dominant kernel, for profiling it in isolation."""
+    import torch
+
+    from speculative_drafting_expand_gb300 import binding as B
+
+    torch.cuda.set_device(local)
+    M = int(args.workload[len("lmhead-"):])
+    full = W.gpt_oss_b1().shape
+    sh = W.small_shape("lm-head", d=full.d, n_layers=1, n_heads=1, n_kv_heads=1, head_dim=64,
+                       ffn=64, vocab=full.vocab)
+    z = np.zeros(64, np.uint16)
+    g = torch.Generator().manual_seed(7)
+    lm = (torch.randn(sh.vocab, sh.d, generator=g) * 0.02).to(torch.bfloat16)
+    w = {k: z for k in ("emb", "fc", "norm_final")}
+    w["lm_head"] = lm.view(torch.int16).numpy().view(np.uint16)
+    w["h_shared"] = np.zeros(sh.hidden3, np.uint16)
+    w["layers"] = [dict(qkv=z, o=z, gate=z, up=z, down=z, norm_e=z, norm_h=z, norm_in=z,
+                        norm_post=z)]
+    dr = B.Drafter(sh, w, max(M, 16), 1)
+    hid = torch.randn(M, sh.d, generator=g).to(torch.bfloat16).cuda()
+    tok = torch.empty(M, dtype=torch.int32, device="cuda")
+    for _ in range(args.warmup):
+        B.pe_lmhead_argmax(dr, hid, tok)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        B.pe_lmhead_argmax(dr, hid, tok)
+    e1.record()
+    torch.cuda.synchronize()
+    check_device(B, dr)
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    print(json.dumps({"mode": "lm_head", "rows": M, "d": sh.d, "vocab": sh.vocab,
+                      "us_per_launch": us, "weight_gbs": sh.vocab * sh.d * 2 / us / 1e3,
+                      "tflops": 2.0 * M * sh.vocab * sh.d / us / 1e6}), flush=True)
+    dr.close()
+    return 0
+
+
 def run_ar(args, world, rank, local):
     """Autoregressive drafting of the same K tokens on the same kernels: K
     sequential passes of the K = 1 step (the pages' baseline, whose cost
@@ -600,6 +642,8 @@ def main():
         return run_reference(args, world, rank)
     if args.workload.startswith("ar-"):
         return run_ar(args, world, rank, local)
+    if args.workload.startswith("lmhead-"):
+        return run_lmhead(args, local)
     return run_ours(args, world, rank, local)
 
 
