@@ -16,7 +16,7 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
                                 const EpiArgs& epi, const TcGemmWorkspace& ws, int* err,
                                 cudaStream_t s);
 int tc_pick_bn(int M, bool dual);
-int tc_b_box_rows(int M, int N, int sm_count, bool dual);
+int tc_b_box_rows(int M, int N, int sm_count, bool dual, bool live_rows);
 cudaError_t init_gemm_tc();
 size_t tc_partial_floats(int grid, int bn, bool dual);
 cudaError_t init_attention_tc();
@@ -58,6 +58,16 @@ struct pe_handle {
   size_t attn_partial_floats = 0;
   int* attn_counters = nullptr;
   size_t attn_n_counters = 0;
+  // live-row compaction of the expanded batch (compact.cu)
+  int32_t* row_map = nullptr;      // [max_tokens]
+  int32_t* live_before = nullptr;  // [max_tokens + 1]
+  int32_t* live_row = nullptr;     // [max_tokens]
+  int32_t* ids_c = nullptr;        // [max_tokens]
+  int32_t* pos_c = nullptr;
+  int32_t* slot_c = nullptr;
+  int32_t* cu_live = nullptr;      // [max_reqs + 1]
+  int32_t* new_c = nullptr;        // [max_tokens]
+  int32_t* n_live = nullptr;       // [1]
   float* trace = nullptr;
   void* attn_trace = nullptr;
   long long launches = 0;
@@ -118,7 +128,7 @@ cudaError_t linear(pe_handle* h, const void* x, int ldx, const void* w, const vo
                                        static_cast<const float*>(w2), M, N, K, epi, h->err, s));
   const CUtensorMap* wa = get_map(h, w, N, K, K, 128);
   const CUtensorMap* wa2 = w2 ? get_map(h, w2, N, K, K, 128) : wa;
-  const CUtensorMap* xb = get_map(h, x, M, K, ldx, tc_b_box_rows(M, N, h->sm_count, w2 != nullptr));
+  const CUtensorMap* xb = get_map(h, x, M, K, ldx, tc_b_box_rows(M, N, h->sm_count, w2 != nullptr, epi.m_live != nullptr));
   if (!wa || !wa2 || !xb) return cudaErrorInvalidValue;
   return counted(h, launch_gemm_tc_maps(*wa, *wa2, *xb, w2 != nullptr, M, N, K, epi, tc_ws(h),
                                         h->err, s));
@@ -216,6 +226,11 @@ pe_status pe_create(const pe_model_desc* desc, const pe_weights* weights, int32_
   if (e == cudaSuccess) e = alloc_bytes(&h->xn, T * d.d * es);
   if (e == cudaSuccess) e = alloc_bytes(&h->act, T * d.ffn * es);
   if (e == cudaSuccess) e = dev_alloc(h, &h->keys, T);
+  for (int32_t** p : {&h->row_map, &h->live_row, &h->ids_c, &h->pos_c, &h->slot_c, &h->new_c})
+    if (e == cudaSuccess) e = dev_alloc(h, p, T);
+  if (e == cudaSuccess) e = dev_alloc(h, &h->live_before, T + 1);
+  if (e == cudaSuccess) e = dev_alloc(h, &h->cu_live, static_cast<size_t>(max_reqs) + 1);
+  if (e == cudaSuccess) e = dev_alloc(h, &h->n_live, 1);
   if (e == cudaSuccess) e = dev_alloc(h, &h->inv_freq64, d.head_dim / 2);
   if (e == cudaSuccess) {
     std::vector<double> inv(d.head_dim / 2);
@@ -330,7 +345,8 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
   if (!h || !ex || !block_table || !k_cache || !v_cache || !out_hidden || bt_stride < 1 ||
       num_blocks < 1)
     return PE_ERR_INVALID_ARGUMENT;
-  if (ex->B != B || ex->K != K || ex->T_out < 1 || ex->T_out > h->max_tokens ||
+  if (B < 1 || B > h->max_reqs || ex->B != B || ex->K != K || ex->T_out < 1 ||
+      ex->T_out > h->max_tokens ||
       ex->T_out != ex->T + B * (K - 1))
     return PE_ERR_INVALID_ARGUMENT;
   const pe_model_desc& d = h->desc;
@@ -372,7 +388,59 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     }
   }
 
-  // fc: projected target hidden state -> residual stream (fp32)
+  // Rejected rows (window rows after the accepted count) write no KV and
+  // feed no sampled row: after fc the layers run on the live rows only.  A
+  // batch of one window row per request has none, and skips the compaction.
+  const bool compact = ex->T > B;
+  const int32_t* live = nullptr;
+  const int32_t* ids_l = ex->ids;
+  const int32_t* pos_l = ex->pos;
+  const int32_t* slot_l = ex->slot;
+  const int32_t* cu_l = ex->cu_out;
+  const int32_t* new_l = ex->new_idx;
+  const uint8_t* rej_l = ex->is_rejected;
+  if (compact) {
+    CompactArgs ca = {};
+    ca.B = B;
+    ca.K = K;
+    ca.T_out = rows;
+    ca.cu_out = ex->cu_out;
+    ca.is_rejected = ex->is_rejected;
+    ca.ids = ex->ids;
+    ca.pos = ex->pos;
+    ca.slot = ex->slot;
+    ca.new_idx = ex->new_idx;
+    ca.row_map = h->row_map;
+    ca.live_before = h->live_before;
+    ca.live_row = h->live_row;
+    ca.ids_c = h->ids_c;
+    ca.pos_c = h->pos_c;
+    ca.slot_c = h->slot_c;
+    ca.cu_live = h->cu_live;
+    ca.new_c = h->new_c;
+    ca.n_live = h->n_live;
+    if ((e = counted(h, launch_compact_rows(ca, s)))) return PE_ERR_CUDA;
+    live = h->n_live;
+    ids_l = h->ids_c;
+    pos_l = h->pos_c;
+    slot_l = h->slot_c;
+    cu_l = h->cu_live;
+    new_l = h->new_c;
+    rej_l = nullptr;
+  }
+  // debug copies of per-row activations, in the expanded row order (zero
+  // for rejected rows)
+  auto trace_rows = [&](void* dst, const void* src, size_t row_bytes) -> cudaError_t {
+    if (!compact) return cudaMemcpyAsync(dst, src, rows * row_bytes, cudaMemcpyDeviceToDevice, s);
+    cudaError_t r = cudaMemsetAsync(dst, 0, rows * row_bytes, s);
+    if (r == cudaSuccess)
+      r = counted(h, launch_scatter_rows(dst, src, h->live_row, h->n_live, rows,
+                                         static_cast<int>(row_bytes), s));
+    return r;
+  };
+
+  // fc: projected target hidden state -> residual stream (fp32), live rows
+  // to their compact rows
   EpiArgs ep = epi_none();
   ep.kind = EPI_STORE;
   ep.M = rows;
@@ -380,14 +448,16 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
   ep.out = h->resid;
   ep.ldo = d.d;
   ep.out_f32 = 1;
+  ep.row_map = compact ? h->row_map : nullptr;
   if ((e = linear(h, ex->hidden, d.hidden3, h->w.fc, nullptr, rows, d.d, d.hidden3, ep, s)))
     return PE_ERR_CUDA;
   // layer-0 input: [RMSNorm_e(emb[id]) ; RMSNorm_h(fc h)]
-  EmbedConcatArgs ec;
+  EmbedConcatArgs ec = {};
   ec.rows = rows;
   ec.d = d.d;
   ec.vocab = d.vocab;
-  ec.ids = ex->ids;
+  ec.ids = ids_l;
+  ec.live = live;
   ec.emb = h->w.emb;
   ec.h = h->resid;
   ec.g_e = h->layers[0].norm_e;
@@ -410,6 +480,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
       rn.eps = d.rms_eps;
       rn.y = h->x_in;
       rn.err = h->err;
+      rn.live = live;
       if ((e = counted(h, launch_rmsnorm(dt, rn, s)))) return PE_ERR_CUDA;
     }
     // QKV projection
@@ -420,18 +491,20 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     ep.out = h->qkv;
     ep.ldo = qkv_rows;
     ep.out_f32 = dt == PE_DTYPE_F32 ? 1 : 0;
+    ep.m_live = live;
     if ((e = linear(h, h->x_in, d_in, L.qkv, nullptr, rows, qkv_rows, d_in, ep, s)))
       return PE_ERR_CUDA;
     // RoPE + paged KV write (slot -1: nothing written)
-    RopeKvArgs rk;
+    RopeKvArgs rk = {};
     rk.rows = rows;
     rk.Hq = d.n_heads;
     rk.Hkv = d.n_kv_heads;
     rk.dh = d.head_dim;
     rk.num_blocks = num_blocks;
     rk.qkv = h->qkv;
-    rk.pos = ex->pos;
-    rk.slot = ex->slot;
+    rk.pos = pos_l;
+    rk.slot = slot_l;
+    rk.live = live;
     rk.inv_freq = nullptr;
     rk.inv_freq64 = h->inv_freq64;
     rk.q_out = h->q;
@@ -440,7 +513,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     rk.err = h->err;
     if ((e = counted(h, launch_rope_kv(dt, rk, s)))) return PE_ERR_CUDA;
     // paged causal attention
-    AttnArgs at;
+    AttnArgs at = {};
     at.rows = rows;
     at.B = B;
     at.Hq = d.n_heads;
@@ -452,9 +525,10 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     at.q = h->q;
     at.k_cache = k_cache[l];
     at.v_cache = v_cache[l];
-    at.pos = ex->pos;
-    at.is_rejected = ex->is_rejected;
-    at.cu_out = ex->cu_out;
+    at.live = live;
+    at.pos = pos_l;
+    at.is_rejected = rej_l;
+    at.cu_out = cu_l;
     at.block_table = block_table;
     at.out = h->attn;
     at.scale = 1.0f / std::sqrt(static_cast<float>(d.head_dim));
@@ -472,9 +546,9 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     }
     if (h->attn_trace) {
       const size_t per = static_cast<size_t>(qd) * h->esize;
-      e = cudaMemcpyAsync(static_cast<char*>(h->attn_trace) + l * h->max_tokens * per, h->attn,
-                          rows * per, cudaMemcpyDeviceToDevice, s);
-      if (e) return PE_ERR_CUDA;
+      if ((e = trace_rows(static_cast<char*>(h->attn_trace) + l * h->max_tokens * per, h->attn,
+                          per)))
+        return PE_ERR_CUDA;
     }
     // O projection + residual
     ep = epi_none();
@@ -483,6 +557,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     ep.N = d.d;
     ep.resid = h->resid;
     ep.ldr = d.d;
+    ep.m_live = live;
     if ((e = linear(h, h->attn, qd, L.o, nullptr, rows, d.d, qd, ep, s))) return PE_ERR_CUDA;
     // MLP
     RmsNormArgs rn = {};
@@ -494,6 +569,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     rn.eps = d.rms_eps;
     rn.y = h->xn;
     rn.err = h->err;
+    rn.live = live;
     if ((e = counted(h, launch_rmsnorm(dt, rn, s)))) return PE_ERR_CUDA;
     ep = epi_none();
     ep.kind = EPI_SILU_MUL;
@@ -502,6 +578,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     ep.out = h->act;
     ep.ldo = d.ffn;
     ep.out_f32 = dt == PE_DTYPE_F32 ? 1 : 0;
+    ep.m_live = live;
     if ((e = linear(h, h->xn, d.d, L.gate, L.up, rows, d.ffn, d.d, ep, s))) return PE_ERR_CUDA;
     ep = epi_none();
     ep.kind = EPI_ADD;
@@ -509,13 +586,13 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     ep.N = d.d;
     ep.resid = h->resid;
     ep.ldr = d.d;
+    ep.m_live = live;
     if ((e = linear(h, h->act, d.ffn, L.down, nullptr, rows, d.d, d.ffn, ep, s)))
       return PE_ERR_CUDA;
     if (h->trace) {
-      e = cudaMemcpyAsync(h->trace + static_cast<size_t>(l) * h->max_tokens * d.d, h->resid,
-                          static_cast<size_t>(rows) * d.d * sizeof(float),
-                          cudaMemcpyDeviceToDevice, s);
-      if (e) return PE_ERR_CUDA;
+      if ((e = trace_rows(h->trace + static_cast<size_t>(l) * h->max_tokens * d.d, h->resid,
+                          static_cast<size_t>(d.d) * sizeof(float))))
+        return PE_ERR_CUDA;
     }
   }
   // final norm of the B*K sampled rows
@@ -523,7 +600,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
   rn.rows = B * K;
   rn.d = d.d;
   rn.x = h->resid;
-  rn.row_index = ex->new_idx;
+  rn.row_index = new_l;
   rn.rows_in = rows;
   rn.g = h->w.norm_final;
   rn.eps = d.rms_eps;

@@ -19,8 +19,9 @@ __global__ void __launch_bounds__(128) attention_simt_kernel(const AttnArgs a) {
   const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (h >= a.Hq) return;
+  if (a.live && i >= __ldcg(a.live)) return;  // past the live rows
   T* out = static_cast<T*>(a.out) + static_cast<size_t>(i) * a.Hq * DH + h * DH;
-  if (a.is_rejected[i]) {
+  if (a.is_rejected && a.is_rejected[i]) {
 #pragma unroll
     for (int e = 0; e < E; ++e) out[lane + 32 * e] = from_f<T>(0.f);
     return;

@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(AttnCfg<DH>::THREADS, 1)
     const int row = row0 + tile_row0 + lr;          // expanded row
     const int head = g * p.G + hl;
     int P = -1;                                     // last key this row reads
-    if (in_tile && a.is_rejected[row] == 0) P = a.pos[row];
+    if (in_tile && (a.is_rejected == nullptr || a.is_rejected[row] == 0)) P = a.pos[row];
     // Q -> shared memory (128-byte swizzle; zero for padding / rejected rows)
     {
       const uint4* src = reinterpret_cast<const uint4*>(
@@ -582,15 +582,18 @@ static AttnPlan plan_attention(const AttnArgs& a, int max_rows_per_req, int sm_c
   const long long pairs = static_cast<long long>(a.B) * a.Hkv * pl.qtiles;
   const int want = static_cast<int>(std::max<long long>(1, (sm_count + pairs - 1) / pairs));
   // A split is at most 32 chunks (its block ids fit the CTA's table).
-  // Fewer units than SMs: about 8 splits per unit; otherwise enough splits
-  // to give every SM a unit, 2 to 32 chunks each (32 measured best at
-  // batch 64).  The splits of a unit are merged through global memory by
+  // Fewer units than SMs: about 8 splits per unit, 16 where 8 would leave
+  // more than half of the SMs idle (batch 1: 1.5 % faster step; at 16
+  // requests 16 splits lost 5 %); otherwise enough splits to give every SM
+  // a unit, 2 to 32 chunks each (32 measured best at batch 64).  The splits of a unit are merged through global memory by
   // the last one to finish: at batch 16 that beat merging the splits of a
   // thread-block cluster through distributed shared memory by a sixth of
   // the step (8-CTA clusters of one-CTA-per-SM kernels leave SMs idle), and
   // tied with it at batch 1.
   constexpr int kMaxCps = 32;
-  int cps = pairs < sm_count ? (chunks_max + 7) / 8 : (chunks_max + want - 1) / want;
+  int cps = pairs * 16 <= sm_count ? (chunks_max + 15) / 16
+            : pairs < sm_count     ? (chunks_max + 7) / 8
+                                   : (chunks_max + want - 1) / want;
   cps = std::max(2, std::min(kMaxCps, cps));
   pl.split_keys = cps * 128;
   pl.max_splits = (max_seq + pl.split_keys - 1) / pl.split_keys;

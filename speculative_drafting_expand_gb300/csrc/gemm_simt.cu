@@ -19,6 +19,11 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const float* __restrict_
   grid_dep_wait();
   grid_dep_launch();
   const int f0 = blockIdx.x * SBF, t0 = blockIdx.y * SBT;
+  if (epi.m_live) {
+    // compacted batch: tokens at or past the live count are skipped
+    M = min(M, __ldcg(epi.m_live));
+    if (t0 >= M) return;
+  }
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
   float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
   for (int k0 = 0; k0 < K; k0 += SBK) {
@@ -52,9 +57,11 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const float* __restrict_
     if (f >= N) continue;
     const float v = acc[q];
     switch (epi.kind) {
-      case EPI_STORE:
-        static_cast<float*>(epi.out)[static_cast<size_t>(t) * epi.ldo + f] = v;
+      case EPI_STORE: {
+        const int tr = epi.row_map ? __ldcg(epi.row_map + t) : t;
+        if (tr >= 0) static_cast<float*>(epi.out)[static_cast<size_t>(tr) * epi.ldo + f] = v;
         break;
+      }
       case EPI_ADD:
         epi.resid[static_cast<size_t>(t) * epi.ldr + f] += v;
         break;

@@ -47,6 +47,11 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
   volatile int* flag = reinterpret_cast<volatile int*>(tmem_slot + 1);     // reducer election
   volatile int* epi_ok = reinterpret_cast<volatile int*>(tmem_slot + 2);   // epilogue wait result
 
+  // Live token count of a compacted batch.  It was written two or more
+  // launches back, so it is read before the wait, and its latency hides
+  // behind the setup below.
+  const int m_live = p.epi.m_live ? __ldcg(p.epi.m_live) : 0;
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -74,8 +79,41 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const long long U = p.units;
-  const int G = gridDim.x, cta = blockIdx.x, kb = p.kb;
+  // Dead token tiles (past the live count) are skipped: a cluster split
+  // drops the clusters of dead tiles, stream-K deals the live units out
+  // again.  With fewer live tiles than CTAs, every live tile gets the same
+  // number of CTAs (an equal k-split, so each tile has a fixed number of
+  // contributors) and the rest stay idle.  A dead CTA exits without waiting
+  // on the previous kernel; token tile 0 is always live (every request
+  // keeps its next-token row), so some CTA still waits before the grid lets
+  // its dependents start.
+  int tiles_m = p.tiles_m;
+  long long U = p.units;
+  int G = gridDim.x;
+  const int cta = blockIdx.x, kb = p.kb;
+  if (p.epi.m_live) {
+    const int tm = (max(0, min(p.M, m_live)) + BN - 1) / BN;
+    bool dead;
+    if (p.split_s >= 1) {
+      dead = (cta / p.split_s) % p.tiles_m >= tm;  // the same for the whole cluster
+    } else {
+      tiles_m = tm;
+      U = p.units / p.tiles_m * tm;
+      const long long live_tiles = U / kb;
+      if (live_tiles < G)
+        G = live_tiles > 0 ? static_cast<int>(live_tiles * std::min<long long>(G / live_tiles, kb))
+                           : 0;
+      dead = cta >= G;
+    }
+    if (dead) {
+      if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+      }
+      return;
+    }
+  }
+
   long long lo, hi;
   if (p.split_s >= 1) {
     // cluster split: CTA s of the tile's cluster takes k-blocks
@@ -90,7 +128,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
 
   if (warp == 4) {
     if (lane == 0) {
-      const uint64_t pol_a = p.tiles_m == 1 ? l2_policy_evict_first() : l2_policy_evict_last();
+      const uint64_t pol_a = tiles_m == 1 ? l2_policy_evict_first() : l2_policy_evict_last();
       const uint64_t pol_b = l2_policy_evict_last();
       const long long n = hi - lo;
       const int npre = static_cast<int>(n < C::STAGES ? n : C::STAGES);
@@ -98,7 +136,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
       for (int i = 0; i < npre; ++i) {
         const long long u = lo + i;
         const int tile = static_cast<int>(u / kb), kk = static_cast<int>(u % kb);
-        const int f = tile / p.tiles_m;
+        const int f = tile / tiles_m;
         uint8_t* st = smem + i * C::STAGE_BYTES;
         mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
         tma_load_2d(st, &tmA, &full[i], kk * 64, f * 128, pol_a);
@@ -112,7 +150,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
       for (int i = 0; i < npre; ++i) {
         const long long u = lo + i;
         const int tile = static_cast<int>(u / kb), kk = static_cast<int>(u % kb);
-        const int m = tile % p.tiles_m;
+        const int m = tile % tiles_m;
         tma_load_2d(smem + i * C::STAGE_BYTES + C::NA * C::A_BYTES, &tmB, &full[i], kk * 64,
                     m * BN, pol_b);
       }
@@ -123,7 +161,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
         if (!mbar_wait(&empty[stage], (round - 1) & 1, p.err)) break;
         const long long u = lo + i;
         const int tile = static_cast<int>(u / kb), kk = static_cast<int>(u % kb);
-        const int f = tile / p.tiles_m, m = tile % p.tiles_m;
+        const int f = tile / tiles_m, m = tile % tiles_m;
         uint8_t* st = smem + stage * C::STAGE_BYTES;
         mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
         tma_load_2d(st, &tmA, &full[stage], kk * 64, f * 128, pol_a);
@@ -196,7 +234,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
       named_bar_sync(1, 128);
       if (!*epi_ok) break;
       tc_fence_after();
-      const int f = tile / p.tiles_m, m = tile % p.tiles_m;
+      const int f = tile / tiles_m, m = tile % tiles_m;
       const int o = f * 128 + row;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * C::ACC_COLS;
       if (k_lo == 0 && k_hi == kb) {
@@ -356,7 +394,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
     const int S = p.split_s, tile = cta / S;
     const int rk = static_cast<int>(cluster_ctarank());
     if (warp < 4) {
-      const int f = tile / p.tiles_m, m = tile % p.tiles_m;
+      const int f = tile / tiles_m, m = tile % tiles_m;
       const int row = warp * 32 + lane;
       const uint32_t base = smem_u32(smem);
       constexpr int kMaxS = 8;  // cluster split sizes are at most 8
@@ -561,11 +599,11 @@ int tc_pick_bn(int M, bool dual) {
 
 // Rows of the token box in the x tensor map that launch_gemm_tc_maps
 // expects for an M x N projection: the token tile, or its slice when the
-// multicast kernel takes the projection.
-int tc_b_box_rows(int M, int N, int sm_count, bool dual) {
+// multicast kernel takes the projection (never with a live-row count).
+int tc_b_box_rows(int M, int N, int sm_count, bool dual, bool live_rows) {
   const int bn = tc_pick_bn(M, dual);
   const long long tiles = static_cast<long long>((N + 127) / 128) * ((M + bn - 1) / bn);
-  return bn / gemm_mc_cluster(bn, dual, tiles, sm_count);
+  return live_rows ? bn : bn / gemm_mc_cluster(bn, dual, tiles, sm_count);
 }
 
 size_t tc_partial_floats(int grid, int bn, bool dual) {
@@ -577,6 +615,8 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
                                 const EpiArgs& epi, const TcGemmWorkspace& ws, int* err,
                                 cudaStream_t s) {
   if (M <= 0 || N <= 0) return cudaSuccess;
+  if ((epi.m_live && epi.kind == EPI_ARGMAX) || (epi.row_map && !epi.out_f32))
+    return cudaErrorInvalidValue;
   const int bn = tc_pick_bn(M, dual);
   TcParams p;
   p.M = M;
@@ -593,7 +633,7 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
   p.err = err;
   const int tiles = tiles_n * p.tiles_m;
   p.split_s = 0;
-  const int cs = gemm_mc_cluster(bn, dual, tiles, ws.sm_count);
+  const int cs = epi.m_live ? 1 : gemm_mc_cluster(bn, dual, tiles, ws.sm_count);
   if (cs > 1) return launch_gemm_mc(wa, wa2, xb, dual, bn, cs, p, s);
   if (tiles > ws.max_tiles) return cudaErrorInvalidValue;
 #define PE_TC_CASE(BNV)                                                                       \
@@ -622,7 +662,7 @@ cudaError_t launch_gemm_tc(const void* x, int ldx, const void* w, const void* w2
   if (!tensor_map_2d_bf16(&wa, w, N, K, K, 64, 128)) return cudaErrorInvalidValue;
   wa2 = wa;
   if (w2 && !tensor_map_2d_bf16(&wa2, w2, N, K, K, 64, 128)) return cudaErrorInvalidValue;
-  if (!tensor_map_2d_bf16(&xb, x, M, K, ldx, 64, tc_b_box_rows(M, N, ws.sm_count, w2 != nullptr)))
+  if (!tensor_map_2d_bf16(&xb, x, M, K, ldx, 64, tc_b_box_rows(M, N, ws.sm_count, w2 != nullptr, epi.m_live != nullptr)))
     return cudaErrorInvalidValue;
   return launch_gemm_tc_maps(wa, wa2, xb, w2 != nullptr, M, N, K, epi, ws, err, s);
 }

@@ -68,7 +68,18 @@ __device__ __forceinline__ void epi_chunk(const EpiArgs& e, int o, int t0, const
   const bool of = o < e.N;
   switch (e.kind) {
     case EPI_STORE:
-      if (e.out_f32) {
+      if (e.row_map) {
+        // rows through the map (fp32 output; the map is read-only while this
+        // kernel runs, and all 16 entries are read before any store, so no
+        // load waits behind a store it cannot be told apart from)
+        float* out = static_cast<float*>(e.out);
+        int tr[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) tr[j] = (of && t0 + j < e.M) ? __ldg(e.row_map + t0 + j) : -1;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (tr[j] >= 0) out[static_cast<size_t>(tr[j]) * e.ldo + o] = v[j];
+      } else if (e.out_f32) {
         float* out = static_cast<float*>(e.out);
 #pragma unroll
         for (int j = 0; j < 16; ++j)

@@ -26,7 +26,7 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
                                 const CUtensorMap& xb, bool dual, int M, int N, int K,
                                 const EpiArgs& epi, const TcGemmWorkspace& ws, int* err,
                                 cudaStream_t s);
-int tc_b_box_rows(int M, int N, int sm_count, bool dual);
+int tc_b_box_rows(int M, int N, int sm_count, bool dual, bool live_rows);
 }  // namespace pe
 
 namespace {
@@ -100,7 +100,7 @@ extern "C" pe_status pe_linear_static(const void* x, const void* w, float* y, in
   const int sms = slot->sm_count < kMaxCtas ? slot->sm_count : kMaxCtas;
   CUtensorMap wa, xb;
   if (!tensor_map_2d_bf16(&wa, w, N, K, K, 64, 128) ||
-      !tensor_map_2d_bf16(&xb, x, M, K, K, 64, tc_b_box_rows(M, N, sms, false)))
+      !tensor_map_2d_bf16(&xb, x, M, K, K, 64, tc_b_box_rows(M, N, sms, false, false)))
     return PE_ERR_INVALID_ARGUMENT;
   TcGemmWorkspace ws;
   ws.partials = partials;

@@ -74,10 +74,46 @@ struct ExpandArgs {
 };
 cudaError_t launch_expand(const ExpandArgs& a, cudaStream_t s);
 
+// Live-row compaction of the expanded batch: the rejected rows of a request
+// (window rows after its accepted count) never write the KV cache and feed
+// no sampled row, so the drafter layers skip them.  One CTA scans the
+// is_rejected flags and writes, for the n_live live rows in expanded order:
+// ids/pos/slot copies, the compact index of every expanded row (-1 when
+// rejected), the expanded row of every compact row, the compact request
+// offsets and the compact index of every sampled row.
+struct CompactArgs {
+  int B, K, T_out;
+  const int32_t* cu_out;        // [B + 1]
+  const uint8_t* is_rejected;   // [T_out]
+  const int32_t* ids;           // [T_out]
+  const int32_t* pos;
+  const int32_t* slot;
+  const int32_t* new_idx;       // [B K]
+  int32_t* row_map;             // [T_out] expanded -> compact, -1 rejected
+  int32_t* live_before;         // [T_out + 1] live rows before each expanded row
+  int32_t* live_row;            // [T_out] compact -> expanded
+  int32_t* ids_c;               // [T_out] (first n_live used)
+  int32_t* pos_c;
+  int32_t* slot_c;
+  int32_t* cu_live;             // [B + 1]
+  int32_t* new_c;               // [B K]
+  int32_t* n_live;              // [1]
+};
+cudaError_t launch_compact_rows(const CompactArgs& a, cudaStream_t s);
+
+// dst[live_row[c]] = src[c] for the first *n_live compact rows (row_bytes a
+// multiple of 16); the other dst rows are left as they are.
+cudaError_t launch_scatter_rows(void* dst, const void* src, const int32_t* live_row,
+                                const int32_t* n_live, int rows_max, int row_bytes,
+                                cudaStream_t s);
+
 // ---------------------------------------------------------------- row ops
 // dtype tag: 0 = bf16, 1 = f32 (activations, weights, caches share it)
+// `live` (optional, device): rows at or past *live are skipped -- the
+// compacted row count, written by a kernel earlier on the stream.
 struct EmbedConcatArgs {
   int rows, d, vocab;
+  const int32_t* live;
   const int32_t* ids;
   const void* emb;      // [V, d]
   const float* h;       // [rows, d] fp32 fc output (the residual)
@@ -91,6 +127,7 @@ cudaError_t launch_embed_concat(int dtype, const EmbedConcatArgs& a, cudaStream_
 
 struct RmsNormArgs {
   int rows, d;
+  const int32_t* live;
   const float* x;       // [*, d] fp32 residual
   const int32_t* row_index;  // optional gather: out row i reads x[row_index[i]]
   int rows_in;          // bound for row_index values
@@ -103,6 +140,7 @@ cudaError_t launch_rmsnorm(int dtype, const RmsNormArgs& a, cudaStream_t s);
 
 struct RopeKvArgs {
   int rows, Hq, Hkv, dh, num_blocks;
+  const int32_t* live;
   const void* qkv;          // [rows, (Hq + 2 Hkv) dh]
   const int32_t* pos;       // [rows]
   const int32_t* slot;      // [rows], -1 = no KV write
@@ -117,12 +155,13 @@ cudaError_t launch_rope_kv(int dtype, const RopeKvArgs& a, cudaStream_t s);
 
 struct AttnArgs {
   int rows, B, Hq, Hkv, dh, bt_stride, num_blocks, max_seq;
+  const int32_t* live;       // optional live-row count (per-row kernel only)
   const void* q;             // [rows, Hq dh] (roped)
   const void* k_cache;
   const void* v_cache;
   const int32_t* pos;        // [rows]
-  const uint8_t* is_rejected;
-  const int32_t* cu_out;     // [B+1]
+  const uint8_t* is_rejected;  // nullable: no rejected rows (compacted batch)
+  const int32_t* cu_out;     // [B+1] first row of each request
   const int32_t* block_table;
   void* out;                 // [rows, Hq dh]
   float scale;
@@ -145,6 +184,14 @@ struct EpiArgs {
   int ldl;
   unsigned long long* keys; // ARGMAX: [M] packed (value, index), zero on entry
   int32_t* tokens;          // ARGMAX: [M] result
+  const int32_t* row_map;   // STORE (optional): token t goes to row row_map[t], skipped if < 0
+  // Optional live token count (device): token tiles at or past *m_live are
+  // skipped and the work of the live ones is dealt out again.  The
+  // tensor-core kernel reads it before waiting on the previous kernel, so
+  // it must be written at least two launches earlier on the stream (every
+  // kernel here waits on its predecessor before it lets its dependents
+  // start).  Not used with the ARGMAX epilogue.
+  const int32_t* m_live;
 };
 
 // y = x . w^T (+ epilogue) with tcgen05 tensor cores (bf16 in, fp32 accumulate).

@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(kRowThreads) embed_concat_kernel(const EmbedCo
   grid_dep_wait();
   grid_dep_launch();
   const int i = blockIdx.x;
+  if (a.live && i >= __ldcg(a.live)) return;  // past the live rows
   int id = a.ids[i];
   if (id < 0 || id >= a.vocab) {
     if (threadIdx.x == 0) record_error(a.err, PE_DEV_BAD_TOKEN);
@@ -68,6 +69,7 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_kernel(const RmsNormArgs 
   grid_dep_wait();
   grid_dep_launch();
   const int i = blockIdx.x;
+  if (a.live && i >= __ldcg(a.live)) return;  // past the live rows
   int src = a.row_index ? a.row_index[i] : i;
   T* y = static_cast<T*>(a.y) + static_cast<size_t>(i) * a.d;
   if (src < 0 || src >= a.rows_in) {
@@ -90,6 +92,7 @@ __global__ void __launch_bounds__(kRowThreads) rope_kv_kernel(const RopeKvArgs a
   grid_dep_wait();
   grid_dep_launch();
   const int i = blockIdx.x;
+  if (a.live && i >= __ldcg(a.live)) return;  // past the live rows
   const int half = a.dh / 2;
   const int p = a.pos[i];
   if (threadIdx.x < half) {
@@ -188,6 +191,7 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_vec_kernel(const RmsNormA
   grid_dep_wait();
   grid_dep_launch();
   const int i = blockIdx.x;
+  if (a.live && i >= __ldcg(a.live)) return;  // past the live rows
   const int src = a.row_index ? a.row_index[i] : i;
   T* __restrict__ y = static_cast<T*>(a.y) + static_cast<size_t>(i) * a.d;
   const bool bad = src < 0 || src >= a.rows_in;
@@ -240,6 +244,7 @@ __global__ void __launch_bounds__(kRowThreads) embed_concat_vec_kernel(const Emb
   grid_dep_wait();
   grid_dep_launch();
   const int i = blockIdx.x;
+  if (a.live && i >= __ldcg(a.live)) return;  // past the live rows
   int id = a.ids[i];
   if (id < 0 || id >= a.vocab) {
     if (threadIdx.x == 0) record_error(a.err, PE_DEV_BAD_TOKEN);
@@ -343,6 +348,7 @@ __global__ void __launch_bounds__(kRowThreads) rope_kv_vec_kernel(const RopeKvAr
   grid_dep_wait();
   grid_dep_launch();
   const int i = blockIdx.x;
+  if (a.live && i >= __ldcg(a.live)) return;  // past the live rows
   const int half = a.dh / 2;
   if (threadIdx.x < half) {
     // angle in fp64, reduced to [-pi, pi] before the fp32 sine/cosine

@@ -47,6 +47,22 @@ def test_small_bf16_batches(B, K):
     G.full_parity(wl, TOL_BF16)
 
 
+@pytest.mark.parametrize("B", [22, 40])
+def test_rejected_rows_are_skipped_by_whole_token_tiles(B):
+    """Every request accepts nothing (a = 0 of an 8-row window), so the
+    layers run on B*K live rows of the 2*B*K expanded ones.  B = 22: 308
+    rows in two 224-row token tiles, the second one dead (cluster split:
+    its clusters exit); B = 40: 560 rows in three tiles, one dead.  The
+    attention trace of every rejected row must still read zero and the KV
+    cache must change at the live slots only."""
+    K = 7
+    rng = np.random.default_rng(900 + B)
+    ctx = rng.integers(1, 400, size=B)
+    wl = W.custom(f"dead-b{B}", 90 + B, SMALL, K, ctx, np.full(B, K + 1), np.zeros(B, int),
+                  gains="random")
+    G.full_parity(wl, TOL_BF16)
+
+
 def test_small_bf16_head_dim_128():
     sh = W.small_shape("small-dh128", d=512, n_layers=2, n_heads=4, n_kv_heads=2,
                        head_dim=128, ffn=768, vocab=2048)
