@@ -14,7 +14,7 @@ drafts its own batch (requests are independent: weak scaling, no
 collective on the data path).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload b1|b16|b64|qwen-k<K>|expand|ar-<workload>|lmhead-<rows>]
+                  [--workload b1|b16|b64|qwen-k<K>|expand|ar-<workload>|lmhead-<rows>|train-mask|train-partition]
 """
 
 from __future__ import annotations
@@ -357,6 +357,77 @@ def run_lmhead(args, local):
     return 0
 
 
+def run_train(args, local):
+    """Training-side index work (paper summary section 3) on the section 3.2
+    example: 8192 tokens, K = 8.  train-mask: the amortized additive bf16
+    mask over the 65,536 rows (8.59 GB written; HBM-write bound).
+    train-partition: COD sampling (r = 0.8) and the partition into four
+    equal segments of one sample."""
+    import torch
+
+    from speculative_drafting_expand_gb300 import binding as B
+
+    torch.cuda.set_device(local)
+    n, K = 8192, 8
+    pk, src = peaks()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if args.workload == "train-mask":
+        N = n * K
+        out = torch.empty((N, N), dtype=torch.bfloat16, device="cuda")
+        for _ in range(args.warmup):
+            B.pe_train_build_mask(out, n, K, B.PE_MASK_ADDITIVE_BF16)
+        torch.cuda.synchronize()
+        clk = ClockSampler(local)
+        clk.start()
+        e0.record()
+        for _ in range(args.steps):
+            B.pe_train_build_mask(out, n, K, B.PE_MASK_ADDITIVE_BF16)
+        e1.record()
+        torch.cuda.synchronize()
+        clk.stop()
+        us = e0.elapsed_time(e1) * 1e3 / args.steps
+        nbytes = N * N * 2
+        gbs = nbytes / us / 1e3
+        peak = pk["hbm_gbs"]
+        print(json.dumps({
+            "mode": "train_mask", "metric": "amortized mask build (GB/s written)",
+            "value": gbs, "unit": "GB/s", "us_per_build": us, "bytes": nbytes,
+            "config": {"workload": "mask 8192 tokens x K=8 (65536 rows), additive bf16"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "peak_source": src},
+            "steps": args.steps, "warmup": args.warmup, "clocks": clk.summary()}), flush=True)
+        return 0
+    r, bounds = 0.8, [0, 2048, 4096, 6144, 8192]
+    u = torch.rand((n, K), generator=torch.Generator().manual_seed(3)).cuda()
+    for _ in range(args.warmup):
+        o = B.pe_train_partition(n, K, r, u, bounds)
+    torch.cuda.synchronize()
+    kept = int(o["keep"].sum())
+    # outputs preallocated once: time the calls alone
+    lib = B.lib()
+    S = len(bounds) - 1
+    import ctypes
+    hb = (ctypes.c_int32 * (S + 1))(*bounds)
+    cap = int(sum(bounds[:-1])) + n * K
+    st = B.stream_ptr()
+    args_c = [B.ptr(o[k]) for k in ("keep", "seg", "counts", "offsets", "rows", "owned")]
+    e0.record()
+    for _ in range(args.steps):
+        rc = lib.pe_train_partition(n, K, ctypes.c_float(r), B.ptr(u), S, hb, *args_c, cap, st)
+        if rc != 0:
+            raise SystemExit(f"pe_train_partition failed: {rc}")
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    print(json.dumps({
+        "mode": "train_partition", "metric": "COD sampling + sequence partition latency",
+        "value": us, "unit": "us/sample", "higher_is_better": False, "rows": n * K,
+        "kept_rows": kept, "segments": S, "rows_listed": int(o["offsets"][-1]),
+        "config": {"workload": "8192 tokens, K=8, r=0.8, 4 equal segments"},
+        "steps": args.steps, "warmup": args.warmup}), flush=True)
+    return 0
+
+
 def run_ar(args, world, rank, local):
     """Autoregressive drafting of the same K tokens on the same kernels: K
     sequential passes of the K = 1 step (the pages' baseline, whose cost
@@ -644,6 +715,8 @@ def main():
         return run_ar(args, world, rank, local)
     if args.workload.startswith("lmhead-"):
         return run_lmhead(args, local)
+    if args.workload in ("train-mask", "train-partition"):
+        return run_train(args, local)
     return run_ours(args, world, rank, local)
 
 

@@ -26,9 +26,15 @@ PE_ERR_DEVICE = 5
 PE_DTYPE_BF16 = 0
 PE_DTYPE_F32 = 1
 
+PE_MASK_BOOL_U8 = 0
+PE_MASK_ADDITIVE_BF16 = 1
+
+# include/peagle.h and include/peagle_train.h (pe_status_string last: it is
+# the one that does not return a pe_status)
 EXPORTED = ("pe_create", "pe_destroy", "pe_expand_batch", "pe_draft_forward",
             "pe_lmhead_argmax", "pe_get_device_error", "pe_set_trace", "pe_linear",
-            "pe_get_launch_count", "pe_linear_static", "pe_status_string")
+            "pe_get_launch_count", "pe_linear_static", "pe_train_build_mask",
+            "pe_train_mask_view", "pe_train_partition", "pe_status_string")
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -81,6 +87,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pe_linear.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp]
     lib.pe_get_launch_count.argtypes = [_vp, P(ctypes.c_int64)]
     lib.pe_linear_static.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _vp]
+    lib.pe_train_build_mask.argtypes = [_i32, _i32, _i32, _vp, ctypes.c_int64, _vp]
+    lib.pe_train_mask_view.argtypes = [_vp, ctypes.c_int64, _i32, _i32, _i32, P(_vp),
+                                       P(ctypes.c_int64), P(ctypes.c_int64)]
+    lib.pe_train_partition.argtypes = [_i32, _i32, ctypes.c_float, _vp, _i32, P(_i32), _vp, _vp,
+                                       _vp, _vp, _vp, _vp, ctypes.c_int64, _vp]
     lib.pe_status_string.argtypes = [_i32]
     lib.pe_status_string.restype = ctypes.c_char_p
     for name in EXPORTED[:-1]:
@@ -282,3 +293,54 @@ def pe_linear_static(x, w, y, stream=None):
     _check("pe_linear_static", lib().pe_linear_static(ptr(x), ptr(w), ptr(y), M, N, K,
                                                       stream_ptr(stream)))
     return y
+
+
+# ---------------------------------------------------------------------------
+# training-side index work (include/peagle_train.h)
+# ---------------------------------------------------------------------------
+
+def pe_train_build_mask(out, n_max: int, K: int, mask_type: int, stream=None):
+    """Fill out [n_max*K, ld] (uint8 for PE_MASK_BOOL_U8, bfloat16 for
+    PE_MASK_ADDITIVE_BF16; ld = out.shape[1]) with the amortized mask."""
+    if out.dim() != 2 or out.stride(1) != 1:
+        raise ValueError("out must be a row-major 2-D tensor")
+    _check("pe_train_build_mask", lib().pe_train_build_mask(
+        n_max, K, mask_type, ptr(out), out.stride(0), stream_ptr(stream)))
+    return out
+
+
+def pe_train_mask_view(mask, n_max: int, K: int, n: int):
+    """The mask of an n-token sample: a view of the top-left block of the mask
+    built for n_max (no copy)."""
+    v = _vp()
+    rows = ctypes.c_int64(0)
+    ld = ctypes.c_int64(0)
+    _check("pe_train_mask_view", lib().pe_train_mask_view(
+        ptr(mask), mask.stride(0), n_max, K, n, ctypes.byref(v), ctypes.byref(rows),
+        ctypes.byref(ld)))
+    if v.value != mask.data_ptr() or ld.value != mask.stride(0):
+        raise RuntimeError("pe_train_mask_view returned an unexpected view")
+    return mask[: rows.value, : rows.value]
+
+
+def pe_train_partition(n: int, K: int, r: float, u, bounds: Sequence[int], stream=None):
+    """COD sampling + sequence partitioning of one n-token sample; u is a
+    [n, K] float32 device tensor of draws.  Returns device tensors keep,
+    seg, offsets, rows, owned (rows / owned trimmed to offsets[-1] by the
+    caller)."""
+    torch = _torch()
+    S = len(bounds) - 1
+    hb = (_i32 * (S + 1))(*[int(b) for b in bounds])
+    cap = int(sum(bounds[:-1])) + n * K
+    dev = u.device
+    out = dict(keep=torch.empty(n, K, dtype=torch.uint8, device=dev),
+               seg=torch.empty(n, K, dtype=torch.int32, device=dev),
+               counts=torch.empty(max(S, 1), dtype=torch.int32, device=dev),
+               offsets=torch.empty(S + 1, dtype=torch.int32, device=dev),
+               rows=torch.empty(cap, dtype=torch.int32, device=dev),
+               owned=torch.empty(cap, dtype=torch.uint8, device=dev))
+    _check("pe_train_partition", lib().pe_train_partition(
+        n, K, ctypes.c_float(r), ptr(u), S, hb, ptr(out["keep"]), ptr(out["seg"]),
+        ptr(out["counts"]), ptr(out["offsets"]), ptr(out["rows"]), ptr(out["owned"]), cap,
+        stream_ptr(stream)))
+    return out

@@ -1,5 +1,5 @@
 """The C ABI without a GPU: the library builds, loads, exports every function
-include/peagle.h declares, its structs match the binding's layout, and host
+include/peagle.h and include/peagle_train.h declare, its structs match the binding's layout, and host
 validation rejects bad arguments before touching the device."""
 
 import ctypes
@@ -11,7 +11,7 @@ import tempfile
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "peagle.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("peagle.h", "peagle_train.h")]
 
 
 @pytest.fixture(scope="module")
@@ -24,7 +24,7 @@ def B():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     return sorted(set(re.findall(r"^(?:pe_status|const char\*)\s+(pe_\w+)\(", text, re.M)))
 
 
@@ -97,3 +97,32 @@ def test_host_validation_rejects_bad_arguments_without_a_device(B):
                                 None) == 1
     assert lib.pe_lmhead_argmax(None, None, 1, None, None, None) == 1
     assert lib.pe_destroy(None) == 1
+
+
+def test_training_entry_points_validate_on_the_host(B):
+    lib = B.lib()
+    buf = ctypes.create_string_buffer(64)
+    # bad sizes, leading dimension, mask type
+    assert lib.pe_train_build_mask(0, 4, 0, buf, 64, None) == 1
+    assert lib.pe_train_build_mask(4, 4, 0, None, 16, None) == 1
+    assert lib.pe_train_build_mask(4, 4, 0, buf, 8, None) == 1      # ld < n_max K
+    assert lib.pe_train_build_mask(4, 4, 1, buf, 20, None) == 1     # 40-byte rows
+    assert lib.pe_train_build_mask(4, 4, 7, buf, 16, None) == 1
+    # the per-sample mask is a view of the amortized one: host arithmetic only
+    v = ctypes.c_void_p()
+    rows, ld = ctypes.c_int64(), ctypes.c_int64()
+    assert lib.pe_train_mask_view(buf, 48, 12, 4, 5, ctypes.byref(v), ctypes.byref(rows),
+                                  ctypes.byref(ld)) == 0
+    assert v.value == ctypes.addressof(buf) and rows.value == 20 and ld.value == 48
+    assert lib.pe_train_mask_view(buf, 48, 12, 4, 13, ctypes.byref(v), ctypes.byref(rows),
+                                  ctypes.byref(ld)) == 1
+    # partition: boundaries must run 0 < ... < n, capacity must hold every row
+    b = (ctypes.c_int32 * 3)(0, 8, 16)
+    args = [buf, buf, buf, buf, buf, buf]
+    bad = (ctypes.c_int32 * 3)(0, 8, 15)
+    assert lib.pe_train_partition(16, 4, 0.5, buf, 2, bad, *args, 100, None) == 1
+    bad = (ctypes.c_int32 * 3)(0, 8, 8)
+    assert lib.pe_train_partition(8, 4, 0.5, buf, 2, bad, *args, 100, None) == 1
+    assert lib.pe_train_partition(16, 4, 0.5, buf, 2, b, *args, 8 + 64 - 1, None) == 1
+    assert lib.pe_train_partition(16, 4, 0.5, buf, 65, b, *args, 1000, None) == 1
+    assert lib.pe_train_partition(16, 4, 0.5, None, 2, b, *args, 100, None) == 1
