@@ -193,9 +193,14 @@ pe_status pe_expand_batch(pe_handle* h, int32_t B, int32_t K, int32_t T,
  * positions 0..pos of its request (GQA), O projection + residual, RMSNorm,
  * SwiGLU MLP + residual.  Finally the rows new_idx are gathered and
  * RMSNorm'ed with norm_final into out_hidden [B*K, d] (model dtype).
+ * Rejected rows write nothing and feed no sampled row, so after fc the
+ * layers run on the live rows only (found on the device, so the call's
+ * launches do not depend on the accepted counts and can be captured in a
+ * CUDA graph); this changes no result.
  * k_cache/v_cache: HOST arrays of n_layers device pointers, each a pool
  * [num_blocks, Hkv, 16, dh] (model dtype, 16-byte aligned); block_table as
- * in pe_expand_batch.  B and K must match the values recorded in *ex.
+ * in pe_expand_batch.  B and K must match the values recorded in *ex, and
+ * B <= max_reqs.
  * Each request's verify window is expected to hold at most K + 1 rows (the
  * previous step's drafts plus one); a request with more rows than that is
  * reported as PE_DEV_BAD_ROW.  The bf16 path keeps a split-KV workspace
@@ -222,9 +227,11 @@ pe_status pe_get_device_error(pe_handle* h, int32_t* code, void* stream);
 
 /* Optional diagnostics: when residual_trace is non-NULL, every later
  * pe_draft_forward copies the fp32 residual stream [T', d] after each layer
+ * (rows in expanded order; rows the layers skipped as rejected read zero)
  * into residual_trace + layer * max_tokens * d (caller-owned device buffer of
  * n_layers * max_tokens * d floats).  When attn_trace is non-NULL, it copies
- * each layer's attention output [T', Hq * dh] (model dtype) into
+ * each layer's attention output [T', Hq * dh] (model dtype, rejected rows
+ * zero) into
  * attn_trace + layer * max_tokens * Hq * dh elements.  NULL turns a trace
  * off. */
 pe_status pe_set_trace(pe_handle* h, float* residual_trace, void* attn_trace);

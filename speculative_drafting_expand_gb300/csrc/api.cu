@@ -389,9 +389,17 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
   }
 
   // Rejected rows (window rows after the accepted count) write no KV and
-  // feed no sampled row: after fc the layers run on the live rows only.  A
-  // batch of one window row per request has none, and skips the compaction.
-  const bool compact = ex->T > B;
+  // feed no sampled row: after fc the layers run on the live rows only.
+  // The compaction pays only if the live rows can need fewer token tiles
+  // in some projection: a batch of one window row per request has no
+  // rejected rows, and when even B*K live rows (every request accepting
+  // nothing) fill as many tiles as the expanded batch, nothing shrinks.
+  auto tiles_of = [&](int m, bool dual) {
+    const int bn = d.dtype == PE_DTYPE_BF16 ? tc_pick_bn(rows, dual) : 16;
+    return (m + bn - 1) / bn;
+  };
+  const bool compact = ex->T > B && (tiles_of(B * K, false) < tiles_of(rows, false) ||
+                                     tiles_of(B * K, true) < tiles_of(rows, true));
   const int32_t* live = nullptr;
   const int32_t* ids_l = ex->ids;
   const int32_t* pos_l = ex->pos;
