@@ -14,7 +14,7 @@ drafts its own batch (requests are independent: weak scaling, no
 collective on the data path).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload b1|b16|b64|qwen-k<K>|expand|ar-<workload>|lmhead-<rows>|train-mask|train-partition]
+                  [--workload b1|b16|b64|qwen-k<K>|expand|ar-<workload>|lmhead-<rows>|train-mask[-<tokens>]|train-partition]
 """
 
 from __future__ import annotations
@@ -369,9 +369,11 @@ def run_train(args, local):
 
     torch.cuda.set_device(local)
     n, K = 8192, 8
+    if args.workload.startswith("train-mask-"):          # a smaller mask (profiling)
+        n = int(args.workload[len("train-mask-"):])
     pk, src = peaks()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if args.workload == "train-mask":
+    if args.workload.startswith("train-mask"):
         N = n * K
         out = torch.empty((N, N), dtype=torch.bfloat16, device="cuda")
         for _ in range(args.warmup):
@@ -392,11 +394,13 @@ def run_train(args, local):
         print(json.dumps({
             "mode": "train_mask", "metric": "amortized mask build (GB/s written)",
             "value": gbs, "unit": "GB/s", "us_per_build": us, "bytes": nbytes,
-            "config": {"workload": "mask 8192 tokens x K=8 (65536 rows), additive bf16"},
+            "config": {"workload": f"mask {n} tokens x K={K} ({N} rows), additive bf16"},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                          "frac": gbs / peak, "peak_source": src},
             "steps": args.steps, "warmup": args.warmup, "clocks": clk.summary()}), flush=True)
         return 0
+    if args.workload != "train-partition":
+        raise SystemExit(f"unknown workload {args.workload}")
     r, bounds = 0.8, [0, 2048, 4096, 6144, 8192]
     u = torch.rand((n, K), generator=torch.Generator().manual_seed(3)).cuda()
     for _ in range(args.warmup):
@@ -616,6 +620,30 @@ def run_ours(args, world, rank, local):
                    "peak": hbm, "unit": "GB/s", "peak_source": f"{pk_kind} hbm_gbs"}
     lm_roof["frac"] = lm_roof["achieved"] / lm_roof["peak"]
 
+    # ---- the expansion kernel alone (steps a1 + a2), L2 flushed before each --
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    ex_ev = []
+    for _ in range(n_lm):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        B.pe_expand_batch(dr, wl.K, st.target_ids, st.target_pos, st.cu_in, st.num_accepted,
+                          st.sampled_ids, st.block_table, inp.num_blocks, st.target_hidden, ex)
+        b.record(stream)
+        ex_ev.append((a, b))
+    torch.cuda.synchronize()
+    del flush
+    ex_s = statistics.mean(a.elapsed_time(b) for a, b in ex_ev) / 1e3
+    es = 2 if sh.dtype == "bf16" else 4
+    Bn, Tn, To = wl.B, wl.T, wl.T_out
+    # hidden rows read once (h_shared once) and written once; metadata in and out
+    ex_bytes = (Tn + 1) * sh.hidden3 * es + To * sh.hidden3 * es + \
+        Tn * 8 + Bn * 12 + To * 4 + To * 14 + Bn * wl.K * 4 + Tn * 4 + (2 * Bn + 1) * 4
+    expand_roof = {"bound": "hbm", "launch_us": ex_s * 1e6, "bytes_per_launch": ex_bytes,
+                   "achieved": ex_bytes / ex_s / 1e9, "peak": hbm, "unit": "GB/s",
+                   "frac": ex_bytes / ex_s / 1e9 / hbm,
+                   "note": "expansion kernel alone, L2 flushed before each launch"}
+
     # ---- end to end through the public calls with host buffers -------------
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
     h_ids, h_pos, h_cu = pin(inp.target_ids), pin(inp.target_pos), pin(inp.cu_in)
@@ -675,6 +703,7 @@ def run_ours(args, world, rank, local):
                              traffic=traffic, bytes_per_launch=work["lm_head_bytes"],
                              flops_per_launch=work["lm_head_flops"],
                              launch_us=lm_avg_s * 1e6),
+            "expand_roofline": expand_roof,
             "step_roofline": {"bytes": work["bytes"], "flops": work["flops"],
                               "floor_us": step_floor_s * 1e6,
                               "frac": step_floor_s / step_s,
@@ -715,7 +744,7 @@ def main():
         return run_ar(args, world, rank, local)
     if args.workload.startswith("lmhead-"):
         return run_lmhead(args, local)
-    if args.workload in ("train-mask", "train-partition"):
+    if args.workload.startswith("train-"):
         return run_train(args, local)
     return run_ours(args, world, rank, local)
 
