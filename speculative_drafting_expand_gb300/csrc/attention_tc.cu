@@ -6,9 +6,11 @@
 // head h reads kv head h / (Hq / Hkv); softmax of q.k / sqrt(dh); rejected
 // rows (vLLM blog summary "P-EAGLE: Faster LLM Inference with Parallel
 // Speculative Decoding in vLLM", KV-cache bullet) produce zeros.  The rows of
-// one request are [accepted window rows, next-token row, MASK rows], so a
-// shorter request's mask is the top-left block of a longer one's (paper
-// summary "P-EAGLE: Parallel-Drafting EAGLE with Scalable Training", Fig. 3).
+// one request are [accepted window rows, next-token row, MASK rows] (after
+// the live-row compaction there are no rejected rows and is_rejected is
+// null), so a shorter request's mask is the top-left block of a longer
+// one's (paper summary "P-EAGLE: Parallel-Drafting EAGLE with Scalable
+// Training", Fig. 3).
 //
 // Work unit (one CTA): request r, kv head g, a tile of up to 128 query rows
 // (the request's rows x the g-th group of q heads -- GQA packs the group
