@@ -208,6 +208,12 @@ def barrier(world):
         dist.barrier()
 
 
+def aggregate_rate(world: int, steps_per_rank: int, elapsed_s: float) -> float:
+    """Whole-job rate: every rank ran the same number of steps on its own batch
+    (weak scaling), timed by the slowest rank."""
+    return world * steps_per_rank / elapsed_s
+
+
 def max_over_ranks(world, v: float) -> float:
     if world == 1:
         return v
@@ -512,7 +518,7 @@ def run_ar(args, world, rank, local):
     check_device(B, dr)
     if rank == 0:
         ms = elapsed_ms / args.steps
-        value = world * args.steps / (elapsed_ms / 1e3)
+        value = aggregate_rate(world, args.steps, elapsed_ms / 1e3)
         cfg = config_of(wl, args)
         cfg["workload"] = wl.name + "-autoregressive"
         cfg["drafting"] = f"autoregressive: {K} sequential passes of the K=1 step per draft step"
@@ -589,7 +595,7 @@ def run_ours(args, world, rank, local):
     elapsed_ms = max_over_ranks(world, e0.elapsed_time(e1))
     clocks.stop()
     ms_per_step = elapsed_ms / args.steps
-    value = world * args.steps / (elapsed_ms / 1e3)
+    value = aggregate_rate(world, args.steps, elapsed_ms / 1e3)
     check_device(B, dr)
 
     # ---- dominant kernel: the LM-head GEMM + argmax, timed on its stream ----
@@ -675,7 +681,7 @@ def run_ours(args, world, rank, local):
         e2e_step()
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(world, time.perf_counter() - t0)
-    e2e_value = world * n_e2e / e2e_s
+    e2e_value = aggregate_rate(world, n_e2e, e2e_s)
     check_device(B, dr)
 
     # ---- CPU oracle baseline (rank 0, one GPU only) -------------------------
