@@ -256,26 +256,36 @@ class DrafterOut:
 
 def gather_request_cache(cache_layer: np.ndarray, block_table_row,
                          seq_len: int, page_size: int,
-                         dtype: str) -> np.ndarray:
+                         dtype: str, scale: Optional[float] = None) -> np.ndarray:
     """Dense fp64 [S, Hkv, dh] copy of one request's paged cache.
 
     cache_layer layout [num_blocks, Hkv, page, dh]; position p lives in block
-    block_table_row[p // page] at offset p % page.
+    block_table_row[p // page] at offset p % page.  With a scale the pool
+    holds e4m3 codes and the value is code * scale (oracle/fp8_kv.py).
     """
     nblk = (seq_len + page_size - 1) // page_size
     blocks = [int(b) for b in block_table_row[:nblk]]
-    pages = to_f64(cache_layer[blocks], dtype)     # [nblk, Hkv, page, dh]
+    if scale is None:
+        pages = to_f64(cache_layer[blocks], dtype)     # [nblk, Hkv, page, dh]
+    else:
+        from . import fp8_kv
+        pages = fp8_kv.dequantize(cache_layer[blocks], scale)
     dense = pages.transpose(0, 2, 1, 3).reshape(nblk * page_size,
                                                 pages.shape[1], pages.shape[3])
     return dense[:seq_len].copy()
 
 
 def drafter_forward_rows(shape, weights, rows: DrafterRows, block_table,
-                         seq_lens: Dict[int, int], k_cache, v_cache) -> DrafterOut:
+                         seq_lens: Dict[int, int], k_cache, v_cache,
+                         kv_scales=None) -> DrafterOut:
     """Run the N drafter layers on explicit rows ([paper] section 2, Fig. 2).
 
     Every row writes its k, v at its own position before the layer's
     attention; each row then attends positions 0..P of its request.
+    kv_scales: None (the cache holds the model dtype) or one (k_scale,
+    v_scale) pair per layer for an fp8 e4m3 cache: the pools hold codes, a
+    new row is written as the code of k / k_scale, and attention reads
+    code * scale (oracle/fp8_kv.py, readings F1-F3).
     """
     dt = shape.dtype
     d, Hq, Hkv, dh = shape.d, shape.n_heads, shape.n_kv_heads, shape.head_dim
@@ -304,19 +314,29 @@ def drafter_forward_rows(shape, weights, rows: DrafterRows, block_table,
 
         attn = np.zeros((R, Hq, dh), np.float64)
         slots = np.zeros(R, np.int64)
+        ks, vs = (None, None) if kv_scales is None else kv_scales[l]
+        if kv_scales is not None:
+            from . import fp8_kv
+            k_codes, v_codes = fp8_kv.quantize(k, ks), fp8_kv.quantize(v, vs)
         for r in requests:
             sel = np.nonzero(rows.request == r)[0]
             S = int(seq_lens[r])
-            kd = gather_request_cache(k_cache[l], block_table[r], S, P, dt)
-            vd = gather_request_cache(v_cache[l], block_table[r], S, P, dt)
+            kd = gather_request_cache(k_cache[l], block_table[r], S, P, dt, ks)
+            vd = gather_request_cache(v_cache[l], block_table[r], S, P, dt, vs)
             for i in sel:                     # writes first ...
                 p = int(rows.positions[i])
-                kd[p] = k[i]
-                vd[p] = v[i]
+                if kv_scales is None:
+                    kd[p] = k[i]
+                    vd[p] = v[i]
+                else:
+                    kd[p] = fp8_kv.dequantize(k_codes[i], ks)
+                    vd[p] = fp8_kv.dequantize(v_codes[i], vs)
                 slots[i] = int(block_table[r][p // P]) * P + p % P
             for i in sel:                     # ... then attention
                 attn[i] = attention_one_row(q[i], kd, vd, int(rows.positions[i]))
-        kv_writes.append({"slot": slots, "k": k, "v": v})
+        kv_writes.append({"slot": slots, "k": k, "v": v} if kv_scales is None else
+                         {"slot": slots, "k": k, "v": v, "k_codes": k_codes,
+                          "v_codes": v_codes})
         layer_attn.append(attn)
 
         residual = residual + linear(attn.reshape(R, Hq * dh), lw["o"], dt)
@@ -362,14 +382,16 @@ class StepResult:
 
 
 def draft_step(shape, weights, K: int, inp, k_cache, v_cache,
-               requests: Optional[Sequence[int]] = None) -> StepResult:
+               requests: Optional[Sequence[int]] = None, kv_scales=None) -> StepResult:
     """One parallel drafting step: all K draft tokens from one pass.
 
     [blog] input formula: row 1 is emb(new) (+) h_context and rows 2..K are
     emb(mask) (+) h_shared; [paper] section 2: every row goes through the N
     layers at once, then the LM head.  Only non-rejected rows are computed
     (rejected rows produce nothing and write nothing).  ``requests`` selects
-    a subset of the batch (requests are independent).
+    a subset of the batch (requests are independent).  ``kv_scales`` selects
+    the fp8 (e4m3) KV cache: one (k_scale, v_scale) per layer, the pools
+    holding e4m3 codes (oracle/fp8_kv.py).
     """
     ex = expand_batch(K, inp.target_ids, inp.target_pos, inp.cu_in,
                       inp.num_accepted, inp.sampled_ids, inp.block_table,
@@ -386,7 +408,7 @@ def draft_step(shape, weights, K: int, inp, k_cache, v_cache,
                        ex.request_of_row[rowsel].astype(np.int64))
     seq = {r: int(ex.seq_lens[r]) for r in reqs}
     dout = drafter_forward_rows(shape, weights, rows, inp.block_table, seq,
-                                k_cache, v_cache)
+                                k_cache, v_cache, kv_scales)
     new_rows = np.concatenate([ex.new_idx[r * K:(r + 1) * K] for r in reqs])
     where = {int(e): i for i, e in enumerate(rowsel)}
     take = np.array([where[int(e)] for e in new_rows], np.int64)
