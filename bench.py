@@ -15,6 +15,7 @@ collective on the data path).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload b1|b16|b64|qwen-k<K>|expand|ar-<workload>|lmhead-<rows>|train-mask[-<tokens>]|train-partition]
+                  (b1, b16, b64 take a "-fp8" suffix: e4m3 KV pools)
 """
 
 from __future__ import annotations
@@ -41,7 +42,14 @@ METRIC = "P-EAGLE draft steps/s & drafted tok/s at K=7, 1 GB300; % of HBM/tensor
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+# fp8 (e4m3) KV pools of the "-fp8" workloads: one scale for every layer's K
+# and V (the N(0,1) context values stay well inside the e4m3 range)
+FP8_KV_SCALE = 0.05
+
+
 def workload(name: str):
+    if name.endswith("-fp8"):
+        return workload(name[: -len("-fp8")])
     if name == "b1":
         return W.gpt_oss_b1()
     if name == "b64":
@@ -67,9 +75,10 @@ def peaks():
 # algorithmic work of one step (bytes that must move, flops that must run)
 # ---------------------------------------------------------------------------
 
-def step_work(wl, inp):
+def step_work(wl, inp, kv_es=None):
     sh = wl.shape
     es = 2 if sh.dtype == "bf16" else 4
+    kv_es = es if kv_es is None else kv_es
     d, F, V = sh.d, sh.ffn, sh.vocab
     qd = sh.n_heads * sh.head_dim
     rows = wl.T_out
@@ -84,7 +93,7 @@ def step_work(wl, inp):
                  (2 * F * d, valid), (F * d, valid)]
     lm = (V * d, wl.B * wl.K)
     parts = [(n * es, 2.0 * m * n) for n, m in proj + [lm]]
-    kv_bytes = sh.n_layers * 2 * sum(seq) * sh.n_kv_heads * sh.head_dim * es
+    kv_bytes = sh.n_layers * 2 * sum(seq) * sh.n_kv_heads * sh.head_dim * kv_es
     attn_flops = 0.0
     for r in range(wl.B):
         a = int(wl.accepted[r])
@@ -290,6 +299,8 @@ def config_of(wl, args):
             "d": sh.d, "layers": sh.n_layers, "heads": f"{sh.n_heads}x{sh.head_dim}",
             "kv_heads": sh.n_kv_heads, "ffn": sh.ffn, "vocab": sh.vocab,
             "page_size": sh.page_size, "parallelism": f"replicas x{args.gpus}",
+            "kv_cache": (f"fp8 e4m3, scale {FP8_KV_SCALE}" if args.workload.endswith("-fp8")
+                         else sh.dtype),
             "l2": "weights stream from HBM every step (working set > 129 MB L2)",
             "graph": "step replayed as one CUDA graph"}
 
@@ -548,6 +559,14 @@ def run_ours(args, world, rank, local):
     kc, vc = W.make_kv_cache(wl, inp)
     dr = B.Drafter(sh, w, max(wl.T_out, wl.B * wl.K), wl.B)
     st = DeviceInputs(wl, inp, kc, vc, B, torch)
+    kv_fp8 = args.workload.endswith("-fp8")
+    if kv_fp8:
+        # e4m3 codes of the same draws (torch's float8 conversion: input
+        # preparation only; the step's own KV writes are the library's)
+        to8 = lambda t: (t.float() / FP8_KV_SCALE).to(torch.float8_e4m3fn).view(torch.uint8)
+        st.kc = [to8(k) for k in st.kc]
+        st.vc = [to8(v) for v in st.vc]
+        B.pe_set_kv_cache_fp8(dr, [FP8_KV_SCALE] * sh.n_layers, [FP8_KV_SCALE] * sh.n_layers)
     ex = B.Expanded(wl.T_out, wl.T, wl.B, wl.K, sh.hidden3, sh.dtype)
     tdt = torch.bfloat16 if sh.dtype == "bf16" else torch.float32
     out_hidden = torch.empty(wl.B * wl.K, sh.d, dtype=tdt, device="cuda")
@@ -599,7 +618,7 @@ def run_ours(args, world, rank, local):
     check_device(B, dr)
 
     # ---- dominant kernel: the LM-head GEMM + argmax, timed on its stream ----
-    work = step_work(wl, inp)
+    work = step_work(wl, inp, 1 if kv_fp8 else None)
     stream = torch.cuda.current_stream()
     n_lm = max(20, min(args.steps, 200))
     lm_ms = []

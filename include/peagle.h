@@ -225,6 +225,18 @@ pe_status pe_lmhead_argmax(pe_handle* h, const void* hidden, int32_t M,
  * since the last call (PE_DEV_*), and clear it. */
 pe_status pe_get_device_error(pe_handle* h, int32_t* code, void* stream);
 
+/* fp8 KV cache (the pages' deployment runs with --kv-cache-dtype fp8): after
+ * this call the k_cache / v_cache pools that pe_draft_forward receives hold
+ * OCP FP8 E4M3 codes, one byte per element in the same [num_blocks, Hkv, 16,
+ * dh] layout; layer l stores k / k_scales[l] and v / v_scales[l], rounded to
+ * the nearest e4m3 value (ties to even) and saturated to +-448, and its
+ * attention reads code * scale.  k_scales, v_scales: HOST arrays of
+ * n_layers positive finite floats, copied; both NULL return to pools of the
+ * model dtype.  PE_ERR_UNSUPPORTED unless the model is bf16 with head_dim
+ * 64; PE_ERR_INVALID_ARGUMENT for a non-positive or non-finite scale or only
+ * one of the two arrays. */
+pe_status pe_set_kv_cache_fp8(pe_handle* h, const float* k_scales, const float* v_scales);
+
 /* Optional diagnostics: when residual_trace is non-NULL, every later
  * pe_draft_forward copies the fp32 residual stream [T', d] after each layer
  * (rows in expanded order; rows the layers skipped as rejected read zero)

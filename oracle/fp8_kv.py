@@ -44,36 +44,27 @@ def e4m3_decode(codes) -> np.ndarray:
 
 
 # the non-negative finite codes in increasing order of value (0x00 .. 0x7E)
-_POS_CODES = np.arange(0x7F, dtype=np.int64)
 _POS_VALUES = E4M3_TABLE[:0x7F]
 
 
 def e4m3_encode(x) -> np.ndarray:
     """Nearest e4m3 code to each value, ties to the even code, saturating to
-    +-448, NaN to 0x7F (F2).  Plain search over the 127 non-negative values."""
+    +-448, NaN to 0x7F (F2): the two neighbours of |x| among the 127
+    non-negative values, the nearer one, the even code on a tie."""
     x = np.asarray(x, dtype=np.float64)
-    out = np.empty(x.shape, dtype=np.uint8)
-    flat, res = x.reshape(-1), out.reshape(-1)
-    for i, v in enumerate(flat):
-        if np.isnan(v):
-            res[i] = 0x7F
-            continue
-        sign = 0x80 if (v < 0 or (v == 0 and np.signbit(v))) else 0
-        a = min(abs(v), E4M3_MAX)
-        hi = int(np.searchsorted(_POS_VALUES, a, side="left"))   # first value >= a
-        if hi < len(_POS_VALUES) and _POS_VALUES[hi] == a:
-            c = hi
-        else:
-            lo = hi - 1
-            d_lo, d_hi = a - _POS_VALUES[lo], _POS_VALUES[hi] - a
-            if d_lo < d_hi:
-                c = lo
-            elif d_hi < d_lo:
-                c = hi
-            else:
-                c = lo if lo % 2 == 0 else hi      # tie: the even code
-        res[i] = sign | int(_POS_CODES[c])
-    return out
+    nan = np.isnan(x)
+    a = np.minimum(np.abs(np.where(nan, 0.0, x)), E4M3_MAX)
+    n = len(_POS_VALUES)
+    hi = np.clip(np.searchsorted(_POS_VALUES, a, side="left"), 0, n - 1)  # first value >= a
+    lo = np.clip(hi - 1, 0, n - 1)
+    d_lo = a - _POS_VALUES[lo]
+    d_hi = _POS_VALUES[hi] - a
+    c = np.where(_POS_VALUES[hi] == a, hi,
+                 np.where(d_lo < d_hi, lo,
+                          np.where(d_hi < d_lo, hi, np.where(lo % 2 == 0, lo, hi))))
+    sign = (x < 0) | ((x == 0) & np.signbit(x))
+    code = (c | np.where(sign, 0x80, 0)).astype(np.uint8)
+    return np.where(nan, np.uint8(0x7F), code).astype(np.uint8)
 
 
 def quantize(x, scale: float) -> np.ndarray:

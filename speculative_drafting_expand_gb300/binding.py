@@ -33,7 +33,8 @@ PE_MASK_ADDITIVE_BF16 = 1
 # the one that does not return a pe_status)
 EXPORTED = ("pe_create", "pe_destroy", "pe_expand_batch", "pe_draft_forward",
             "pe_lmhead_argmax", "pe_get_device_error", "pe_set_trace", "pe_linear",
-            "pe_get_launch_count", "pe_linear_static", "pe_train_build_mask",
+            "pe_get_launch_count", "pe_linear_static", "pe_set_kv_cache_fp8",
+            "pe_train_build_mask",
             "pe_train_mask_view", "pe_train_partition", "pe_status_string")
 
 _vp = ctypes.c_void_p
@@ -87,6 +88,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pe_linear.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp]
     lib.pe_get_launch_count.argtypes = [_vp, P(ctypes.c_int64)]
     lib.pe_linear_static.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _vp]
+    lib.pe_set_kv_cache_fp8.argtypes = [_vp, P(ctypes.c_float), P(ctypes.c_float)]
     lib.pe_train_build_mask.argtypes = [_i32, _i32, _i32, _vp, ctypes.c_int64, _vp]
     lib.pe_train_mask_view.argtypes = [_vp, ctypes.c_int64, _i32, _i32, _i32, P(_vp),
                                        P(ctypes.c_int64), P(ctypes.c_int64)]
@@ -269,6 +271,17 @@ def pe_get_device_error(dr: Drafter, stream=None) -> int:
 
 def pe_set_trace(dr: Drafter, residual_trace=None, attn_trace=None) -> None:
     _check("pe_set_trace", lib().pe_set_trace(dr.handle, ptr(residual_trace), ptr(attn_trace)))
+
+
+def pe_set_kv_cache_fp8(dr: Drafter, k_scales=None, v_scales=None) -> None:
+    """Switch the drafter to e4m3 KV pools with per-layer scales (None, None:
+    back to pools of the model dtype)."""
+    if k_scales is None and v_scales is None:
+        _check("pe_set_kv_cache_fp8", lib().pe_set_kv_cache_fp8(dr.handle, None, None))
+        return
+    ks = (ctypes.c_float * len(k_scales))(*[float(x) for x in k_scales])
+    vs = (ctypes.c_float * len(v_scales))(*[float(x) for x in v_scales])
+    _check("pe_set_kv_cache_fp8", lib().pe_set_kv_cache_fp8(dr.handle, ks, vs))
 
 
 def pe_get_launch_count(dr: Drafter) -> int:

@@ -20,6 +20,8 @@ int tc_b_box_rows(int M, int N, int sm_count, bool dual, bool live_rows);
 cudaError_t init_gemm_tc();
 size_t tc_partial_floats(int grid, int bn, bool dual);
 cudaError_t init_attention_tc();
+bool tensor_map_2d_u8(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows);
 size_t attention_tc_partial_floats(const AttnArgs& a, int max_rows_per_req, int sm_count);
 size_t attention_tc_counters(const AttnArgs& a, int max_rows_per_req, int sm_count);
 cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
@@ -68,11 +70,15 @@ struct pe_handle {
   int32_t* cu_live = nullptr;      // [max_reqs + 1]
   int32_t* new_c = nullptr;        // [max_tokens]
   int32_t* n_live = nullptr;       // [1]
+  // fp8 (e4m3) KV pools: one K and one V scale per layer
+  bool kv_fp8 = false;
+  std::vector<float> k_scales, v_scales;
   float* trace = nullptr;
   void* attn_trace = nullptr;
   long long launches = 0;
 
   std::map<std::tuple<const void*, uint64_t, uint64_t, uint64_t, uint32_t>, CUtensorMap> maps;
+  std::map<std::pair<const void*, uint64_t>, CUtensorMap> maps_u8;  // fp8 pools
   std::vector<void*> allocations;
 };
 
@@ -106,6 +112,15 @@ const CUtensorMap* get_map(pe_handle* h, const void* ptr, uint64_t rows, uint64_
   CUtensorMap m;
   if (!tensor_map_2d_bf16(&m, ptr, rows, cols, ld, 64, box_rows)) return nullptr;
   return &h->maps.emplace(key, m).first->second;
+}
+
+const CUtensorMap* get_map_u8(pe_handle* h, const void* ptr, uint64_t rows) {
+  auto key = std::make_pair(ptr, rows);
+  auto it = h->maps_u8.find(key);
+  if (it != h->maps_u8.end()) return &it->second;
+  CUtensorMap m;
+  if (!tensor_map_2d_u8(&m, ptr, rows, h->desc.head_dim, 16)) return nullptr;
+  return &h->maps_u8.emplace(key, m).first->second;
 }
 
 TcGemmWorkspace tc_ws(pe_handle* h) {
@@ -262,6 +277,24 @@ pe_status pe_create(const pe_model_desc* desc, const pe_weights* weights, int32_
 pe_status pe_get_launch_count(pe_handle* h, int64_t* count) {
   if (!h || !count) return PE_ERR_INVALID_ARGUMENT;
   *count = h->launches;
+  return PE_OK;
+}
+
+pe_status pe_set_kv_cache_fp8(pe_handle* h, const float* k_scales, const float* v_scales) {
+  if (!h || (!k_scales) != (!v_scales)) return PE_ERR_INVALID_ARGUMENT;
+  if (!k_scales) {
+    h->kv_fp8 = false;
+    return PE_OK;
+  }
+  if (h->desc.dtype != PE_DTYPE_BF16 || h->desc.head_dim != 64) return PE_ERR_UNSUPPORTED;
+  std::vector<float> ks(k_scales, k_scales + h->desc.n_layers);
+  std::vector<float> vs(v_scales, v_scales + h->desc.n_layers);
+  for (int l = 0; l < h->desc.n_layers; ++l)
+    if (!(ks[l] > 0.f) || !(vs[l] > 0.f) || !std::isfinite(ks[l]) || !std::isfinite(vs[l]))
+      return PE_ERR_INVALID_ARGUMENT;
+  h->k_scales = ks;
+  h->v_scales = vs;
+  h->kv_fp8 = true;
   return PE_OK;
 }
 
@@ -519,6 +552,11 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     rk.k_cache = k_cache[l];
     rk.v_cache = v_cache[l];
     rk.err = h->err;
+    if (h->kv_fp8) {
+      rk.kv_fp8 = 1;
+      rk.k_inv_scale = 1.f / h->k_scales[l];
+      rk.v_inv_scale = 1.f / h->v_scales[l];
+    }
     if ((e = counted(h, launch_rope_kv(dt, rk, s)))) return PE_ERR_CUDA;
     // paged causal attention
     AttnArgs at = {};
@@ -544,8 +582,15 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     if (dt == PE_DTYPE_F32) {
       if ((e = counted(h, launch_attention_simt(dt, at, s)))) return PE_ERR_CUDA;
     } else {
-      const CUtensorMap* tk = get_map(h, k_cache[l], cache_rows, d.head_dim, d.head_dim, 16);
-      const CUtensorMap* tv = get_map(h, v_cache[l], cache_rows, d.head_dim, d.head_dim, 16);
+      if (h->kv_fp8) {
+        at.kv_fp8 = 1;
+        at.k_scale = h->k_scales[l];
+        at.v_scale = h->v_scales[l];
+      }
+      const CUtensorMap* tk = h->kv_fp8 ? get_map_u8(h, k_cache[l], cache_rows)
+                                        : get_map(h, k_cache[l], cache_rows, d.head_dim, d.head_dim, 16);
+      const CUtensorMap* tv = h->kv_fp8 ? get_map_u8(h, v_cache[l], cache_rows)
+                                        : get_map(h, v_cache[l], cache_rows, d.head_dim, d.head_dim, 16);
       if (!tk || !tv) return PE_ERR_INVALID_ARGUMENT;
       e = counted(h, launch_attention_tc(at, *tk, *tv, ex->seq_lens, max_rows_per_req,
                                          h->sm_count, h->attn_partials, h->attn_partial_floats,

@@ -28,6 +28,9 @@
 // 128-byte swizzle) into a 3-stage ring (2 for dh=128).  Splits of one
 // (r, g, tile) are merged by the CTA that finishes last, in split order
 // (deterministic).
+#include <cudaTypedefs.h>
+
+#include "fp8_common.cuh"
 #include "pe_common.cuh"
 #include "pe_kernels.h"
 
@@ -45,7 +48,10 @@ struct AttnTcParams {
   int* counters;     // [B, Hkv, qtiles]
 };
 
-template <int DH>
+// FP8: the pools hold e4m3 codes.  Their pages come by TMA into a two-stage
+// staging ring, the producer warp widens them to f16 in the K/V stages
+// (every e4m3 value is an f16), and the MMAs run on f16 Q, K, V and P.
+template <int DH, bool FP8 = false>
 struct AttnCfg {
   static constexpr int NH = DH / 64;            // 64-wide halves of the head dim
   static constexpr int KEYS = 128;              // keys per chunk (two 64-key halves)
@@ -69,23 +75,29 @@ struct AttnCfg {
   // BT_ENTRIES pages of 16 keys (32 chunks)
   static constexpr int BT_ENTRIES = 256;
   static constexpr int BT_OFF = BAR_OFF + 256;
-  static constexpr int SMEM = 1024 + BT_OFF + BT_ENTRIES * 4;
+  // fp8 staging: [stage][K pages 8 x 1 KB | V pages 8 x 1 KB]
+  static constexpr int F8_STAGES = 2;
+  static constexpr int F8_STAGE = 2 * 8 * 16 * DH;
+  static constexpr int F8_OFF = (BT_OFF + BT_ENTRIES * 4 + 1023) / 1024 * 1024;
+  static constexpr int SMEM = 1024 + (FP8 ? F8_OFF + F8_STAGES * F8_STAGE : BT_OFF + BT_ENTRIES * 4);
   // TMEM: two S buffers at columns 0..255 (S of chunk c in buffer c % 2);
   // O of key slice h at 256 + h * DH
   static constexpr int O_COL = 256;
   static constexpr int TMEM_COLS = 512;
   static constexpr int THREADS = 64 + SOFT;     // producer, MMA, softmax warps
-  static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128);
-  static constexpr uint32_t IDESC_PV = idesc_bf16_f32_bmn(128, 64);
+  static constexpr uint32_t IDESC_S = FP8 ? idesc_f16_f32(128, 128) : idesc_bf16_f32(128, 128);
+  static constexpr uint32_t IDESC_PV =
+      FP8 ? idesc_f16_f32_bmn(128, 64) : idesc_bf16_f32_bmn(128, 64);
   static_assert(SMEM <= 232448, "shared memory");
+  static_assert(!FP8 || DH == 64, "the fp8 pools are read at dh 64");
   static_assert(O_COL + NQ * DH <= TMEM_COLS && KPW % 16 == 0, "slices");
 };
 
-template <int DH>
-__global__ void __launch_bounds__(AttnCfg<DH>::THREADS, 1)
+template <int DH, bool FP8 = false>
+__global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const AttnTcParams p) {
-  using C = AttnCfg<DH>;
+  using C = AttnCfg<DH, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -108,6 +120,7 @@ __global__ void __launch_bounds__(AttnCfg<DH>::THREADS, 1)
   uint64_t* pv_done = q_ready + 5;                // [2]: one per P buffer
   uint64_t* drain = q_ready + 7;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 12);
+  uint64_t* kv8_full = q_ready + 14;               // [2]: fp8 staging stages landed
   volatile int* flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
   float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
@@ -155,6 +168,10 @@ __global__ void __launch_bounds__(AttnCfg<DH>::THREADS, 1)
     mbar_init(&pv_done[0], 1);
     mbar_init(&pv_done[1], 1);
     mbar_init(drain, 1);
+    if (FP8) {
+      mbar_init(&kv8_full[0], 1);
+      mbar_init(&kv8_full[1], 1);
+    }
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -197,40 +214,121 @@ __global__ void __launch_bounds__(AttnCfg<DH>::THREADS, 1)
       }
       __syncwarp();
     }
-    if (lane == 0) {
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
+    if constexpr (!FP8) {
+      if (lane == 0) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        const uint64_t pol = l2_policy_evict_first();
+        for (int c = 0; c < nchunks; ++c) {
+          const int st = c % C::KV_STAGES;
+          const int round = c / C::KV_STAGES;
+          if (round > 0 && !mbar_wait(&kv_empty[st], (round - 1) & 1, a.err)) break;
+          const int t0 = key0 + c * C::KEYS;
+          int blks[8];
+          uint32_t bytes = 0;
+  #pragma unroll
+          for (int pg = 0; pg < 8; ++pg) {
+            const int t = t0 + pg * 16;
+            blks[pg] = t < key1 ? bt_s[c * 8 + pg] : -1;
+            if (blks[pg] >= 0) bytes += 2u * C::NH * 2048u;
+          }
+          mbar_arrive_expect_tx(&kv_full[st], bytes);
+  #pragma unroll
+          for (int pg = 0; pg < 8; ++pg) {
+            if (blks[pg] < 0) continue;
+            const int row = (blks[pg] * a.Hkv + g) * 16;
+  #pragma unroll
+            for (int h = 0; h < C::NH; ++h) {
+              uint8_t* kd = smem + C::K_OFF + (st * C::NH + h) * C::TILE + pg * 2048;
+              uint8_t* vd = smem + C::V_OFF + (st * C::NH + h) * C::TILE + pg * 2048;
+              tma_load_2d(kd, &tmK, &kv_full[st], h * 64, row, pol);
+              tma_load_2d(vd, &tmV, &kv_full[st], h * 64, row, pol);
+            }
+          }
+        }
+        // drain: the copies of the last stages have landed before exit
+        for (int c = max(0, nchunks - C::KV_STAGES); c < nchunks; ++c)
+          mbar_wait(&kv_full[c % C::KV_STAGES], (c / C::KV_STAGES) & 1, a.err);
+      }
+    } else {
+      // fp8 pages by TMA into the staging ring (lane 0), widened to f16 in
+      // the chunk's K/V stage by the whole warp: per chunk 2 x 8 pages x 16
+      // keys x 4 groups of 16 codes, 32 groups a lane.  Keys past the split
+      // (and pages whose block id was bad) become zeros, so no stale value
+      // reaches S or O.
+      uint8_t* f8 = smem + C::F8_OFF;
       const uint64_t pol = l2_policy_evict_first();
-      for (int c = 0; c < nchunks; ++c) {
-        const int st = c % C::KV_STAGES;
-        const int round = c / C::KV_STAGES;
-        if (round > 0 && !mbar_wait(&kv_empty[st], (round - 1) & 1, a.err)) break;
+      auto issue8 = [&](int c) {
+        const int s8 = c & 1;
         const int t0 = key0 + c * C::KEYS;
         int blks[8];
         uint32_t bytes = 0;
 #pragma unroll
         for (int pg = 0; pg < 8; ++pg) {
-          const int t = t0 + pg * 16;
-          blks[pg] = t < key1 ? bt_s[c * 8 + pg] : -1;
-          if (blks[pg] >= 0) bytes += 2u * C::NH * 2048u;
+          blks[pg] = t0 + pg * 16 < key1 ? bt_s[c * 8 + pg] : -1;
+          if (blks[pg] >= 0) bytes += 2u * 16u * DH;
         }
-        mbar_arrive_expect_tx(&kv_full[st], bytes);
+        mbar_arrive_expect_tx(&kv8_full[s8], bytes);
 #pragma unroll
         for (int pg = 0; pg < 8; ++pg) {
           if (blks[pg] < 0) continue;
           const int row = (blks[pg] * a.Hkv + g) * 16;
-#pragma unroll
-          for (int h = 0; h < C::NH; ++h) {
-            uint8_t* kd = smem + C::K_OFF + (st * C::NH + h) * C::TILE + pg * 2048;
-            uint8_t* vd = smem + C::V_OFF + (st * C::NH + h) * C::TILE + pg * 2048;
-            tma_load_2d(kd, &tmK, &kv_full[st], h * 64, row, pol);
-            tma_load_2d(vd, &tmV, &kv_full[st], h * 64, row, pol);
-          }
+          uint8_t* base = f8 + s8 * C::F8_STAGE + pg * 16 * DH;
+          tma_load_2d(base, &tmK, &kv8_full[s8], 0, row, pol);
+          tma_load_2d(base + 8 * 16 * DH, &tmV, &kv8_full[s8], 0, row, pol);
         }
+      };
+      if (lane == 0) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        for (int c = 0; c < min(nchunks, C::F8_STAGES); ++c) issue8(c);
       }
-      // drain: the copies of the last stages have landed before exit
-      for (int c = max(0, nchunks - C::KV_STAGES); c < nchunks; ++c)
-        mbar_wait(&kv_full[c % C::KV_STAGES], (c / C::KV_STAGES) & 1, a.err);
+      int issued = min(nchunks, C::F8_STAGES), consumed = 0;
+      for (int c = 0; c < nchunks; ++c) {
+        const int s8 = c & 1, st = c % C::KV_STAGES, round = c / C::KV_STAGES;
+        // every lane waits (each needs the barrier's acquire); the outcome is
+        // made warp-uniform so the lanes leave together
+        if (!__all_sync(0xffffffffu, mbar_wait(&kv8_full[s8], (c >> 1) & 1, a.err))) break;
+        consumed = c + 1;
+        if (round > 0 &&
+            !__all_sync(0xffffffffu, mbar_wait(&kv_empty[st], (round - 1) & 1, a.err)))
+          break;
+        const int t0 = key0 + c * C::KEYS;
+        const uint8_t* src = f8 + s8 * C::F8_STAGE;
+#pragma unroll 4
+        for (int k = 0; k < 32; ++k) {
+          const int item = lane + 32 * k;
+          const int which = item >> 9, pg = (item >> 6) & 7, kr = (item >> 2) & 15, q4 = item & 3;
+          const int kk = pg * 16 + kr;                 // key within the chunk
+          uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+          if (t0 + kk < key1 && bt_s[c * 8 + pg] >= 0) {
+            const uint4 x = *reinterpret_cast<const uint4*>(src + which * 8 * 16 * DH +
+                                                            pg * 16 * DH + kr * DH + q4 * 16);
+            lo = make_uint4(e4m3x2_to_f16x2(x.x), e4m3x2_to_f16x2(x.x >> 16),
+                            e4m3x2_to_f16x2(x.y), e4m3x2_to_f16x2(x.y >> 16));
+            hi = make_uint4(e4m3x2_to_f16x2(x.z), e4m3x2_to_f16x2(x.z >> 16),
+                            e4m3x2_to_f16x2(x.w), e4m3x2_to_f16x2(x.w >> 16));
+          }
+          // row kk of the 128-byte-swizzled stage: dims q4*16 .. +15 are its
+          // 16-byte chunks 2 q4 and 2 q4 + 1
+          uint8_t* dst = smem + (which ? C::V_OFF : C::K_OFF) + st * C::TILE + kk * 128;
+          *reinterpret_cast<uint4*>(dst + (((2 * q4) ^ (kk & 7)) * 16)) = lo;
+          *reinterpret_cast<uint4*>(dst + (((2 * q4 + 1) ^ (kk & 7)) * 16)) = hi;
+        }
+        fence_proxy_async_smem();   // the stage's f16 rows, for the MMA's reads
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&kv_full[st]);
+          if (c + C::F8_STAGES < nchunks) issue8(c + C::F8_STAGES);
+        }
+        if (c + C::F8_STAGES < nchunks) issued = c + C::F8_STAGES + 1;
+        __syncwarp();
+      }
+      // drain: staging copies issued but not waited for (after a stop) land
+      // before the CTA exits
+      if (lane == 0)
+        for (int c = consumed; c < issued; ++c)
+          mbar_wait(&kv8_full[c & 1], (c >> 1) & 1, a.err);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -306,6 +404,9 @@ __global__ void __launch_bounds__(AttnCfg<DH>::THREADS, 1)
         const int tl = ch >> 3, cc = ch & 7;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (P >= 0) v = src[ch];
+        if (FP8)  // the MMAs run on f16 operands
+          v = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                         bf16x2_to_f16x2(v.w));
         *reinterpret_cast<uint4*>(smem + C::Q_OFF + tl * C::TILE + qrow * 128 +
                                   ((cc ^ (qrow & 7)) * 16)) = v;
       }
@@ -314,7 +415,9 @@ __global__ void __launch_bounds__(AttnCfg<DH>::THREADS, 1)
     named_bar_sync(1, C::SOFT);
     if (threadIdx.x == 64) mbar_arrive(q_ready);
 
-    const float sc = a.scale * 1.4426950408889634f;   // log2(e) / sqrt(dh)
+    // log2(e) / sqrt(dh), times the K scale of an fp8 pool (S holds
+    // q . code; the score is q . code * k_scale)
+    const float sc = a.scale * 1.4426950408889634f * (FP8 ? a.k_scale : 1.f);
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     const uint32_t o_col = C::O_COL + h * DH;
@@ -361,7 +464,8 @@ __global__ void __launch_bounds__(AttnCfg<DH>::THREADS, 1)
         }
       }
       // probabilities: one FFMA and one MUFU.EX2 a score; the row sum is
-      // kept in fp32 (two chains), P goes to the MMA as bf16 pairs
+      // kept in fp32 (two chains), P goes to the MMA as bf16 pairs (f16
+      // with fp8 pools)
       uint32_t pk[KPW / 2];
       float ps0 = 0.f, ps1 = 0.f;
       const float nm = -m_new;
@@ -372,7 +476,7 @@ __global__ void __launch_bounds__(AttnCfg<DH>::THREADS, 1)
           const float p1 = fast_exp2(fmaf(s[j + 1], sc, nm));
           ps0 += p0;
           ps1 += p1;
-          pk[j / 2] = pack_bf16x2(p0, p1);
+          pk[j / 2] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
         }
       } else {
 #pragma unroll
@@ -383,7 +487,7 @@ __global__ void __launch_bounds__(AttnCfg<DH>::THREADS, 1)
           const float p1 = (tb + j + 1 <= P) ? e1 : 0.f;
           ps0 += p0;
           ps1 += p1;
-          pk[j / 2] = pack_bf16x2(p0, p1);
+          pk[j / 2] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
         }
       }
       const float psum = ps0 + ps1;
@@ -472,7 +576,7 @@ __global__ void __launch_bounds__(AttnCfg<DH>::THREADS, 1)
           float acc = 0.f;
 #pragma unroll
           for (int i = 0; i < C::NQ; ++i) acc += x[i][j] * wi[i];
-          o[c0 + j] = acc;
+          o[c0 + j] = FP8 ? acc * a.v_scale : acc;   // O holds P . code for fp8 pools
         }
       }
       bf16* out = static_cast<bf16*>(a.out) + (static_cast<size_t>(row) * a.Hq + head) * DH + h * HC;
@@ -612,6 +716,32 @@ size_t attention_tc_counters(const AttnArgs& a, int max_rows_per_req, int sm_cou
   return static_cast<size_t>(a.B) * a.Hkv * pl.qtiles;
 }
 
+// Tensor map of an fp8 pool viewed as [rows, cols] bytes (rows = blocks x
+// kv heads x 16 keys, cols = dh), boxes of box_rows keys x cols bytes,
+// unswizzled (the pages are widened by threads, not read by the MMA).
+bool tensor_map_2d_u8(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) != 0 || cols % 16 != 0 || cols > 256) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(cols), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t init_attention_tc() {
   cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel<64>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -619,6 +749,9 @@ cudaError_t init_attention_tc() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(attention_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              AttnCfg<128>::SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attention_tc_kernel<64, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<64, true>::SMEM);
   return e;
 }
 
@@ -644,6 +777,11 @@ cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const
   if (need > part_floats || static_cast<size_t>(a.B) * a.Hkv * pl.qtiles > n_counters)
     return cudaErrorInvalidValue;
   dim3 grid(pl.max_splits, a.Hkv * pl.qtiles, a.B);
+  if (a.kv_fp8) {
+    if (a.dh != 64 || !(a.k_scale > 0.f) || !(a.v_scale > 0.f)) return cudaErrorInvalidValue;
+    return launch_pdl(attention_tc_kernel<64, true>, grid, dim3(AttnCfg<64, true>::THREADS),
+                      AttnCfg<64, true>::SMEM, s, tmK, tmV, p);
+  }
   if (a.dh == 64)
     return launch_pdl(attention_tc_kernel<64>, grid, dim3(AttnCfg<64>::THREADS),
                       AttnCfg<64>::SMEM, s, tmK, tmV, p);

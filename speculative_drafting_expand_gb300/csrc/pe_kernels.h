@@ -150,11 +150,16 @@ struct RopeKvArgs {
   void* k_cache;            // [num_blocks, Hkv, 16, dh]
   void* v_cache;
   int* err;
+  // fp8 (e4m3) pools: k / k_scale and v / v_scale are stored as codes
+  int kv_fp8;
+  float k_inv_scale, v_inv_scale;
 };
 cudaError_t launch_rope_kv(int dtype, const RopeKvArgs& a, cudaStream_t s);
 
 struct AttnArgs {
   int rows, B, Hq, Hkv, dh, bt_stride, num_blocks, max_seq;
+  int kv_fp8;                // pools hold e4m3 codes; values are code * scale
+  float k_scale, v_scale;
   const int32_t* live;       // optional live-row count (per-row kernel only)
   const void* q;             // [rows, Hq dh] (roped)
   const void* k_cache;

@@ -8,6 +8,7 @@
 //   * rotate-half RoPE of q and k at the row's position, with k and v written
 //     into the paged KV cache at the row's slot (slot -1: no write, as the
 //     vLLM blog summary's KV-cache bullet requires for rejected tokens).
+#include "fp8_common.cuh"
 #include "pe_common.cuh"
 #include "pe_kernels.h"
 
@@ -339,8 +340,18 @@ __device__ __forceinline__ void stv(bf16* p, const float v[8]) {
   *reinterpret_cast<uint4*>(p) = r;
 }
 __device__ __forceinline__ void stv(float* p, const float v[4]) { st4(p, v); }
+// eight values -> eight e4m3 codes of v * inv (an fp8 pool row, 8 bytes)
+__device__ __forceinline__ void stv_e4m3(uint8_t* p, const float v[8], float inv) {
+  uint2 r;
+  r.x = static_cast<uint32_t>(f32x2_to_e4m3x2(v[0] * inv, v[1] * inv)) |
+        (static_cast<uint32_t>(f32x2_to_e4m3x2(v[2] * inv, v[3] * inv)) << 16);
+  r.y = static_cast<uint32_t>(f32x2_to_e4m3x2(v[4] * inv, v[5] * inv)) |
+        (static_cast<uint32_t>(f32x2_to_e4m3x2(v[6] * inv, v[7] * inv)) << 16);
+  *reinterpret_cast<uint2*>(p) = r;
+}
 
-template <typename T>
+// FP8: the K and V rows go to e4m3 pools (bf16 activations only).
+template <typename T, bool FP8 = false>
 __global__ void __launch_bounds__(kRowThreads) rope_kv_vec_kernel(const RopeKvArgs a) {
   using R = RopeVec<T>;
   constexpr int E = R::EPV;
@@ -409,14 +420,22 @@ __global__ void __launch_bounds__(kRowThreads) rope_kv_vec_kernel(const RopeKvAr
         stv(qo + h * a.dh + t, y1);
         stv(qo + h * a.dh + half + t, y2);
       } else if (blk >= 0) {
-        T* dst = kc + ((static_cast<size_t>(blk) * a.Hkv + (h - a.Hq)) * 16 + off) * a.dh;
-        stv(dst + t, y1);
-        stv(dst + half + t, y2);
+        const size_t row = ((static_cast<size_t>(blk) * a.Hkv + (h - a.Hq)) * 16 + off) * a.dh;
+        if constexpr (FP8) {
+          uint8_t* dst = static_cast<uint8_t*>(a.k_cache) + row;
+          stv_e4m3(dst + t, y1, a.k_inv_scale);
+          stv_e4m3(dst + half + t, y2, a.k_inv_scale);
+        } else {
+          stv(kc + row + t, y1);
+          stv(kc + row + half + t, y2);
+        }
       }
     } else if (it < n_rope + n_v) {
       const int w = (it - n_rope) * E;
       const int g = w / a.dh, t = w % a.dh;
-      stv(vc + ((static_cast<size_t>(blk) * a.Hkv + g) * 16 + off) * a.dh + t, x1[k]);
+      const size_t row = ((static_cast<size_t>(blk) * a.Hkv + g) * 16 + off) * a.dh;
+      if constexpr (FP8) stv_e4m3(static_cast<uint8_t*>(a.v_cache) + row + t, x1[k], a.v_inv_scale);
+      else stv(vc + row + t, x1[k]);
     }
   }
 }
@@ -471,6 +490,12 @@ cudaError_t rope_launch(const RopeKvArgs& a, cudaStream_t s) {
                   half % E == 0 &&
                   (a.Hq + a.Hkv) * (half / E) + a.Hkv * a.dh / E <=
                       RopeVec<T>::PER_THREAD * kRowThreads;
+  if (a.kv_fp8) {
+    if constexpr (sizeof(T) == 2) {
+      if (ok) return launch_pdl(rope_kv_vec_kernel<T, true>, dim3(a.rows), dim3(kRowThreads), 0, s, a);
+    }
+    return cudaErrorInvalidValue;
+  }
   if (ok) return launch_pdl(rope_kv_vec_kernel<T>, dim3(a.rows), dim3(kRowThreads), 0, s, a);
   return launch_pdl(rope_kv_kernel<T>, dim3(a.rows), dim3(kRowThreads), 0, s, a);
 }

@@ -97,6 +97,7 @@ def test_host_validation_rejects_bad_arguments_without_a_device(B):
                                 None) == 1
     assert lib.pe_lmhead_argmax(None, None, 1, None, None, None) == 1
     assert lib.pe_destroy(None) == 1
+    assert lib.pe_set_kv_cache_fp8(None, None, None) == 1
 
 
 def test_training_entry_points_validate_on_the_host(B):
