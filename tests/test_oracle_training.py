@@ -198,3 +198,37 @@ def test_segmented_attention_equals_whole_sequence_attention():
         out = TO.masked_attention(q[rows[own]], k[rows], v[rows], full[np.ix_(rows[own], rows)])
         for j, i in enumerate(rows[own]):
             assert np.allclose(out[j], at[int(i)], rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------- hand-worked fixtures
+
+def _golden():
+    import json
+    import os
+    p = os.path.join(os.path.dirname(__file__), "golden", "training_worked_examples.json")
+    return json.load(open(p))
+
+
+def test_mask_matches_the_hand_worked_example():
+    g = _golden()["mask"]
+    m = TO.build_mask(g["n"], g["K"])
+    got = [np.nonzero(m[i])[0].tolist() for i in range(g["n"] * g["K"])]
+    assert got == g["allowed_columns"]
+
+
+def test_partition_matches_the_hand_worked_example():
+    g = _golden()["partition"]
+    keep = np.zeros((g["n"], g["K"]), dtype=bool)
+    for p, d in g["kept"]:
+        keep[p, d] = True
+    parts = TO.partition(keep, g["bounds"])
+    for key, s in g["expected_segment"].items():
+        p, d = (int(x) for x in key.split(","))
+        assert parts.seg[p, d] == s, key
+    assert TO.partition_by_index(keep, g["bounds"])[4, 2] == g["naive_segment_of_4_2"]
+    assert parts.offsets.tolist() == g["offsets"]
+    assert parts.rows.tolist() == g["rows"]
+    assert parts.owned.tolist() == g["owned"]
+    # the same keep pattern drawn through COD: draws below r on kept rows
+    u = np.where(keep, 0.0, 0.99).astype(np.float32)
+    assert np.array_equal(TO.cod_keep(g["n"], g["K"], 0.5, u), keep)
