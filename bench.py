@@ -117,7 +117,7 @@ def kernel_source_hash() -> str:
     only reported while the kernel it was measured on is unchanged."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("gemm_tc.cu", "gemm_tc.cuh", "gemm_mc.cu", "pe_common.cuh"):
+    for f in ("gemm_tc.cu", "gemm_tc.cuh", "pe_common.cuh"):
         with open(os.path.join(ROOT, "speculative_drafting_expand_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

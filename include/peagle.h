@@ -225,6 +225,16 @@ pe_status pe_lmhead_argmax(pe_handle* h, const void* hidden, int32_t M,
  * since the last call (PE_DEV_*), and clear it. */
 pe_status pe_get_device_error(pe_handle* h, int32_t* code, void* stream);
 
+/* Self-check of the bounded waits (no counterpart on the pages; the
+ * failure handling of every kernel here rests on it).  Launches one kernel
+ * that waits on an mbarrier nobody arrives on and then on a global flag
+ * nobody sets; each wait gives up after the library's wait limit (2 s),
+ * records PE_DEV_TIMEOUT in the handle's error word and the kernel returns.
+ * out: caller-owned device int32[2], set to 1 for each wait that gave up
+ * (0 if it was satisfied).  Asynchronous on `stream`; takes about 4 s of
+ * GPU time; the context stays usable afterwards. */
+pe_status pe_check_bounded_wait(pe_handle* h, int32_t* out, void* stream);
+
 /* fp8 KV cache (the pages' deployment runs with --kv-cache-dtype fp8): after
  * this call the k_cache / v_cache pools that pe_draft_forward receives hold
  * OCP FP8 E4M3 codes, one byte per element in the same [num_blocks, Hkv, 16,
@@ -262,16 +272,24 @@ pe_status pe_linear(pe_handle* h, const void* x, const void* w, float* y,
  * that owns every byte of device memory, or on a path that must never enter
  * the driver's allocator.  x [M, K] and w [N, K] are 16-byte-aligned bf16,
  * y [M, N] fp32, all caller-owned device memory; K % 8 == 0.
- * The split-K scratch is one static device array of about 4 MiB, reserved
+ * The split-K scratch is one static device array of about 5.3 MB, reserved
  * on every GPU that loads the library until the process exits; it bounds
  * M <= 32 and N <= 4096 * 128, and larger sizes return PE_ERR_UNSUPPORTED
- * before launching anything.  The first call on a device looks up the
+ * before launching anything.  It holds split-K partials for up to 160 SMs:
+ * a GPU with more runs the projection on 160 of them.  The first call on a device looks up the
  * array's device address and prepares the kernels for that device; make
  * that first call before any stream capture.  All calls share the array,
  * so calls that overlap on the GPU race on it and must be serialised by the
  * caller.  Asynchronous on `stream`. */
 pe_status pe_linear_static(const void* x, const void* w, float* y, int32_t M,
                            int32_t N, int32_t K, void* stream);
+
+/* Read and clear the device error word that pe_linear_static's kernels
+ * write into the same static array (0: nothing recorded since the last
+ * read; PE_DEV_TIMEOUT: a bounded wait gave up and y may be incomplete).
+ * The word persists across calls until this reads it.  Synchronises
+ * `stream`; allocates nothing.  No counterpart on the P-EAGLE pages. */
+pe_status pe_linear_static_error(int32_t* code, void* stream);
 
 /* Number of kernels this handle has launched since pe_create (host-side
  * count, incremented per launch, including launches captured into a CUDA

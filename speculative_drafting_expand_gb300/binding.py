@@ -33,7 +33,9 @@ PE_MASK_ADDITIVE_BF16 = 1
 # the one that does not return a pe_status)
 EXPORTED = ("pe_create", "pe_destroy", "pe_expand_batch", "pe_draft_forward",
             "pe_lmhead_argmax", "pe_get_device_error", "pe_set_trace", "pe_linear",
-            "pe_get_launch_count", "pe_linear_static", "pe_set_kv_cache_fp8",
+            "pe_get_launch_count", "pe_check_bounded_wait", "pe_linear_static",
+            "pe_linear_static_error",
+            "pe_set_kv_cache_fp8",
             "pe_train_build_mask",
             "pe_train_mask_view", "pe_train_partition", "pe_status_string")
 
@@ -88,6 +90,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pe_linear.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp]
     lib.pe_get_launch_count.argtypes = [_vp, P(ctypes.c_int64)]
     lib.pe_linear_static.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _vp]
+    lib.pe_check_bounded_wait.argtypes = [_vp, _vp, _vp]
+    lib.pe_linear_static_error.argtypes = [P(_i32), _vp]
     lib.pe_set_kv_cache_fp8.argtypes = [_vp, P(ctypes.c_float), P(ctypes.c_float)]
     lib.pe_train_build_mask.argtypes = [_i32, _i32, _i32, _vp, ctypes.c_int64, _vp]
     lib.pe_train_mask_view.argtypes = [_vp, ctypes.c_int64, _i32, _i32, _i32, P(_vp),
@@ -269,6 +273,12 @@ def pe_get_device_error(dr: Drafter, stream=None) -> int:
     return code.value
 
 
+def pe_check_bounded_wait(dr: Drafter, out, stream=None) -> None:
+    """Launch the bounded-wait self-check (out: device int32[2])."""
+    _check("pe_check_bounded_wait", lib().pe_check_bounded_wait(dr.handle, ptr(out),
+                                                                stream_ptr(stream)))
+
+
 def pe_set_trace(dr: Drafter, residual_trace=None, attn_trace=None) -> None:
     _check("pe_set_trace", lib().pe_set_trace(dr.handle, ptr(residual_trace), ptr(attn_trace)))
 
@@ -306,6 +316,15 @@ def pe_linear_static(x, w, y, stream=None):
     _check("pe_linear_static", lib().pe_linear_static(ptr(x), ptr(w), ptr(y), M, N, K,
                                                       stream_ptr(stream)))
     return y
+
+
+def pe_linear_static_error(stream=None) -> int:
+    """Read and clear the device error word of pe_linear_static's static
+    array (0: nothing recorded since the last read)."""
+    code = _i32(0)
+    _check("pe_linear_static_error", lib().pe_linear_static_error(ctypes.byref(code),
+                                                                  stream_ptr(stream)))
+    return code.value
 
 
 # ---------------------------------------------------------------------------

@@ -15,7 +15,8 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
                                 const CUtensorMap& xb, bool dual, int M, int N, int K,
                                 const EpiArgs& epi, const TcGemmWorkspace& ws, int* err,
                                 cudaStream_t s);
-int tc_pick_bn(int M, bool dual);
+int tc_pick_bn(int M, bool dual, bool wide);
+bool tc_wide(int N, int sm_count, bool dual, bool live_rows);
 int tc_b_box_rows(int M, int N, int sm_count, bool dual, bool live_rows);
 cudaError_t init_gemm_tc();
 size_t tc_partial_floats(int grid, int bn, bool dual);
@@ -28,6 +29,7 @@ cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const
                                 const int32_t* seq_lens, int max_rows_per_req, int sm_count,
                                 float* part, size_t part_floats, int* counters,
                                 size_t n_counters, cudaStream_t s);
+cudaError_t launch_bounded_wait_check(int* flag, int32_t* out, int* err, cudaStream_t s);
 }  // namespace pe
 
 using namespace pe;
@@ -42,6 +44,7 @@ struct pe_handle {
   size_t esize = 2;  // bytes per element of the model dtype
 
   int* err = nullptr;
+  int* diag_flag = nullptr;  // the flag the bounded-wait self-check waits on
   float* resid = nullptr;   // [max_tokens, d] fp32 residual stream
   void* x_in = nullptr;     // [max_tokens, 2d] QKV input
   void* qkv = nullptr;      // [max_tokens, (Hq + 2Hkv) dh]
@@ -233,6 +236,7 @@ pe_status pe_create(const pe_model_desc* desc, const pe_weights* weights, int32_
     return r;
   };
   if (e == cudaSuccess) e = dev_alloc(h, &h->err, 1);
+  if (e == cudaSuccess) e = dev_alloc(h, &h->diag_flag, 1);
   if (e == cudaSuccess) e = dev_alloc(h, &h->resid, T * d.d);
   if (e == cudaSuccess) e = alloc_bytes(&h->x_in, T * 2 * d.d * es);
   if (e == cudaSuccess) e = alloc_bytes(&h->qkv, T * qkv_rows * es);
@@ -257,7 +261,7 @@ pe_status pe_create(const pe_model_desc* desc, const pe_weights* weights, int32_
   if (e == cudaSuccess && d.dtype == PE_DTYPE_BF16) e = init_attention_tc();
   if (e == cudaSuccess && d.dtype == PE_DTYPE_BF16) {
     // the widest token tile any row count up to max_tokens can take
-    const int bn = max_tokens > 128 ? 256 : tc_pick_bn(max_tokens, false);
+    const int bn = max_tokens > 128 ? 256 : tc_pick_bn(max_tokens, false, false);
     // stream-K runs two CTAs an SM for token tiles up to 32 wide
     h->gemm_partial_floats = tc_partial_floats((bn <= 32 ? 2 : 1) * h->sm_count, bn, true);
     e = dev_alloc(h, &h->gemm_partials, h->gemm_partial_floats);
@@ -315,6 +319,12 @@ pe_status pe_get_device_error(pe_handle* h, int32_t* code, void* stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   *code = v;
   return cuda_status(e);
+}
+
+pe_status pe_check_bounded_wait(pe_handle* h, int32_t* out, void* stream) {
+  if (!h || !out) return PE_ERR_INVALID_ARGUMENT;
+  return cuda_status(counted(
+      h, launch_bounded_wait_check(h->diag_flag, out, h->err, static_cast<cudaStream_t>(stream))));
 }
 
 pe_status pe_expand_batch(pe_handle* h, int32_t B, int32_t K, int32_t T, const int32_t* target_ids,
@@ -428,7 +438,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
   // rejected rows, and when even B*K live rows (every request accepting
   // nothing) fill as many tiles as the expanded batch, nothing shrinks.
   auto tiles_of = [&](int m, bool dual) {
-    const int bn = d.dtype == PE_DTYPE_BF16 ? tc_pick_bn(rows, dual) : 16;
+    const int bn = d.dtype == PE_DTYPE_BF16 ? tc_pick_bn(rows, dual, false) : 16;
     return (m + bn - 1) / bn;
   };
   const bool compact = ex->T > B && (tiles_of(B * K, false) < tiles_of(rows, false) ||
@@ -690,7 +700,7 @@ pe_status pe_linear(pe_handle* h, const void* x, const void* w, float* y, int32_
   if (h->desc.dtype == PE_DTYPE_BF16 && (K % 8 || !aligned16(x) || !aligned16(w)))
     return PE_ERR_INVALID_ARGUMENT;
   if (h->desc.dtype == PE_DTYPE_BF16) {
-    const int bn = tc_pick_bn(M, false);
+    const int bn = tc_pick_bn(M, false, tc_wide(N, h->sm_count, false, false));
     const long long tiles = static_cast<long long>((N + 127) / 128) * ((M + bn - 1) / bn);
     if (tiles > h->max_tiles) return PE_ERR_INVALID_ARGUMENT;
   }

@@ -151,8 +151,10 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
         const long long u = lo + i;
         const int tile = static_cast<int>(u / kb), kk = static_cast<int>(u % kb);
         const int m = tile % tiles_m;
-        tma_load_2d(smem + i * C::STAGE_BYTES + C::NA * C::A_BYTES, &tmB, &full[i], kk * 64,
-                    m * BN, pol_b);
+#pragma unroll
+        for (int h = 0; h < C::NMMA; ++h)
+          tma_load_2d(smem + i * C::STAGE_BYTES + C::NA * C::A_BYTES + h * C::B_HALF_BYTES, &tmB,
+                      &full[i], kk * 64, m * BN + h * C::MMA_N, pol_b);
       }
       long long issued = npre;
       for (long long i = npre; i < n; ++i) {
@@ -166,7 +168,10 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
         mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
         tma_load_2d(st, &tmA, &full[stage], kk * 64, f * 128, pol_a);
         if (DUAL) tma_load_2d(st + C::A_BYTES, &tmA2, &full[stage], kk * 64, f * 128, pol_a);
-        tma_load_2d(st + C::NA * C::A_BYTES, &tmB, &full[stage], kk * 64, m * BN, pol_b);
+#pragma unroll
+        for (int h = 0; h < C::NMMA; ++h)
+          tma_load_2d(st + C::NA * C::A_BYTES + h * C::B_HALF_BYTES, &tmB, &full[stage], kk * 64,
+                      m * BN + h * C::MMA_N, pol_b);
         issued = i + 1;
       }
       // drain: every copy this thread issued has landed before the CTA exits
@@ -200,12 +205,17 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
           const uint32_t b_addr = a_addr + C::NA * C::A_BYTES;
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
-            const uint64_t bdesc = sw128_kmajor_desc(b_addr + k4 * 32);
             const uint32_t accum = (kk > k_lo || k4 > 0) ? 1u : 0u;
-            umma_bf16(d, sw128_kmajor_desc(a_addr + k4 * 32), bdesc, C::IDESC, accum);
-            if (DUAL)
-              umma_bf16(d + BN, sw128_kmajor_desc(a_addr + C::A_BYTES + k4 * 32), bdesc,
-                        C::IDESC, accum);
+            const uint64_t adesc = sw128_kmajor_desc(a_addr + k4 * 32);
+#pragma unroll
+            for (int h = 0; h < C::NMMA; ++h) {
+              // token half h of a wide tile: its own rows of B, its own columns
+              const uint64_t bdesc = sw128_kmajor_desc(b_addr + h * C::B_HALF_BYTES + k4 * 32);
+              umma_bf16(d + h * C::MMA_N, adesc, bdesc, C::IDESC, accum);
+              if (DUAL)
+                umma_bf16(d + BN, sw128_kmajor_desc(a_addr + C::A_BYTES + k4 * 32), bdesc,
+                          C::IDESC, accum);
+            }
           }
           umma_commit(&empty[stage]);
         }
@@ -496,7 +506,8 @@ static cudaError_t set_smem_attr() {
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-  for (int S = 2; S <= 8 && e == cudaSuccess; ++S) {
+  // the wide tile's accumulator does not fit its stages: never cluster-split
+  for (int S = 2; S <= 8 && e == cudaSuccess && BN <= 256; ++S) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S * 32);
     cfg.blockDim = dim3(192);
@@ -529,7 +540,7 @@ cudaError_t init_gemm_tc() {
   PE_TC_ATTR(224)
   PE_TC_ATTR(256)
 #undef PE_TC_ATTR
-  if (e == cudaSuccess) e = init_gemm_mc();
+  if (e == cudaSuccess) e = set_smem_attr<448, false>();
   return e;
 }
 
@@ -588,22 +599,31 @@ static cudaError_t run_tc(const CUtensorMap& a, const CUtensorMap& a2, const CUt
 // three (measured 136 us against about 90 us at 128 on 896 x 15360 x 2880).
 // Above 128 rows the others take ceil(M / 256) tiles of 224 tokens when
 // they cover M (448 and 896 rows: no padded columns) and of 256 otherwise.
-int tc_pick_bn(int M, bool dual) {
+// `wide` (many more feature tiles than SMs, e.g. the LM head): above 256
+// rows, 448-token tiles where they pad no more than 256-token tiles do, so
+// each weight tile is streamed once per 448 tokens.
+int tc_pick_bn(int M, bool dual, bool wide) {
   if (M <= 16) return 16;
   if (M <= 32) return 32;
   if (M <= 64) return 64;
   if (M <= 128 || dual) return 128;
   const int tm = (M + 255) / 256;
+  if (wide && M > 256 && ((M + 447) / 448) * 448 <= tm * 256) return 448;
   return (M + tm - 1) / tm <= 224 ? 224 : 256;
 }
 
+// Whether an M x N projection takes the wide token tiles: at least four
+// feature tiles per SM (the weights dwarf the tokens), and no live-row count.
+bool tc_wide(int N, int sm_count, bool dual, bool live_rows) {
+  return !dual && !live_rows && (N + 127) / 128 >= 4 * sm_count;
+}
+
 // Rows of the token box in the x tensor map that launch_gemm_tc_maps
-// expects for an M x N projection: the token tile, or its slice when the
-// multicast kernel takes the projection (never with a live-row count).
+// expects for an M x N projection: the token tile, or half of it for the
+// wide tile (loaded as two boxes).
 int tc_b_box_rows(int M, int N, int sm_count, bool dual, bool live_rows) {
-  const int bn = tc_pick_bn(M, dual);
-  const long long tiles = static_cast<long long>((N + 127) / 128) * ((M + bn - 1) / bn);
-  return live_rows ? bn : bn / gemm_mc_cluster(bn, dual, tiles, sm_count);
+  const int bn = tc_pick_bn(M, dual, tc_wide(N, sm_count, dual, live_rows));
+  return bn > 256 ? bn / 2 : bn;
 }
 
 size_t tc_partial_floats(int grid, int bn, bool dual) {
@@ -617,7 +637,7 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
   if (M <= 0 || N <= 0) return cudaSuccess;
   if ((epi.m_live && epi.kind == EPI_ARGMAX) || (epi.row_map && !epi.out_f32))
     return cudaErrorInvalidValue;
-  const int bn = tc_pick_bn(M, dual);
+  const int bn = tc_pick_bn(M, dual, tc_wide(N, ws.sm_count, dual, epi.m_live != nullptr));
   TcParams p;
   p.M = M;
   p.N = N;
@@ -633,8 +653,6 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
   p.err = err;
   const int tiles = tiles_n * p.tiles_m;
   p.split_s = 0;
-  const int cs = epi.m_live ? 1 : gemm_mc_cluster(bn, dual, tiles, ws.sm_count);
-  if (cs > 1) return launch_gemm_mc(wa, wa2, xb, dual, bn, cs, p, s);
   if (tiles > ws.max_tiles) return cudaErrorInvalidValue;
 #define PE_TC_CASE(BNV)                                                                       \
   case BNV:                                                                                   \
@@ -649,6 +667,9 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
     PE_TC_CASE(128)
     PE_TC_CASE(224)
     PE_TC_CASE(256)
+    case 448:
+      if (dual) return cudaErrorInvalidValue;
+      return run_tc<448, false>(wa, wa2, xb, p, tiles, p.units, ws.sm_count, ws.partial_floats, s);
   }
 #undef PE_TC_CASE
   return cudaErrorInvalidValue;

@@ -15,6 +15,10 @@
 // device current and caches it; make that first call before any stream
 // capture.  All calls share the one array: calls that overlap on the GPU
 // (different streams, or different host threads on one device) race on it.
+//
+// A bounded wait inside the GEMM that gives up records PE_DEV_TIMEOUT in an
+// error word that also lives in the array; it stays set across calls until
+// pe_linear_static_error reads and clears it.
 #include <mutex>
 
 #include "pe_common.cuh"
@@ -32,13 +36,15 @@ int tc_b_box_rows(int M, int N, int sm_count, bool dual, bool live_rows);
 namespace {
 
 // Limits of the static workspace: at most 32 tokens (one 32-wide token
-// tile), at most 128 CTAs, at most kMaxTiles output tiles of 128 features.
+// tile), at most kMaxTiles output tiles of 128 features, and split-K
+// partials for one CTA per SM on GPUs of up to kMaxSms SMs (two CTAs per SM
+// at 16 tokens or fewer); a GPU with more SMs runs on kMaxSms of them.
 constexpr int kMaxTokens = 32;
-constexpr int kMaxCtas = 128;
+constexpr int kMaxSms = 160;
 constexpr int kMaxTiles = 4096;
-constexpr size_t kPartialFloats = static_cast<size_t>(kMaxCtas) * 2 * 128 * kMaxTokens;
+constexpr size_t kPartialFloats = static_cast<size_t>(kMaxSms) * 2 * 128 * kMaxTokens;
 constexpr size_t kScratchBytes =
-    kPartialFloats * sizeof(float) + (kMaxTiles + 64) * sizeof(int);  // ~4 MiB
+    kPartialFloats * sizeof(float) + (kMaxTiles + 64) * sizeof(int);  // ~5.3 MB
 
 // [partials: kPartialFloats floats][tile counters: kMaxTiles ints][error word]
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
@@ -94,10 +100,11 @@ extern "C" pe_status pe_linear_static(const void* x, const void* w, float* y, in
   float* partials = reinterpret_cast<float*>(slot->scratch);
   int* counters = reinterpret_cast<int*>(slot->scratch + kPartialFloats * sizeof(float));
   int* err = counters + kMaxTiles;
-  // the tile counters must start at zero; clear them (and the error word)
-  if (cudaMemsetAsync(counters, 0, (kMaxTiles + 1) * sizeof(int), s) != cudaSuccess)
+  // the tile counters must start at zero; the error word is left for
+  // pe_linear_static_error
+  if (cudaMemsetAsync(counters, 0, kMaxTiles * sizeof(int), s) != cudaSuccess)
     return PE_ERR_CUDA;
-  const int sms = slot->sm_count < kMaxCtas ? slot->sm_count : kMaxCtas;
+  const int sms = slot->sm_count < kMaxSms ? slot->sm_count : kMaxSms;
   CUtensorMap wa, xb;
   if (!tensor_map_2d_bf16(&wa, w, N, K, K, 64, 128) ||
       !tensor_map_2d_bf16(&xb, x, M, K, K, 64, tc_b_box_rows(M, N, sms, false, false)))
@@ -118,5 +125,23 @@ extern "C" pe_status pe_linear_static(const void* x, const void* w, float* y, in
   ep.out_f32 = 1;
   const cudaError_t e = launch_gemm_tc_maps(wa, wa, xb, false, M, N, K, ep, ws, err, s);
   if (e == cudaErrorInvalidValue) return PE_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+}
+
+// Read and clear the error word of the static array (0: no violation
+// recorded since the last read).  Copies on `stream` and waits for it, so
+// it also orders after every pe_linear_static call issued there.
+extern "C" pe_status pe_linear_static_error(int32_t* code, void* stream) {
+  if (!code) return PE_ERR_INVALID_ARGUMENT;
+  DeviceSlot* slot = nullptr;
+  if (device_setup(&slot) != cudaSuccess) return PE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* err = reinterpret_cast<int*>(slot->scratch + kPartialFloats * sizeof(float)) + kMaxTiles;
+  int v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, err, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(err, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  *code = v;
   return e == cudaSuccess ? PE_OK : PE_ERR_CUDA;
 }

@@ -97,6 +97,34 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   }
 }
 
+// ---------------------------------------------------------------------------
+// flags in global memory (a producer CTA publishes, others wait, bounded)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Spin until *flag >= target (acquire: the publisher's writes before its
+// release are visible afterwards).  Returns false (and records
+// PE_DEV_TIMEOUT) if that does not happen within kWaitTimeoutNs.
+__device__ __forceinline__ bool flag_wait_geq(const int* flag, int target, int* err) {
+  if (ld_acquire_gpu(flag) >= target) return true;
+  const unsigned long long t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (ld_acquire_gpu(flag) >= target) return true;
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      record_error(err, PE_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 
 // ---------------------------------------------------------------------------
 // TMA (tiled tensor copies global -> shared, completion on an mbarrier)
@@ -110,18 +138,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uin
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
       "l"(m), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
-      : "memory");
-}
-// The same box into the same shared-memory offset of every CTA in `mask`
-// (cluster multicast); each of them receives the bytes on its own mbarrier
-// at bar's offset.
-__device__ __forceinline__ void tma_load_2d_mcast(void* dst, const CUtensorMap* m, uint64_t* bar,
-                                                  int x, int y, uint16_t mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(
-          smem_u32(dst)),
-      "l"(m), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(mask), "l"(policy)
       : "memory");
 }
 // L2 eviction policies for the cache hints above.
@@ -173,15 +189,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
-      : "memory");
-}
-// One arrive on the mbarrier at bar's offset in every CTA of `mask` once
-// all earlier tcgen05 operations of this thread have completed.
-__device__ __forceinline__ void umma_commit_mcast(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
       : "memory");
 }
 // 32 lanes x 32 bits, 16 consecutive columns: thread i gets lane (base + i).

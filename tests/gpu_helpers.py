@@ -1,6 +1,9 @@
 """Helpers for the GPU parity tests: run one drafting step through the C ABI
 on seeded synthetic inputs and compare it with the CPU oracle."""
 
+import json
+import os
+
 import numpy as np
 
 import oracle as O
@@ -77,6 +80,31 @@ def margin_ok_tokens(ref_logits, ref_tokens, got_tokens, margin=1e-2):
     return int((gap <= margin).sum())
 
 
+def token_rule_stats(name, ref_logits, ref_tokens, got_tokens, loose_margin):
+    """How many draft tokens the spec rule (identical wherever the
+    oracle's top-2 margin exceeds 1e-2) pins, how many the rule this suite
+    applies end to end (margin above `loose_margin`) pins, and how many
+    tokens with 1e-2 < margin <= loose_margin disagree.  Printed, and
+    appended as a JSON line to $PE_TOKEN_STATS when that is set."""
+    srt = np.sort(ref_logits, axis=1)
+    gap = srt[:, -1] - srt[:, -2]
+    agree = np.asarray(got_tokens) == np.asarray(ref_tokens)
+    between = (gap > 1e-2) & (gap <= loose_margin)
+    st = {"workload": name, "tokens": int(len(gap)),
+          "pinned_at_1e-2": int((gap > 1e-2).sum()),
+          "pinned_at_loose": int((gap > loose_margin).sum()),
+          "loose_margin": float(loose_margin),
+          "disagree_between": int((between & ~agree).sum()),
+          "disagree_at_or_below_1e-2": int(((gap <= 1e-2) & ~agree).sum()),
+          "min_margin_of_a_disagreement": (float(gap[~agree].min()) if (~agree).any() else None)}
+    print("TOKEN-RULE", json.dumps(st))
+    path = os.environ.get("PE_TOKEN_STATS")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(st) + "\n")
+    return st
+
+
 def check_expand(res_ex, ref_ex, T):
     B = library()
     for f in ("ids", "pos", "slot", "new_idx", "cu_out", "seq_lens"):
@@ -127,8 +155,13 @@ def make_drafter(shape, weights, max_tokens, max_reqs):
     return B.Drafter(shape, weights, max_tokens, max_reqs)
 
 
-def full_parity(wl, tol, gains=None, requests=None, check_cache=True):
-    """Run one step on the GPU and the oracle; assert parity.  Returns both."""
+def full_parity(wl, tol, gains=None, requests=None, check_cache=True, strict_tokens=False):
+    """Run one step on the GPU and the oracle; assert parity.  Returns both.
+
+    strict_tokens: hold the end-to-end tokens to the spec rule itself
+    (identical wherever the fp64 oracle's top-2 margin exceeds 1e-2) instead
+    of twice the logit tolerance; used for the configurations where the
+    measured disagreement count in between is zero."""
     sh = wl.shape
     inp = W.make_step_inputs(wl)
     w = W.make_weights(sh, wl.config_id, gains=gains or wl.gains)
@@ -171,7 +204,9 @@ def full_parity(wl, tol, gains=None, requests=None, check_cache=True):
     # End to end the logits may differ from the fp64 statement by up to
     # tol x max|logit|, so a token is pinned wherever the oracle's top-2
     # margin is more than twice that (for fp32 the stated 1e-2 margin).
-    margin_ok_tokens(ref.logits, ref.tokens, got_t, margin=max(1e-2, 2 * tol * ls))
+    loose = max(1e-2, 2 * tol * ls)
+    token_rule_stats(wl.name, ref.logits, ref.tokens, got_t, loose)
+    margin_ok_tokens(ref.logits, ref.tokens, got_t, margin=1e-2 if strict_tokens else loose)
     # The argmax decision itself, taken in the same precision on both sides:
     # the oracle's LM head on the GPU's own final hidden rows.  Logits agree
     # to the GEMM's fp32 accumulation and tokens wherever the margin > 1e-3.
@@ -182,3 +217,29 @@ def full_parity(wl, tol, gains=None, requests=None, check_cache=True):
     if check_cache and requests is None:
         check_kv(st, ref, sh, tol * 2)
     return res, ref, dr, st
+
+
+def tokens_only_parity(wl, tol, requests=None):
+    """The benchmarked path: pe_lmhead_argmax with no logits buffer (the
+    argmax epilogue alone).  Its tokens must equal the oracle's LM head on
+    the GPU's own final hidden rows wherever that margin exceeds 1e-3, and
+    the fp64 oracle's end to end under the same rule as full_parity."""
+    sh = wl.shape
+    inp = W.make_step_inputs(wl)
+    w = W.make_weights(sh, wl.config_id, gains=wl.gains)
+    kc, vc = W.make_kv_cache(wl, inp)
+    dr = make_drafter(sh, w, max(wl.T_out, wl.B * wl.K), wl.B)
+    st = DeviceStep(wl, inp, kc, vc)
+    res = run_step(dr, st, want_logits=False)
+    assert res["err"] == 0, res["err"]
+    B = library()
+    ref = O.draft_step(sh, w, wl.K, inp, kc, vc, requests=requests)
+    rows = np.concatenate([np.arange(r * wl.K, (r + 1) * wl.K) for r in ref.requests])
+    got_t = B.to_host(res["tokens"])[rows]
+    hid = f64(B.to_host(res["out_hidden"]), sh.dtype)[rows]
+    lm_logits, lm_tokens = O.lm_head_argmax(sh, w, hid)
+    margin_ok_tokens(lm_logits, lm_tokens, got_t, margin=1e-3)
+    ls = np.abs(ref.logits).max()
+    margin_ok_tokens(ref.logits, ref.tokens, got_t, margin=max(1e-2, 2 * tol * ls))
+    dr.close()
+    return got_t, ref

@@ -4,7 +4,8 @@ y = x w^T with bf16 operands and fp32 accumulation (tcgen05, TMEM) against
 an fp64 product of the same bf16 values.  The shapes cover one tile, many
 tiles, ragged token/feature/k tails, every token-tile width (16..224, 256) and
 stream-K splits of a tile across CTAs (the deterministic fix-up path) and
-clusters that share one token tile by TMA multicast (many tiles per SM).
+the 448-token wide tile (two MMAs into one accumulator) that projections
+with many feature tiles per SM take above 256 rows.
 """
 
 import numpy as np
@@ -25,10 +26,13 @@ CASES = [
     (100, 640, 1024),   # token tile 128
     (300, 384, 256),    # token tile 256, two token tiles, ragged
     (896, 2880, 2880),  # batch-64 shape
-    # at least four tiles per SM with 128- or 256-token tiles: clusters of
-    # CTAs sharing the token tile by multicast; ragged tokens, features, k
-    (300, 40000, 200),   # two 224-token tiles, ragged
-    (500, 40000, 200),   # two 256-token tiles, ragged
+    # at least four feature tiles per SM: above 256 rows the wide 448-token
+    # tile where it pads no more than 256-token tiles; ragged tokens,
+    # features, k
+    (300, 80000, 200),   # one 448-token tile, ragged
+    (448, 80000, 2880),  # the batch-64 LM-head row count, long k
+    (896, 80000, 200),   # two 448-token tiles
+    (500, 80000, 200),   # two 256-token tiles (448 would pad more)
     (100, 80000, 256),
 ]
 

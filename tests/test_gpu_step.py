@@ -109,11 +109,22 @@ def test_gpt_oss_b64_full_size_sampled_requests():
     G.full_parity(wl, TOL_BF16, requests=_sample_requests(wl))
 
 
-@pytest.mark.parametrize("K", [1, 4, 8])
+@pytest.mark.parametrize("K", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_qwen_b16_full_size_sampled_requests(K):
-    """Qwen3-Coder-30B-shaped drafter (head_dim 128), batch 16, K sweep."""
+    """Qwen3-Coder-30B-shaped drafter (head_dim 128), batch 16, the K sweep
+    1..8 of the configuration (K = 1 is one autoregressive EAGLE step)."""
     wl = W.qwen_b16(K)
     G.full_parity(wl, TOL_BF16, requests=_sample_requests(wl, 2))
+
+
+@pytest.mark.parametrize("make_wl,sample", [(W.gpt_oss_b1, False), (W.gpt_oss_b64, True)],
+                         ids=["gpt-oss-b1", "gpt-oss-b64"])
+def test_benchmarked_path_without_logits(make_wl, sample):
+    """pe_lmhead_argmax with out_logits = NULL, the call the benchmark
+    times: tokens against the oracle's LM head on the GPU's own hidden rows
+    (margin 1e-3) and against the fp64 oracle end to end."""
+    wl = make_wl()
+    G.tokens_only_parity(wl, TOL_BF16, requests=_sample_requests(wl) if sample else None)
 
 
 @pytest.mark.parametrize("make_wl,repeats", [(W.gpt_oss_b1, 40), (W.gpt_oss_b64, 40)],

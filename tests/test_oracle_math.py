@@ -135,3 +135,30 @@ def test_linear_matches_explicit_loops_and_chunking():
 def test_bf16_decoding_known_values():
     bits = np.array([0x3F80, 0xC000, 0x0000, 0x3E80, 0x4049], np.uint16)
     assert O.to_f64(bits, "bf16").tolist() == [1.0, -2.0, 0.0, 0.25, 3.140625]
+
+
+def test_lm_head_argmax_ties_take_the_lowest_index():
+    """Reading R8: greedy argmax, lowest vocabulary index on exact ties.
+    Duplicated LM-head rows give bit-identical logits; a hidden row equal to
+    the duplicated row makes them the maximum (|w|^2 against cross terms of
+    a few percent of it), so the oracle must return the lower copy."""
+    from synthetic import workloads as W
+    V, d = 96, 32
+    sh = W.small_shape("tie", d=d, n_layers=1, n_heads=1, n_kv_heads=1, head_dim=32,
+                       ffn=32, vocab=V)
+    lm = W.normal(5, "tie-lm", (V, d), 0.02, "bf16")
+    pairs = [(9, 40), (0, V - 1), (70, 71), (3, 95 - 1)]
+    for lo, hi in pairs:
+        lm[lo] = lm[hi]
+    y = O.to_f64(np.stack([lm[hi] for _, hi in pairs]), "bf16")
+    logits, tokens = O.lm_head_argmax(sh, {"lm_head": lm}, y)
+    for r, (lo, hi) in enumerate(pairs):
+        assert logits[r, lo] == logits[r, hi]
+        others = np.delete(logits[r], [lo, hi])
+        assert logits[r, lo] > others.max()
+        assert tokens[r] == lo
+    # three-way tie: the first of the three
+    lm2 = lm.copy()
+    lm2[50] = lm2[20] = lm2[80]
+    _, t2 = O.lm_head_argmax(sh, {"lm_head": lm2}, O.to_f64(lm2[80][None], "bf16"))
+    assert t2[0] == 20

@@ -5,7 +5,9 @@ a static array inside the library, so it needs no handle.
 
 Checked through the C ABI against pe_linear (the handle-based entry point) on
 two calls in a row -- the second call reuses the array the first one left
-behind -- and for its refusal of sizes beyond the array.  This file is
+behind -- against an fp64 product of the same bf16 values, for its error
+word (read and cleared by pe_linear_static_error), and for its refusal of
+sizes beyond the array.  This file is
 collected last so that a run stopping at the first failure has run every
 other test already.
 """
@@ -13,6 +15,7 @@ other test already.
 import numpy as np
 import pytest
 
+import oracle as O
 from synthetic import workloads as W
 from tests import gpu_helpers as G
 
@@ -50,6 +53,27 @@ def test_static_entry_point_matches_pe_linear_twice(M, N, K):
         g = got.cpu().numpy().astype(np.float64)
         assert np.isfinite(g).all()
         assert np.abs(g - ref).max() <= tol
+    assert B.pe_linear_static_error() == 0
+
+
+def test_static_entry_point_matches_fp64_product():
+    """The static entry point against x . w^T in fp64 on the same bf16
+    values (not only against the handle-based call, which runs the same
+    kernel): the bf16 drafter tolerance of 2e-2 x max|y|."""
+    B = G.library()
+    torch = G.torch_mod()
+    M, N, K = 14, 5120, 2880
+    x = W.normal(11, "sx", (M, K), 1.0, "bf16", M, N)
+    w = W.normal(11, "sw", (N, K), 0.05, "bf16", M, N)
+    want = O.to_f64(x, "bf16") @ O.to_f64(w, "bf16").T
+    for _ in range(2):
+        got = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        B.pe_linear_static(B.to_device(x, "bf16"), B.to_device(w, "bf16"), got)
+        torch.cuda.synchronize()
+        g = got.cpu().numpy().astype(np.float64)
+        assert np.isfinite(g).all()
+        assert np.abs(g - want).max() <= 2e-2 * np.abs(want).max()
+    assert B.pe_linear_static_error() == 0
 
 
 def test_static_entry_point_refuses_sizes_beyond_its_array():
