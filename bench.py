@@ -14,8 +14,16 @@ drafts its own batch (requests are independent: weak scaling, no
 collective on the data path).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload b1|b16|b64|qwen-k<K>|expand|ar-<workload>|lmhead-<rows>|train-mask[-<tokens>]|train-partition]
+                  [--workload b1|b16|b64|qwen-k<K>|expand|tiny|ar-<workload>|lmhead-<rows>|train-mask[-<tokens>]|train-partition]
+                  [--no-configs]
                   (b1, b16, b64 take a "-fp8" suffix: e4m3 KV pools)
+
+The default run (b1) also times the other configurations in the same
+process and reports them under "configs": the batch-64 step, the Qwen-shaped
+K sweep 1..8 and the expansion microbenchmark, each with its step roofline
+and (for the steps) the split into attention and the rest from phase events.
+With --gpus N > 1 and no launcher, bench.py starts the N ranks itself (one
+process per GPU, 127.0.0.1 rendezvous).
 """
 
 from __future__ import annotations
@@ -50,6 +58,8 @@ FP8_KV_SCALE = 0.05
 def workload(name: str):
     if name.endswith("-fp8"):
         return workload(name[: -len("-fp8")])
+    if name == "tiny":
+        return W.tiny_fp32()
     if name == "b1":
         return W.gpt_oss_b1()
     if name == "b64":
@@ -215,6 +225,24 @@ def barrier(world):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+
+
+def spawn_ranks(n: int) -> int:
+    """Run this command as n ranks (one process per GPU, LOCAL_RANK = GPU
+    index) with a 127.0.0.1 rendezvous, as a launcher would; rank 0's output
+    is this process's output.  Returns the worst exit code."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    procs = []
+    for r in range(n):
+        env = dict(os.environ, RANK=str(r), LOCAL_RANK=str(r), WORLD_SIZE=str(n),
+                   LOCAL_WORLD_SIZE=str(n), MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        procs.append(subprocess.Popen([sys.executable, os.path.abspath(__file__)] + sys.argv[1:],
+                                      env=env))
+    codes = [p.wait() for p in procs]
+    return max(codes, key=abs)
 
 
 def aggregate_rate(world: int, steps_per_rank: int, elapsed_s: float) -> float:
@@ -545,6 +573,209 @@ def run_ar(args, world, rank, local):
     return 0
 
 
+def step_floor(work, hbm, tflops_sus):
+    """Sum over the projections and the attention of the slower of bytes /
+    measured HBM and flops / sustained bf16 peak (seconds)."""
+    return sum(max(b / (hbm * 1e9), f / (tflops_sus * 1e12)) for b, f in work["parts"])
+
+
+def step_roofline_of(work, step_s, hbm, tflops_sus):
+    floor = step_floor(work, hbm, tflops_sus)
+    return {"bytes": work["bytes"], "flops": work["flops"], "floor_us": floor * 1e6,
+            "frac": floor / step_s, "peak_source": "measured HBM copy and sustained bf16",
+            "hbm_frac": work["bytes"] / step_s / (hbm * 1e9),
+            "tensor_frac": work["flops"] / step_s / (tflops_sus * 1e12),
+            "tensor_peak": tflops_sus, "hbm_peak": hbm,
+            "frac_vs_nominal_7900_gbs": work["bytes"] / step_s / 7.9e12,
+            "gemm_flops": work["gemm_flops"], "attn_flops": work["attn_flops"]}
+
+
+class StepRig:
+    """One workload's step on the device: drafter, resident inputs, the
+    step captured as a CUDA graph."""
+
+    def __init__(self, wl, weights, torch, B, kc=None, vc=None, kv_seed=0, inp=None):
+        self.wl, self.torch, self.B = wl, torch, B
+        sh = wl.shape
+        self.inp = inp if inp is not None else W.make_step_inputs(wl)
+        self.dr = B.Drafter(sh, weights, max(wl.T_out, wl.B * wl.K), wl.B)
+        if kc is None:
+            kc, vc = W.device_kv_pools(sh, self.inp.num_blocks, kv_seed)
+        self.st = DeviceInputs(wl, self.inp, kc, vc, B, torch)
+        self.ex = B.Expanded(wl.T_out, wl.T, wl.B, wl.K, sh.hidden3, sh.dtype)
+        tdt = torch.bfloat16 if sh.dtype == "bf16" else torch.float32
+        self.out_hidden = torch.empty(wl.B * wl.K, sh.d, dtype=tdt, device="cuda")
+        self.tokens = torch.empty(wl.B * wl.K, dtype=torch.int32, device="cuda")
+        self.graph = None
+
+    def step(self):
+        B, wl, st, inp = self.B, self.wl, self.st, self.inp
+        B.pe_expand_batch(self.dr, wl.K, st.target_ids, st.target_pos, st.cu_in,
+                          st.num_accepted, st.sampled_ids, st.block_table, inp.num_blocks,
+                          st.target_hidden, self.ex)
+        B.pe_draft_forward(self.dr, self.ex, st.block_table, st.kc, st.vc, inp.num_blocks,
+                           self.out_hidden)
+        B.pe_lmhead_argmax(self.dr, self.out_hidden, self.tokens)
+
+    def capture(self):
+        """Eager warm-up, then the step as one CUDA graph; launches per step."""
+        torch, B = self.torch, self.B
+        for _ in range(2):
+            self.step()
+        torch.cuda.synchronize()
+        check_device(B, self.dr)
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        n0 = B.pe_get_launch_count(self.dr)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                self.step()
+        torch.cuda.synchronize()
+        self.graph = g
+        return B.pe_get_launch_count(self.dr) - n0
+
+    def time_ms(self, n, warmup=3):
+        torch = self.torch
+        for _ in range(warmup):
+            self.graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            self.graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        check_device(self.B, self.dr)
+        return e0.elapsed_time(e1) / n
+
+    def phase_split(self, n):
+        """Attention vs the rest of pe_draft_forward, from events recorded
+        between its kernels in a separately captured graph (the events break
+        the overlap of neighbouring kernels, so both parts read a little
+        slow).  Mean over n replays, microseconds."""
+        torch, B, L = self.torch, self.B, self.wl.shape.n_layers
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 + 2 * L)]
+        B.pe_set_phase_events(self.dr, ev)
+        try:
+            self.step()
+            torch.cuda.synchronize()
+            cap = torch.cuda.Stream()
+            cap.wait_stream(torch.cuda.current_stream())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(cap):
+                with torch.cuda.graph(g, stream=cap):
+                    self.step()
+            torch.cuda.synchronize()
+            attn = total = 0.0
+            for _ in range(n):
+                g.replay()
+                torch.cuda.synchronize()
+                attn += sum(ev[1 + 2 * l].elapsed_time(ev[2 + 2 * l]) for l in range(L))
+                total += ev[0].elapsed_time(ev[1 + 2 * L])
+        finally:
+            B.pe_set_phase_events(self.dr, None)
+        check_device(B, self.dr)
+        return {"attention_us": 1e3 * attn / n, "forward_us": 1e3 * total / n,
+                "rest_of_forward_us": 1e3 * (total - attn) / n}
+
+    def close(self):
+        self.dr.close()
+
+
+def measure_config(rig, n, hbm, tflops_sus, label):
+    """A configuration's line under "configs": throughput, its step roofline
+    and the attention / projection split."""
+    wl = rig.wl
+    launches = rig.capture()
+    ms = rig.time_ms(n)
+    work = step_work(wl, rig.inp)
+    ph = rig.phase_split(max(5, n // 10))
+    attn_s, rest_s = ph["attention_us"] * 1e-6, ph["rest_of_forward_us"] * 1e-6
+    lm_flops = work["lm_head_flops"]
+    proj_flops = work["gemm_flops"] - lm_flops
+    proj_bytes = work["weight_bytes"] - work["lm_head_bytes"]
+    ph.update({
+        "attention_hbm_frac": work["kv_bytes"] / attn_s / (hbm * 1e9) if attn_s > 0 else None,
+        "projections_tensor_frac": proj_flops / rest_s / (tflops_sus * 1e12) if rest_s > 0 else None,
+        "projections_hbm_frac": proj_bytes / rest_s / (hbm * 1e9) if rest_s > 0 else None,
+        "note": "rest_of_forward = fc, row kernels and the layer projections (the LM head "
+                "is outside pe_draft_forward); events between kernels cost their overlap"})
+    return {"workload": wl.name, "label": label, "B": wl.B, "K": wl.K,
+            "steps_per_s": 1e3 / ms, "ms_per_step": ms, "steps": n,
+            "drafted_tok_per_s": 1e3 / ms * wl.B * wl.K, "launches_per_step": launches,
+            "step_roofline": step_roofline_of(work, ms * 1e-3, hbm, tflops_sus),
+            "phase_split": ph,
+            "inputs": "seeded synthetic; KV pools and (Qwen) weights drawn on the device"}
+
+
+def expand_only(wl, torch, B, hbm, n):
+    """The expansion kernel alone (steps a1 + a2), L2 flushed before each
+    launch, on a drafter whose only live weight is h_shared."""
+    sh = wl.shape
+    z = np.zeros(64, np.uint16)
+    w = {k: z for k in ("emb", "fc", "norm_final", "lm_head")}
+    w["h_shared"] = W.normal(wl.config_id, "h_shared", (sh.hidden3,), 0.02, sh.dtype)
+    w["layers"] = [dict(qkv=z, o=z, gate=z, up=z, down=z, norm_e=z, norm_h=z, norm_in=z,
+                        norm_post=z) for _ in range(sh.n_layers)]
+    dr = B.Drafter(sh, w, wl.T_out, wl.B)
+    inp = W.make_step_inputs(wl)
+    st = DeviceInputs(wl, inp, [], [], B, torch)
+    ex = B.Expanded(wl.T_out, wl.T, wl.B, wl.K, sh.hidden3, sh.dtype)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    evs = []
+    for i in range(n + 3):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        B.pe_expand_batch(dr, wl.K, st.target_ids, st.target_pos, st.cu_in, st.num_accepted,
+                          st.sampled_ids, st.block_table, inp.num_blocks, st.target_hidden, ex)
+        b.record(stream)
+        if i >= 3:
+            evs.append((a, b))
+    torch.cuda.synchronize()
+    check_device(B, dr)
+    dr.close()
+    del flush
+    s_ = statistics.mean(a.elapsed_time(b) for a, b in evs) / 1e3
+    es = 2 if sh.dtype == "bf16" else 4
+    Bn, Tn, To = wl.B, wl.T, wl.T_out
+    # hidden rows read once (h_shared once) and written once; metadata in and out
+    nbytes = (Tn + 1) * sh.hidden3 * es + To * sh.hidden3 * es + \
+        Tn * 8 + Bn * 12 + To * 4 + To * 14 + Bn * wl.K * 4 + Tn * 4 + (2 * Bn + 1) * 4
+    return {"bound": "hbm", "workload": wl.name, "launch_us": s_ * 1e6,
+            "bytes_per_launch": nbytes, "achieved": nbytes / s_ / 1e9, "peak": hbm,
+            "unit": "GB/s", "frac": nbytes / s_ / 1e9 / hbm, "launches": n,
+            "note": "expansion kernel alone, L2 flushed before each launch"}
+
+
+def other_configs(args, torch, B, b1_weights, hbm, tflops_sus):
+    """The batch-64 step, the Qwen-shaped K sweep and the expansion
+    microbenchmark, timed in the same run as the headline."""
+    out = {}
+    wl = W.gpt_oss_b64()
+    rig = StepRig(wl, b1_weights, torch, B, kv_seed=64)
+    out["gpt-oss-b64-k7"] = measure_config(rig, 200, hbm, tflops_sus,
+                                           "GPT-OSS-20B-shaped, batch 64, K 7, lognormal contexts")
+    rig.close()
+    del rig
+    torch.cuda.empty_cache()
+    qw = W.device_weights(W.QWEN3_CODER_30B, seed=4)
+    sweep = {}
+    for K in range(1, 9):
+        rig = StepRig(W.qwen_b16(K), qw, torch, B, kv_seed=100 + K)
+        sweep[f"k{K}"] = measure_config(rig, 200, hbm, tflops_sus,
+                                        f"Qwen3-Coder-30B-shaped, batch 16, K {K}")
+        rig.close()
+        del rig
+    out["qwen-b16-k-sweep"] = sweep
+    del qw
+    torch.cuda.empty_cache()
+    out["expand-b256-k7"] = expand_only(W.expand_b256(), torch, B, hbm, 100)
+    return out
+
+
 def run_ours(args, world, rank, local):
     import torch
 
@@ -711,11 +942,16 @@ def run_ours(args, world, rank, local):
         cpu = {"value": sps, "unit": "steps/s", "cores": oracle_threads(), "kind": "oracle",
                "sample": f"{n} full oracle steps of the same workload in {dt:.1f} s"}
 
+    configs = None
+    if rank == 0 and world == 1 and not args.no_configs and args.workload == "b1":
+        dr.close()
+        del st
+        torch.cuda.empty_cache()
+        configs = other_configs(args, torch, B, w, hbm, tflops_sus)
+
     if rank == 0:
         # each projection and the attention at the slower of its bytes and
         # its flops (sustained tensor peak: they run inside a long step)
-        step_floor_s = sum(max(b / (hbm * 1e9), f / (tflops_sus * 1e12))
-                           for b, f in work["parts"])
         step_s = ms_per_step / 1e3
         line = {
             "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
@@ -724,19 +960,14 @@ def run_ours(args, world, rank, local):
             "dtype": sh.dtype, "data": "synthetic (seeded random-init weights and inputs)",
             "config": config_of(wl, args),
             "drafted_tok_per_s": value * wl.B * wl.K,
+            "step_roofline": step_roofline_of(work, step_s, hbm, tflops_sus),
             "roofline": dict(lm_roof, kernel="LM-head GEMM + fused argmax",
+                             scope="the dominant kernel alone; the whole step's fraction of "
+                                   "its HBM floor is step_roofline.frac",
                              traffic=traffic, bytes_per_launch=work["lm_head_bytes"],
                              flops_per_launch=work["lm_head_flops"],
                              launch_us=lm_avg_s * 1e6),
             "expand_roofline": expand_roof,
-            "step_roofline": {"bytes": work["bytes"], "flops": work["flops"],
-                              "floor_us": step_floor_s * 1e6,
-                              "frac": step_floor_s / step_s,
-                              "hbm_frac": work["bytes"] / step_s / (hbm * 1e9),
-                              "tensor_frac": work["flops"] / step_s / (tflops_sus * 1e12),
-                              "tensor_peak": tflops_sus, "hbm_peak": hbm,
-                              "gemm_flops": work["gemm_flops"],
-                              "attn_flops": work["attn_flops"]},
             "e2e": {"value": e2e_value, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
@@ -744,6 +975,8 @@ def run_ours(args, world, rank, local):
             "clocks": clocks.summary(),
             "cpu_baseline": cpu,
         }
+        if configs is not None:
+            line["configs"] = configs
         print(json.dumps(line), flush=True)
     dr.close()
     if world > 1:
@@ -760,9 +993,17 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="b1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time the headline workload only (not the batch-64 step, "
+                         "the Qwen K sweep and the expansion microbenchmark)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return spawn_ranks(args.gpus)
     world, rank, local = dist_setup()
+    if world != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+        return 2
     if args.impl == "reference":
         return run_reference(args, world, rank)
     if args.workload.startswith("ar-"):

@@ -258,6 +258,18 @@ pe_status pe_set_kv_cache_fp8(pe_handle* h, const float* k_scales, const float* 
  * off. */
 pe_status pe_set_trace(pe_handle* h, float* residual_trace, void* attn_trace);
 
+/* Phase timing (diagnostic; no counterpart on the pages).  events: n =
+ * 2 + 2 * n_layers caller-created CUDA events (cudaEvent_t, passed as
+ * void*), or n = 0 to turn it off.  While set, pe_draft_forward records
+ * event 0 when it starts, event 1 + 2l just before layer l's attention,
+ * event 2 + 2l just after it, and event 1 + 2 n_layers at its end, on its
+ * stream, so that the caller can split the step's time into attention and
+ * the rest.  Recording events between kernels breaks the overlap of
+ * consecutive kernels, so a timed step runs a little slower with them.
+ * The handle keeps the event handles, not the events: they must outlive
+ * their use. */
+pe_status pe_set_phase_events(pe_handle* h, void* const* events, int32_t n);
+
 /* y[M, N] = x[M, K] . w[N, K]^T with the library's GEMM for the model dtype
  * (tcgen05 tensor cores for bf16, FFMA for f32); y is fp32.  A diagnostic
  * entry point for checking the projection kernels in isolation; K % 64 == 0

@@ -32,7 +32,8 @@ PE_MASK_ADDITIVE_BF16 = 1
 # include/peagle.h and include/peagle_train.h (pe_status_string last: it is
 # the one that does not return a pe_status)
 EXPORTED = ("pe_create", "pe_destroy", "pe_expand_batch", "pe_draft_forward",
-            "pe_lmhead_argmax", "pe_get_device_error", "pe_set_trace", "pe_linear",
+            "pe_lmhead_argmax", "pe_get_device_error", "pe_set_trace", "pe_set_phase_events",
+            "pe_linear",
             "pe_get_launch_count", "pe_check_bounded_wait", "pe_linear_static",
             "pe_linear_static_error",
             "pe_set_kv_cache_fp8",
@@ -91,6 +92,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pe_get_launch_count.argtypes = [_vp, P(ctypes.c_int64)]
     lib.pe_linear_static.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _vp]
     lib.pe_check_bounded_wait.argtypes = [_vp, _vp, _vp]
+    lib.pe_set_phase_events.argtypes = [_vp, P(_vp), _i32]
     lib.pe_linear_static_error.argtypes = [P(_i32), _vp]
     lib.pe_set_kv_cache_fp8.argtypes = [_vp, P(ctypes.c_float), P(ctypes.c_float)]
     lib.pe_train_build_mask.argtypes = [_i32, _i32, _i32, _vp, ctypes.c_int64, _vp]
@@ -144,8 +146,11 @@ def stream_ptr(stream=None) -> int:
 
 
 def to_device(a: np.ndarray, dtype: str, device="cuda"):
-    """Host array (bf16 bits as uint16, or float32 / int32 / uint8) -> tensor."""
+    """Host array (bf16 bits as uint16, or float32 / int32 / uint8) -> tensor
+    (a tensor is moved as it is)."""
     torch = _torch()
+    if isinstance(a, torch.Tensor):
+        return a.to(device)
     if dtype == "bf16" and a.dtype == np.uint16:
         t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
     else:
@@ -277,6 +282,18 @@ def pe_check_bounded_wait(dr: Drafter, out, stream=None) -> None:
     """Launch the bounded-wait self-check (out: device int32[2])."""
     _check("pe_check_bounded_wait", lib().pe_check_bounded_wait(dr.handle, ptr(out),
                                                                 stream_ptr(stream)))
+
+
+def pe_set_phase_events(dr: Drafter, events=None) -> None:
+    """events: torch.cuda.Event objects (2 + 2 n_layers, timing enabled), or
+    None to turn phase timing off."""
+    events = list(events or [])
+    for e in events:
+        if e.cuda_event == 0:      # torch creates the event on first record
+            e.record()
+    arr = (_vp * max(1, len(events)))(*[e.cuda_event for e in events])
+    dr._phase_events = events      # the library keeps the handles
+    _check("pe_set_phase_events", lib().pe_set_phase_events(dr.handle, arr, len(events)))
 
 
 def pe_set_trace(dr: Drafter, residual_trace=None, attn_trace=None) -> None:

@@ -15,8 +15,7 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
                                 const CUtensorMap& xb, bool dual, int M, int N, int K,
                                 const EpiArgs& epi, const TcGemmWorkspace& ws, int* err,
                                 cudaStream_t s);
-int tc_pick_bn(int M, bool dual, bool wide);
-bool tc_wide(int N, int sm_count, bool dual, bool live_rows);
+int tc_pick_bn(int M, bool dual);
 int tc_b_box_rows(int M, int N, int sm_count, bool dual, bool live_rows);
 cudaError_t init_gemm_tc();
 size_t tc_partial_floats(int grid, int bn, bool dual);
@@ -78,6 +77,7 @@ struct pe_handle {
   std::vector<float> k_scales, v_scales;
   float* trace = nullptr;
   void* attn_trace = nullptr;
+  std::vector<cudaEvent_t> phase_events;  // 2 + 2 L events, or none
   long long launches = 0;
 
   std::map<std::tuple<const void*, uint64_t, uint64_t, uint64_t, uint32_t>, CUtensorMap> maps;
@@ -261,7 +261,7 @@ pe_status pe_create(const pe_model_desc* desc, const pe_weights* weights, int32_
   if (e == cudaSuccess && d.dtype == PE_DTYPE_BF16) e = init_attention_tc();
   if (e == cudaSuccess && d.dtype == PE_DTYPE_BF16) {
     // the widest token tile any row count up to max_tokens can take
-    const int bn = max_tokens > 128 ? 256 : tc_pick_bn(max_tokens, false, false);
+    const int bn = max_tokens > 128 ? 256 : tc_pick_bn(max_tokens, false);
     // stream-K runs two CTAs an SM for token tiles up to 32 wide
     h->gemm_partial_floats = tc_partial_floats((bn <= 32 ? 2 : 1) * h->sm_count, bn, true);
     e = dev_alloc(h, &h->gemm_partials, h->gemm_partial_floats);
@@ -299,6 +299,17 @@ pe_status pe_set_kv_cache_fp8(pe_handle* h, const float* k_scales, const float* 
   h->k_scales = ks;
   h->v_scales = vs;
   h->kv_fp8 = true;
+  return PE_OK;
+}
+
+pe_status pe_set_phase_events(pe_handle* h, void* const* events, int32_t n) {
+  if (!h || n < 0 || (n > 0 && !events)) return PE_ERR_INVALID_ARGUMENT;
+  if (n != 0 && n != 2 + 2 * h->desc.n_layers) return PE_ERR_INVALID_ARGUMENT;
+  h->phase_events.clear();
+  for (int i = 0; i < n; ++i) {
+    if (!events[i]) return PE_ERR_INVALID_ARGUMENT;
+    h->phase_events.push_back(static_cast<cudaEvent_t>(events[i]));
+  }
   return PE_OK;
 }
 
@@ -438,7 +449,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
   // rejected rows, and when even B*K live rows (every request accepting
   // nothing) fill as many tiles as the expanded batch, nothing shrinks.
   auto tiles_of = [&](int m, bool dual) {
-    const int bn = d.dtype == PE_DTYPE_BF16 ? tc_pick_bn(rows, dual, false) : 16;
+    const int bn = d.dtype == PE_DTYPE_BF16 ? tc_pick_bn(rows, dual) : 16;
     return (m + bn - 1) / bn;
   };
   const bool compact = ex->T > B && (tiles_of(B * K, false) < tiles_of(rows, false) ||
@@ -479,6 +490,12 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     new_l = h->new_c;
     rej_l = nullptr;
   }
+  // phase timing (diagnostic): event 0 here, 1 + 2 l before layer l's
+  // attention, 2 + 2 l after it, 1 + 2 L at the end
+  auto mark = [&](int i) -> cudaError_t {
+    return h->phase_events.empty() ? cudaSuccess : cudaEventRecord(h->phase_events[i], s);
+  };
+  if ((e = mark(0))) return PE_ERR_CUDA;
   // debug copies of per-row activations, in the expanded row order (zero
   // for rejected rows)
   auto trace_rows = [&](void* dst, const void* src, size_t row_bytes) -> cudaError_t {
@@ -569,6 +586,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     }
     if ((e = counted(h, launch_rope_kv(dt, rk, s)))) return PE_ERR_CUDA;
     // paged causal attention
+    if ((e = mark(1 + 2 * l))) return PE_ERR_CUDA;
     AttnArgs at = {};
     at.rows = rows;
     at.B = B;
@@ -607,6 +625,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
                                          h->attn_counters, h->attn_n_counters, s));
       if (e) return PE_ERR_CUDA;
     }
+    if ((e = mark(2 + 2 * l))) return PE_ERR_CUDA;
     if (h->attn_trace) {
       const size_t per = static_cast<size_t>(qd) * h->esize;
       if ((e = trace_rows(static_cast<char*>(h->attn_trace) + l * h->max_tokens * per, h->attn,
@@ -670,6 +689,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
   rn.y = out_hidden;
   rn.err = h->err;
   if ((e = counted(h, launch_rmsnorm(dt, rn, s)))) return PE_ERR_CUDA;
+  if ((e = mark(1 + 2 * d.n_layers))) return PE_ERR_CUDA;
   return PE_OK;
 }
 
@@ -700,7 +720,7 @@ pe_status pe_linear(pe_handle* h, const void* x, const void* w, float* y, int32_
   if (h->desc.dtype == PE_DTYPE_BF16 && (K % 8 || !aligned16(x) || !aligned16(w)))
     return PE_ERR_INVALID_ARGUMENT;
   if (h->desc.dtype == PE_DTYPE_BF16) {
-    const int bn = tc_pick_bn(M, false, tc_wide(N, h->sm_count, false, false));
+    const int bn = tc_pick_bn(M, false);
     const long long tiles = static_cast<long long>((N + 127) / 128) * ((M + bn - 1) / bn);
     if (tiles > h->max_tiles) return PE_ERR_INVALID_ARGUMENT;
   }

@@ -151,10 +151,8 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
         const long long u = lo + i;
         const int tile = static_cast<int>(u / kb), kk = static_cast<int>(u % kb);
         const int m = tile % tiles_m;
-#pragma unroll
-        for (int h = 0; h < C::NMMA; ++h)
-          tma_load_2d(smem + i * C::STAGE_BYTES + C::NA * C::A_BYTES + h * C::B_HALF_BYTES, &tmB,
-                      &full[i], kk * 64, m * BN + h * C::MMA_N, pol_b);
+        tma_load_2d(smem + i * C::STAGE_BYTES + C::NA * C::A_BYTES, &tmB, &full[i], kk * 64,
+                    m * BN, pol_b);
       }
       long long issued = npre;
       for (long long i = npre; i < n; ++i) {
@@ -168,10 +166,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
         mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
         tma_load_2d(st, &tmA, &full[stage], kk * 64, f * 128, pol_a);
         if (DUAL) tma_load_2d(st + C::A_BYTES, &tmA2, &full[stage], kk * 64, f * 128, pol_a);
-#pragma unroll
-        for (int h = 0; h < C::NMMA; ++h)
-          tma_load_2d(st + C::NA * C::A_BYTES + h * C::B_HALF_BYTES, &tmB, &full[stage], kk * 64,
-                      m * BN + h * C::MMA_N, pol_b);
+        tma_load_2d(st + C::NA * C::A_BYTES, &tmB, &full[stage], kk * 64, m * BN, pol_b);
         issued = i + 1;
       }
       // drain: every copy this thread issued has landed before the CTA exits
@@ -205,17 +200,12 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
           const uint32_t b_addr = a_addr + C::NA * C::A_BYTES;
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
+            const uint64_t bdesc = sw128_kmajor_desc(b_addr + k4 * 32);
             const uint32_t accum = (kk > k_lo || k4 > 0) ? 1u : 0u;
-            const uint64_t adesc = sw128_kmajor_desc(a_addr + k4 * 32);
-#pragma unroll
-            for (int h = 0; h < C::NMMA; ++h) {
-              // token half h of a wide tile: its own rows of B, its own columns
-              const uint64_t bdesc = sw128_kmajor_desc(b_addr + h * C::B_HALF_BYTES + k4 * 32);
-              umma_bf16(d + h * C::MMA_N, adesc, bdesc, C::IDESC, accum);
-              if (DUAL)
-                umma_bf16(d + BN, sw128_kmajor_desc(a_addr + C::A_BYTES + k4 * 32), bdesc,
-                          C::IDESC, accum);
-            }
+            umma_bf16(d, sw128_kmajor_desc(a_addr + k4 * 32), bdesc, C::IDESC, accum);
+            if (DUAL)
+              umma_bf16(d + BN, sw128_kmajor_desc(a_addr + C::A_BYTES + k4 * 32), bdesc,
+                        C::IDESC, accum);
           }
           umma_commit(&empty[stage]);
         }
@@ -506,8 +496,7 @@ static cudaError_t set_smem_attr() {
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-  // the wide tile's accumulator does not fit its stages: never cluster-split
-  for (int S = 2; S <= 8 && e == cudaSuccess && BN <= 256; ++S) {
+  for (int S = 2; S <= 8 && e == cudaSuccess; ++S) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S * 32);
     cfg.blockDim = dim3(192);
@@ -540,7 +529,6 @@ cudaError_t init_gemm_tc() {
   PE_TC_ATTR(224)
   PE_TC_ATTR(256)
 #undef PE_TC_ATTR
-  if (e == cudaSuccess) e = set_smem_attr<448, false>();
   return e;
 }
 
@@ -599,31 +587,28 @@ static cudaError_t run_tc(const CUtensorMap& a, const CUtensorMap& a2, const CUt
 // three (measured 136 us against about 90 us at 128 on 896 x 15360 x 2880).
 // Above 128 rows the others take ceil(M / 256) tiles of 224 tokens when
 // they cover M (448 and 896 rows: no padded columns) and of 256 otherwise.
-// `wide` (many more feature tiles than SMs, e.g. the LM head): above 256
-// rows, 448-token tiles where they pad no more than 256-token tiles do, so
-// each weight tile is streamed once per 448 tokens.
-int tc_pick_bn(int M, bool dual, bool wide) {
+//
+// (A 448-token tile -- two 224-token MMAs into one 448-column accumulator,
+// so that the LM head at 448 rows streams each weight tile once -- measured
+// slower: 495 us against about 445 us on 448 x 201088 x 2880.  One
+// accumulator leaves the tensor cores idle during the argmax epilogue of
+// every tile, and that kernel is bound by the tensor pipe, not by memory.)
+int tc_pick_bn(int M, bool dual) {
   if (M <= 16) return 16;
   if (M <= 32) return 32;
   if (M <= 64) return 64;
   if (M <= 128 || dual) return 128;
   const int tm = (M + 255) / 256;
-  if (wide && M > 256 && ((M + 447) / 448) * 448 <= tm * 256) return 448;
   return (M + tm - 1) / tm <= 224 ? 224 : 256;
 }
 
-// Whether an M x N projection takes the wide token tiles: at least four
-// feature tiles per SM (the weights dwarf the tokens), and no live-row count.
-bool tc_wide(int N, int sm_count, bool dual, bool live_rows) {
-  return !dual && !live_rows && (N + 127) / 128 >= 4 * sm_count;
-}
-
 // Rows of the token box in the x tensor map that launch_gemm_tc_maps
-// expects for an M x N projection: the token tile, or half of it for the
-// wide tile (loaded as two boxes).
+// expects for an M x N projection: the token tile.
 int tc_b_box_rows(int M, int N, int sm_count, bool dual, bool live_rows) {
-  const int bn = tc_pick_bn(M, dual, tc_wide(N, sm_count, dual, live_rows));
-  return bn > 256 ? bn / 2 : bn;
+  (void)N;
+  (void)sm_count;
+  (void)live_rows;
+  return tc_pick_bn(M, dual);
 }
 
 size_t tc_partial_floats(int grid, int bn, bool dual) {
@@ -637,7 +622,7 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
   if (M <= 0 || N <= 0) return cudaSuccess;
   if ((epi.m_live && epi.kind == EPI_ARGMAX) || (epi.row_map && !epi.out_f32))
     return cudaErrorInvalidValue;
-  const int bn = tc_pick_bn(M, dual, tc_wide(N, ws.sm_count, dual, epi.m_live != nullptr));
+  const int bn = tc_pick_bn(M, dual);
   TcParams p;
   p.M = M;
   p.N = N;
@@ -667,9 +652,6 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
     PE_TC_CASE(128)
     PE_TC_CASE(224)
     PE_TC_CASE(256)
-    case 448:
-      if (dual) return cudaErrorInvalidValue;
-      return run_tc<448, false>(wa, wa2, xb, p, tiles, p.units, ws.sm_count, ws.partial_floats, s);
   }
 #undef PE_TC_CASE
   return cudaErrorInvalidValue;

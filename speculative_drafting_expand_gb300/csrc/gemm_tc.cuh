@@ -8,18 +8,11 @@
 
 namespace pe {
 
-// BN tokens per tile.  Up to 256 one MMA covers the tile; the 448-token
-// tile (LM head at a few hundred rows) is two MMAs of 224 tokens into one
-// 448-column accumulator, so each weight tile is read from memory once for
-// all of them instead of once per 224-token tile.
 template <int BN, bool DUAL>
 struct TcCfg {
   static constexpr int BM = 128, BK = 64;
-  static constexpr int NMMA = BN > 256 ? 2 : 1;
-  static constexpr int MMA_N = BN / NMMA;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int B_HALF_BYTES = MMA_N * BK * 2;
   static constexpr int NA = DUAL ? 2 : 1;
   static constexpr int STAGE_BYTES = A_BYTES * NA + B_BYTES;
   static constexpr int ACC_COLS = BN * NA;
@@ -33,15 +26,13 @@ struct TcCfg {
   // Narrow token tiles (a few rows, weight streaming) keep the CTA near
   // 100 KB of shared memory so that the next projection's CTA fits on the
   // same SM and prefetches its weights while this one drains.
-  static constexpr int SMEM_BUDGET = BN <= 32 ? 104 * 1024 : BN > 256 ? 220 * 1024 : 200 * 1024;
+  static constexpr int SMEM_BUDGET = BN <= 32 ? 104 * 1024 : 200 * 1024;
   static constexpr int STAGES_RAW = SMEM_BUDGET / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
-  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, MMA_N);
-  static_assert(MMA_N % 16 == 0 && MMA_N >= 16 && MMA_N <= 256, "MMA N");
-  static_assert(B_HALF_BYTES % 1024 == 0 || NMMA == 1, "swizzle atoms of the second half");
-  static_assert(ACC_COLS <= 512 && STAGES >= 2, "tile too large");
+  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
   static_assert(2 * STAGES + 5 <= BAR_BYTES / 8, "barrier space");
 };
 

@@ -369,3 +369,50 @@ def custom(name: str, config_id: int, shape: DrafterShape, K: int,
     return StepWorkload(name, config_id, shape, K, np.asarray(contexts),
                         np.asarray(window), np.asarray(accepted),
                         block_order, gains)
+
+
+# --------------------------------------------------------------------------
+# device-side draws for timing-only runs (no oracle comparison): the same
+# distributions, seeded, generated on the GPU so that large pools cost no
+# host time.  torch is imported lazily (the CPU tests never call these).
+# --------------------------------------------------------------------------
+
+def device_weights(shape: DrafterShape, seed: int, std: float = 0.02, device="cuda"):
+    """Random-init drafter weights as device tensors (bf16), unit norm gains;
+    the same keys and layouts as make_weights."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    dt = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
+    d, F, V = shape.d, shape.ffn, shape.vocab
+    qd = shape.n_heads * shape.head_dim
+
+    def mat(*s):
+        return (torch.randn(*s, generator=g, device=device) * std).to(dt)
+
+    ones = lambda: torch.ones(d, dtype=dt, device=device)
+    w = {"emb": mat(V, d), "fc": mat(d, shape.hidden3), "h_shared": mat(shape.hidden3),
+         "norm_final": ones(), "lm_head": mat(V, d)}
+    layers = []
+    for l in range(shape.n_layers):
+        lw = {"qkv": mat(shape.qkv_rows, 2 * d if l == 0 else d), "o": mat(d, qd),
+              "gate": mat(F, d), "up": mat(F, d), "down": mat(d, F), "norm_post": ones()}
+        if l == 0:
+            lw["norm_e"], lw["norm_h"] = ones(), ones()
+        else:
+            lw["norm_in"] = ones()
+        layers.append(lw)
+    w["layers"] = layers
+    return w
+
+
+def device_kv_pools(shape: DrafterShape, num_blocks: int, seed: int, device="cuda"):
+    """Paged KV pools [num_blocks, Hkv, page, head_dim] per layer, N(0,1)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    dt = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
+    shp = (num_blocks, shape.n_kv_heads, shape.page_size, shape.head_dim)
+    ks = [torch.randn(*shp, generator=g, device=device).to(dt) for _ in range(shape.n_layers)]
+    vs = [torch.randn(*shp, generator=g, device=device).to(dt) for _ in range(shape.n_layers)]
+    return ks, vs

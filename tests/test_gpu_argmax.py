@@ -6,8 +6,8 @@ logit bit for bit (k = 64: one k-block, so every output tile is one
 accumulation with the same order); a hidden row equal to the duplicated row
 makes the pair the maximum.  The lower index must win whether the two rows
 sit in one warp, in different tiles and CTAs, or at the two ends of the
-vocabulary; with logits written and without (the benchmarked path), on the
-narrow token tile and on the 448-token wide tile of the batch-64 LM head.
+vocabulary; with logits written and without (the benchmarked path), on
+narrow token tiles and on the 224-token tiles of the batch-64 LM head.
 """
 
 import numpy as np
@@ -32,7 +32,7 @@ def _lm_drafter(V, d, lm, max_tokens):
 
 
 @pytest.mark.parametrize("V,M", [(4096, 7), (4096, 30), (80000, 300), (80000, 448)],
-                         ids=["narrow-7", "narrow-30", "wide-300", "wide-448"])
+                         ids=["rows-7", "rows-30", "rows-300", "rows-448"])
 @pytest.mark.parametrize("with_logits", [True, False], ids=["logits", "tokens-only"])
 def test_exact_ties_return_the_lowest_index(V, M, with_logits):
     B = G.library()

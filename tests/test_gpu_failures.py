@@ -99,8 +99,12 @@ def test_token_id_out_of_range_is_reported():
 
 
 def test_window_longer_than_k_plus_one_is_reported():
-    K = 3
-    wl = W.custom("bad-row", 304, SMALL, K, [50], [K + 3], [K + 2])
+    """The attention plans its query tiles for at most K + 1 window rows per
+    request (reading R11); with 4 query heads per KV head a tile holds 32
+    rows, so at K = 16 request 0's 19 window rows + 15 MASK rows overflow the
+    one tile planned for 32 and are reported (not read past)."""
+    K = 16
+    wl = W.custom("bad-row", 304, SMALL, K, [50, 30], [K + 3, 1], [K + 2, 0])
     code, slots, before, after = _step(wl, lambda inp: None)
     assert code == BAD_ROW
     _only_live_slots_written(slots, before, after, 16)

@@ -3,9 +3,9 @@
 y = x w^T with bf16 operands and fp32 accumulation (tcgen05, TMEM) against
 an fp64 product of the same bf16 values.  The shapes cover one tile, many
 tiles, ragged token/feature/k tails, every token-tile width (16..224, 256) and
-stream-K splits of a tile across CTAs (the deterministic fix-up path) and
-the 448-token wide tile (two MMAs into one accumulator) that projections
-with many feature tiles per SM take above 256 rows.
+stream-K splits of a tile across CTAs (the deterministic fix-up path),
+including projections with many feature tiles per SM at a few hundred rows
+(the LM head at batch 64).
 """
 
 import numpy as np
@@ -26,13 +26,10 @@ CASES = [
     (100, 640, 1024),   # token tile 128
     (300, 384, 256),    # token tile 256, two token tiles, ragged
     (896, 2880, 2880),  # batch-64 shape
-    # at least four feature tiles per SM: above 256 rows the wide 448-token
-    # tile where it pads no more than 256-token tiles; ragged tokens,
-    # features, k
-    (300, 80000, 200),   # one 448-token tile, ragged
+    # at least four feature tiles per SM; ragged tokens, features, k
+    (300, 80000, 200),   # two 224-token tiles, ragged
     (448, 80000, 2880),  # the batch-64 LM-head row count, long k
-    (896, 80000, 200),   # two 448-token tiles
-    (500, 80000, 200),   # two 256-token tiles (448 would pad more)
+    (500, 80000, 200),   # two 256-token tiles, ragged
     (100, 80000, 256),
 ]
 

@@ -67,3 +67,37 @@ def test_single_rank_needs_no_process_group():
     assert bench.max_over_ranks(1, 12.5) == 12.5
     bench.barrier(1)
     assert bench.aggregate_rate(1, 100, 0.5) == 200.0
+
+
+def test_gpus_flag_starts_the_ranks_itself():
+    """`bench.py --gpus 2` without a launcher spawns two ranks (127.0.0.1
+    rendezvous); on the reference arm rank 0 alone runs the oracle and
+    prints one line whose n_gpus is the real world size, rank 1 exits 0."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    env["PE_REF_BUDGET_S"] = "5"
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2",
+                        "--impl", "reference", "--workload", "tiny", "--steps", "1",
+                        "--warmup", "3"], capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
+    assert d["config"]["parallelism"] == "replicas x2"
+
+
+def test_gpus_flag_must_match_the_launcher_world_size():
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2",
+                        "--impl", "reference", "--workload", "tiny", "--steps", "1"],
+                       capture_output=True, text=True, env=env, timeout=120)
+    assert r.returncode == 2
+    assert "WORLD_SIZE=1" in r.stderr
