@@ -270,6 +270,16 @@ pe_status pe_set_trace(pe_handle* h, float* residual_trace, void* attn_trace);
  * their use. */
 pe_status pe_set_phase_events(pe_handle* h, void* const* events, int32_t n);
 
+/* Small-batch streaming (on by default).  When a step's expanded rows fit
+ * one 16- or 32-row token tile, pe_draft_forward runs the projections
+ * between two attention launches (fc, the layer-0 input and QKV; then O,
+ * gate/up, down and the next QKV or the final norm) as one persistent
+ * kernel per segment, with RMSNorm, RoPE and the KV write fused into it,
+ * instead of one launch per projection.  enable = 0 selects the
+ * per-projection path for every batch (the same results up to fp32
+ * summation order); used to compare the two. */
+pe_status pe_set_small_batch_stream(pe_handle* h, int32_t enable);
+
 /* y[M, N] = x[M, K] . w[N, K]^T with the library's GEMM for the model dtype
  * (tcgen05 tensor cores for bf16, FFMA for f32); y is fp32.  A diagnostic
  * entry point for checking the projection kernels in isolation; K % 64 == 0

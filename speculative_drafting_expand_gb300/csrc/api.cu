@@ -31,6 +31,12 @@ cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const
 cudaError_t launch_bounded_wait_check(int* flag, int32_t* out, int* err, cudaStream_t s);
 }  // namespace pe
 
+namespace {
+// streaming-segment workspace: tile counters and sums of squares per phase
+constexpr int kStreamCounterStride = 1024;  // tiles of one phase, at most
+constexpr int kStreamSsqTiles = 256;        // residual tiles of 128 features, at most
+}  // namespace
+
 using namespace pe;
 
 struct pe_handle {
@@ -78,6 +84,13 @@ struct pe_handle {
   float* trace = nullptr;
   void* attn_trace = nullptr;
   std::vector<cudaEvent_t> phase_events;  // 2 + 2 L events, or none
+  // small batches: projections between attention launches as one
+  // persistent kernel per segment (stream.cu)
+  bool stream_on = true;
+  float* stream_ws = nullptr;
+  int* stream_sync = nullptr;
+  int* stream_counters = nullptr;
+  float* stream_ssq = nullptr;
   long long launches = 0;
 
   std::map<std::tuple<const void*, uint64_t, uint64_t, uint64_t, uint32_t>, CUtensorMap> maps;
@@ -259,6 +272,15 @@ pe_status pe_create(const pe_model_desc* desc, const pe_weights* weights, int32_
   }
   if (e == cudaSuccess && d.dtype == PE_DTYPE_BF16) e = init_gemm_tc();
   if (e == cudaSuccess && d.dtype == PE_DTYPE_BF16) e = init_attention_tc();
+  if (e == cudaSuccess && d.dtype == PE_DTYPE_BF16) e = init_stream();
+  if (e == cudaSuccess && d.dtype == PE_DTYPE_BF16) {
+    e = dev_alloc(h, &h->stream_ws, stream_ws_floats(h->sm_count));
+    if (e == cudaSuccess) e = dev_alloc(h, &h->stream_sync, kStreamSyncInts);
+    if (e == cudaSuccess)
+      e = dev_alloc(h, &h->stream_counters, kStreamMaxPhases * kStreamCounterStride);
+    if (e == cudaSuccess)
+      e = dev_alloc(h, &h->stream_ssq, static_cast<size_t>(kStreamMaxPhases) * kStreamSsqTiles * 32);
+  }
   if (e == cudaSuccess && d.dtype == PE_DTYPE_BF16) {
     // the widest token tile any row count up to max_tokens can take
     const int bn = max_tokens > 128 ? 256 : tc_pick_bn(max_tokens, false);
@@ -299,6 +321,12 @@ pe_status pe_set_kv_cache_fp8(pe_handle* h, const float* k_scales, const float* 
   h->k_scales = ks;
   h->v_scales = vs;
   h->kv_fp8 = true;
+  return PE_OK;
+}
+
+pe_status pe_set_small_batch_stream(pe_handle* h, int32_t enable) {
+  if (!h) return PE_ERR_INVALID_ARGUMENT;
+  h->stream_on = enable != 0;
   return PE_OK;
 }
 
@@ -507,6 +535,205 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     return r;
   };
 
+  // paged causal attention of layer l (with the phase marks and the
+  // attention trace around it)
+  auto attention = [&](int l) -> pe_status {
+    cudaError_t e;
+    if ((e = mark(1 + 2 * l))) return PE_ERR_CUDA;
+    AttnArgs at = {};
+    at.rows = rows;
+    at.B = B;
+    at.Hq = d.n_heads;
+    at.Hkv = d.n_kv_heads;
+    at.dh = d.head_dim;
+    at.bt_stride = bt_stride;
+    at.num_blocks = num_blocks;
+    at.max_seq = bt_stride * d.page_size;
+    at.q = h->q;
+    at.k_cache = k_cache[l];
+    at.v_cache = v_cache[l];
+    at.live = live;
+    at.pos = pos_l;
+    at.is_rejected = rej_l;
+    at.cu_out = cu_l;
+    at.block_table = block_table;
+    at.out = h->attn;
+    at.scale = 1.0f / std::sqrt(static_cast<float>(d.head_dim));
+    at.err = h->err;
+    if (dt == PE_DTYPE_F32) {
+      if ((e = counted(h, launch_attention_simt(dt, at, s)))) return PE_ERR_CUDA;
+    } else {
+      if (h->kv_fp8) {
+        at.kv_fp8 = 1;
+        at.k_scale = h->k_scales[l];
+        at.v_scale = h->v_scales[l];
+      }
+      const CUtensorMap* tk = h->kv_fp8 ? get_map_u8(h, k_cache[l], cache_rows)
+                                        : get_map(h, k_cache[l], cache_rows, d.head_dim, d.head_dim, 16);
+      const CUtensorMap* tv = h->kv_fp8 ? get_map_u8(h, v_cache[l], cache_rows)
+                                        : get_map(h, v_cache[l], cache_rows, d.head_dim, d.head_dim, 16);
+      if (!tk || !tv) return PE_ERR_INVALID_ARGUMENT;
+      e = counted(h, launch_attention_tc(at, *tk, *tv, ex->seq_lens, max_rows_per_req,
+                                         h->sm_count, h->attn_partials, h->attn_partial_floats,
+                                         h->attn_counters, h->attn_n_counters, s));
+      if (e) return PE_ERR_CUDA;
+    }
+    if ((e = mark(2 + 2 * l))) return PE_ERR_CUDA;
+    if (h->attn_trace) {
+      const size_t per = static_cast<size_t>(qd) * h->esize;
+      if ((e = trace_rows(static_cast<char*>(h->attn_trace) + l * h->max_tokens * per, h->attn,
+                          per)))
+        return PE_ERR_CUDA;
+    }
+    return PE_OK;
+  };
+
+  // ---- small batches: one persistent kernel per segment of projections ----
+  // (stream.cu): fc -> layer-0 input -> QKV_0, then after each layer's
+  // attention O -> gate/up -> down -> next QKV (or the final norm).  Used
+  // when the rows fit one 16- or 32-token tile and every phase's share of
+  // activations fits a CTA's panel.
+  const int G = h->sm_count;
+  auto units_per_cta = [&](int N, int K) {
+    const long long U = static_cast<long long>((N + 127) / 128) * ((K + 63) / 64);
+    return (U + G - 1) / G;
+  };
+  const int pkb = stream_panel_kb(std::min(rows, 32));
+  const bool use_stream =
+      dt == PE_DTYPE_BF16 && h->stream_on && rows <= 32 && !compact && !h->kv_fp8 &&
+      qd % 128 == 0 && (d.n_kv_heads * d.head_dim) % 128 == 0 && (d.head_dim == 64 || d.head_dim == 128) &&
+      (d.d + 127) / 128 <= kStreamSsqTiles &&
+      (std::max({d.d, d.ffn, qkv_rows}) + 127) / 128 <= kStreamCounterStride &&
+      units_per_cta(d.d, d.hidden3) <= pkb && units_per_cta(qkv_rows, 2 * d.d) <= pkb &&
+      units_per_cta(qkv_rows, d.d) <= pkb && units_per_cta(d.d, qd) <= pkb &&
+      units_per_cta(d.ffn, d.d) <= pkb && units_per_cta(d.d, d.ffn) <= pkb;
+  if (use_stream) {
+    StreamMaps sm;
+    StreamParams sp;
+    int nmaps = 0;
+    bool maps_ok = true;
+    const int bn = rows <= 16 ? 16 : 32;
+    auto add_map = [&](const CUtensorMap* m) {
+      if (!m || nmaps >= kStreamMaxMaps) {
+        maps_ok = false;
+        return 0;
+      }
+      sm.m[nmaps] = *m;
+      return nmaps++;
+    };
+    auto begin = [&]() {
+      sp = StreamParams{};
+      nmaps = 0;
+      sp.rows = rows;
+      sp.d = d.d;
+      sp.resid = h->resid;
+      sp.eps = d.rms_eps;
+      sp.ids = ex->ids;
+      sp.emb = h->w.emb;
+      sp.vocab = d.vocab;
+      sp.g_e = h->layers[0].norm_e;
+      sp.g_h = h->layers[0].norm_h;
+      sp.x_in = h->x_in;
+      sp.pos = ex->pos;
+      sp.slot = ex->slot;
+      sp.Hq = d.n_heads;
+      sp.Hkv = d.n_kv_heads;
+      sp.dh = d.head_dim;
+      sp.num_blocks = num_blocks;
+      sp.inv_freq64 = h->inv_freq64;
+      sp.q_out = h->q;
+      sp.new_idx = ex->new_idx;
+      sp.final_rows = B * K;
+      sp.g_final = h->w.norm_final;
+      sp.out_hidden = out_hidden;
+      sp.ws = h->stream_ws;
+      sp.sync = h->stream_sync;
+      sp.counters = h->stream_counters;
+      sp.n_counters = kStreamMaxPhases * kStreamCounterStride;
+      sp.err = h->err;
+    };
+    // a GEMM phase: y[rows, N] = x[rows, K] . w[N, K]^T (+ w2 for gate/up)
+    auto gemm = [&](int epi, const void* w, const void* w2, int N, int Kd, const void* x,
+                    int ldx) {
+      StreamPhase& P = sp.ph[sp.nphases];
+      P = StreamPhase{};
+      P.kind = SK_GEMM;
+      P.epi = epi;
+      P.dual = w2 != nullptr;
+      P.N = N;
+      P.K = Kd;
+      P.kb = (Kd + 63) / 64;
+      P.tiles = (N + 127) / 128;
+      P.map_a = add_map(get_map(h, w, N, Kd, Kd, 128));
+      P.map_a2 = w2 ? add_map(get_map(h, w2, N, Kd, Kd, 128)) : P.map_a;
+      P.map_b = add_map(get_map(h, x, rows, Kd, ldx, bn));
+      P.norm_src = -1;
+      P.counters = h->stream_counters + sp.nphases * kStreamCounterStride;
+      return sp.nphases++;
+    };
+    auto row_phase = [&](int kind) {
+      StreamPhase& P = sp.ph[sp.nphases];
+      P = StreamPhase{};
+      P.kind = kind;
+      P.norm_src = -1;
+      return sp.nphases++;
+    };
+    auto ssq_of = [&](int ph) {
+      return h->stream_ssq + static_cast<size_t>(ph) * kStreamSsqTiles * 32;
+    };
+    auto launch = [&]() -> cudaError_t {
+      if (!maps_ok) return cudaErrorInvalidValue;
+      return counted(h, launch_stream(sm, sp, G, s));
+    };
+    // segment 0: fc, the layer-0 input, QKV_0 (+ RoPE and the KV write)
+    begin();
+    sp.k_cache = k_cache[0];
+    sp.v_cache = v_cache[0];
+    gemm(SE_STORE, h->w.fc, nullptr, d.d, d.hidden3, ex->hidden, d.hidden3);
+    row_phase(SK_EMBED);
+    gemm(SE_ROPE_KV, h->layers[0].qkv, nullptr, qkv_rows, 2 * d.d, h->x_in, 2 * d.d);
+    if ((e = launch())) return PE_ERR_CUDA;
+    for (int l = 0; l < d.n_layers; ++l) {
+      if (const pe_status st = attention(l); st != PE_OK) return st;
+      const pe_layer_weights& L = h->layers[l];
+      const bool last = l + 1 == d.n_layers;
+      begin();
+      if (!last) {
+        sp.k_cache = k_cache[l + 1];
+        sp.v_cache = v_cache[l + 1];
+      }
+      const int o_ph = gemm(SE_ADD, L.o, nullptr, d.d, qd, h->attn, qd);
+      sp.ph[o_ph].g_next = L.norm_post;
+      sp.ph[o_ph].xg = h->xn;
+      sp.ph[o_ph].ssq = ssq_of(o_ph);
+      const int gu_ph = gemm(SE_SILU_MUL, L.gate, L.up, d.ffn, d.d, h->xn, d.d);
+      sp.ph[gu_ph].norm_src = o_ph;
+      sp.ph[gu_ph].norm_d = d.d;
+      sp.ph[gu_ph].out = h->act;
+      sp.ph[gu_ph].ldo = d.ffn;
+      const int dn_ph = gemm(SE_ADD, L.down, nullptr, d.d, d.ffn, h->act, d.ffn);
+      if (!last) {
+        sp.ph[dn_ph].g_next = h->layers[l + 1].norm_in;
+        sp.ph[dn_ph].xg = h->x_in;
+        sp.ph[dn_ph].ssq = ssq_of(dn_ph);
+        const int q_ph = gemm(SE_ROPE_KV, h->layers[l + 1].qkv, nullptr, qkv_rows, d.d,
+                              h->x_in, d.d);
+        sp.ph[q_ph].norm_src = dn_ph;
+        sp.ph[q_ph].norm_d = d.d;
+      } else {
+        row_phase(SK_FINAL);
+      }
+      if ((e = launch())) return PE_ERR_CUDA;
+      if (h->trace) {
+        if ((e = trace_rows(h->trace + static_cast<size_t>(l) * h->max_tokens * d.d, h->resid,
+                            static_cast<size_t>(d.d) * sizeof(float))))
+          return PE_ERR_CUDA;
+      }
+    }
+    if ((e = mark(1 + 2 * d.n_layers))) return PE_ERR_CUDA;
+    return PE_OK;
+  }
+
   // fc: projected target hidden state -> residual stream (fp32), live rows
   // to their compact rows
   EpiArgs ep = epi_none();
@@ -586,52 +813,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     }
     if ((e = counted(h, launch_rope_kv(dt, rk, s)))) return PE_ERR_CUDA;
     // paged causal attention
-    if ((e = mark(1 + 2 * l))) return PE_ERR_CUDA;
-    AttnArgs at = {};
-    at.rows = rows;
-    at.B = B;
-    at.Hq = d.n_heads;
-    at.Hkv = d.n_kv_heads;
-    at.dh = d.head_dim;
-    at.bt_stride = bt_stride;
-    at.num_blocks = num_blocks;
-    at.max_seq = bt_stride * d.page_size;
-    at.q = h->q;
-    at.k_cache = k_cache[l];
-    at.v_cache = v_cache[l];
-    at.live = live;
-    at.pos = pos_l;
-    at.is_rejected = rej_l;
-    at.cu_out = cu_l;
-    at.block_table = block_table;
-    at.out = h->attn;
-    at.scale = 1.0f / std::sqrt(static_cast<float>(d.head_dim));
-    at.err = h->err;
-    if (dt == PE_DTYPE_F32) {
-      if ((e = counted(h, launch_attention_simt(dt, at, s)))) return PE_ERR_CUDA;
-    } else {
-      if (h->kv_fp8) {
-        at.kv_fp8 = 1;
-        at.k_scale = h->k_scales[l];
-        at.v_scale = h->v_scales[l];
-      }
-      const CUtensorMap* tk = h->kv_fp8 ? get_map_u8(h, k_cache[l], cache_rows)
-                                        : get_map(h, k_cache[l], cache_rows, d.head_dim, d.head_dim, 16);
-      const CUtensorMap* tv = h->kv_fp8 ? get_map_u8(h, v_cache[l], cache_rows)
-                                        : get_map(h, v_cache[l], cache_rows, d.head_dim, d.head_dim, 16);
-      if (!tk || !tv) return PE_ERR_INVALID_ARGUMENT;
-      e = counted(h, launch_attention_tc(at, *tk, *tv, ex->seq_lens, max_rows_per_req,
-                                         h->sm_count, h->attn_partials, h->attn_partial_floats,
-                                         h->attn_counters, h->attn_n_counters, s));
-      if (e) return PE_ERR_CUDA;
-    }
-    if ((e = mark(2 + 2 * l))) return PE_ERR_CUDA;
-    if (h->attn_trace) {
-      const size_t per = static_cast<size_t>(qd) * h->esize;
-      if ((e = trace_rows(static_cast<char*>(h->attn_trace) + l * h->max_tokens * per, h->attn,
-                          per)))
-        return PE_ERR_CUDA;
-    }
+    if (const pe_status st = attention(l); st != PE_OK) return st;
     // O projection + residual
     ep = epi_none();
     ep.kind = EPI_ADD;

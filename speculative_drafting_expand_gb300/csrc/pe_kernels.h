@@ -219,6 +219,77 @@ cudaError_t launch_gemm_simt(const float* x, int ldx, const float* w, const floa
 cudaError_t launch_argmax_finalize(int M, unsigned long long* keys, int32_t* tokens,
                                    cudaStream_t s);
 
+// ---------------------------------------------------------------- streaming segments
+// The layer projections between two attention launches as one persistent
+// kernel for small row counts (at most 32 rows: one token tile), stream.cu.
+// A segment is a short program of phases: GEMM phases (fc, O, gate/up,
+// down, QKV) and row phases (the layer-0 input, the final norm).
+constexpr int kStreamMaxPhases = 5;
+constexpr int kStreamMaxMaps = 12;
+constexpr int kStreamSyncInts = 16;   // [0, kStreamMaxPhases): phase done counts
+constexpr int kStreamSyncExit = 8;    // CTAs that finished the kernel
+constexpr int kStreamSyncAbort = 9;   // set when a bounded wait gave up
+enum StreamKind { SK_GEMM = 0, SK_EMBED = 1, SK_FINAL = 2 };
+enum StreamEpi { SE_STORE = 0, SE_ADD = 1, SE_SILU_MUL = 2, SE_ROPE_KV = 3 };
+
+struct StreamPhase {
+  int kind, epi, dual;
+  int N, K, kb, tiles;     // GEMM: y[rows, N] = x[rows, K] . w[N, K]^T
+  int map_a, map_a2, map_b;
+  int norm_src;            // phase whose sums of squares scale this GEMM's rows (-1: none)
+  int norm_d;              // width of that norm
+  const void* g_next;      // ADD: gain of the next norm; xg = bf16(residual * g_next)
+  void* xg;                // ADD: [rows, N] bf16 (nullable)
+  float* ssq;              // ADD: [tiles][32] sums of squares of the new residual
+  void* out;               // SILU_MUL: [rows, ldo] bf16
+  int ldo;
+  int* counters;           // [tiles] arrivals (zeroed at kernel exit)
+};
+
+struct StreamParams {
+  int rows, nphases, final_rows, d;
+  StreamPhase ph[kStreamMaxPhases];
+  float* resid;            // [rows, d] fp32 residual stream
+  float eps;
+  // layer-0 input: x_in[r] = [RMSNorm_e(emb[ids[r]]) ; RMSNorm_h(resid[r])]
+  const int32_t* ids;
+  const void* emb;
+  int vocab;
+  const void* g_e;
+  const void* g_h;
+  void* x_in;              // [rows, 2d] bf16
+  // QKV epilogue: rotate-half RoPE of q and k, k and v to the paged cache
+  const int32_t* pos;
+  const int32_t* slot;
+  int Hq, Hkv, dh, num_blocks;
+  const double* inv_freq64;
+  void* q_out;             // [rows, Hq dh] bf16
+  void* k_cache;           // [num_blocks, Hkv, 16, dh] bf16
+  void* v_cache;
+  // final norm of the sampled rows
+  const int32_t* new_idx;  // [final_rows]
+  const void* g_final;
+  void* out_hidden;        // [final_rows, d] bf16
+  float* ws;               // split-K partials [grid][2][128 * 32 * 2]
+  int* sync;               // [kStreamSyncInts], zero on entry, left zero
+  int* counters;           // every phase's tile counters, zero on entry, left zero
+  int n_counters;
+  int* err;
+};
+
+struct StreamMaps {
+  CUtensorMap m[kStreamMaxMaps];
+};
+
+// Launch one segment (rows <= 32); grid = one CTA per SM.
+cudaError_t launch_stream(const StreamMaps& maps, const StreamParams& p, int grid,
+                          cudaStream_t s);
+cudaError_t init_stream();
+// Largest number of k-blocks one CTA may take in a GEMM phase (its
+// activation panel), for rows token rows.
+int stream_panel_kb(int rows);
+size_t stream_ws_floats(int grid);
+
 // tensor-map encoder (fetched once through cudart)
 bool tensor_map_2d_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
                         uint64_t ld_elems, uint32_t box_cols, uint32_t box_rows);

@@ -160,3 +160,49 @@ def test_repeated_steps_are_bitwise_identical(make_wl, repeats):
         assert torch.equal(trace, trace0), ("attention", i)
         assert torch.equal(res["out_hidden"], first["out_hidden"]), ("hidden", i)
         assert torch.equal(res["tokens"], first["tokens"]), ("tokens", i)
+
+
+@pytest.mark.parametrize("B,K,shape", [(1, 7, "small"), (2, 7, "small"), (3, 5, "dh128"),
+                                       (1, 7, "gpt-oss")],
+                         ids=["small-b1-k7", "small-b2-k7-tile32", "dh128-b3-k5",
+                              "gpt-oss-b1-k7"])
+def test_small_batch_stream_matches_the_per_projection_path(B, K, shape):
+    """Up to 32 expanded rows the step runs its projections as persistent
+    segments (RMSNorm folded into the consuming projection as a row scale,
+    RoPE and the KV write in the QKV epilogue).  The same step with the
+    per-projection kernels must agree with it to the bf16 tolerance, and
+    both with the oracle (full_parity runs the default, streaming path)."""
+    torch = G.torch_mod()
+    Bm = G.library()
+    if shape == "gpt-oss":
+        wl = W.gpt_oss_b1()
+    else:
+        sh = SMALL if shape == "small" else W.small_shape(
+            "small-dh128", d=512, n_layers=2, n_heads=4, n_kv_heads=1, head_dim=128, ffn=768,
+            vocab=2048)
+        rng = np.random.default_rng(700 + B * 10 + K)
+        wl = W.custom(f"stream-{shape}-b{B}", 700 + B, sh, K, rng.integers(20, 500, size=B),
+                      np.full(B, K + 1), rng.integers(0, K + 1, size=B), gains="random")
+        G.full_parity(wl, TOL_BF16)
+    sh = wl.shape
+    inp = W.make_step_inputs(wl)
+    w = W.make_weights(sh, wl.config_id, gains=wl.gains)
+    kc, vc = W.make_kv_cache(wl, inp)
+    outs = []
+    for stream in (True, False):
+        dr = G.make_drafter(sh, w, max(wl.T_out, wl.B * wl.K), wl.B)
+        Bm.pe_set_small_batch_stream(dr, stream)
+        st = G.DeviceStep(wl, inp, kc, vc)
+        res = G.run_step(dr, st, want_logits=True)
+        assert res["err"] == 0
+        outs.append((G.f64(Bm.to_host(res["out_hidden"]), sh.dtype),
+                     Bm.to_host(res["logits"]).astype(np.float64),
+                     [G.f64(Bm.to_host(k), sh.dtype) for k in st.kc]))
+        dr.close()
+    (h1, l1, k1), (h2, l2, k2) = outs
+    assert np.abs(h1 - h2).max() <= TOL_BF16 * np.abs(h2).max()
+    assert np.abs(l1 - l2).max() <= TOL_BF16 * np.abs(l2).max()
+    for a, b in zip(k1, k2):
+        fin = np.isfinite(b)
+        assert np.array_equal(np.isfinite(a), fin)          # the same slots written
+        assert np.abs(a[fin] - b[fin]).max() <= TOL_BF16 * np.abs(b[fin]).max()
