@@ -521,7 +521,11 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
   // phase timing (diagnostic): event 0 here, 1 + 2 l before layer l's
   // attention, 2 + 2 l after it, 1 + 2 L at the end
   auto mark = [&](int i) -> cudaError_t {
-    return h->phase_events.empty() ? cudaSuccess : cudaEventRecord(h->phase_events[i], s);
+    // an external record: inside a stream capture it becomes an event node
+    // that every replay of the graph records
+    return h->phase_events.empty()
+               ? cudaSuccess
+               : cudaEventRecordWithFlags(h->phase_events[i], s, cudaEventRecordExternal);
   };
   if ((e = mark(0))) return PE_ERR_CUDA;
   // debug copies of per-row activations, in the expanded row order (zero

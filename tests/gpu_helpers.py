@@ -155,13 +155,14 @@ def make_drafter(shape, weights, max_tokens, max_reqs):
     return B.Drafter(shape, weights, max_tokens, max_reqs)
 
 
-def full_parity(wl, tol, gains=None, requests=None, check_cache=True, strict_tokens=False):
+def full_parity(wl, tol, gains=None, requests=None, check_cache=True, strict_tokens=True):
     """Run one step on the GPU and the oracle; assert parity.  Returns both.
 
-    strict_tokens: hold the end-to-end tokens to the spec rule itself
-    (identical wherever the fp64 oracle's top-2 margin exceeds 1e-2) instead
-    of twice the logit tolerance; used for the configurations where the
-    measured disagreement count in between is zero."""
+    strict_tokens (default): end-to-end tokens identical to the fp64
+    oracle's wherever its top-2 margin exceeds 1e-2, the spec rule
+    itself.  Measured on every configuration of the suite, no token with a
+    margin between 1e-2 and twice the logit tolerance disagreed, so the
+    looser bound (strict_tokens=False) is only reported, not applied."""
     sh = wl.shape
     inp = W.make_step_inputs(wl)
     w = W.make_weights(sh, wl.config_id, gains=gains or wl.gains)
@@ -240,6 +241,8 @@ def tokens_only_parity(wl, tol, requests=None):
     lm_logits, lm_tokens = O.lm_head_argmax(sh, w, hid)
     margin_ok_tokens(lm_logits, lm_tokens, got_t, margin=1e-3)
     ls = np.abs(ref.logits).max()
-    margin_ok_tokens(ref.logits, ref.tokens, got_t, margin=max(1e-2, 2 * tol * ls))
+    token_rule_stats(wl.name + "-tokens-only", ref.logits, ref.tokens, got_t,
+                     max(1e-2, 2 * tol * ls))
+    margin_ok_tokens(ref.logits, ref.tokens, got_t, margin=1e-2)
     dr.close()
     return got_t, ref

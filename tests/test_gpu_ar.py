@@ -46,7 +46,9 @@ def _pass_parity(wl_pass, w, inp, kc, vc, dr):
     ls = np.abs(ref.logits).max()
     assert np.abs(got_l - ref.logits).max() <= TOL_BF16 * ls
     got_t = B.to_host(res["tokens"])
-    G.margin_ok_tokens(ref.logits, ref.tokens, got_t, margin=max(1e-2, 2 * TOL_BF16 * ls))
+    G.token_rule_stats(wl_pass.name, ref.logits, ref.tokens, got_t,
+                       max(1e-2, 2 * TOL_BF16 * ls))
+    G.margin_ok_tokens(ref.logits, ref.tokens, got_t, margin=1e-2)
     G.check_kv(st, ref, sh, TOL_BF16 * 2)
     return got_t, [B.to_host(k) for k in st.kc], [B.to_host(v) for v in st.vc]
 

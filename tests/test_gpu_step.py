@@ -3,11 +3,11 @@
 
 Bar: metadata bit-exact; final hidden states and logits within
 max-abs <= tol x max|value| (1e-4 for the fp32 path, 2e-2 for bf16); draft
-tokens identical wherever the oracle's top-2 logit margin exceeds twice the
-logit tolerance (1e-2 for fp32); the LM-head argmax decision on the GPU's
-own final hidden rows identical to the oracle's wherever the margin exceeds
-1e-3; KV writes at exactly the non-rejected slots, every other slot
-untouched.
+tokens identical wherever the fp64 oracle's top-2 logit margin exceeds 1e-2
+(elsewhere within 1e-2 of the top logit); the LM-head argmax decision on
+the GPU's own final hidden rows identical to the oracle's wherever the
+margin exceeds 1e-3; KV writes at exactly the non-rejected slots, every
+other slot untouched.
 """
 
 import numpy as np
@@ -78,8 +78,9 @@ def test_k1_is_one_autoregressive_step_on_gpu():
     logits, tokens = O.ar_eagle_step(SMALL, W.make_weights(SMALL, 81, gains="random"),
                                      st.inp, kc, vc)
     B = G.library()
-    G.margin_ok_tokens(logits, tokens, B.to_host(res["tokens"]),
-                       margin=2 * TOL_BF16 * np.abs(logits).max())
+    G.token_rule_stats("k1-ar-eagle", logits, tokens, B.to_host(res["tokens"]),
+                       2 * TOL_BF16 * np.abs(logits).max())
+    G.margin_ok_tokens(logits, tokens, B.to_host(res["tokens"]), margin=1e-2)
 
 
 def test_gpt_oss_b1_full_size():
