@@ -604,7 +604,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
   };
   const int pkb = stream_panel_kb(std::min(rows, 32));
   const bool use_stream =
-      dt == PE_DTYPE_BF16 && h->stream_on && rows <= 32 && !compact && !h->kv_fp8 &&
+      dt == PE_DTYPE_BF16 && h->stream_on && rows <= 32 && !compact &&
       qd % 128 == 0 && (d.n_kv_heads * d.head_dim) % 128 == 0 && (d.head_dim == 64 || d.head_dim == 128) &&
       (d.d + 127) / 128 <= kStreamSsqTiles &&
       (std::max({d.d, d.ffn, qkv_rows}) + 127) / 128 <= kStreamCounterStride &&
@@ -690,9 +690,17 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
       return counted(h, launch_stream(sm, sp, G, s));
     };
     // segment 0: fc, the layer-0 input, QKV_0 (+ RoPE and the KV write)
+    auto set_kv = [&](int l) {
+      sp.k_cache = k_cache[l];
+      sp.v_cache = v_cache[l];
+      sp.kv_fp8 = h->kv_fp8 ? 1 : 0;
+      if (h->kv_fp8) {
+        sp.k_inv_scale = 1.f / h->k_scales[l];
+        sp.v_inv_scale = 1.f / h->v_scales[l];
+      }
+    };
     begin();
-    sp.k_cache = k_cache[0];
-    sp.v_cache = v_cache[0];
+    set_kv(0);
     gemm(SE_STORE, h->w.fc, nullptr, d.d, d.hidden3, ex->hidden, d.hidden3);
     row_phase(SK_EMBED);
     gemm(SE_ROPE_KV, h->layers[0].qkv, nullptr, qkv_rows, 2 * d.d, h->x_in, 2 * d.d);
@@ -702,10 +710,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
       const pe_layer_weights& L = h->layers[l];
       const bool last = l + 1 == d.n_layers;
       begin();
-      if (!last) {
-        sp.k_cache = k_cache[l + 1];
-        sp.v_cache = v_cache[l + 1];
-      }
+      if (!last) set_kv(l + 1);
       const int o_ph = gemm(SE_ADD, L.o, nullptr, d.d, qd, h->attn, qd);
       sp.ph[o_ph].g_next = L.norm_post;
       sp.ph[o_ph].xg = h->xn;

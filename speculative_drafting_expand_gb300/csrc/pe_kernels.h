@@ -264,8 +264,10 @@ struct StreamParams {
   int Hq, Hkv, dh, num_blocks;
   const double* inv_freq64;
   void* q_out;             // [rows, Hq dh] bf16
-  void* k_cache;           // [num_blocks, Hkv, 16, dh] bf16
+  void* k_cache;           // [num_blocks, Hkv, 16, dh] bf16 (e4m3 codes when kv_fp8)
   void* v_cache;
+  int kv_fp8;              // pools hold e4m3 codes of k / k_scale and v / v_scale
+  float k_inv_scale, v_inv_scale;
   // final norm of the sampled rows
   const int32_t* new_idx;  // [final_rows]
   const void* g_final;

@@ -41,6 +41,7 @@
 // Every wait is bounded; a wait that gives up records PE_DEV_TIMEOUT, sets
 // an abort word that the other CTAs' waits watch, and the kernel unwinds
 // after its own copies and MMAs have drained.
+#include "fp8_common.cuh"
 #include "gemm_tc.cuh"
 
 namespace pe {
@@ -122,12 +123,22 @@ __device__ __forceinline__ float bf(const void* p, size_t i) {
   return __bfloat162float(static_cast<const bf16*>(p)[i]);
 }
 
-// The units [lo, hi) of phase P that CTA `cta` of G takes.
+// CTAs that take part in phase P: all G, or one per unit when the phase
+// has fewer units than that -- every participant then holds at least one
+// unit, so every CTA between a tile's first and last contributor arrives
+// at the tile's counter.
+__device__ __forceinline__ int phase_ctas(const StreamPhase& P, int G) {
+  const long long U = static_cast<long long>(P.tiles) * P.kb;
+  return U < G ? static_cast<int>(U) : G;
+}
+// The units [lo, hi) of phase P that CTA `cta` takes (empty past the
+// participants).
 __device__ __forceinline__ void phase_range(const StreamPhase& P, int cta, int G, long long& lo,
                                             long long& hi) {
   const long long U = static_cast<long long>(P.tiles) * P.kb;
-  lo = unit_lo(cta, U, G);
-  hi = unit_lo(cta + 1, U, G);
+  const int Gp = phase_ctas(P, G);
+  lo = cta < Gp ? unit_lo(cta, U, Gp) : U;
+  hi = cta < Gp ? unit_lo(cta + 1, U, Gp) : U;
 }
 
 __device__ __forceinline__ int phase_target(const StreamParams& p, int i) {
@@ -265,7 +276,8 @@ __device__ void finish_tile(const StreamParams& p, const StreamPhase& P, int til
       } else {
         const bool is_k = o < qd + kd;
         const int g = (o - (is_k ? qd : qd + kd)) / p.dh;
-        bf16* cache = static_cast<bf16*>(is_k ? p.k_cache : p.v_cache);
+        void* cache = is_k ? p.k_cache : p.v_cache;
+        const float inv = is_k ? p.k_inv_scale : p.v_inv_scale;
 #pragma unroll
         for (int j = 0; j < BN; ++j) {
           const int sl = slot_s[j];
@@ -274,8 +286,12 @@ __device__ void finish_tile(const StreamParams& p, const StreamPhase& P, int til
             if (blk >= p.num_blocks) {
               if (jd == 0) record_error(p.err, PE_DEV_BAD_BLOCK);
             } else {
-              cache[((static_cast<size_t>(blk) * p.Hkv + g) * 16 + off) * p.dh + jd] =
-                  __float2bfloat16_rn(v2[j]);
+              const size_t at = ((static_cast<size_t>(blk) * p.Hkv + g) * 16 + off) * p.dh + jd;
+              if (p.kv_fp8)
+                static_cast<uint8_t*>(cache)[at] =
+                    static_cast<uint8_t>(f32x2_to_e4m3x2(v2[j] * inv, 0.f) & 0xffu);
+              else
+                static_cast<bf16*>(cache)[at] = __float2bfloat16_rn(v2[j]);
             }
           }
         }
@@ -576,6 +592,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       ++bph;
       const long long U = static_cast<long long>(P.tiles) * P.kb;
+      const int Gp = phase_ctas(P, G);
       for (long long u = lo; u < hi;) {
         const int tile = static_cast<int>(u / P.kb);
         const int k_lo = static_cast<int>(u - static_cast<long long>(tile) * P.kb);
@@ -601,8 +618,8 @@ __global__ void __launch_bounds__(192, 1)
           v[j] = va[j / 16][j % 16];
           v2[j] = P.dual ? vb[j / 16][j % 16] : 0.f;
         }
-        const int c_first = cta_of_unit(static_cast<long long>(tile) * P.kb, U, G);
-        const int c_last = cta_of_unit(static_cast<long long>(tile + 1) * P.kb - 1, U, G);
+        const int c_first = cta_of_unit(static_cast<long long>(tile) * P.kb, U, Gp);
+        const int c_last = cta_of_unit(static_cast<long long>(tile + 1) * P.kb - 1, U, Gp);
         bool finisher = true;
         if (c_first != c_last) {
           // partial tile: to this CTA's slot, then the last contributor sums
@@ -635,7 +652,7 @@ __global__ void __launch_bounds__(192, 1)
               for (int q = 0; q < UNR; ++q) {
                 if (c + q > c_last) break;
                 const int cq = c + q;
-                const int cs = unit_lo(cq, U, G) >= static_cast<long long>(tile) * P.kb ? 0 : 1;
+                const int cs = unit_lo(cq, U, Gp) >= static_cast<long long>(tile) * P.kb ? 0 : 1;
                 const float* src = p.ws + (static_cast<size_t>(cq) * 2 + cs) * (128 * 64) + row;
 #pragma unroll
                 for (int j = 0; j < BN; ++j) {
