@@ -270,15 +270,34 @@ pe_status pe_set_trace(pe_handle* h, float* residual_trace, void* attn_trace);
  * their use. */
 pe_status pe_set_phase_events(pe_handle* h, void* const* events, int32_t n);
 
-/* Small-batch streaming (on by default).  When a step's expanded rows fit
- * one 16- or 32-row token tile, pe_draft_forward runs the projections
- * between two attention launches (fc, the layer-0 input and QKV; then O,
- * gate/up, down and the next QKV or the final norm) as one persistent
- * kernel per segment, with RMSNorm, RoPE and the KV write fused into it,
- * instead of one launch per projection.  enable = 0 selects the
- * per-projection path for every batch (the same results up to fp32
- * summation order); used to compare the two. */
+/* Small-batch streaming (off by default).  With enable = 1, when a step's
+ * expanded rows fit one 16- or 32-row token tile, pe_draft_forward runs the
+ * projections between two attention launches (fc, the layer-0 input and
+ * QKV; then O, gate/up, down and the next QKV or the final norm) as one
+ * persistent kernel per segment, with RMSNorm, RoPE and the KV write fused
+ * into it, instead of one launch per projection.  The results agree with
+ * the per-projection path up to fp32 summation order.  Measured slower on
+ * the GPT-OSS-20B-shaped batch-1 step (about 655 against 515 us): every
+ * phase boundary waits for the slowest tile's split-K finisher, a chain of
+ * dependent L2 round trips of about 1 us each. */
 pe_status pe_set_small_batch_stream(pe_handle* h, int32_t enable);
+
+/* Tuning of the small-batch streaming kernel.  tiles: how many 16 KB
+ * weight tiles each CTA brings into L2 ahead of its shared-memory ring
+ * (default 0 = none; at most 4096).  boundary_tiles: how many weight tiles
+ * a CTA may load into a phase whose inputs are not complete yet (default
+ * -1 = no limit). */
+pe_status pe_set_stream_prefetch(pe_handle* h, int32_t tiles, int32_t boundary_tiles);
+
+/* Diagnostic timeline of the small-batch streaming kernel (no counterpart
+ * on the pages).  stamps: caller-owned device buffer of sm_count * 64
+ * uint64 (NULL turns it off); every segment launch overwrites it with
+ * %globaltimer stamps in ns per CTA: [0] start, [1] tensor memory held,
+ * [2] first weight load issued, then for phase p at 4 + 4p: [+0] previous
+ * phase complete on every CTA, [+1] activation panel landed, [+2] last MMA
+ * of the phase issued, [+3] the CTA's last tile of the phase done; [60] end.
+ * Slots a launch does not reach keep their old contents. */
+pe_status pe_set_stream_timeline(pe_handle* h, uint64_t* stamps);
 
 /* y[M, N] = x[M, K] . w[N, K]^T with the library's GEMM for the model dtype
  * (tcgen05 tensor cores for bf16, FFMA for f32); y is fp32.  A diagnostic

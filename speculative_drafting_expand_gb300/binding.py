@@ -33,7 +33,7 @@ PE_MASK_ADDITIVE_BF16 = 1
 # the one that does not return a pe_status)
 EXPORTED = ("pe_create", "pe_destroy", "pe_expand_batch", "pe_draft_forward",
             "pe_lmhead_argmax", "pe_get_device_error", "pe_set_trace", "pe_set_phase_events",
-            "pe_set_small_batch_stream",
+            "pe_set_small_batch_stream", "pe_set_stream_prefetch", "pe_set_stream_timeline",
             "pe_linear",
             "pe_get_launch_count", "pe_check_bounded_wait", "pe_linear_static",
             "pe_linear_static_error",
@@ -95,6 +95,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pe_check_bounded_wait.argtypes = [_vp, _vp, _vp]
     lib.pe_set_phase_events.argtypes = [_vp, P(_vp), _i32]
     lib.pe_set_small_batch_stream.argtypes = [_vp, _i32]
+    lib.pe_set_stream_timeline.argtypes = [_vp, _vp]
+    lib.pe_set_stream_prefetch.argtypes = [_vp, _i32, _i32]
     lib.pe_linear_static_error.argtypes = [P(_i32), _vp]
     lib.pe_set_kv_cache_fp8.argtypes = [_vp, P(ctypes.c_float), P(ctypes.c_float)]
     lib.pe_train_build_mask.argtypes = [_i32, _i32, _i32, _vp, ctypes.c_int64, _vp]
@@ -288,6 +290,16 @@ def pe_check_bounded_wait(dr: Drafter, out, stream=None) -> None:
 
 def pe_set_small_batch_stream(dr: Drafter, enable: bool) -> None:
     _check("pe_set_small_batch_stream", lib().pe_set_small_batch_stream(dr.handle, int(enable)))
+
+
+def pe_set_stream_prefetch(dr: Drafter, tiles: int, boundary_tiles: int = -1) -> None:
+    _check("pe_set_stream_prefetch",
+           lib().pe_set_stream_prefetch(dr.handle, int(tiles), int(boundary_tiles)))
+
+
+def pe_set_stream_timeline(dr: Drafter, stamps=None) -> None:
+    """stamps: int64 device tensor of sm_count * 64 entries, or None."""
+    _check("pe_set_stream_timeline", lib().pe_set_stream_timeline(dr.handle, ptr(stamps)))
 
 
 def pe_set_phase_events(dr: Drafter, events=None) -> None:

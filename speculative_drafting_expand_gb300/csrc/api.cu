@@ -86,7 +86,10 @@ struct pe_handle {
   std::vector<cudaEvent_t> phase_events;  // 2 + 2 L events, or none
   // small batches: projections between attention launches as one
   // persistent kernel per segment (stream.cu)
-  bool stream_on = true;
+  bool stream_on = false;
+  unsigned long long* stream_timeline = nullptr;  // diagnostic, caller-owned
+  int stream_prefetch = 0;  // weight tiles prefetched into L2 ahead of the ring
+  int stream_boundary = -1;  // loads into a phase before its inputs are ready (-1: any)
   float* stream_ws = nullptr;
   int* stream_sync = nullptr;
   int* stream_counters = nullptr;
@@ -330,6 +333,19 @@ pe_status pe_set_small_batch_stream(pe_handle* h, int32_t enable) {
   return PE_OK;
 }
 
+pe_status pe_set_stream_prefetch(pe_handle* h, int32_t tiles, int32_t boundary_tiles) {
+  if (!h || tiles < 0 || tiles > 4096 || boundary_tiles < -1) return PE_ERR_INVALID_ARGUMENT;
+  h->stream_prefetch = tiles;
+  h->stream_boundary = boundary_tiles;
+  return PE_OK;
+}
+
+pe_status pe_set_stream_timeline(pe_handle* h, uint64_t* stamps) {
+  if (!h) return PE_ERR_INVALID_ARGUMENT;
+  h->stream_timeline = reinterpret_cast<unsigned long long*>(stamps);
+  return PE_OK;
+}
+
 pe_status pe_set_phase_events(pe_handle* h, void* const* events, int32_t n) {
   if (!h || n < 0 || (n > 0 && !events)) return PE_ERR_INVALID_ARGUMENT;
   if (n != 0 && n != 2 + 2 * h->desc.n_layers) return PE_ERR_INVALID_ARGUMENT;
@@ -521,11 +537,15 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
   // phase timing (diagnostic): event 0 here, 1 + 2 l before layer l's
   // attention, 2 + 2 l after it, 1 + 2 L at the end
   auto mark = [&](int i) -> cudaError_t {
-    // an external record: inside a stream capture it becomes an event node
-    // that every replay of the graph records
-    return h->phase_events.empty()
-               ? cudaSuccess
-               : cudaEventRecordWithFlags(h->phase_events[i], s, cudaEventRecordExternal);
+    // inside a stream capture an external record becomes an event node that
+    // every replay of the graph records; outside one, a plain record
+    if (h->phase_events.empty()) return cudaSuccess;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const cudaError_t q = cudaStreamIsCapturing(s, &cs);
+    if (q != cudaSuccess) return q;
+    return cs == cudaStreamCaptureStatusActive
+               ? cudaEventRecordWithFlags(h->phase_events[i], s, cudaEventRecordExternal)
+               : cudaEventRecord(h->phase_events[i], s);
   };
   if ((e = mark(0))) return PE_ERR_CUDA;
   // debug copies of per-row activations, in the expanded row order (zero
@@ -606,7 +626,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
   const bool use_stream =
       dt == PE_DTYPE_BF16 && h->stream_on && rows <= 32 && !compact &&
       qd % 128 == 0 && (d.n_kv_heads * d.head_dim) % 128 == 0 && (d.head_dim == 64 || d.head_dim == 128) &&
-      (d.d + 127) / 128 <= kStreamSsqTiles &&
+      (d.d + 127) / 128 <= 128 &&  // a norm's per-tile sums fit the CTA's exchange buffer
       (std::max({d.d, d.ffn, qkv_rows}) + 127) / 128 <= kStreamCounterStride &&
       units_per_cta(d.d, d.hidden3) <= pkb && units_per_cta(qkv_rows, 2 * d.d) <= pkb &&
       units_per_cta(qkv_rows, d.d) <= pkb && units_per_cta(d.d, qd) <= pkb &&
@@ -616,7 +636,6 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     StreamParams sp;
     int nmaps = 0;
     bool maps_ok = true;
-    const int bn = rows <= 16 ? 16 : 32;
     auto add_map = [&](const CUtensorMap* m) {
       if (!m || nmaps >= kStreamMaxMaps) {
         maps_ok = false;
@@ -650,6 +669,9 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
       sp.final_rows = B * K;
       sp.g_final = h->w.norm_final;
       sp.out_hidden = out_hidden;
+      sp.timeline = h->stream_timeline;
+      sp.prefetch_tiles = h->stream_prefetch;
+      sp.boundary_tiles = h->stream_boundary;
       sp.ws = h->stream_ws;
       sp.sync = h->stream_sync;
       sp.counters = h->stream_counters;
@@ -670,7 +692,10 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
       P.tiles = (N + 127) / 128;
       P.map_a = add_map(get_map(h, w, N, Kd, Kd, 128));
       P.map_a2 = w2 ? add_map(get_map(h, w2, N, Kd, Kd, 128)) : P.map_a;
-      P.map_b = add_map(get_map(h, x, rows, Kd, ldx, bn));
+      P.w = w;
+      P.w2 = w2 ? w2 : w;
+      P.x = x;
+      P.ldx = ldx;
       P.norm_src = -1;
       P.counters = h->stream_counters + sp.nphases * kStreamCounterStride;
       return sp.nphases++;

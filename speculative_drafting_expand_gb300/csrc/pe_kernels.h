@@ -229,13 +229,24 @@ constexpr int kStreamMaxMaps = 12;
 constexpr int kStreamSyncInts = 16;   // [0, kStreamMaxPhases): phase done counts
 constexpr int kStreamSyncExit = 8;    // CTAs that finished the kernel
 constexpr int kStreamSyncAbort = 9;   // set when a bounded wait gave up
+// Diagnostic timeline of one segment launch (%globaltimer, ns), per CTA:
+// [0] start, [1] tensor memory held, [2] weight stream issued its first
+// load; then per phase ph at 4 + 4 ph: [+0] previous phase complete
+// everywhere, [+1] activation panel landed (MMA issuer), [+2] the issuer
+// committed its last MMA of the phase, [+3] this CTA's last tile of the
+// phase done (partial stored, or finished and published); [60] end.
+constexpr int kStreamTimelineSlots = 64;
 enum StreamKind { SK_GEMM = 0, SK_EMBED = 1, SK_FINAL = 2 };
 enum StreamEpi { SE_STORE = 0, SE_ADD = 1, SE_SILU_MUL = 2, SE_ROPE_KV = 3 };
 
 struct StreamPhase {
   int kind, epi, dual;
   int N, K, kb, tiles;     // GEMM: y[rows, N] = x[rows, K] . w[N, K]^T
-  int map_a, map_a2, map_b;
+  int map_a, map_a2;       // weight tensor maps (indices into StreamMaps)
+  const void* w;           // the same weights [N, K] bf16 (row stride K), for L2 prefetch
+  const void* w2;
+  const void* x;           // activations [rows, K] bf16, row stride ldx (16-byte aligned)
+  int ldx;
   int norm_src;            // phase whose sums of squares scale this GEMM's rows (-1: none)
   int norm_d;              // width of that norm
   const void* g_next;      // ADD: gain of the next norm; xg = bf16(residual * g_next)
@@ -272,6 +283,9 @@ struct StreamParams {
   const int32_t* new_idx;  // [final_rows]
   const void* g_final;
   void* out_hidden;        // [final_rows, d] bf16
+  int prefetch_tiles;      // weight tiles brought into L2 ahead of the ring (0: none)
+  int boundary_tiles;      // loads into a phase before its inputs are ready (-1: no limit)
+  unsigned long long* timeline;  // diagnostic: [grid][kStreamTimelineSlots] ns stamps, or null
   float* ws;               // split-K partials [grid][2][128 * 32 * 2]
   int* sync;               // [kStreamSyncInts], zero on entry, left zero
   int* counters;           // every phase's tile counters, zero on entry, left zero

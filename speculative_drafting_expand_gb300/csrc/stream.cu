@@ -13,7 +13,7 @@
 //   last:    O_l -> gate/up_l -> down_l -> final norm of the sampled rows
 // with the paged attention of each layer launched between segments.
 //
-// Roles (192 threads): warp 4 streams weight tiles (128 features x 64 k,
+// Roles (224 threads): warp 4 streams weight tiles (128 features x 64 k,
 // 16 KB) through a ring of shared-memory stages, phase after phase, waiting
 // only for free stages -- weights do not depend on activations, so the
 // stream runs across phase boundaries and across the wait for the previous
@@ -78,9 +78,13 @@ __device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
 __device__ __forceinline__ void red_release_add(int* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-// Generic-proxy global writes <-> asynchronous-proxy (TMA) global reads.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
+// Fetch-and-add with acquire and release at GPU scope: publishes what this
+// CTA wrote before its barrier, and sees what earlier arrivals published.
+__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
 }
 __device__ __forceinline__ void give_up(int* abort_word, int* err) {
   record_error(err, PE_DEV_TIMEOUT);
@@ -119,6 +123,22 @@ __device__ __forceinline__ bool flag_wait_ab(const int* flag, int target, int* a
   }
 }
 
+// 16 bytes global -> shared without the TMA unit (src_bytes 0: zeros)
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// diagnostic timeline stamp (no-op unless a buffer was given)
+__device__ __forceinline__ void stamp(const StreamParams& p, int slot) {
+  if (p.timeline)
+    p.timeline[static_cast<size_t>(blockIdx.x) * kStreamTimelineSlots + slot] = global_timer_ns();
+}
+
 __device__ __forceinline__ float bf(const void* p, size_t i) {
   return __bfloat162float(static_cast<const bf16*>(p)[i]);
 }
@@ -139,6 +159,39 @@ __device__ __forceinline__ void phase_range(const StreamPhase& P, int cta, int G
   const int Gp = phase_ctas(P, G);
   lo = cta < Gp ? unit_lo(cta, U, Gp) : U;
   hi = cta < Gp ? unit_lo(cta + 1, U, Gp) : U;
+}
+
+// This CTA's weight tiles in stream order: phase, unit, and for the gate/up
+// pair which of the two matrices.
+struct WeightCursor {
+  int ph, a;
+  long long u, hi;
+};
+__device__ __forceinline__ bool wc_next_phase(const StreamParams& p, int cta, int G,
+                                              WeightCursor& c) {
+  for (++c.ph; c.ph < p.nphases; ++c.ph) {
+    const StreamPhase& P = p.ph[c.ph];
+    if (P.kind != SK_GEMM) continue;
+    long long lo, hi;
+    phase_range(P, cta, G, lo, hi);
+    if (lo < hi) {
+      c.u = lo;
+      c.hi = hi;
+      c.a = 0;
+      return true;
+    }
+  }
+  return false;
+}
+__device__ __forceinline__ bool wc_advance(const StreamParams& p, int cta, int G,
+                                           WeightCursor& c) {
+  if (c.a < p.ph[c.ph].dual) {
+    ++c.a;
+    return true;
+  }
+  c.a = 0;
+  if (++c.u < c.hi) return true;
+  return wc_next_phase(p, cta, G, c);
 }
 
 __device__ __forceinline__ int phase_target(const StreamParams& p, int i) {
@@ -185,11 +238,24 @@ __device__ __forceinline__ float sum_over_features(float (&a)[BN], float* red, i
 // ---------------------------------------------------------------------------
 // tile epilogues (all 128 epilogue threads together; thread = feature row)
 // ---------------------------------------------------------------------------
+// The residual of this thread's feature for the BN tokens (0 past the batch
+// or the features): loaded by the finisher before it sums the partials, so
+// that the two sets of loads are in flight together.
+template <int BN>
+__device__ __forceinline__ void load_resid(const StreamParams& p, const StreamPhase& P, int tile,
+                                           float (&old)[BN]) {
+  const int o = tile * 128 + threadIdx.x;
+  const bool valid = o < P.N;
+#pragma unroll
+  for (int j = 0; j < BN; ++j)
+    old[j] = (j < p.rows && valid) ? __ldcg(p.resid + static_cast<size_t>(j) * p.d + o) : 0.f;
+}
+
 template <int BN>
 __device__ void finish_tile(const StreamParams& p, const StreamPhase& P, int tile,
-                            float (&v)[BN], float (&v2)[BN], const float* rms, float* xchg,
-                            const float* cosT, const float* sinT, const int* slot_s, int warp,
-                            int lane) {
+                            float (&v)[BN], float (&v2)[BN], const float (&old)[BN],
+                            const float* rms, float* xchg, const float* cosT, const float* sinT,
+                            const int* slot_s, int warp, int lane) {
   const int row = threadIdx.x;
   const int o = tile * 128 + row;
   const bool valid = o < P.N;
@@ -210,10 +276,6 @@ __device__ void finish_tile(const StreamParams& p, const StreamPhase& P, int til
     }
     case SE_ADD: {
       float* r = p.resid + o;
-      float old[BN];
-#pragma unroll
-      for (int j = 0; j < BN; ++j)
-        old[j] = (j < rows && valid) ? r[static_cast<size_t>(j) * p.d] : 0.f;
       const float gn = (valid && P.g_next) ? bf(P.g_next, o) : 0.f;
       float sq[BN];
 #pragma unroll
@@ -366,7 +428,7 @@ __device__ void final_row(const StreamParams& p, int i, float* red) {
 // the kernel
 // ---------------------------------------------------------------------------
 template <int BN>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     stream_kernel(const __grid_constant__ StreamMaps maps, const __grid_constant__ StreamParams p) {
   using C = SCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
@@ -392,12 +454,17 @@ __global__ void __launch_bounds__(192, 1)
   float* rms = reinterpret_cast<float*>(misc + 512);                     // [32]
   int* slot_s = reinterpret_cast<int*>(misc + 640);                      // [32]
   float* red = reinterpret_cast<float*>(misc + 768);                     // [8]
+  volatile int* loaded = reinterpret_cast<volatile int*>(misc + 800);     // weight tiles issued
+  volatile int* open_ph = reinterpret_cast<volatile int*>(misc + 804);    // phases whose inputs are ready
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, cta = blockIdx.x;
   int* const abort_word = p.sync + kStreamSyncAbort;
 
   if (threadIdx.x == 0) {
+    stamp(p, 0);
+    *loaded = 0;
+    *open_ph = 0;
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
@@ -417,33 +484,79 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       for (int i = 0; i < kStreamMaxMaps; ++i) tma_prefetch_desc(&maps.m[i]);
       const uint64_t pol = l2_policy_evict_first();
+      WeightCursor ld{-1, 0, 0, 0};
+      bool has_ld = wc_next_phase(p, cta, G, ld);
+      stamp(p, 2);
       long long ring_i = 0;
-      bool ok = true;
-      for (int ph = 0; ph < p.nphases && ok; ++ph) {
-        const StreamPhase& P = p.ph[ph];
-        if (P.kind != SK_GEMM) continue;
-        long long lo, hi;
-        phase_range(P, cta, G, lo, hi);
-        for (long long u = lo; u < hi && ok; ++u) {
-          const int tile = static_cast<int>(u / P.kb), kk = static_cast<int>(u % P.kb);
-          for (int a = 0; a <= P.dual; ++a) {
-            const int st = static_cast<int>(ring_i % C::NST);
-            const long long rnd = ring_i / C::NST;
-            if (rnd > 0 && !mbar_wait_ab(&empty[st], static_cast<uint32_t>(rnd - 1) & 1,
-                                         abort_word, p.err)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&full[st], C::STAGE);
-            tma_load_2d(ring + st * C::STAGE, &maps.m[a ? P.map_a2 : P.map_a], &full[st], kk * 64,
-                        tile * 128, pol);
-            ++ring_i;
-          }
+      int cur_ph = -1, in_ph = 0;   // phase of the last load, loads issued into it
+      while (has_ld) {
+        const StreamPhase& P = p.ph[ld.ph];
+        if (ld.ph != cur_ph) {
+          cur_ph = ld.ph;
+          in_ph = 0;
         }
+        // At most boundary_tiles loads into a phase whose inputs are not
+        // ready yet: the refill burst at a phase boundary would otherwise
+        // delay the finishers' and the next panel's memory accesses.
+        if (p.boundary_tiles >= 0 && in_ph >= p.boundary_tiles && *open_ph < ld.ph) {
+          const unsigned long long t0 = global_timer_ns();
+          while (*open_ph < ld.ph && global_timer_ns() - t0 < kWaitTimeoutNs) __nanosleep(64);
+        }
+        ++in_ph;
+        const int st = static_cast<int>(ring_i % C::NST);
+        const long long rnd = ring_i / C::NST;
+        if (rnd > 0 && !mbar_wait_ab(&empty[st], static_cast<uint32_t>(rnd - 1) & 1, abort_word,
+                                     p.err))
+          break;
+        mbar_arrive_expect_tx(&full[st], C::STAGE);
+        tma_load_2d(ring + st * C::STAGE, &maps.m[ld.a ? P.map_a2 : P.map_a], &full[st],
+                    static_cast<int>(ld.u % P.kb) * 64, static_cast<int>(ld.u / P.kb) * 128, pol);
+        ++ring_i;
+        *loaded = static_cast<int>(ring_i);
+        has_ld = wc_advance(p, cta, G, ld);
       }
+      *loaded = 0x7fffffff;   // done (or gave up): the prefetcher stops
       // every copy this thread issued has landed before the CTA exits
       for (long long i = ring_i - 1; i >= 0 && i >= ring_i - C::NST; --i)
         mbar_wait(&full[i % C::NST], static_cast<uint32_t>(i / C::NST) & 1, p.err);
+    }
+  } else if (warp == 6) {
+    // ---- L2 prefetch --------------------------------------------------------
+    // Up to prefetch_tiles weight tiles ahead of the ring, one 128-byte line
+    // per weight row and k-block, with prefetch.global.L2 (the load/store
+    // path, not the TMA unit, whose queue carries the ring's copies): HBM
+    // keeps streaming while the ring is full and the MMAs wait for a phase's
+    // activations, and the ring refills from L2 afterwards.
+    if (p.prefetch_tiles > 0) {
+      WeightCursor pf{-1, 0, 0, 0};
+      bool has = wc_next_phase(p, cta, G, pf);
+      long long issued = 0;
+      const unsigned long long t0 = global_timer_ns();
+      while (has) {
+        // lane 0 reads the producer's progress and the clock for the warp,
+        // so all lanes take the same path
+        const int done = __shfl_sync(0xffffffffu, *loaded, 0);
+        if (done == 0x7fffffff) break;
+        if (issued >= done + p.prefetch_tiles) {
+          const int late = __shfl_sync(0xffffffffu, global_timer_ns() - t0 > kWaitTimeoutNs, 0);
+          if (late) break;
+          __nanosleep(256);
+          continue;
+        }
+        const StreamPhase& P = p.ph[pf.ph];
+        const int tile = static_cast<int>(pf.u / P.kb), kk = static_cast<int>(pf.u % P.kb);
+        const char* w = static_cast<const char*>(pf.a ? P.w2 : P.w);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int r = tile * 128 + q * 32 + lane;
+          if (r < P.N) {
+            const char* line = w + (static_cast<size_t>(r) * P.K + kk * 64) * 2;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
+          }
+        }
+        ++issued;
+        has = wc_advance(p, cta, G, pf);
+      }
     }
   } else if (warp == 5) {
     // ---- MMA issuer -------------------------------------------------------
@@ -464,6 +577,7 @@ __global__ void __launch_bounds__(192, 1)
         phase_range(P, cta, G, lo, hi);
         if (lo >= hi) continue;
         if (!mbar_wait_ab(b_full, bph & 1, abort_word, p.err)) break;
+        stamp(p, 4 + 4 * ph + 1);
         ++bph;
         for (long long u = lo; u < hi && ok;) {
           const int tile = static_cast<int>(u / P.kb);
@@ -509,6 +623,7 @@ __global__ void __launch_bounds__(192, 1)
           ++seg;
           u += k_hi - k_lo;
         }
+        stamp(p, 4 + 4 * ph + 2);
       }
       // all MMAs of this thread complete before the tensor memory is freed
       umma_commit(drain);
@@ -520,12 +635,12 @@ __global__ void __launch_bounds__(192, 1)
     named_bar_sync(2, 160);
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (threadIdx.x == 0) stamp(p, 1);
     grid_dep_wait();
     // dependents may start once this CTA has waited for its inputs and holds
     // its tensor memory
     if (threadIdx.x == 0) grid_dep_launch();
     const int row = threadIdx.x;
-    const uint64_t pol_b = l2_policy_evict_last();
     int seg = 0, bph = 0;
     bool dead = false;
     for (int ph = 0; ph < p.nphases && !dead; ++ph) {
@@ -539,28 +654,35 @@ __global__ void __launch_bounds__(192, 1)
           dead = true;
           break;
         }
-        fence_proxy_async_global();
+        if (threadIdx.x == 0) {
+          stamp(p, 4 + 4 * ph);
+          *open_ph = ph;
+        }
       }
       if (P.kind == SK_EMBED || P.kind == SK_FINAL) {
         const int n = P.kind == SK_EMBED ? p.rows : p.final_rows;
         if (cta < n) {
           if (P.kind == SK_EMBED) embed_row(p, cta, red);
           else final_row(p, cta, red);
-          fence_proxy_async_global();
-          __threadfence();
           named_bar_sync(1, 128);
           if (threadIdx.x == 0) red_release_add(p.sync + ph, 1);
         }
         continue;
       }
       // ---- GEMM phase ----
-      if (P.norm_src >= 0 && row < BN) {
-        // r = rsqrt(mean x^2 + eps) of each row, from the producing phase's
-        // per-tile sums (tile order: deterministic)
+      if (P.norm_src >= 0) {
+        // r = rsqrt(mean x^2 + eps) of each row from the producing phase's
+        // per-tile sums: all of them loaded at once (one round trip) into
+        // the exchange buffer, then summed in tile order (deterministic)
         const StreamPhase& S = p.ph[P.norm_src];
-        float s = 0.f;
-        for (int t = 0; t < S.tiles; ++t) s += S.ssq[t * 32 + row];
-        rms[row] = rsqrtf(s / P.norm_d + p.eps);
+        for (int idx = row; idx < S.tiles * BN; idx += 128)
+          xchg[idx] = __ldcg(S.ssq + (idx / BN) * 32 + idx % BN);
+        named_bar_sync(1, 128);
+        if (row < BN) {
+          float s = 0.f;
+          for (int t = 0; t < S.tiles; ++t) s += xchg[t * BN + row];
+          rms[row] = rsqrtf(s / P.norm_d + p.eps);
+        }
       }
       if (P.epi == SE_ROPE_KV) {
         const int half = p.dh / 2;
@@ -583,16 +705,39 @@ __global__ void __launch_bounds__(192, 1)
       long long lo, hi;
       phase_range(P, cta, G, lo, hi);
       if (lo >= hi) continue;
-      if (threadIdx.x == 0) {
-        // this CTA's activation k-blocks, one panel slot per unit
-        mbar_arrive_expect_tx(b_full, static_cast<uint32_t>(hi - lo) * C::PANEL_SLOT);
-        for (long long u = lo; u < hi; ++u)
-          tma_load_2d(panel + (u - lo) * C::PANEL_SLOT, &maps.m[P.map_b], b_full,
-                      static_cast<int>(u % P.kb) * 64, 0, pol_b);
+      {
+        // This CTA's activation k-blocks, one panel slot per unit, in the
+        // 128-byte-swizzled K-major layout the MMA reads (16-byte chunk j of
+        // row r at r * 128 + ((j ^ (r & 7)) * 16)); rows past the batch and
+        // k past K are zero.  Copied with cp.async by the 128 threads, not
+        // by TMA: the TMA unit of this SM is busy streaming weights, and a
+        // panel queued behind that stream would wait for it.
+        // thread t copies chunk t % 8 of rows t / 8 (+ 16 for 32-row tiles)
+        // of every slot
+        const bf16* x = static_cast<const bf16*>(P.x);
+        const int j = row & 7, r0 = row >> 3;
+        const int n = static_cast<int>(hi - lo);
+        int kk = static_cast<int>(lo % P.kb);
+        for (int sl = 0; sl < n; ++sl) {
+          const int k = kk * 64 + j * 8;
+#pragma unroll
+          for (int r = r0; r < BN; r += 16) {
+            const bool in = r < p.rows && k < P.K;
+            const bf16* src = x + (in ? static_cast<size_t>(r) * P.ldx + k : 0);
+            cp_async_16(panel + sl * C::PANEL_SLOT + r * 128 + ((j ^ (r & 7)) * 16), src,
+                        in ? 16 : 0);
+          }
+          if (++kk == P.kb) kk = 0;
+        }
+        cp_async_wait_all();
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (threadIdx.x == 0) mbar_arrive(b_full);
       }
       ++bph;
       const long long U = static_cast<long long>(P.tiles) * P.kb;
       const int Gp = phase_ctas(P, G);
+      int fin[2], nfin = 0;   // at most the first and the last segment are partial
       for (long long u = lo; u < hi;) {
         const int tile = static_cast<int>(u / P.kb);
         const int k_lo = static_cast<int>(u - static_cast<long long>(tile) * P.kb);
@@ -620,9 +765,17 @@ __global__ void __launch_bounds__(192, 1)
         }
         const int c_first = cta_of_unit(static_cast<long long>(tile) * P.kb, U, Gp);
         const int c_last = cta_of_unit(static_cast<long long>(tile + 1) * P.kb - 1, U, Gp);
-        bool finisher = true;
-        if (c_first != c_last) {
-          // partial tile: to this CTA's slot, then the last contributor sums
+        if (c_first == c_last) {
+          // the whole tile is this CTA's: finish and publish it now
+          float old[BN];
+          if (P.epi == SE_ADD) load_resid<BN>(p, P, tile, old);
+          finish_tile<BN>(p, P, tile, v, v2, old, rms, xchg, cosT, sinT, slot_s, warp, lane);
+          named_bar_sync(1, 128);
+          if (threadIdx.x == 0) red_release_add(p.sync + ph, 1);
+        } else {
+          // partial tile: to this CTA's slot, published by thread 0's release
+          // after the barrier; the last arrival (acquire) finishes the tile,
+          // but only after this CTA's other partials are out too
           const int slot = (u == lo) ? 0 : 1;
           float* wsp = p.ws + (static_cast<size_t>(cta) * 2 + slot) * (128 * 64);
 #pragma unroll
@@ -630,65 +783,77 @@ __global__ void __launch_bounds__(192, 1)
             wsp[j * 128 + row] = v[j];
             if (P.dual) wsp[(BN + j) * 128 + row] = v2[j];
           }
-          __threadfence();
           named_bar_sync(1, 128);
           if (threadIdx.x == 0) {
-            const int old = atomicAdd(P.counters + tile, 1);
+            if (ph < 4) stamp(p, 24 + 4 * ph + (u == lo ? 0 : 2));
+            const int old = atom_add_acq_rel(P.counters + tile, 1);
             bcast[1] = (old == c_last - c_first) ? 1 : 0;
+            if (ph < 4) stamp(p, 24 + 4 * ph + (u == lo ? 1 : 3));
           }
           named_bar_sync(1, 128);
-          finisher = bcast[1] != 0;
-          if (finisher) {
-            // every contributor has arrived: the count can go back to zero
-            if (threadIdx.x == 0) P.counters[tile] = 0;
-            __threadfence();
-#pragma unroll
-            for (int j = 0; j < BN; ++j) v[j] = v2[j] = 0.f;
-            // contributors in CTA order, UNR partials' loads in flight
-            constexpr int UNR = BN == 16 ? 4 : 2;
-            for (int c = c_first; c <= c_last; c += UNR) {
-              float t[UNR][BN], t2[UNR][BN];
-#pragma unroll
-              for (int q = 0; q < UNR; ++q) {
-                if (c + q > c_last) break;
-                const int cq = c + q;
-                const int cs = unit_lo(cq, U, Gp) >= static_cast<long long>(tile) * P.kb ? 0 : 1;
-                const float* src = p.ws + (static_cast<size_t>(cq) * 2 + cs) * (128 * 64) + row;
-#pragma unroll
-                for (int j = 0; j < BN; ++j) {
-                  t[q][j] = __ldcg(src + j * 128);
-                  t2[q][j] = P.dual ? __ldcg(src + (BN + j) * 128) : 0.f;
-                }
-              }
-#pragma unroll
-              for (int q = 0; q < UNR; ++q) {
-                if (c + q > c_last) break;
-#pragma unroll
-                for (int j = 0; j < BN; ++j) {
-                  v[j] += t[q][j];
-                  v2[j] += t2[q][j];
-                }
-              }
-            }
-          }
-        }
-        if (finisher) {
-          finish_tile<BN>(p, P, tile, v, v2, rms, xchg, cosT, sinT, slot_s, warp, lane);
-          fence_proxy_async_global();
-          __threadfence();
-          named_bar_sync(1, 128);
-          if (threadIdx.x == 0) red_release_add(p.sync + ph, 1);
+          if (bcast[1]) fin[nfin++] = tile;
         }
         ++seg;
         u += k_hi - k_lo;
       }
+      // Tiles this CTA arrived last at: sum every contributor's partial in
+      // CTA order (deterministic), finish and publish.  Deferred so that a
+      // finisher never holds back its own next partial, which another
+      // tile's finisher may be waiting for.
+      for (int f = 0; f < nfin && !dead; ++f) {
+        const int tile = fin[f];
+        const int c_first = cta_of_unit(static_cast<long long>(tile) * P.kb, U, Gp);
+        const int c_last = cta_of_unit(static_cast<long long>(tile + 1) * P.kb - 1, U, Gp);
+        if (threadIdx.x == 0) {
+          P.counters[tile] = 0;   // every contributor has arrived
+          if (ph < 4) stamp(p, 40 + 4 * ph);
+        }
+        float v[BN], v2[BN], old[BN];
+        if (P.epi == SE_ADD) load_resid<BN>(p, P, tile, old);
+#pragma unroll
+        for (int j = 0; j < BN; ++j) v[j] = v2[j] = 0.f;
+        // contributors in CTA order, UNR partials' loads in flight
+        constexpr int UNR = BN == 16 ? 4 : 2;
+        for (int c = c_first; c <= c_last; c += UNR) {
+          float t[UNR][BN], t2[UNR][BN];
+#pragma unroll
+          for (int q = 0; q < UNR; ++q) {
+            if (c + q > c_last) break;
+            const int cq = c + q;
+            const int cs = unit_lo(cq, U, Gp) >= static_cast<long long>(tile) * P.kb ? 0 : 1;
+            const float* src = p.ws + (static_cast<size_t>(cq) * 2 + cs) * (128 * 64) + row;
+#pragma unroll
+            for (int j = 0; j < BN; ++j) {
+              t[q][j] = __ldcg(src + j * 128);
+              t2[q][j] = P.dual ? __ldcg(src + (BN + j) * 128) : 0.f;
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < UNR; ++q) {
+            if (c + q > c_last) break;
+#pragma unroll
+            for (int j = 0; j < BN; ++j) {
+              v[j] += t[q][j];
+              v2[j] += t2[q][j];
+            }
+          }
+        }
+        if (threadIdx.x == 0 && ph < 4) stamp(p, 40 + 4 * ph + 1);
+        finish_tile<BN>(p, P, tile, v, v2, old, rms, xchg, cosT, sinT, slot_s, warp, lane);
+        if (threadIdx.x == 0 && ph < 4) stamp(p, 40 + 4 * ph + 2);
+        named_bar_sync(1, 128);
+        if (threadIdx.x == 0) {
+          red_release_add(p.sync + ph, 1);
+          if (ph < 4) stamp(p, 40 + 4 * ph + 3);
+        }
+      }
+      if (threadIdx.x == 0) stamp(p, 4 + 4 * ph + 3);
     }
-    // the last activation panel this CTA requested has landed before exit
-    if (threadIdx.x == 0 && bph > 0) mbar_wait(b_full, (bph - 1) & 1, p.err);
     tc_fence_before();
   }
 
   __syncthreads();
+  if (threadIdx.x == 0) stamp(p, 60);
   if (warp == 5) {
     tc_fence_after();
     tmem_dealloc(*tmem_slot, C::TMEM_COLS);
@@ -739,8 +904,8 @@ cudaError_t launch_stream(const StreamMaps& maps, const StreamParams& p, int gri
                           cudaStream_t s) {
   if (p.rows < 1 || p.rows > 32 || grid < 1) return cudaErrorInvalidValue;
   if (p.rows <= 16)
-    return launch_pdl(stream_kernel<16>, dim3(grid), dim3(192), SCfg<16>::SMEM, s, maps, p);
-  return launch_pdl(stream_kernel<32>, dim3(grid), dim3(192), SCfg<32>::SMEM, s, maps, p);
+    return launch_pdl(stream_kernel<16>, dim3(grid), dim3(224), SCfg<16>::SMEM, s, maps, p);
+  return launch_pdl(stream_kernel<32>, dim3(grid), dim3(224), SCfg<32>::SMEM, s, maps, p);
 }
 
 }  // namespace pe

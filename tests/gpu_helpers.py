@@ -155,7 +155,8 @@ def make_drafter(shape, weights, max_tokens, max_reqs):
     return B.Drafter(shape, weights, max_tokens, max_reqs)
 
 
-def full_parity(wl, tol, gains=None, requests=None, check_cache=True, strict_tokens=True):
+def full_parity(wl, tol, gains=None, requests=None, check_cache=True, strict_tokens=True,
+                configure=None):
     """Run one step on the GPU and the oracle; assert parity.  Returns both.
 
     strict_tokens (default): end-to-end tokens identical to the fp64
@@ -169,6 +170,8 @@ def full_parity(wl, tol, gains=None, requests=None, check_cache=True, strict_tok
     kc, vc = W.make_kv_cache(wl, inp)
     max_tokens = max(wl.T_out, wl.B * wl.K)
     dr = make_drafter(sh, w, max_tokens, wl.B)
+    if configure is not None:
+        configure(dr)      # e.g. select the small-batch streaming path
     st = DeviceStep(wl, inp, kc, vc)
     remember_host_caches(st, kc, vc)
     torch = torch_mod()
