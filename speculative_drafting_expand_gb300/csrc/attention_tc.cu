@@ -45,7 +45,11 @@ struct AttnTcParams {
   int split_keys;    // keys per split (multiple of 128)
   int max_splits;
   float* part;       // [B, Hkv, qtiles, max_splits, 128, dh + 2]
-  int* counters;     // [B, Hkv, qtiles]
+  int* counters;     // [2][B, Hkv, qtiles]: splits written, splits merged
+  // 1: every split CTA merges its own slice of the unit's rows once all the
+  // unit's splits are written (the grid is one wave, so they are all
+  // resident); 0: the last split to finish merges the whole unit
+  int parallel_merge;
 };
 
 // FP8: the pools hold e4m3 codes.  Their pages come by TMA into a two-stage
@@ -602,6 +606,85 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
         }
         __threadfence();
         named_bar_sync(1, C::SOFT);
+        if (p.parallel_merge) {
+          // Wait (bounded) until the unit's splits have all written their
+          // partials, then merge rows [q0, q1) of the unit's 128: the
+          // slice's (m, l) and columns of every split come into shared
+          // memory (the K/V stages, idle now) in one round of cp.async,
+          // and each thread combines one row's group of columns in split
+          // order (deterministic).
+          int* arrived = p.counters + unit;
+          int* merged = arrived + static_cast<size_t>(a.B) * a.Hkv * p.qtiles;
+          if (threadIdx.x == 64) {
+            atomicAdd(arrived, 1);
+            *flag = flag_wait_geq(arrived, nsplits, a.err) ? 1 : 0;
+          }
+          named_bar_sync(1, C::SOFT);
+          const int per = ((128 + nsplits - 1) / nsplits + 3) & ~3;   // rows, a multiple of 4
+          const int q0 = split * per, q1 = min(128, q0 + per);
+          if (*flag && q0 < q1) {
+            const float* base = p.part + unit * p.max_splits * stride;
+            float* stage = reinterpret_cast<float*>(smem + C::K_OFF);   // [split][col][per]
+            const int t = threadIdx.x - 64;
+            const int quads = per / 4;                                   // 16-byte row groups
+            const int items = nsplits * (DH + 2) * quads;
+            for (int it = t; it < items; it += C::SOFT) {
+              const int qd = it % quads, col = (it / quads) % (DH + 2), sp = it / (quads * (DH + 2));
+              const int q = q0 + qd * 4;
+              const float* src = base + sp * stride + col * 128 + q;
+              const uint32_t dst = smem_u32(stage + (sp * (DH + 2) + col) * per + qd * 4);
+              asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                           "r"(q < q1 ? 16 : 0)
+                           : "memory");
+            }
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            named_bar_sync(1, C::SOFT);
+            // thread -> (row slots rr, rr + 16, ..., group of DH / 16 columns)
+            constexpr int NCOL = DH / 16;
+            const int cg = t / 16;
+            for (int rr = t % 16; rr < per; rr += 16) {
+            const int q = q0 + rr;
+            const int mlr = q / p.G, mhl = q % p.G;
+            if (q < q1 && mlr < tile_rows) {
+              float Mx = -INFINITY;
+              for (int sp = 0; sp < nsplits; ++sp) {
+                const float ls = stage[(sp * (DH + 2) + DH + 1) * per + rr];
+                if (ls > 0.f) Mx = fmaxf(Mx, stage[(sp * (DH + 2) + DH) * per + rr]);
+              }
+              float acc[NCOL];
+#pragma unroll
+              for (int j = 0; j < NCOL; ++j) acc[j] = 0.f;
+              float Ls = 0.f;
+              for (int sp = 0; sp < nsplits; ++sp) {
+                const float ls = stage[(sp * (DH + 2) + DH + 1) * per + rr];
+                if (!(ls > 0.f)) continue;
+                const float w = exp2f(stage[(sp * (DH + 2) + DH) * per + rr] - Mx);
+                Ls += w * ls;
+#pragma unroll
+                for (int j = 0; j < NCOL; ++j)
+                  acc[j] += w * stage[(sp * (DH + 2) + cg * NCOL + j) * per + rr];
+              }
+              const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+              bf16* o2 = static_cast<bf16*>(a.out) +
+                         (static_cast<size_t>(row0 + tile_row0 + mlr) * a.Hq + g * p.G + mhl) * DH +
+                         cg * NCOL;
+#pragma unroll
+              for (int j = 0; j < NCOL; j += 2)
+                *reinterpret_cast<__nv_bfloat162*>(o2 + j) =
+                    __floats2bfloat162_rn(acc[j] * inv, acc[j + 1] * inv);
+            }
+            }
+          }
+          // the last split to finish its slice leaves both counts zero
+          named_bar_sync(1, C::SOFT);
+          if (threadIdx.x == 64 && *flag) {
+            const int old = atomicAdd(merged, 1);
+            if (old == nsplits - 1) {
+              *arrived = 0;
+              *merged = 0;
+            }
+          }
+        } else {
         if (threadIdx.x == 64) {
           const int old = atomicAdd(p.counters + unit, 1);
           *flag = (old == nsplits - 1) ? 1 : 0;
@@ -659,6 +742,7 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
           }
           if (threadIdx.x == 64) p.counters[unit] = 0;
         }
+        }
       }
     }
   }
@@ -696,8 +780,11 @@ static AttnPlan plan_attention(const AttnArgs& a, int max_rows_per_req, int sm_c
   // thread-block cluster through distributed shared memory by a sixth of
   // the step (8-CTA clusters of one-CTA-per-SM kernels leave SMs idle), and
   // tied with it at batch 1.
+  // A few units (batch 1): as many splits as keep the grid one wave, two
+  // chunks or more each; their merge is then parallel (every split merges
+  // a slice of the rows, parallel_merge below).
   constexpr int kMaxCps = 32;
-  int cps = pairs * 16 <= sm_count ? (chunks_max + 15) / 16
+  int cps = pairs * 16 <= sm_count ? (chunks_max * static_cast<int>(pairs) + sm_count - 1) / sm_count
             : pairs < sm_count     ? (chunks_max + 7) / 8
                                    : (chunks_max + want - 1) / want;
   cps = std::max(2, std::min(kMaxCps, cps));
@@ -713,7 +800,7 @@ size_t attention_tc_partial_floats(const AttnArgs& a, int max_rows_per_req, int 
 
 size_t attention_tc_counters(const AttnArgs& a, int max_rows_per_req, int sm_count) {
   const AttnPlan pl = plan_attention(a, max_rows_per_req, sm_count);
-  return static_cast<size_t>(a.B) * a.Hkv * pl.qtiles;
+  return 2 * static_cast<size_t>(a.B) * a.Hkv * pl.qtiles;   // splits written, merged
 }
 
 // Tensor map of an fp8 pool viewed as [rows, cols] bytes (rows = blocks x
@@ -771,10 +858,14 @@ cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const
   p.max_splits = pl.max_splits;
   p.part = part;
   p.counters = counters;
+  // every split CTA resident at once (one wave of one CTA per SM), at most
+  // 32 splits: the splits merge their unit in parallel
+  const long long ctas = static_cast<long long>(pl.max_splits) * a.Hkv * pl.qtiles * a.B;
+  p.parallel_merge = (ctas <= sm_count && pl.max_splits <= 32) ? 1 : 0;
   if (pl.split_keys / 16 > AttnCfg<64>::BT_ENTRIES || pl.split_keys / 16 > AttnCfg<128>::BT_ENTRIES)
     return cudaErrorInvalidValue;
   const size_t need = static_cast<size_t>(a.B) * a.Hkv * pl.qtiles * pl.max_splits * 128 * (a.dh + 2);
-  if (need > part_floats || static_cast<size_t>(a.B) * a.Hkv * pl.qtiles > n_counters)
+  if (need > part_floats || 2 * static_cast<size_t>(a.B) * a.Hkv * pl.qtiles > n_counters)
     return cudaErrorInvalidValue;
   dim3 grid(pl.max_splits, a.Hkv * pl.qtiles, a.B);
   if (a.kv_fp8) {
