@@ -125,7 +125,14 @@ typedef struct {
 
 /* The expanded drafting batch.  Device pointers are caller-owned buffers
  * sized for T' = T + B (K - 1) rows; pe_expand_batch fills them and records
- * B, K, T and T_out (host fields) for pe_draft_forward.
+ * B, K, T and T_out (host fields) and the target_hidden pointer it was
+ * given, for pe_draft_forward.  When target_hidden is recorded (not NULL),
+ * pe_draft_forward projects the T target rows through fc and gives every
+ * MASK row the fc of h_shared computed once at pe_create, instead of
+ * projecting all T' rows of `hidden` (the same values: MASK rows carry
+ * h_shared); that buffer must then still hold the same data when
+ * pe_draft_forward runs.  Set it to NULL to make pe_draft_forward project
+ * `hidden`.
  * Layout of request r: rows cu_out[r] .. cu_out[r] + n_r - 1 come from the
  * target window (row j carries the target hidden state of window row j and
  * sits one position after it), rows cu_out[r] + n_r .. + n_r + K - 2 are the
@@ -142,6 +149,7 @@ typedef struct {
   int32_t* seq_lens;     /* [B] drafter sequence length after this step */
   void* hidden;          /* [T', hidden3] expanded target hidden states */
   int32_t B, K, T, T_out;  /* host fields written by pe_expand_batch */
+  const void* target_hidden;  /* [T, hidden3] the target rows (see above), or NULL */
 } pe_expanded;
 
 typedef struct pe_handle pe_handle;
@@ -281,6 +289,24 @@ pe_status pe_set_phase_events(pe_handle* h, void* const* events, int32_t n);
  * phase boundary waits for the slowest tile's split-K finisher, a chain of
  * dependent L2 round trips of about 1 us each. */
 pe_status pe_set_small_batch_stream(pe_handle* h, int32_t enable);
+
+/* Epilogue fusions of the per-projection path (bf16), a bit mask; the
+ * default is PE_FUSE_NORM:
+ *   PE_FUSE_ROPE_KV  at most 32 expanded rows: rotate-half RoPE of q and k
+ *                    and the paged K/V write in the QKV projection's
+ *                    epilogue (no separate kernel and no round trip of the
+ *                    qkv activations through memory);
+ *   PE_FUSE_NORM     at most 32 expanded rows: the RMSNorms before gate/up
+ *                    and before the next layer's QKV folded into the
+ *                    projections (the residual add writes x * g and sums of
+ *                    squares, the next projection scales its rows by
+ *                    rsqrt(mean x^2 + eps)), instead of a norm kernel;
+ * 0 selects the separate kernels.  Measured on the GPT-OSS-20B-shaped
+ * batch-1 step (us per step): none 526, PE_FUSE_ROPE_KV 535,
+ * PE_FUSE_NORM 516, both 521 -- the fused RoPE epilogue loses what the
+ * removed kernel costs, hence the default. */
+enum { PE_FUSE_ROPE_KV = 1, PE_FUSE_NORM = 2, PE_FUSE_ALL = 3 };
+pe_status pe_set_fusions(pe_handle* h, int32_t mask);
 
 /* Tuning of the small-batch streaming kernel.  tiles: how many 16 KB
  * weight tiles each CTA brings into L2 ahead of its shared-memory ring

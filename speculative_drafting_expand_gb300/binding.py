@@ -34,6 +34,7 @@ PE_MASK_ADDITIVE_BF16 = 1
 EXPORTED = ("pe_create", "pe_destroy", "pe_expand_batch", "pe_draft_forward",
             "pe_lmhead_argmax", "pe_get_device_error", "pe_set_trace", "pe_set_phase_events",
             "pe_set_small_batch_stream", "pe_set_stream_prefetch", "pe_set_stream_timeline",
+            "pe_set_fusions",
             "pe_linear",
             "pe_get_launch_count", "pe_check_bounded_wait", "pe_linear_static",
             "pe_linear_static_error",
@@ -65,7 +66,8 @@ class pe_weights(ctypes.Structure):
 class pe_expanded(ctypes.Structure):
     _fields_ = [(n, _vp) for n in ("ids", "pos", "slot", "is_rejected", "is_masked",
                                    "new_idx", "hidden_map", "cu_out", "seq_lens", "hidden")] + \
-               [("B", _i32), ("K", _i32), ("T", _i32), ("T_out", _i32)]
+               [("B", _i32), ("K", _i32), ("T", _i32), ("T_out", _i32),
+                ("target_hidden", _vp)]
 
 
 class PeError(RuntimeError):
@@ -96,6 +98,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pe_set_phase_events.argtypes = [_vp, P(_vp), _i32]
     lib.pe_set_small_batch_stream.argtypes = [_vp, _i32]
     lib.pe_set_stream_timeline.argtypes = [_vp, _vp]
+    lib.pe_set_fusions.argtypes = [_vp, _i32]
     lib.pe_set_stream_prefetch.argtypes = [_vp, _i32, _i32]
     lib.pe_linear_static_error.argtypes = [P(_i32), _vp]
     lib.pe_set_kv_cache_fp8.argtypes = [_vp, P(ctypes.c_float), P(ctypes.c_float)]
@@ -242,7 +245,7 @@ class Expanded:
         self.struct = pe_expanded(*(ptr(getattr(self, f)) for f in
                                     ("ids", "pos", "slot", "is_rejected", "is_masked",
                                      "new_idx", "hidden_map", "cu_out", "seq_lens", "hidden")),
-                                  0, 0, 0, 0)
+                                  0, 0, 0, 0, None)
 
 
 def pe_expand_batch(dr: Drafter, K: int, target_ids, target_pos, cu_in, num_accepted,
@@ -290,6 +293,15 @@ def pe_check_bounded_wait(dr: Drafter, out, stream=None) -> None:
 
 def pe_set_small_batch_stream(dr: Drafter, enable: bool) -> None:
     _check("pe_set_small_batch_stream", lib().pe_set_small_batch_stream(dr.handle, int(enable)))
+
+
+PE_FUSE_ROPE_KV = 1
+PE_FUSE_NORM = 2
+PE_FUSE_ALL = 3
+
+
+def pe_set_fusions(dr: Drafter, mask: int) -> None:
+    _check("pe_set_fusions", lib().pe_set_fusions(dr.handle, int(mask)))
 
 
 def pe_set_stream_prefetch(dr: Drafter, tiles: int, boundary_tiles: int = -1) -> None:

@@ -59,6 +59,13 @@ struct pe_handle {
   void* act = nullptr;      // [max_tokens, F]
   unsigned long long* keys = nullptr;  // [max_tokens] argmax keys (kept zero)
   double* inv_freq64 = nullptr;        // [dh / 2]
+  float* rope_tab = nullptr;           // [max_tokens, dh] cos / sin of each row's angles
+  int fusions = PE_FUSE_NORM;          // epilogue fusions of the per-projection path
+  float* fc_hs = nullptr;              // [d] fc(h_shared), the projected hidden of every MASK row
+  int32_t* fc_map = nullptr;           // [max_tokens] target row -> compact row
+  uint8_t* masked_c = nullptr;         // [max_tokens] MASK flag of every compact row
+  float* ssq_post = nullptr;           // [ceil(d / 32), max_tokens] folded-norm sums
+  float* ssq_in = nullptr;
   float* gemm_partials = nullptr;
   size_t gemm_partial_floats = 0;
   int* tile_counters = nullptr;
@@ -98,6 +105,7 @@ struct pe_handle {
 
   std::map<std::tuple<const void*, uint64_t, uint64_t, uint64_t, uint32_t>, CUtensorMap> maps;
   std::map<std::pair<const void*, uint64_t>, CUtensorMap> maps_u8;  // fp8 pools
+  std::map<std::pair<const void*, uint64_t>, CUtensorMap> maps_qkv;  // interleaved QKV weights
   std::vector<void*> allocations;
 };
 
@@ -140,6 +148,17 @@ const CUtensorMap* get_map_u8(pe_handle* h, const void* ptr, uint64_t rows) {
   CUtensorMap m;
   if (!tensor_map_2d_u8(&m, ptr, rows, h->desc.head_dim, 16)) return nullptr;
   return &h->maps_u8.emplace(key, m).first->second;
+}
+
+const CUtensorMap* get_map_qkv(pe_handle* h, const void* ptr, uint64_t K) {
+  auto key = std::make_pair(ptr, K);
+  auto it = h->maps_qkv.find(key);
+  if (it != h->maps_qkv.end()) return &it->second;
+  CUtensorMap m;
+  const pe_model_desc& d = h->desc;
+  if (!tensor_map_qkv_interleaved(&m, ptr, d.n_heads + 2 * d.n_kv_heads, d.head_dim, K))
+    return nullptr;
+  return &h->maps_qkv.emplace(key, m).first->second;
 }
 
 TcGemmWorkspace tc_ws(pe_handle* h) {
@@ -267,6 +286,12 @@ pe_status pe_create(const pe_model_desc* desc, const pe_weights* weights, int32_
   if (e == cudaSuccess) e = dev_alloc(h, &h->cu_live, static_cast<size_t>(max_reqs) + 1);
   if (e == cudaSuccess) e = dev_alloc(h, &h->n_live, 1);
   if (e == cudaSuccess) e = dev_alloc(h, &h->inv_freq64, d.head_dim / 2);
+  if (e == cudaSuccess) e = dev_alloc(h, &h->rope_tab, T * d.head_dim);
+  if (e == cudaSuccess) e = dev_alloc(h, &h->fc_hs, d.d);
+  if (e == cudaSuccess) e = dev_alloc(h, &h->fc_map, T);
+  if (e == cudaSuccess) e = dev_alloc(h, &h->masked_c, T);
+  if (e == cudaSuccess) e = dev_alloc(h, &h->ssq_post, T * ((d.d + 31) / 32));
+  if (e == cudaSuccess) e = dev_alloc(h, &h->ssq_in, T * ((d.d + 31) / 32));
   if (e == cudaSuccess) {
     std::vector<double> inv(d.head_dim / 2);
     for (int i = 0; i < d.head_dim / 2; ++i)
@@ -294,6 +319,19 @@ pe_status pe_create(const pe_model_desc* desc, const pe_weights* weights, int32_
     h->max_tiles = ((widest + 127) / 128) * ((max_tokens + 15) / 16);
     if (e == cudaSuccess) e = dev_alloc(h, &h->tile_counters, h->max_tiles);
     if (e == cudaSuccess) e = dev_alloc(h, &h->done_counter, 1);
+  }
+  if (e == cudaSuccess) {
+    // fc(h_shared): every MASK row carries h_shared, so its projection is a
+    // constant of the weights, computed once here
+    EpiArgs ep = epi_none();
+    ep.kind = EPI_STORE;
+    ep.M = 1;
+    ep.N = d.d;
+    ep.out = h->fc_hs;
+    ep.ldo = d.d;
+    ep.out_f32 = 1;
+    e = linear(h, w.h_shared, d.hidden3, w.fc, nullptr, 1, d.d, d.hidden3, ep, nullptr);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);
   }
   if (e != cudaSuccess) {
     pe_destroy(h);
@@ -324,6 +362,12 @@ pe_status pe_set_kv_cache_fp8(pe_handle* h, const float* k_scales, const float* 
   h->k_scales = ks;
   h->v_scales = vs;
   h->kv_fp8 = true;
+  return PE_OK;
+}
+
+pe_status pe_set_fusions(pe_handle* h, int32_t mask) {
+  if (!h || (mask & ~PE_FUSE_ALL)) return PE_ERR_INVALID_ARGUMENT;
+  h->fusions = mask;
   return PE_OK;
 }
 
@@ -433,6 +477,7 @@ pe_status pe_expand_batch(pe_handle* h, int32_t B, int32_t K, int32_t T, const i
   out->K = K;
   out->T = T;
   out->T_out = a.T_out;
+  out->target_hidden = target_hidden;
   return PE_OK;
 }
 
@@ -525,6 +570,13 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     ca.cu_live = h->cu_live;
     ca.new_c = h->new_c;
     ca.n_live = h->n_live;
+    if (ex->target_hidden) {
+      ca.T = ex->T;
+      ca.hidden_map = ex->hidden_map;
+      ca.is_masked = ex->is_masked;
+      ca.fc_map = h->fc_map;
+      ca.masked_c = h->masked_c;
+    }
     if ((e = counted(h, launch_compact_rows(ca, s)))) return PE_ERR_CUDA;
     live = h->n_live;
     ids_l = h->ids_c;
@@ -769,17 +821,28 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
   }
 
   // fc: projected target hidden state -> residual stream (fp32), live rows
-  // to their compact rows
+  // to their compact rows.  With the target rows recorded, fc runs on those
+  // T rows only (through the hidden map) and the MASK rows take fc(h_shared)
+  // in the layer-0 input kernel below.
+  const bool fc_once = ex->target_hidden != nullptr;
   EpiArgs ep = epi_none();
   ep.kind = EPI_STORE;
-  ep.M = rows;
   ep.N = d.d;
   ep.out = h->resid;
   ep.ldo = d.d;
   ep.out_f32 = 1;
-  ep.row_map = compact ? h->row_map : nullptr;
-  if ((e = linear(h, ex->hidden, d.hidden3, h->w.fc, nullptr, rows, d.d, d.hidden3, ep, s)))
-    return PE_ERR_CUDA;
+  if (fc_once) {
+    ep.M = ex->T;
+    ep.row_map = compact ? h->fc_map : ex->hidden_map;
+    if ((e = linear(h, ex->target_hidden, d.hidden3, h->w.fc, nullptr, ex->T, d.d, d.hidden3, ep,
+                    s)))
+      return PE_ERR_CUDA;
+  } else {
+    ep.M = rows;
+    ep.row_map = compact ? h->row_map : nullptr;
+    if ((e = linear(h, ex->hidden, d.hidden3, h->w.fc, nullptr, rows, d.d, d.hidden3, ep, s)))
+      return PE_ERR_CUDA;
+  }
   // layer-0 input: [RMSNorm_e(emb[id]) ; RMSNorm_h(fc h)]
   EmbedConcatArgs ec = {};
   ec.rows = rows;
@@ -794,12 +857,50 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
   ec.eps = d.rms_eps;
   ec.x = h->x_in;
   ec.err = h->err;
+  if (fc_once) {
+    ec.masked = compact ? h->masked_c : ex->is_masked;
+    ec.fc_hs = h->fc_hs;
+    ec.h_w = h->resid;
+  }
+  // RoPE and the KV write in the QKV projection's epilogue (bf16): the
+  // rotary table of every row comes with the layer-0 input
+  // (one token tile of at most 32 rows whose rotary table fits the tile's
+  // staged [tile][64] floats; larger batches keep the separate kernel)
+  const bool fuse_rope = dt == PE_DTYPE_BF16 && (h->fusions & PE_FUSE_ROPE_KV) &&
+                         (qkv_rows % 128) == 0 && rows <= 32 && live == nullptr &&
+                         rows * d.head_dim <= tc_pick_bn(rows, false) * 64;
+  if (fuse_rope) {
+    ec.pos = pos_l;
+    ec.inv_freq64 = h->inv_freq64;
+    ec.rope_tab = h->rope_tab;
+    ec.dh = d.head_dim;
+  }
   if ((e = counted(h, launch_embed_concat(dt, ec, s)))) return PE_ERR_CUDA;
+  // RMSNorm folded into the projections (bf16, one token tile of at most 32
+  // rows): O and down write x g_next and per-group sums of squares, the
+  // next projection scales its rows by r
+  const bool fuse_norm = dt == PE_DTYPE_BF16 && (h->fusions & PE_FUSE_NORM) && rows <= 32 &&
+                         live == nullptr;
+  const int ssq_groups = (d.d + 31) / 32;
+  auto fold_out = [&](EpiArgs& ep2, const void* g, void* xg, float* ssq) {
+    ep2.g_next = g;
+    ep2.xg = xg;
+    ep2.ldxg = d.d;
+    ep2.ssq = ssq;
+    ep2.ssq_ld = h->max_tokens;
+  };
+  auto fold_in = [&](EpiArgs& ep2, const float* ssq) {
+    ep2.rs_ssq = ssq;
+    ep2.rs_groups = ssq_groups;
+    ep2.rs_ld = h->max_tokens;
+    ep2.rs_d = static_cast<float>(d.d);
+    ep2.rs_eps = d.rms_eps;
+  };
 
   for (int l = 0; l < d.n_layers; ++l) {
     const pe_layer_weights& L = h->layers[l];
     const int d_in = l == 0 ? 2 * d.d : d.d;
-    if (l > 0) {
+    if (l > 0 && !fuse_norm) {
       RmsNormArgs rn = {};
       rn.rows = rows;
       rn.d = d.d;
@@ -812,40 +913,75 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
       rn.live = live;
       if ((e = counted(h, launch_rmsnorm(dt, rn, s)))) return PE_ERR_CUDA;
     }
-    // QKV projection
-    ep = epi_none();
-    ep.kind = EPI_STORE;
-    ep.M = rows;
-    ep.N = qkv_rows;
-    ep.out = h->qkv;
-    ep.ldo = qkv_rows;
-    ep.out_f32 = dt == PE_DTYPE_F32 ? 1 : 0;
-    ep.m_live = live;
-    if ((e = linear(h, h->x_in, d_in, L.qkv, nullptr, rows, qkv_rows, d_in, ep, s)))
-      return PE_ERR_CUDA;
-    // RoPE + paged KV write (slot -1: nothing written)
-    RopeKvArgs rk = {};
-    rk.rows = rows;
-    rk.Hq = d.n_heads;
-    rk.Hkv = d.n_kv_heads;
-    rk.dh = d.head_dim;
-    rk.num_blocks = num_blocks;
-    rk.qkv = h->qkv;
-    rk.pos = pos_l;
-    rk.slot = slot_l;
-    rk.live = live;
-    rk.inv_freq = nullptr;
-    rk.inv_freq64 = h->inv_freq64;
-    rk.q_out = h->q;
-    rk.k_cache = k_cache[l];
-    rk.v_cache = v_cache[l];
-    rk.err = h->err;
-    if (h->kv_fp8) {
-      rk.kv_fp8 = 1;
-      rk.k_inv_scale = 1.f / h->k_scales[l];
-      rk.v_inv_scale = 1.f / h->v_scales[l];
+    if (fuse_rope) {
+      // QKV projection, rotate-half RoPE of q and k, q stored, k and v to
+      // the paged cache (slot -1: nothing written), all in the epilogue
+      ep = epi_none();
+      ep.kind = EPI_ROPE_KV;
+      ep.M = rows;
+      ep.N = qkv_rows;
+      ep.m_live = live;
+      ep.q_out = h->q;
+      ep.k_cache = k_cache[l];
+      ep.v_cache = v_cache[l];
+      ep.slot = slot_l;
+      ep.rope_tab = h->rope_tab;
+      ep.Hq = d.n_heads;
+      ep.Hkv = d.n_kv_heads;
+      ep.dh = d.head_dim;
+      ep.num_blocks = num_blocks;
+      ep.err = h->err;
+      if (l > 0 && fuse_norm) fold_in(ep, h->ssq_in);
+      if (h->kv_fp8) {
+        ep.kv_fp8 = 1;
+        ep.k_inv_scale = 1.f / h->k_scales[l];
+        ep.v_inv_scale = 1.f / h->v_scales[l];
+      }
+      const CUtensorMap* wa = get_map_qkv(h, L.qkv, d_in);
+      const CUtensorMap* xb =
+          get_map(h, h->x_in, rows, d_in, d_in,
+                  tc_b_box_rows(rows, qkv_rows, h->sm_count, false, live != nullptr));
+      if (!wa || !xb) return PE_ERR_INVALID_ARGUMENT;
+      if ((e = counted(h, launch_gemm_tc_maps(*wa, *wa, *xb, false, rows, qkv_rows, d_in, ep,
+                                              tc_ws(h), h->err, s))))
+        return PE_ERR_CUDA;
+    } else {
+      // QKV projection
+      ep = epi_none();
+      ep.kind = EPI_STORE;
+      ep.M = rows;
+      ep.N = qkv_rows;
+      ep.out = h->qkv;
+      ep.ldo = qkv_rows;
+      ep.out_f32 = dt == PE_DTYPE_F32 ? 1 : 0;
+      ep.m_live = live;
+      if (l > 0 && fuse_norm) fold_in(ep, h->ssq_in);
+      if ((e = linear(h, h->x_in, d_in, L.qkv, nullptr, rows, qkv_rows, d_in, ep, s)))
+        return PE_ERR_CUDA;
+      // RoPE + paged KV write (slot -1: nothing written)
+      RopeKvArgs rk = {};
+      rk.rows = rows;
+      rk.Hq = d.n_heads;
+      rk.Hkv = d.n_kv_heads;
+      rk.dh = d.head_dim;
+      rk.num_blocks = num_blocks;
+      rk.qkv = h->qkv;
+      rk.pos = pos_l;
+      rk.slot = slot_l;
+      rk.live = live;
+      rk.inv_freq = nullptr;
+      rk.inv_freq64 = h->inv_freq64;
+      rk.q_out = h->q;
+      rk.k_cache = k_cache[l];
+      rk.v_cache = v_cache[l];
+      rk.err = h->err;
+      if (h->kv_fp8) {
+        rk.kv_fp8 = 1;
+        rk.k_inv_scale = 1.f / h->k_scales[l];
+        rk.v_inv_scale = 1.f / h->v_scales[l];
+      }
+      if ((e = counted(h, launch_rope_kv(dt, rk, s)))) return PE_ERR_CUDA;
     }
-    if ((e = counted(h, launch_rope_kv(dt, rk, s)))) return PE_ERR_CUDA;
     // paged causal attention
     if (const pe_status st = attention(l); st != PE_OK) return st;
     // O projection + residual
@@ -856,19 +992,22 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     ep.resid = h->resid;
     ep.ldr = d.d;
     ep.m_live = live;
+    if (fuse_norm) fold_out(ep, L.norm_post, h->xn, h->ssq_post);
     if ((e = linear(h, h->attn, qd, L.o, nullptr, rows, d.d, qd, ep, s))) return PE_ERR_CUDA;
     // MLP
-    RmsNormArgs rn = {};
-    rn.rows = rows;
-    rn.d = d.d;
-    rn.x = h->resid;
-    rn.rows_in = rows;
-    rn.g = L.norm_post;
-    rn.eps = d.rms_eps;
-    rn.y = h->xn;
-    rn.err = h->err;
-    rn.live = live;
-    if ((e = counted(h, launch_rmsnorm(dt, rn, s)))) return PE_ERR_CUDA;
+    if (!fuse_norm) {
+      RmsNormArgs rn = {};
+      rn.rows = rows;
+      rn.d = d.d;
+      rn.x = h->resid;
+      rn.rows_in = rows;
+      rn.g = L.norm_post;
+      rn.eps = d.rms_eps;
+      rn.y = h->xn;
+      rn.err = h->err;
+      rn.live = live;
+      if ((e = counted(h, launch_rmsnorm(dt, rn, s)))) return PE_ERR_CUDA;
+    }
     ep = epi_none();
     ep.kind = EPI_SILU_MUL;
     ep.M = rows;
@@ -877,6 +1016,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     ep.ldo = d.ffn;
     ep.out_f32 = dt == PE_DTYPE_F32 ? 1 : 0;
     ep.m_live = live;
+    if (fuse_norm) fold_in(ep, h->ssq_post);
     if ((e = linear(h, h->xn, d.d, L.gate, L.up, rows, d.ffn, d.d, ep, s))) return PE_ERR_CUDA;
     ep = epi_none();
     ep.kind = EPI_ADD;
@@ -885,6 +1025,8 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     ep.resid = h->resid;
     ep.ldr = d.d;
     ep.m_live = live;
+    if (fuse_norm && l + 1 < d.n_layers)
+      fold_out(ep, h->layers[l + 1].norm_in, h->x_in, h->ssq_in);
     if ((e = linear(h, h->act, d.ffn, L.down, nullptr, rows, d.d, d.ffn, ep, s)))
       return PE_ERR_CUDA;
     if (h->trace) {

@@ -58,6 +58,7 @@ __global__ void __launch_bounds__(kCompactThreads) compact_rows_kernel(const Com
         a.ids_c[c] = a.ids[p];
         a.pos_c[c] = a.pos[p];
         a.slot_c[c] = a.slot[p];
+        if (a.masked_c) a.masked_c[c] = a.is_masked[p];
       }
     }
     __syncthreads();  // every thread has read s_base and warp_excl
@@ -79,6 +80,11 @@ __global__ void __launch_bounds__(kCompactThreads) compact_rows_kernel(const Com
     const int q = a.new_idx[i];
     a.new_c[i] = (q >= 0 && q < a.T_out) ? a.row_map[q] : -1;
   }
+  if (a.fc_map)
+    for (int t = tid; t < a.T; t += kCompactThreads) {
+      const int q = a.hidden_map[t];
+      a.fc_map[t] = (q >= 0 && q < a.T_out) ? a.row_map[q] : -1;
+    }
 }
 
 __global__ void __launch_bounds__(128) scatter_rows_kernel(uint8_t* dst, const uint8_t* src,

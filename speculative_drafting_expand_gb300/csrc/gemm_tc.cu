@@ -46,6 +46,14 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* flag = reinterpret_cast<volatile int*>(tmem_slot + 1);     // reducer election
   volatile int* epi_ok = reinterpret_cast<volatile int*>(tmem_slot + 2);   // epilogue wait result
+  float* rs_part = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES + C::RS_OFF);
+  float* rs_smem = rs_part + 128;
+  int* slot_smem = reinterpret_cast<int*>(rs_smem + 32);
+  float* tab_smem = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES + C::TAB_OFF);
+  EpiStaged staged;
+  staged.rs = p.epi.rs_ssq ? rs_smem : nullptr;      // row scales of a folded RMSNorm
+  staged.tab = tab_smem;                             // fused RoPE: rotary table, slots
+  staged.slot = slot_smem;
 
   // Live token count of a compacted batch.  It was written two or more
   // launches back, so it is read before the wait, and its latency hides
@@ -132,6 +140,11 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
       const uint64_t pol_b = l2_policy_evict_last();
       const long long n = hi - lo;
       const int npre = static_cast<int>(n < C::STAGES ? n : C::STAGES);
+      // weight tile f at k-block kk: a 2-D box, or the interleaved QKV box
+      auto load_a = [&](uint8_t* dst, const CUtensorMap* m, uint64_t* bar, int kk, int f) {
+        if (p.a_heads) tma_load_4d(dst, m, bar, kk * 64, 0, 0, f * p.a_heads, pol_a);
+        else tma_load_2d(dst, m, bar, kk * 64, f * 128, pol_a);
+      };
       // weight tiles of the first stages do not depend on earlier kernels
       for (int i = 0; i < npre; ++i) {
         const long long u = lo + i;
@@ -139,8 +152,8 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
         const int f = tile / tiles_m;
         uint8_t* st = smem + i * C::STAGE_BYTES;
         mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
-        tma_load_2d(st, &tmA, &full[i], kk * 64, f * 128, pol_a);
-        if (DUAL) tma_load_2d(st + C::A_BYTES, &tmA2, &full[i], kk * 64, f * 128, pol_a);
+        load_a(st, &tmA, &full[i], kk, f);
+        if (DUAL) load_a(st + C::A_BYTES, &tmA2, &full[i], kk, f);
       }
       grid_dep_wait();
       // Dependents may launch once this CTA has waited for its own inputs;
@@ -164,8 +177,8 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
         const int f = tile / tiles_m, m = tile % tiles_m;
         uint8_t* st = smem + stage * C::STAGE_BYTES;
         mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-        tma_load_2d(st, &tmA, &full[stage], kk * 64, f * 128, pol_a);
-        if (DUAL) tma_load_2d(st + C::A_BYTES, &tmA2, &full[stage], kk * 64, f * 128, pol_a);
+        load_a(st, &tmA, &full[stage], kk, f);
+        if (DUAL) load_a(st + C::A_BYTES, &tmA2, &full[stage], kk, f);
         tma_load_2d(st + C::NA * C::A_BYTES, &tmB, &full[stage], kk * 64, m * BN, pol_b);
         issued = i + 1;
       }
@@ -220,6 +233,32 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
     }
   } else {
     grid_dep_wait();
+    if (p.epi.rs_ssq) {
+      // the folded RMSNorm's row scales of the (single) token tile, while
+      // the mainloop runs: four slices of the 32-feature groups, summed in
+      // a fixed order
+      float* part = rs_part;
+      const int t = threadIdx.x & 31, sl = threadIdx.x >> 5;
+      float s = 0.f;
+      if (t < p.M)
+        for (int gr = sl; gr < p.epi.rs_groups; gr += 4)
+          s += __ldcg(p.epi.rs_ssq + static_cast<size_t>(gr) * p.epi.rs_ld + t);
+      part[sl * 32 + t] = s;
+      named_bar_sync(1, 128);
+      if (threadIdx.x < 32)
+        rs_smem[t] = rsqrtf((((part[t] + part[32 + t]) + part[64 + t]) + part[96 + t]) /
+                                p.epi.rs_d + p.epi.rs_eps);
+      named_bar_sync(1, 128);
+    }
+    if (p.epi.kind == EPI_ROPE_KV) {
+      // the tile's rotary table and slots (tokens of a live count past it
+      // are never stored)
+      const int mt = min(p.M, BN);
+      for (int idx = threadIdx.x; idx < mt * p.epi.dh; idx += 128)
+        tab_smem[idx] = __ldg(p.epi.rope_tab + idx);
+      if (threadIdx.x < mt) slot_smem[threadIdx.x] = __ldg(p.epi.slot + threadIdx.x);
+      named_bar_sync(1, 128);
+    }
     int seg = 0;
     const int row = warp * 32 + lane;
     for (long long u = lo; u < hi;) {
@@ -239,7 +278,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * C::ACC_COLS;
       if (k_lo == 0 && k_hi == kb) {
         tmem_walk<BN, DUAL>(taddr, [&](int c0, const float* v, const float* v2) {
-          epi_chunk<DUAL>(p.epi, o, m * BN + c0, v, v2, lane);
+          epi_chunk<DUAL>(p.epi, o, m * BN + c0, v, v2, lane, staged);
         });
         tc_fence_before();
         mbar_arrive(&acc_empty[acc]);
@@ -321,7 +360,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
                   v[j] += x[q][j];
                   if (DUAL) v2[j] += x[q][16 + j];
                 }
-            epi_chunk<DUAL>(p.epi, o, m * BN + c0, v, v2, lane);
+            epi_chunk<DUAL>(p.epi, o, m * BN + c0, v, v2, lane, staged);
           };
           load(0, xa);
 #pragma unroll 1
@@ -366,7 +405,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
                 }
               }
             }
-            epi_chunk<DUAL>(p.epi, o, m * BN + c0, v, v2, lane);
+            epi_chunk<DUAL>(p.epi, o, m * BN + c0, v, v2, lane, staged);
           }
           if (threadIdx.x == 0) p.counters[tile] = 0;
         }
@@ -422,7 +461,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
 #pragma unroll
               for (int jj = 0; jj < 8; ++jj) dst[jj] += t[q][jj];
         }
-        epi_chunk<DUAL>(p.epi, f * 128 + row, m * BN + c0, v, v2, lane);
+        epi_chunk<DUAL>(p.epi, f * 128 + row, m * BN + c0, v, v2, lane, staged);
       }
     }
     // every CTA keeps its shared memory until all of the cluster has read it
@@ -472,6 +511,31 @@ bool tensor_map_2d_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t
                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tensor_map_qkv_interleaved(CUtensorMap* m, const void* ptr, int heads, int dh, uint64_t K) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) != 0 || (K * 2) % 16 != 0 || dh <= 0 ||
+      128 % dh != 0 || dh % 2 != 0)
+    return false;
+  const uint64_t half = static_cast<uint64_t>(dh / 2);
+  // dims (innermost first): k, half index b, row within the half i, head
+  cuuint64_t dims[4] = {K, 2, half, static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[3] = {half * K * 2, K * 2, static_cast<cuuint64_t>(dh) * K * 2};
+  cuuint32_t box[4] = {64, 2, static_cast<cuuint32_t>(half), static_cast<cuuint32_t>(128 / dh)};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Clusters of S CTAs (2..8) that can be resident at once, per
@@ -638,6 +702,16 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
   p.err = err;
   const int tiles = tiles_n * p.tiles_m;
   p.split_s = 0;
+  p.a_heads = 0;
+  if (epi.kind == EPI_ROPE_KV) {
+    // one token tile whose rotary table fits the staged [BN][64] floats
+    if (dual || epi.dh <= 0 || 128 % epi.dh != 0 || N % 128 != 0 || M > bn || bn > 32 ||
+        static_cast<long long>(M) * epi.dh > bn * 64 || epi.m_live)
+      return cudaErrorInvalidValue;
+    p.a_heads = 128 / epi.dh;
+  }
+  // a folded RMSNorm: one token tile of at most 32 rows
+  if ((epi.rs_ssq || epi.ssq) && (M > 32 || bn > 32 || epi.m_live)) return cudaErrorInvalidValue;
   if (tiles > ws.max_tiles) return cudaErrorInvalidValue;
 #define PE_TC_CASE(BNV)                                                                       \
   case BNV:                                                                                   \

@@ -3,6 +3,7 @@
 // the kernel parameters and the epilogue.
 #pragma once
 
+#include "fp8_common.cuh"
 #include "pe_common.cuh"
 #include "pe_kernels.h"
 
@@ -29,11 +30,18 @@ struct TcCfg {
   static constexpr int SMEM_BUDGET = BN <= 32 ? 104 * 1024 : 200 * 1024;
   static constexpr int STAGES_RAW = SMEM_BUDGET / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
-  static constexpr int BAR_BYTES = 256;
+  // barriers and flags, then (RS_OFF) the row scales of a folded RMSNorm:
+  // float partial[4][32], float r[32], int slot[32]; then (TAB_OFF, token
+  // tiles of at most 32) the rotary table of the tile's tokens for the
+  // fused RoPE epilogue, [BN][64] floats (cos / sin of the dh / 2 angles)
+  static constexpr int RS_OFF = 256;
+  static constexpr int TAB_OFF = RS_OFF + 6 * 32 * 4;
+  static constexpr int TAB_FLOATS = BN <= 32 ? BN * 64 : 0;
+  static constexpr int BAR_BYTES = TAB_OFF + TAB_FLOATS * 4;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
-  static_assert(2 * STAGES + 5 <= BAR_BYTES / 8, "barrier space");
+  static_assert((2 * STAGES + 5) * 8 + 12 <= RS_OFF, "barrier space");
 };
 
 struct TcParams {
@@ -45,6 +53,7 @@ struct TcParams {
   int* done;
   int* err;
   int split_s;  // 0: stream-K over all units; >= 1: S CTAs (one cluster) per tile
+  int a_heads;  // 0: weights by a 2-D map; else a 4-D interleaved QKV map, heads per tile
 };
 
 __device__ __forceinline__ long long unit_lo(int c, long long U, int G) {
@@ -59,12 +68,37 @@ __device__ __forceinline__ int cta_of_unit(long long u, long long U, int G) {
   return c;
 }
 
+// Per-tile values the epilogue warps stage in shared memory while the
+// mainloop runs (single token tile of at most 32 tokens; token t at [t]):
+// the row scales of a folded RMSNorm, and for the fused RoPE epilogue the
+// slots and rotary table (token t: cos at tab[t * dh + i], sin at
+// tab[t * dh + dh / 2 + i]).  Null where unused.
+struct EpiStaged {
+  const float* rs;
+  const float* tab;
+  const int* slot;
+};
+
 // Apply the epilogue to 16 token columns [t0, t0 + 16) of output feature o.
 // Called by all 32 lanes of a warp together (the argmax reduces across them).
 template <bool DUAL>
-__device__ __forceinline__ void epi_chunk(const EpiArgs& e, int o, int t0, const float* v,
-                                          const float* v2, int lane) {
+__device__ __forceinline__ void epi_chunk(const EpiArgs& e, int o, int t0, const float* v_in,
+                                          const float* v2_in, int lane, const EpiStaged& sm) {
+  const float* rs = sm.rs;
   const bool of = o < e.N;
+  float vs[16], vs2[16];
+  const float* v = v_in;
+  const float* v2 = v2_in;
+  if (rs) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float r = t0 + j < 32 ? rs[t0 + j] : 1.f;
+      vs[j] = v_in[j] * r;
+      if (DUAL) vs2[j] = v2_in[j] * r;
+    }
+    v = vs;
+    v2 = vs2;
+  }
   switch (e.kind) {
     case EPI_STORE:
       if (e.row_map) {
@@ -100,9 +134,38 @@ __device__ __forceinline__ void epi_chunk(const EpiArgs& e, int o, int t0, const
 #pragma unroll
       for (int j = 0; j < 16; ++j)
         old[j] = (of && t0 + j < e.M) ? r[static_cast<size_t>(j) * e.ldr] : 0.f;
+      const float gn = (e.xg && of) ? __bfloat162float(static_cast<const bf16*>(e.g_next)[o]) : 0.f;
+      float sq[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (of && t0 + j < e.M) r[static_cast<size_t>(j) * e.ldr] = old[j] + v[j];
+      for (int j = 0; j < 16; ++j) {
+        const float nv = old[j] + v[j];
+        sq[j] = (of && t0 + j < e.M) ? nv * nv : 0.f;
+        if (of && t0 + j < e.M) {
+          r[static_cast<size_t>(j) * e.ldr] = nv;
+          if (e.xg)
+            static_cast<bf16*>(e.xg)[static_cast<size_t>(t0 + j) * e.ldxg + o] =
+                __float2bfloat16_rn(nv * gn);
+        }
+      }
+      if (e.ssq) {
+        // sum of squares over the warp's 32 features for each of the 16
+        // tokens: butterfly reduce-scatter (lane l ends with token
+        // (l >> 1) & 15 over the lanes that differ in bits 1-4), then the
+        // last pair; a fixed order, so deterministic
+#pragma unroll
+        for (int s = 16, L = 16; s >= 2; s >>= 1, L >>= 1) {
+          const bool up = (lane & s) != 0;
+#pragma unroll
+          for (int i = 0; i < L / 2; ++i) {
+            const float send = up ? sq[i] : sq[i + L / 2];
+            const float keep = up ? sq[i + L / 2] : sq[i];
+            sq[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+          }
+        }
+        const float tot = sq[0] + __shfl_xor_sync(0xffffffffu, sq[0], 1);
+        const int t = t0 + ((lane >> 1) & 15);
+        if ((lane & 1) == 0 && t < e.M) e.ssq[static_cast<size_t>(o >> 5) * e.ssq_ld + t] = tot;
+      }
       break;
     }
     case EPI_SILU_MUL: {
@@ -112,6 +175,60 @@ __device__ __forceinline__ void epi_chunk(const EpiArgs& e, int o, int t0, const
         if (of && t0 + j < e.M)
           out[static_cast<size_t>(t0 + j) * e.ldo + o] =
               __float2bfloat16_rn(silu_f(v[j]) * (DUAL ? v2[j] : 1.f));
+      break;
+    }
+    case EPI_ROPE_KV: {
+      // o is an interleaved row: row 2i + b of a head holds feature
+      // i + b dh/2, so lanes 2i and 2i+1 hold a rotate-half pair
+      const int half = e.dh >> 1, rel = o % e.dh, i = rel >> 1, b = rel & 1;
+      const int f = (o - rel) + i + b * half;        // the feature in the standard layout
+      const int qd = e.Hq * e.dh, kd = e.Hkv * e.dh;
+      const int mlim = e.m_live ? min(e.M, __ldg(e.m_live)) : e.M;
+      const bool rot = f < qd + kd;                  // q and k rotate, v does not (warp-uniform)
+      // the projection's output is a bf16 activation: rounded before the
+      // rotation (as when it goes through memory), then rotated in fp32
+      float y[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float x = __bfloat162float(__float2bfloat16_rn(v[j]));
+        const float partner = __shfl_xor_sync(0xffffffffu, x, 1);
+        y[j] = x;
+        if (rot) {
+          const int t = t0 + j < mlim ? t0 + j : 0;   // rows past the batch are not stored
+          const float c = sm.tab[t * e.dh + i];
+          const float s = sm.tab[t * e.dh + half + i];
+          y[j] = b == 0 ? x * c - partner * s : x * c + partner * s;
+        }
+      }
+      if (!of) break;
+      if (f < qd) {
+        bf16* q = static_cast<bf16*>(e.q_out);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (t0 + j < mlim) q[static_cast<size_t>(t0 + j) * qd + f] = __float2bfloat16_rn(y[j]);
+      } else {
+        const bool is_k = f < qd + kd;
+        const int g = (f - (is_k ? qd : qd + kd)) / e.dh, jd = f % e.dh;
+        void* cache = is_k ? e.k_cache : e.v_cache;
+        const float inv = is_k ? e.k_inv_scale : e.v_inv_scale;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if (t0 + j >= mlim) continue;
+          const int sl = sm.slot[t0 + j];
+          if (sl < 0) continue;                      // rejected row: no KV write
+          const int blk = sl / 16, off = sl % 16;
+          if (blk >= e.num_blocks) {
+            if (jd == 0) record_error(e.err, PE_DEV_BAD_BLOCK);
+            continue;
+          }
+          const size_t at = ((static_cast<size_t>(blk) * e.Hkv + g) * 16 + off) * e.dh + jd;
+          if (e.kv_fp8)
+            static_cast<uint8_t*>(cache)[at] =
+                static_cast<uint8_t>(f32x2_to_e4m3x2(y[j] * inv, 0.f) & 0xffu);
+          else
+            static_cast<bf16*>(cache)[at] = __float2bfloat16_rn(y[j]);
+        }
+      }
       break;
     }
     case EPI_ARGMAX: {

@@ -98,6 +98,13 @@ struct CompactArgs {
   int32_t* cu_live;             // [B + 1]
   int32_t* new_c;               // [B K]
   int32_t* n_live;              // [1]
+  // optional (fc of the target rows only): the compact row of every target
+  // row (-1 when rejected) and the MASK flag of every compact row
+  int T;
+  const int32_t* hidden_map;    // [T] target row -> expanded row
+  const uint8_t* is_masked;     // [T_out]
+  int32_t* fc_map;              // [T]
+  uint8_t* masked_c;            // [T_out]
 };
 cudaError_t launch_compact_rows(const CompactArgs& a, cudaStream_t s);
 
@@ -122,6 +129,17 @@ struct EmbedConcatArgs {
   float eps;
   void* x;              // [rows, 2d] activations
   int* err;
+  // optional (fc of the target rows only): MASK rows take the fc of
+  // h_shared as their projected hidden state and write it to the residual
+  const uint8_t* masked;  // [rows] MASK flags
+  const float* fc_hs;     // [d]
+  float* h_w;             // the residual (= h), written for MASK rows
+  // optional: the rotary table of each row, rope_tab[row][k] = cos and
+  // rope_tab[row][dh/2 + k] = sin of pos[row] * inv_freq64[k] (angle in fp64)
+  const int32_t* pos;
+  const double* inv_freq64;
+  float* rope_tab;
+  int dh;
 };
 cudaError_t launch_embed_concat(int dtype, const EmbedConcatArgs& a, cudaStream_t s);
 
@@ -175,7 +193,7 @@ struct AttnArgs {
 cudaError_t launch_attention_simt(int dtype, const AttnArgs& a, cudaStream_t s);
 
 // ---------------------------------------------------------------- GEMM
-enum EpiKind { EPI_STORE = 0, EPI_ADD = 1, EPI_SILU_MUL = 2, EPI_ARGMAX = 3 };
+enum EpiKind { EPI_STORE = 0, EPI_ADD = 1, EPI_SILU_MUL = 2, EPI_ARGMAX = 3, EPI_ROPE_KV = 4 };
 
 struct EpiArgs {
   int kind;
@@ -190,6 +208,35 @@ struct EpiArgs {
   unsigned long long* keys; // ARGMAX: [M] packed (value, index), zero on entry
   int32_t* tokens;          // ARGMAX: [M] result
   const int32_t* row_map;   // STORE (optional): token t goes to row row_map[t], skipped if < 0
+  // ROPE_KV (the QKV projection): the weight rows arrive interleaved so
+  // that features i and i + dh/2 of every head are neighbouring rows (the
+  // A operand through a 4-D tensor map), lanes 2i and 2i+1 of a warp; the
+  // epilogue rotates q and k (rotate-half RoPE, cos / sin of each token row
+  // from rope_tab), stores q and writes k and v to the paged cache at the
+  // row's slot (-1: no write).
+  void* q_out;              // [M, Hq dh]
+  void* k_cache;            // [num_blocks, Hkv, 16, dh]
+  void* v_cache;
+  const int32_t* slot;      // [M]
+  const float* rope_tab;    // [M, dh]: cos of the dh/2 angles, then their sines
+  int Hq, Hkv, dh, num_blocks;
+  int kv_fp8;
+  float k_inv_scale, v_inv_scale;
+  int* err;
+  // RMSNorm folded across two projections (one token tile, M <= 32):
+  // ADD also writes xg[t][o] = bf16(new residual * g_next[o]) and, per 32
+  // features, ssq[(o / 32) * ssq_ld + t] = the sum of the new residual's
+  // squares; a projection of xg with rs_ssq set scales its accumulator row
+  // t by r[t] = rsqrt(sum of rs_ssq over the groups / rs_d + rs_eps), since
+  // W (x r g) = r W (x g).
+  const void* g_next;
+  void* xg;
+  int ldxg;
+  float* ssq;
+  int ssq_ld;
+  const float* rs_ssq;
+  int rs_groups, rs_ld;
+  float rs_d, rs_eps;
   // Optional live token count (device): token tiles at or past *m_live are
   // skipped and the work of the live ones is dealt out again.  The
   // tensor-core kernel reads it before waiting on the previous kernel, so
@@ -309,5 +356,9 @@ size_t stream_ws_floats(int grid);
 // tensor-map encoder (fetched once through cudart)
 bool tensor_map_2d_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
                         uint64_t ld_elems, uint32_t box_cols, uint32_t box_rows);
+// The QKV weight [(Hq + 2 Hkv) dh, K] as [heads][2][dh/2][K]: a box of
+// 128 / dh heads x both halves x dh/2 rows x 64 k lands in shared memory as
+// 128 rows with the halves interleaved (row 2i + b = feature i + b dh/2).
+bool tensor_map_qkv_interleaved(CUtensorMap* m, const void* ptr, int heads, int dh, uint64_t K);
 
 }  // namespace pe

@@ -16,6 +16,23 @@ namespace pe {
 
 constexpr int kRowThreads = 256;
 
+// cos and sin of the rotary angles of one row (threads k < dh / 2; the
+// angle in fp64, reduced to [-pi, pi] before the fp32 sine and cosine, as
+// in the RoPE kernel below)
+__device__ __forceinline__ void rope_table_row(const EmbedConcatArgs& a, int i) {
+  if (!a.rope_tab) return;
+  const int half = a.dh / 2;
+  for (int k = threadIdx.x; k < half; k += blockDim.x) {
+    const double two_pi = 6.283185307179586476925286766559;
+    const double ang = static_cast<double>(a.pos[i]) * a.inv_freq64[k];
+    const double red_ang = ang - rint(ang * (1.0 / two_pi)) * two_pi;
+    float sv, cv;
+    sincosf(static_cast<float>(red_ang), &sv, &cv);
+    a.rope_tab[static_cast<size_t>(i) * a.dh + k] = cv;
+    a.rope_tab[static_cast<size_t>(i) * a.dh + half + k] = sv;
+  }
+}
+
 // Block-wide sum; every thread gets the result.
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
@@ -43,7 +60,12 @@ __global__ void __launch_bounds__(kRowThreads) embed_concat_kernel(const EmbedCo
     id = 0;
   }
   const T* e = static_cast<const T*>(a.emb) + static_cast<size_t>(id) * a.d;
-  const float* h = a.h + static_cast<size_t>(i) * a.d;
+  // a MASK row's projected hidden state is the fc of h_shared
+  const bool mrow = a.masked && a.masked[i];
+  const float* h = mrow ? a.fc_hs : a.h + static_cast<size_t>(i) * a.d;
+  if (mrow)
+    for (int c = threadIdx.x; c < a.d; c += blockDim.x)
+      a.h_w[static_cast<size_t>(i) * a.d + c] = h[c];
   float se = 0.f, sh = 0.f;
   for (int c = threadIdx.x; c < a.d; c += blockDim.x) {
     const float ev = to_f(e[c]);
@@ -62,6 +84,7 @@ __global__ void __launch_bounds__(kRowThreads) embed_concat_kernel(const EmbedCo
     x[c] = from_f<T>(to_f(e[c]) * re * to_f(ge[c]));
     x[a.d + c] = from_f<T>(h[c] * rh * to_f(gh[c]));
   }
+  rope_table_row(a, i);
 }
 
 template <typename T>
@@ -252,7 +275,9 @@ __global__ void __launch_bounds__(kRowThreads) embed_concat_vec_kernel(const Emb
     id = 0;
   }
   const T* __restrict__ e = static_cast<const T*>(a.emb) + static_cast<size_t>(id) * a.d;
-  const float* __restrict__ h = a.h + static_cast<size_t>(i) * a.d;
+  // a MASK row's projected hidden state is the fc of h_shared
+  const bool mrow = a.masked && a.masked[i];
+  const float* __restrict__ h = mrow ? a.fc_hs : a.h + static_cast<size_t>(i) * a.d;
   float ev[NV][4], hv[NV][4];
   float se = 0.f, sh = 0.f;
 #pragma unroll
@@ -261,6 +286,7 @@ __global__ void __launch_bounds__(kRowThreads) embed_concat_vec_kernel(const Emb
     if (c4 < n4) {
       ld4(e + 4 * c4, ev[j]);
       ld4(h + 4 * c4, hv[j]);
+      if (mrow) st4(a.h_w + static_cast<size_t>(i) * a.d + 4 * c4, hv[j]);
     } else {
 #pragma unroll
       for (int q = 0; q < 4; ++q) ev[j][q] = hv[j][q] = 0.f;
@@ -309,6 +335,7 @@ __global__ void __launch_bounds__(kRowThreads) embed_concat_vec_kernel(const Emb
       st4(x + a.d + 4 * c4, oh);
     }
   }
+  rope_table_row(a, i);
 }
 
 // 16-byte vectors of the head dimension: EPV elements each.  A rope item is
