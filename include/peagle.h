@@ -325,6 +325,21 @@ pe_status pe_set_stream_prefetch(pe_handle* h, int32_t tiles, int32_t boundary_t
  * Slots a launch does not reach keep their old contents. */
 pe_status pe_set_stream_timeline(pe_handle* h, uint64_t* stamps);
 
+/* Diagnostic timeline of the projection and attention kernels (no
+ * counterpart on the pages).  stamps: caller-owned device buffer of
+ * launches * 512 * 16 uint64 (NULL turns it off).  Launch k of a step's
+ * projections and attentions (counted from the start of pe_draft_forward,
+ * pe_lmhead_argmax continuing the count) writes per CTA c < 512 at
+ * (k * 512 + c) * 16.  Projection: [0] start, [1] the wait for the
+ * previous kernel returned, [2] first stage landed, [3] last MMA issued,
+ * [4] the epilogue's main loop done, [5] every partial of a cluster split
+ * ready, [8] the first reduction item summed, [7] the CTA's reduction
+ * items applied, [6] exit.  Attention: [0] start, [1] set up, [2] the wait
+ * returned, [3] Q staged, [4] first scores, [5] last P.V, [6] partial
+ * written, [7] every split written, [8] merged, [9] exit.  (%globaltimer,
+ * ns; slots not reached keep their old contents.) */
+pe_status pe_set_gemm_timeline(pe_handle* h, uint64_t* stamps, int32_t launches);
+
 /* y[M, N] = x[M, K] . w[N, K]^T with the library's GEMM for the model dtype
  * (tcgen05 tensor cores for bf16, FFMA for f32); y is fp32.  A diagnostic
  * entry point for checking the projection kernels in isolation; K % 64 == 0

@@ -34,7 +34,7 @@ PE_MASK_ADDITIVE_BF16 = 1
 EXPORTED = ("pe_create", "pe_destroy", "pe_expand_batch", "pe_draft_forward",
             "pe_lmhead_argmax", "pe_get_device_error", "pe_set_trace", "pe_set_phase_events",
             "pe_set_small_batch_stream", "pe_set_stream_prefetch", "pe_set_stream_timeline",
-            "pe_set_fusions",
+            "pe_set_fusions", "pe_set_gemm_timeline",
             "pe_linear",
             "pe_get_launch_count", "pe_check_bounded_wait", "pe_linear_static",
             "pe_linear_static_error",
@@ -99,6 +99,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pe_set_small_batch_stream.argtypes = [_vp, _i32]
     lib.pe_set_stream_timeline.argtypes = [_vp, _vp]
     lib.pe_set_fusions.argtypes = [_vp, _i32]
+    lib.pe_set_gemm_timeline.argtypes = [_vp, _vp, _i32]
     lib.pe_set_stream_prefetch.argtypes = [_vp, _i32, _i32]
     lib.pe_linear_static_error.argtypes = [P(_i32), _vp]
     lib.pe_set_kv_cache_fp8.argtypes = [_vp, P(ctypes.c_float), P(ctypes.c_float)]
@@ -298,6 +299,12 @@ def pe_set_small_batch_stream(dr: Drafter, enable: bool) -> None:
 PE_FUSE_ROPE_KV = 1
 PE_FUSE_NORM = 2
 PE_FUSE_ALL = 3
+
+
+def pe_set_gemm_timeline(dr: Drafter, stamps=None, launches: int = 0) -> None:
+    """stamps: int64 device tensor of launches * 512 * 16 entries, or None."""
+    _check("pe_set_gemm_timeline",
+           lib().pe_set_gemm_timeline(dr.handle, ptr(stamps), int(launches) if stamps is not None else 0))
 
 
 def pe_set_fusions(dr: Drafter, mask: int) -> None:

@@ -27,7 +27,7 @@ size_t attention_tc_counters(const AttnArgs& a, int max_rows_per_req, int sm_cou
 cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                 const int32_t* seq_lens, int max_rows_per_req, int sm_count,
                                 float* part, size_t part_floats, int* counters,
-                                size_t n_counters, cudaStream_t s);
+                                size_t n_counters, unsigned long long* timeline, cudaStream_t s);
 cudaError_t launch_bounded_wait_check(int* flag, int32_t* out, int* err, cudaStream_t s);
 }  // namespace pe
 
@@ -95,6 +95,9 @@ struct pe_handle {
   // persistent kernel per segment (stream.cu)
   bool stream_on = false;
   unsigned long long* stream_timeline = nullptr;  // diagnostic, caller-owned
+  unsigned long long* gemm_timeline = nullptr;    // diagnostic, caller-owned
+  int gemm_timeline_launches = 0;
+  int gemm_ordinal = 0;                           // projection launches since the step began
   int stream_prefetch = 0;  // weight tiles prefetched into L2 ahead of the ring
   int stream_boundary = -1;  // loads into a phase before its inputs are ready (-1: any)
   float* stream_ws = nullptr;
@@ -106,6 +109,9 @@ struct pe_handle {
   std::map<std::tuple<const void*, uint64_t, uint64_t, uint64_t, uint32_t>, CUtensorMap> maps;
   std::map<std::pair<const void*, uint64_t>, CUtensorMap> maps_u8;  // fp8 pools
   std::map<std::pair<const void*, uint64_t>, CUtensorMap> maps_qkv;  // interleaved QKV weights
+  // the QKV weights with each head's halves interleaved (row 2i + b = row
+  // i + b dh/2), one copy per layer, for the fused RoPE epilogue
+  std::vector<void*> qkv_il;
   std::vector<void*> allocations;
 };
 
@@ -161,8 +167,34 @@ const CUtensorMap* get_map_qkv(pe_handle* h, const void* ptr, uint64_t K) {
   return &h->maps_qkv.emplace(key, m).first->second;
 }
 
+// Copy every layer's QKV weight with each head's halves interleaved (one
+// strided copy per head half; synchronous, at set-up).
+cudaError_t make_interleaved_qkv(pe_handle* h) {
+  const pe_model_desc& d = h->desc;
+  const int heads = d.n_heads + 2 * d.n_kv_heads, half = d.head_dim / 2;
+  for (int l = 0; l < d.n_layers; ++l) {
+    const size_t K = l == 0 ? 2 * d.d : d.d, rb = K * 2;
+    unsigned char* dst = nullptr;
+    cudaError_t e = dev_alloc(h, &dst, static_cast<size_t>(heads) * d.head_dim * rb);
+    if (e != cudaSuccess) return e;
+    const unsigned char* src = static_cast<const unsigned char*>(h->layers[l].qkv);
+    for (int hd = 0; hd < heads && e == cudaSuccess; ++hd)
+      for (int b = 0; b < 2 && e == cudaSuccess; ++b)
+        e = cudaMemcpy2D(dst + (static_cast<size_t>(hd) * d.head_dim + b) * rb, 2 * rb,
+                         src + (static_cast<size_t>(hd) * d.head_dim + b * half) * rb, rb, rb, half,
+                         cudaMemcpyDeviceToDevice);
+    if (e != cudaSuccess) return e;
+    h->qkv_il.push_back(dst);
+  }
+  return cudaDeviceSynchronize();
+}
+
 TcGemmWorkspace tc_ws(pe_handle* h) {
   TcGemmWorkspace ws;
+  ws.timeline = nullptr;
+  if (h->gemm_timeline && h->gemm_ordinal < h->gemm_timeline_launches)
+    ws.timeline = h->gemm_timeline + static_cast<size_t>(h->gemm_ordinal) * 512 * 16;
+  ++h->gemm_ordinal;
   ws.partials = h->gemm_partials;
   ws.partial_floats = h->gemm_partial_floats;
   ws.tile_counters = h->tile_counters;
@@ -367,6 +399,10 @@ pe_status pe_set_kv_cache_fp8(pe_handle* h, const float* k_scales, const float* 
 
 pe_status pe_set_fusions(pe_handle* h, int32_t mask) {
   if (!h || (mask & ~PE_FUSE_ALL)) return PE_ERR_INVALID_ARGUMENT;
+  if ((mask & PE_FUSE_ROPE_KV) && h->desc.dtype == PE_DTYPE_BF16 && h->qkv_il.empty()) {
+    const cudaError_t e = make_interleaved_qkv(h);
+    if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? PE_ERR_OUT_OF_MEMORY : PE_ERR_CUDA;
+  }
   h->fusions = mask;
   return PE_OK;
 }
@@ -381,6 +417,13 @@ pe_status pe_set_stream_prefetch(pe_handle* h, int32_t tiles, int32_t boundary_t
   if (!h || tiles < 0 || tiles > 4096 || boundary_tiles < -1) return PE_ERR_INVALID_ARGUMENT;
   h->stream_prefetch = tiles;
   h->stream_boundary = boundary_tiles;
+  return PE_OK;
+}
+
+pe_status pe_set_gemm_timeline(pe_handle* h, uint64_t* stamps, int32_t launches) {
+  if (!h || launches < 0) return PE_ERR_INVALID_ARGUMENT;
+  h->gemm_timeline = reinterpret_cast<unsigned long long*>(stamps);
+  h->gemm_timeline_launches = stamps ? launches : 0;
   return PE_OK;
 }
 
@@ -497,6 +540,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     if (!k_cache[l] || !v_cache[l]) return PE_ERR_INVALID_ARGUMENT;
   if (static_cast<long long>(B) * K > h->max_tokens) return PE_ERR_INVALID_ARGUMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  h->gemm_ordinal = 0;
   const int rows = ex->T_out;
   const int dt = d.dtype;
   const int qkv_rows = (d.n_heads + 2 * d.n_kv_heads) * d.head_dim;
@@ -649,9 +693,13 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
       const CUtensorMap* tv = h->kv_fp8 ? get_map_u8(h, v_cache[l], cache_rows)
                                         : get_map(h, v_cache[l], cache_rows, d.head_dim, d.head_dim, 16);
       if (!tk || !tv) return PE_ERR_INVALID_ARGUMENT;
+      unsigned long long* tl = nullptr;
+      if (h->gemm_timeline && h->gemm_ordinal < h->gemm_timeline_launches)
+        tl = h->gemm_timeline + static_cast<size_t>(h->gemm_ordinal) * 512 * 16;
+      ++h->gemm_ordinal;
       e = counted(h, launch_attention_tc(at, *tk, *tv, ex->seq_lens, max_rows_per_req,
                                          h->sm_count, h->attn_partials, h->attn_partial_floats,
-                                         h->attn_counters, h->attn_n_counters, s));
+                                         h->attn_counters, h->attn_n_counters, tl, s));
       if (e) return PE_ERR_CUDA;
     }
     if ((e = mark(2 + 2 * l))) return PE_ERR_CUDA;
@@ -926,6 +974,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
       ep.v_cache = v_cache[l];
       ep.slot = slot_l;
       ep.rope_tab = h->rope_tab;
+      ep.rope_rows_interleaved = h->qkv_il.empty() ? 0 : 1;
       ep.Hq = d.n_heads;
       ep.Hkv = d.n_kv_heads;
       ep.dh = d.head_dim;
@@ -937,7 +986,8 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
         ep.k_inv_scale = 1.f / h->k_scales[l];
         ep.v_inv_scale = 1.f / h->v_scales[l];
       }
-      const CUtensorMap* wa = get_map_qkv(h, L.qkv, d_in);
+      const CUtensorMap* wa = h->qkv_il.empty() ? get_map_qkv(h, L.qkv, d_in)
+                                                : get_map(h, h->qkv_il[l], qkv_rows, d_in, d_in, 128);
       const CUtensorMap* xb =
           get_map(h, h->x_in, rows, d_in, d_in,
                   tc_b_box_rows(rows, qkv_rows, h->sm_count, false, live != nullptr));

@@ -50,7 +50,18 @@ struct AttnTcParams {
   // unit's splits are written (the grid is one wave, so they are all
   // resident); 0: the last split to finish merges the whole unit
   int parallel_merge;
+  // diagnostic timeline, or null: [cta][16] %globaltimer stamps (ns): [0]
+  // start, [1] set up (barriers, tensor memory, block ids), [2] the wait
+  // for the previous kernel returned, [3] Q in shared memory, [4] the first
+  // scores ready, [5] the last P.V done, [6] the partial written, [7] every
+  // split of the unit written, [8] merged, [9] exit
+  unsigned long long* tl;
 };
+
+__device__ __forceinline__ void attn_stamp(const AttnTcParams& p, int slot) {
+  const unsigned cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+  if (p.tl && cta < 512) p.tl[static_cast<size_t>(cta) * 16 + slot] = global_timer_ns();
+}
 
 // FP8: the pools hold e4m3 codes.  Their pages come by TMA into a two-stage
 // staging ring, the producer warp widens them to f16 in the K/V stages
@@ -137,7 +148,12 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- which rows and keys this CTA covers (uniform across the CTA) ------
-  grid_dep_wait();
+  // The request offsets, sequence lengths, positions and block ids come
+  // from the expansion (several launches back) or the caller, so they are
+  // read, and the barriers and tensor memory set up, before the wait for
+  // the previous kernel (which writes q and this step's K/V): that wait
+  // sits right before the Q and K/V loads.
+  if (threadIdx.x == 0) attn_stamp(p, 0);
   const int row0 = a.cu_out[r];
   const int nrows = a.cu_out[r + 1] - row0;
   const int tile_row0 = qt * p.rows_per_qt;
@@ -151,6 +167,7 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
   if (tile_rows <= 0 || key0 >= seq || seq > a.bt_stride * 16) {
     if (threadIdx.x == 0 && seq > a.bt_stride * 16 && split == 0 && g == 0 && qt == 0)
       record_error(a.err, PE_DEV_BAD_POSITION);
+    grid_dep_wait();
     grid_dep_launch();
     return;
   }
@@ -218,6 +235,9 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
       }
       __syncwarp();
     }
+    if (lane == 0) attn_stamp(p, 1);
+    grid_dep_wait();   // the previous kernel wrote this step's K/V
+    if (lane == 0) attn_stamp(p, 2);
     if constexpr (!FP8) {
       if (lane == 0) {
         tma_prefetch_desc(&tmK);
@@ -398,6 +418,7 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
     const int head = g * p.G + hl;
     int P = -1;                                     // last key this row reads
     if (in_tile && (a.is_rejected == nullptr || a.is_rejected[row] == 0)) P = a.pos[row];
+    grid_dep_wait();   // the previous kernel wrote q
     // Q -> shared memory (128-byte swizzle; zero for padding / rejected rows)
     {
       const uint4* src = reinterpret_cast<const uint4*>(
@@ -417,7 +438,10 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
     }
     fence_proxy_async_smem();
     named_bar_sync(1, C::SOFT);
-    if (threadIdx.x == 64) mbar_arrive(q_ready);
+    if (threadIdx.x == 64) {
+      mbar_arrive(q_ready);
+      attn_stamp(p, 3);
+    }
 
     // log2(e) / sqrt(dh), times the K scale of an fp8 pool (S holds
     // q . code; the score is q . code * k_scale)
@@ -427,6 +451,7 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
     const uint32_t o_col = C::O_COL + h * DH;
     for (int c = 0; c < nchunks; ++c) {
       if (!mbar_wait(&s_full[c & 1], (c >> 1) & 1, a.err)) { ok = false; break; }
+      if (c == 0 && threadIdx.x == 64) attn_stamp(p, 4);
       tc_fence_after();
       constexpr int KPW = C::KPW;
       float sv[KPW / 16][16];
@@ -543,6 +568,7 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
       mbar_arrive(&p_full[c & 1]);
     }
     if (ok && !mbar_wait(&pv_done[(nchunks - 1) & 1], ((nchunks - 1) >> 1) & 1, a.err)) ok = false;
+    if (threadIdx.x == 64) attn_stamp(p, 5);
     if (!ok) *abort_flag = 1;
     // combine the slices: (m, l) through shared memory
     red[h * 128 + qrow] = m_used;
@@ -616,8 +642,10 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
           int* arrived = p.counters + unit;
           int* merged = arrived + static_cast<size_t>(a.B) * a.Hkv * p.qtiles;
           if (threadIdx.x == 64) {
+            attn_stamp(p, 6);
             atomicAdd(arrived, 1);
             *flag = flag_wait_geq(arrived, nsplits, a.err) ? 1 : 0;
+            attn_stamp(p, 7);
           }
           named_bar_sync(1, C::SOFT);
           const int per = ((128 + nsplits - 1) / nsplits + 3) & ~3;   // rows, a multiple of 4
@@ -677,6 +705,7 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
           }
           // the last split to finish its slice leaves both counts zero
           named_bar_sync(1, C::SOFT);
+          if (threadIdx.x == 64) attn_stamp(p, 8);
           if (threadIdx.x == 64 && *flag) {
             const int old = atomicAdd(merged, 1);
             if (old == nsplits - 1) {
@@ -748,6 +777,7 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) attn_stamp(p, 9);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -845,7 +875,7 @@ cudaError_t init_attention_tc() {
 cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                 const int32_t* seq_lens, int max_rows_per_req, int sm_count,
                                 float* part, size_t part_floats, int* counters,
-                                size_t n_counters, cudaStream_t s) {
+                                size_t n_counters, unsigned long long* timeline, cudaStream_t s) {
   if (a.rows <= 0) return cudaSuccess;
   const AttnPlan pl = plan_attention(a, max_rows_per_req, sm_count);
   AttnTcParams p;
@@ -858,6 +888,7 @@ cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const
   p.max_splits = pl.max_splits;
   p.part = part;
   p.counters = counters;
+  p.tl = timeline;
   // every split CTA resident at once (one wave of one CTA per SM), at most
   // 32 splits: the splits merge their unit in parallel
   const long long ctas = static_cast<long long>(pl.max_splits) * a.Hkv * pl.qtiles * a.B;

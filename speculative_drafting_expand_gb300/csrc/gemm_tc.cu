@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
+    tc_stamp(p, 0);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
@@ -156,6 +157,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
         if (DUAL) load_a(st + C::A_BYTES, &tmA2, &full[i], kk, f);
       }
       grid_dep_wait();
+      tc_stamp(p, 1);
       // Dependents may launch once this CTA has waited for its own inputs;
       // TMEM is already held, so their allocation can only wait for this
       // grid to finish, never the other way round.
@@ -208,6 +210,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
             ok = false;
             break;
           }
+          if (i == 0) tc_stamp(p, 2);
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
           const uint32_t b_addr = a_addr + C::NA * C::A_BYTES;
@@ -227,6 +230,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
         u += k_hi - k_lo;
         ++seg;
       }
+      tc_stamp(p, 3);
       // drain: all MMAs of this thread are complete before TMEM is freed
       umma_commit(drain);
       mbar_wait(drain, 0, p.err);
@@ -286,12 +290,14 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
         // cluster split: the partial goes to this CTA's own shared memory
         // (the operand stages are all consumed); rank 0 sums the cluster's
         // partials after the cluster barrier below
-        float* part = reinterpret_cast<float*>(smem);
+        float* part = reinterpret_cast<float*>(smem) + row * C::PS;
         tmem_walk<BN, DUAL>(taddr, [&](int c0, const float* v, const float* v2) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            part[(c0 + j) * 128 + row] = v[j];
-            if (DUAL) part[(BN + c0 + j) * 128 + row] = v2[j];
+          for (int j = 0; j < 16; j += 4) {
+            *reinterpret_cast<float4*>(part + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            if (DUAL)
+              *reinterpret_cast<float4*>(part + BN + c0 + j) =
+                  make_float4(v2[j], v2[j + 1], v2[j + 2], v2[j + 3]);
           }
         });
         tc_fence_before();
@@ -415,6 +421,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
     }
   }
 
+  if (threadIdx.x == 0) tc_stamp(p, 4);
   tc_fence_before();
   __syncthreads();
   if (warp == 5) {
@@ -426,16 +433,30 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
     // is scattered over the cluster: the tile's (32-row group, 16-column
     // chunk) items go round-robin to the S CTAs, and the warp of that row
     // group reads its item from all S partials with the loads of 8 columns
-    // in flight together (one DSMEM round trip per 8 columns, not one per
-    // CTA), adds them in rank order (deterministic) and applies the
-    // epilogue.
-    cluster_sync_all();
+    // in flight together (two 16-byte DSMEM loads per partial, one round
+    // trip per 8 columns), adds them in rank order (deterministic) and
+    // applies the epilogue.  A residual-add epilogue's residual (untouched
+    // by this kernel) is loaded before the cluster barrier, for one chunk.
     const int S = p.split_s, tile = cta / S;
     const int rk = static_cast<int>(cluster_ctarank());
+    const int f = tile / tiles_m, m = tile % tiles_m;
+    const int row = warp * 32 + lane;
+    float old_pre[17];
+    const bool pre = p.epi.kind == EPI_ADD && BN == 16 && warp < 4 && warp % S == rk;
+    if (pre) {
+      const int o = f * 128 + row, t0 = m * BN;
+      const float* r = p.epi.resid + static_cast<size_t>(t0) * p.epi.ldr + o;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        old_pre[j] = (o < p.epi.N && t0 + j < p.epi.M) ? r[static_cast<size_t>(j) * p.epi.ldr] : 0.f;
+      old_pre[16] = (p.epi.xg && o < p.epi.N)
+                        ? __bfloat162float(static_cast<const bf16*>(p.epi.g_next)[o])
+                        : 0.f;
+    }
+    cluster_sync_all();
+    if (threadIdx.x == 0) tc_stamp(p, 5);
     if (warp < 4) {
-      const int f = tile / tiles_m, m = tile % tiles_m;
-      const int row = warp * 32 + lane;
-      const uint32_t base = smem_u32(smem);
+      const uint32_t base = smem_u32(smem) + row * C::PS * 4;
       constexpr int kMaxS = 8;  // cluster split sizes are at most 8
       for (int c0 = 0; c0 < BN; c0 += 16) {
         if (((c0 / 16) * 4 + warp) % S != rk) continue;
@@ -445,27 +466,37 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
 #pragma unroll
         for (int part = 0; part < (DUAL ? 4 : 2); ++part) {
           const int col = (part & 2 ? BN : 0) + c0 + (part & 1) * 8;
-          float t[kMaxS][8];
+          float4 t[kMaxS][2];
 #pragma unroll
           for (int q = 0; q < kMaxS; ++q) {
             if (q < S) {
-              const uint32_t rb = cluster_map_shared(base, q) + (col * 128 + row) * 4;
-#pragma unroll
-              for (int jj = 0; jj < 8; ++jj) t[q][jj] = ld_shared_cluster_f32(rb + jj * 128 * 4);
+              const uint32_t rb = cluster_map_shared(base, q) + col * 4;
+              t[q][0] = ld_shared_cluster_v4(rb);
+              t[q][1] = ld_shared_cluster_v4(rb + 16);
             }
           }
           float* dst = (part & 2 ? v2 : v) + (part & 1) * 8;
 #pragma unroll
           for (int q = 0; q < kMaxS; ++q)
-            if (q < S)
-#pragma unroll
-              for (int jj = 0; jj < 8; ++jj) dst[jj] += t[q][jj];
+            if (q < S) {
+              dst[0] += t[q][0].x;
+              dst[1] += t[q][0].y;
+              dst[2] += t[q][0].z;
+              dst[3] += t[q][0].w;
+              dst[4] += t[q][1].x;
+              dst[5] += t[q][1].y;
+              dst[6] += t[q][1].z;
+              dst[7] += t[q][1].w;
+            }
         }
-        epi_chunk<DUAL>(p.epi, f * 128 + row, m * BN + c0, v, v2, lane, staged);
+        if (threadIdx.x == 0 && c0 == 0) tc_stamp(p, 8);
+        epi_chunk<DUAL>(p.epi, f * 128 + row, m * BN + c0, v, v2, lane, staged,
+                        pre && c0 == 0 ? old_pre : nullptr);
       }
     }
+    if (threadIdx.x == 0) tc_stamp(p, 7);
     // every CTA keeps its shared memory until all of the cluster has read it
-    cluster_sync_all();
+    cluster_sync_relaxed();
   }
   if (p.epi.kind == EPI_ARGMAX) {
     // the last CTA turns the packed (value, index) keys into token ids
@@ -484,6 +515,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
       if (threadIdx.x == 0) *p.done = 0;
     }
   }
+  if (threadIdx.x == 0) tc_stamp(p, 6);
 }
 
 // ---------------------------------------------------------------------------
@@ -605,7 +637,7 @@ static cudaError_t run_tc(const CUtensorMap& a, const CUtensorMap& a2, const CUt
   using C = TcCfg<BN, DUAL>;
   // Fewer tiles than SMs: split k across a cluster of S CTAs per tile and
   // reduce through distributed shared memory.  Otherwise stream-K.
-  const bool fits = static_cast<size_t>(C::ACC_COLS) * 128 * 4 <=
+  const bool fits = static_cast<size_t>(C::PS) * 128 * 4 <=
                     static_cast<size_t>(C::STAGES) * C::STAGE_BYTES;
   // S CTAs a tile, about one CTA per SM in all (measured best in the
   // drafting step: with two CTAs an SM resident, the next kernel's CTAs
@@ -703,12 +735,15 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
   const int tiles = tiles_n * p.tiles_m;
   p.split_s = 0;
   p.a_heads = 0;
+  p.tl = ws.timeline;
   if (epi.kind == EPI_ROPE_KV) {
     // one token tile whose rotary table fits the staged [BN][64] floats
     if (dual || epi.dh <= 0 || 128 % epi.dh != 0 || N % 128 != 0 || M > bn || bn > 32 ||
         static_cast<long long>(M) * epi.dh > bn * 64 || epi.m_live)
       return cudaErrorInvalidValue;
-    p.a_heads = 128 / epi.dh;
+    // the weight rows interleaved by a 4-D tensor map, unless the caller
+    // gives an already interleaved copy (epi.rope_rows_interleaved)
+    p.a_heads = epi.rope_rows_interleaved ? 0 : 128 / epi.dh;
   }
   // a folded RMSNorm: one token tile of at most 32 rows
   if ((epi.rs_ssq || epi.ssq) && (M > 32 || bn > 32 || epi.m_live)) return cudaErrorInvalidValue;

@@ -28,6 +28,9 @@ struct TcCfg {
   // 100 KB of shared memory so that the next projection's CTA fits on the
   // same SM and prefetches its weights while this one drains.
   static constexpr int SMEM_BUDGET = BN <= 32 ? 104 * 1024 : 200 * 1024;
+  // a cluster split's partial in shared memory: row-major, rows padded to
+  // PS floats (16-byte aligned rows, few bank conflicts) for vector reads
+  static constexpr int PS = ACC_COLS + 4;
   static constexpr int STAGES_RAW = SMEM_BUDGET / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
   // barriers and flags, then (RS_OFF) the row scales of a folded RMSNorm:
@@ -54,7 +57,17 @@ struct TcParams {
   int* err;
   int split_s;  // 0: stream-K over all units; >= 1: S CTAs (one cluster) per tile
   int a_heads;  // 0: weights by a 2-D map; else a 4-D interleaved QKV map, heads per tile
+  // diagnostic timeline, or null: [cta][16] %globaltimer stamps (ns): [0]
+  // start, [1] the producer's wait for the previous kernel returned, [2]
+  // the first stage landed (MMA issuer), [3] the last MMA issued, [4] the
+  // epilogue's main loop done, [5] every partial of the cluster ready, [8]
+  // the partials of the first item summed, [7] this CTA's share of the
+  // cluster reduction applied, [6] exit
+  unsigned long long* tl;
 };
+__device__ __forceinline__ void tc_stamp(const TcParams& p, int slot) {
+  if (p.tl) p.tl[static_cast<size_t>(blockIdx.x) * 16 + slot] = global_timer_ns();
+}
 
 __device__ __forceinline__ long long unit_lo(int c, long long U, int G) {
   return static_cast<long long>(c) * U / G;
@@ -81,9 +94,12 @@ struct EpiStaged {
 
 // Apply the epilogue to 16 token columns [t0, t0 + 16) of output feature o.
 // Called by all 32 lanes of a warp together (the argmax reduces across them).
+// old_pre (ADD): the residual of these 16 tokens already loaded, then the
+// next norm's gain of feature o (old_pre[16]), or null.
 template <bool DUAL>
 __device__ __forceinline__ void epi_chunk(const EpiArgs& e, int o, int t0, const float* v_in,
-                                          const float* v2_in, int lane, const EpiStaged& sm) {
+                                          const float* v2_in, int lane, const EpiStaged& sm,
+                                          const float* old_pre = nullptr) {
   const float* rs = sm.rs;
   const bool of = o < e.N;
   float vs[16], vs2[16];
@@ -133,8 +149,11 @@ __device__ __forceinline__ void epi_chunk(const EpiArgs& e, int o, int t0, const
       float old[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        old[j] = (of && t0 + j < e.M) ? r[static_cast<size_t>(j) * e.ldr] : 0.f;
-      const float gn = (e.xg && of) ? __bfloat162float(static_cast<const bf16*>(e.g_next)[o]) : 0.f;
+        old[j] = old_pre ? old_pre[j]
+                         : (of && t0 + j < e.M) ? r[static_cast<size_t>(j) * e.ldr] : 0.f;
+      const float gn = old_pre ? old_pre[16]
+                       : (e.xg && of) ? __bfloat162float(static_cast<const bf16*>(e.g_next)[o])
+                                      : 0.f;
       float sq[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {

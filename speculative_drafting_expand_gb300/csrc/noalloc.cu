@@ -115,6 +115,7 @@ extern "C" pe_status pe_linear_static(const void* x, const void* w, float* y, in
   ws.tile_counters = counters;
   ws.max_tiles = kMaxTiles;
   ws.done_counter = nullptr;  // only the argmax epilogue uses it
+  ws.timeline = nullptr;
   ws.sm_count = sms;
   EpiArgs ep = {};
   ep.kind = EPI_STORE;

@@ -278,11 +278,28 @@ __device__ __forceinline__ void cluster_sync_all() {
       "barrier.cluster.arrive.release.aligned;\n\t"
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// The same barrier without release: for a last barrier that only keeps
+// every CTA's shared memory alive until the cluster has read it (the reads
+// are complete when their values are used, and nothing written needs to be
+// published).
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile(
+      "barrier.cluster.arrive.relaxed.aligned;\n\t"
+      "barrier.cluster.wait.aligned;" ::: "memory");
+}
 // Address of the same shared-memory offset in cluster CTA `rank`.
 __device__ __forceinline__ uint32_t cluster_map_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
+}
+__device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
 }
 __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
   float v;

@@ -219,6 +219,7 @@ struct EpiArgs {
   void* v_cache;
   const int32_t* slot;      // [M]
   const float* rope_tab;    // [M, dh]: cos of the dh/2 angles, then their sines
+  int rope_rows_interleaved;  // 1: the weight itself is stored interleaved (2-D map)
   int Hq, Hkv, dh, num_blocks;
   int kv_fp8;
   float k_inv_scale, v_inv_scale;
@@ -255,6 +256,7 @@ struct TcGemmWorkspace {
   int max_tiles;
   int* done_counter;        // zero on entry, left zero on exit
   int sm_count;
+  unsigned long long* timeline;  // diagnostic per-CTA stamps of this launch, or null
 };
 cudaError_t launch_gemm_tc(const void* x, int ldx, const void* w, const void* w2, int M, int N,
                            int K, const EpiArgs& epi, const TcGemmWorkspace& ws, int* err,
