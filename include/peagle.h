@@ -308,6 +308,30 @@ pe_status pe_set_small_batch_stream(pe_handle* h, int32_t enable);
 enum { PE_FUSE_ROPE_KV = 1, PE_FUSE_NORM = 2, PE_FUSE_ALL = 3 };
 pe_status pe_set_fusions(pe_handle* h, int32_t mask);
 
+/* How a projection split over the k dimension across a thread-block
+ * cluster (few token rows: fewer weight tiles than SMs) sums its partial
+ * tiles.  PE_REDUCE_PUSH (the default): every CTA, once the cluster's
+ * operand stages are free, stores each (32-row, 16-column) item of its
+ * fp32 partial into the shared memory of the CTA that owns the item
+ * (st.async, counted on the owner's mbarrier), and the owner adds the
+ * partials in rank order.  PE_REDUCE_PULL: every CTA keeps its partial,
+ * a cluster barrier, and the owner reads the peers' partials with
+ * distributed-shared-memory loads.  Both add in the same order: the
+ * results are bit-identical.  Returns PE_ERR_INVALID_ARGUMENT for another
+ * value. */
+enum { PE_REDUCE_PULL = 0, PE_REDUCE_PUSH = 1 };
+pe_status pe_set_split_reduce(pe_handle* h, int32_t mode);
+
+/* Launch tuning of the projection kernels, one key at a time.
+ *   PE_TUNE_GEMM_PRE_STAGES  how many of a CTA's weight stages it loads
+ *                            before its wait for the previous kernel (the
+ *                            weights do not depend on it); -1 (default):
+ *                            all of its shared-memory stages, 0: none.
+ * Returns PE_ERR_INVALID_ARGUMENT for an unknown key or a value out of
+ * range.  The results do not depend on the setting. */
+enum { PE_TUNE_GEMM_PRE_STAGES = 1 };
+pe_status pe_set_tuning(pe_handle* h, int32_t key, int32_t value);
+
 /* Tuning of the small-batch streaming kernel.  tiles: how many 16 KB
  * weight tiles each CTA brings into L2 ahead of its shared-memory ring
  * (default 0 = none; at most 4096).  boundary_tiles: how many weight tiles

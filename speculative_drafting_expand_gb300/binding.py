@@ -34,7 +34,7 @@ PE_MASK_ADDITIVE_BF16 = 1
 EXPORTED = ("pe_create", "pe_destroy", "pe_expand_batch", "pe_draft_forward",
             "pe_lmhead_argmax", "pe_get_device_error", "pe_set_trace", "pe_set_phase_events",
             "pe_set_small_batch_stream", "pe_set_stream_prefetch", "pe_set_stream_timeline",
-            "pe_set_fusions", "pe_set_gemm_timeline",
+            "pe_set_fusions", "pe_set_split_reduce", "pe_set_tuning", "pe_set_gemm_timeline",
             "pe_linear",
             "pe_get_launch_count", "pe_check_bounded_wait", "pe_linear_static",
             "pe_linear_static_error",
@@ -99,6 +99,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pe_set_small_batch_stream.argtypes = [_vp, _i32]
     lib.pe_set_stream_timeline.argtypes = [_vp, _vp]
     lib.pe_set_fusions.argtypes = [_vp, _i32]
+    lib.pe_set_split_reduce.argtypes = [_vp, _i32]
+    lib.pe_set_tuning.argtypes = [_vp, _i32, _i32]
     lib.pe_set_gemm_timeline.argtypes = [_vp, _vp, _i32]
     lib.pe_set_stream_prefetch.argtypes = [_vp, _i32, _i32]
     lib.pe_linear_static_error.argtypes = [P(_i32), _vp]
@@ -309,6 +311,21 @@ def pe_set_gemm_timeline(dr: Drafter, stamps=None, launches: int = 0) -> None:
 
 def pe_set_fusions(dr: Drafter, mask: int) -> None:
     _check("pe_set_fusions", lib().pe_set_fusions(dr.handle, int(mask)))
+
+
+PE_REDUCE_PULL = 0
+PE_REDUCE_PUSH = 1
+
+
+def pe_set_split_reduce(dr: Drafter, mode: int) -> None:
+    _check("pe_set_split_reduce", lib().pe_set_split_reduce(dr.handle, int(mode)))
+
+
+PE_TUNE_GEMM_PRE_STAGES = 1
+
+
+def pe_set_tuning(dr: Drafter, key: int, value: int) -> None:
+    _check("pe_set_tuning", lib().pe_set_tuning(dr.handle, int(key), int(value)))
 
 
 def pe_set_stream_prefetch(dr: Drafter, tiles: int, boundary_tiles: int = -1) -> None:

@@ -61,6 +61,8 @@ struct pe_handle {
   double* inv_freq64 = nullptr;        // [dh / 2]
   float* rope_tab = nullptr;           // [max_tokens, dh] cos / sin of each row's angles
   int fusions = PE_FUSE_NORM;          // epilogue fusions of the per-projection path
+  int cluster_push = PE_REDUCE_PUSH;   // cluster split-K reduction: push (1) or pull (0)
+  int gemm_pre_stages = -1;            // projection weight stages loaded before the dependency wait
   float* fc_hs = nullptr;              // [d] fc(h_shared), the projected hidden of every MASK row
   int32_t* fc_map = nullptr;           // [max_tokens] target row -> compact row
   uint8_t* masked_c = nullptr;         // [max_tokens] MASK flag of every compact row
@@ -201,6 +203,8 @@ TcGemmWorkspace tc_ws(pe_handle* h) {
   ws.max_tiles = h->max_tiles;
   ws.done_counter = h->done_counter;
   ws.sm_count = h->sm_count;
+  ws.cluster_push = h->cluster_push;
+  ws.pre_stages = h->gemm_pre_stages;
   return ws;
 }
 
@@ -394,6 +398,24 @@ pe_status pe_set_kv_cache_fp8(pe_handle* h, const float* k_scales, const float* 
   h->k_scales = ks;
   h->v_scales = vs;
   h->kv_fp8 = true;
+  return PE_OK;
+}
+
+pe_status pe_set_tuning(pe_handle* h, int32_t key, int32_t value) {
+  if (!h) return PE_ERR_INVALID_ARGUMENT;
+  switch (key) {
+    case PE_TUNE_GEMM_PRE_STAGES:
+      if (value < -1) return PE_ERR_INVALID_ARGUMENT;
+      h->gemm_pre_stages = value;
+      return PE_OK;
+    default:
+      return PE_ERR_INVALID_ARGUMENT;
+  }
+}
+
+pe_status pe_set_split_reduce(pe_handle* h, int32_t mode) {
+  if (!h || (mode != PE_REDUCE_PULL && mode != PE_REDUCE_PUSH)) return PE_ERR_INVALID_ARGUMENT;
+  h->cluster_push = mode;
   return PE_OK;
 }
 

@@ -54,7 +54,8 @@ struct AttnTcParams {
   // start, [1] set up (barriers, tensor memory, block ids), [2] the wait
   // for the previous kernel returned, [3] Q in shared memory, [4] the first
   // scores ready, [5] the last P.V done, [6] the partial written, [7] every
-  // split of the unit written, [8] merged, [9] exit
+  // split of the unit written, [10] the slice's partials in shared memory,
+  // [11] the slice merged, [8] merged (after the barrier), [9] exit
   unsigned long long* tl;
 };
 
@@ -623,12 +624,15 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
         // are contiguous
         const size_t unit = (static_cast<size_t>(r) * a.Hkv + g) * p.qtiles + qt;
         const size_t stride = static_cast<size_t>(128) * (DH + 2);
+        // (rows of the tile only: the merge reads no other)
         float* mine = p.part + (unit * p.max_splits + split) * stride + qrow;
+        if (in_tile) {
 #pragma unroll
-        for (int j = 0; j < HC; ++j) mine[(h * HC + j) * 128] = o[j];
-        if (h == 0) {
-          mine[DH * 128] = M;
-          mine[(DH + 1) * 128] = L;
+          for (int j = 0; j < HC; ++j) mine[(h * HC + j) * 128] = o[j];
+          if (h == 0) {
+            mine[DH * 128] = M;
+            mine[(DH + 1) * 128] = L;
+          }
         }
         __threadfence();
         named_bar_sync(1, C::SOFT);
@@ -648,8 +652,10 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
             attn_stamp(p, 7);
           }
           named_bar_sync(1, C::SOFT);
-          const int per = ((128 + nsplits - 1) / nsplits + 3) & ~3;   // rows, a multiple of 4
-          const int q0 = split * per, q1 = min(128, q0 + per);
+          // the tile's rows are query slots [0, tile_rows G)
+          const int live = tile_rows * p.G;
+          const int per = ((live + nsplits - 1) / nsplits + 3) & ~3;   // rows, a multiple of 4
+          const int q0 = split * per, q1 = min(live, q0 + per);
           if (*flag && q0 < q1) {
             const float* base = p.part + unit * p.max_splits * stride;
             float* stage = reinterpret_cast<float*>(smem + C::K_OFF);   // [split][col][per]
@@ -667,6 +673,7 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
             }
             asm volatile("cp.async.wait_all;" ::: "memory");
             named_bar_sync(1, C::SOFT);
+            if (threadIdx.x == 64) attn_stamp(p, 10);
             // thread -> (row slots rr, rr + 16, ..., group of DH / 16 columns)
             constexpr int NCOL = DH / 16;
             const int cg = t / 16;
@@ -704,6 +711,7 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
             }
           }
           // the last split to finish its slice leaves both counts zero
+          if (threadIdx.x == 64) attn_stamp(p, 11);
           named_bar_sync(1, C::SOFT);
           if (threadIdx.x == 64) attn_stamp(p, 8);
           if (threadIdx.x == 64 && *flag) {

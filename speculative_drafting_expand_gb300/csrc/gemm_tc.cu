@@ -43,7 +43,8 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
   uint64_t* acc_full = empty + C::STAGES;  // [2]
   uint64_t* acc_empty = acc_full + 2;      // [2]
   uint64_t* drain = acc_empty + 2;         // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* recv_bar = drain + 1;          // [1] pushed cluster reduction: items received
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv_bar + 1);
   volatile int* flag = reinterpret_cast<volatile int*>(tmem_slot + 1);     // reducer election
   volatile int* epi_ok = reinterpret_cast<volatile int*>(tmem_slot + 2);   // epilogue wait result
   float* rs_part = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES + C::RS_OFF);
@@ -72,6 +73,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
       mbar_init(&acc_empty[a], 128);
     }
     mbar_init(drain, 1);
+    mbar_init(recv_bar, 1);
     mbar_fence_init();
   }
   if (warp == 4 && lane == 0) {
@@ -140,7 +142,9 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
       const uint64_t pol_a = tiles_m == 1 ? l2_policy_evict_first() : l2_policy_evict_last();
       const uint64_t pol_b = l2_policy_evict_last();
       const long long n = hi - lo;
-      const int npre = static_cast<int>(n < C::STAGES ? n : C::STAGES);
+      // weight stages issued before the wait for the previous kernel
+      const int pre_cap = p.pre_stages < 0 || p.pre_stages > C::STAGES ? C::STAGES : p.pre_stages;
+      const int npre = static_cast<int>(n < pre_cap ? n : pre_cap);
       // weight tile f at k-block kk: a 2-D box, or the interleaved QKV box
       auto load_a = [&](uint8_t* dst, const CUtensorMap* m, uint64_t* bar, int kk, int f) {
         if (p.a_heads) tma_load_4d(dst, m, bar, kk * 64, 0, 0, f * p.a_heads, pol_a);
@@ -265,6 +269,27 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
     }
     int seg = 0;
     const int row = warp * 32 + lane;
+    bool arrived = false;  // pushed cluster reduction: this thread's cluster-barrier arrival
+    // Pushed cluster reduction with a residual-add epilogue: the residual
+    // and gain of this warp's first item, when the item is this CTA's
+    // (warp = rank mod S), loaded while the mainloop runs; at the end of
+    // the kernel the memory system is busy with the next kernel's weights.
+    float old_pre[17];
+    bool pre = false;
+    if (BN <= 32 && p.split_s >= 2 && p.push && p.epi.kind == EPI_ADD) {
+      pre = warp % p.split_s == static_cast<int>(cluster_ctarank());
+      if (pre) {
+        const int tile = static_cast<int>(lo / kb);
+        const int o = (tile / tiles_m) * 128 + row, t0 = (tile % tiles_m) * BN;
+        const float* r = p.epi.resid + static_cast<size_t>(t0) * p.epi.ldr + o;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          old_pre[j] = (o < p.epi.N && t0 + j < p.epi.M) ? r[static_cast<size_t>(j) * p.epi.ldr] : 0.f;
+        old_pre[16] = (p.epi.xg && o < p.epi.N)
+                          ? __bfloat162float(static_cast<const bf16*>(p.epi.g_next)[o])
+                          : 0.f;
+      }
+    }
     for (long long u = lo; u < hi;) {
       const int tile = static_cast<int>(u / kb);
       const int k_lo = static_cast<int>(u - static_cast<long long>(tile) * kb);
@@ -286,6 +311,85 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
         });
         tc_fence_before();
         mbar_arrive(&acc_empty[acc]);
+      } else if (BN <= 32 && p.split_s >= 2 && p.push) {
+        // Pushed cluster reduction.  This CTA's MMAs are complete, so its
+        // operand stages are free: it arrives on the cluster barrier, and
+        // once every CTA of the cluster has, it sends each item's partial
+        // (read from TMEM) straight into the owner's stages with st.async,
+        // counted on the owner's recv_bar.  The owner sums its items in
+        // rank order (the same order as the pulled reduction).
+        const int S = p.split_s;
+        const int rk = static_cast<int>(cluster_ctarank());
+        fence_proxy_async_smem();
+        cluster_arrive_release();
+        arrived = true;
+        cluster_wait_acquire();
+        if (threadIdx.x == 0) tc_stamp(p, 5);
+        constexpr int NQ = C::PW / 4;   // 16-byte chunks of a row
+        auto swz = [&](int q) { return NQ == 4 ? (q ^ ((lane >> 1) & 3)) : (q ^ (lane & 7)); };
+        float* recv = reinterpret_cast<float*>(smem);
+        const uint32_t bar_local = smem_u32(recv_bar);
+        tmem_walk<BN, DUAL>(taddr, [&](int c0, const float* v, const float* v2) {
+          const int item = (c0 / 16) * 4 + warp, owner = item % S;
+          const int off = (((item / S) * S + rk) * 32 + lane) * C::PW;   // floats
+          if (owner == rk) {
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+              const float* s4 = q < 4 ? v + 4 * q : v2 + 4 * (q - 4);
+              *reinterpret_cast<float4*>(recv + off + swz(q) * 4) = make_float4(s4[0], s4[1], s4[2], s4[3]);
+            }
+          } else {
+            const uint32_t dst = cluster_map_shared(smem_u32(recv + off), owner);
+            const uint32_t mb = cluster_map_shared(bar_local, owner);
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+              const float* s4 = q < 4 ? v + 4 * q : v2 + 4 * (q - 4);
+              st_async_v4(dst + swz(q) * 16, s4[0], s4[1], s4[2], s4[3], mb);
+            }
+          }
+        });
+        tc_fence_before();
+        mbar_arrive(&acc_empty[acc]);
+        int mine = 0;   // items of this CTA
+        for (int i = rk; i < C::ITEMS; i += S) ++mine;
+        if (threadIdx.x == 0 && mine > 0)
+          mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(mine * (S - 1) * 32 * C::PW * 4));
+        {
+          bool any = false;
+          for (int c0 = 0; c0 < BN; c0 += 16) any |= ((c0 / 16) * 4 + warp) % S == rk;
+          // warp-uniform outcome: the epilogue below shuffles across lanes
+          const bool got = __all_sync(0xffffffffu, any && mbar_wait(recv_bar, 0, p.err));
+          if (got) {
+            if (lane == 0 && warp == rk % 4) tc_stamp(p, 8);
+            const bool stamp = lane == 0 && warp == rk % 4;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 16) {
+              const int item = (c0 / 16) * 4 + warp;
+              if (item % S != rk) continue;
+              float v[16], v2[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] = v2[j] = 0.f;
+              const float* base = recv + ((item / S) * S * 32 + lane) * C::PW;
+              for (int q = 0; q < S; ++q) {
+                const float* rowp = base + q * 32 * C::PW;
+#pragma unroll
+                for (int c = 0; c < NQ; ++c) {
+                  const float4 t = *reinterpret_cast<const float4*>(rowp + swz(c) * 4);
+                  float* d = c < 4 ? v + 4 * c : v2 + 4 * (c - 4);
+                  d[0] += t.x;
+                  d[1] += t.y;
+                  d[2] += t.z;
+                  d[3] += t.w;
+                }
+              }
+              if (stamp && c0 == 0) tc_stamp(p, 9);
+              epi_chunk<DUAL>(p.epi, o, m * BN + c0, v, v2, lane, staged,
+                              pre && c0 == 0 ? old_pre : nullptr);
+              if (stamp && c0 == 0) tc_stamp(p, 10);
+            }
+          }
+        }
+        if (threadIdx.x == 0) tc_stamp(p, 7);
       } else if (p.split_s >= 2) {
         // cluster split: the partial goes to this CTA's own shared memory
         // (the operand stages are all consumed); rank 0 sums the cluster's
@@ -419,7 +523,11 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
       u += k_hi - k_lo;
       ++seg;
     }
+    // every thread of the cluster arrives once, also after an abort
+    if (p.split_s >= 2 && p.push && !arrived) cluster_arrive_relaxed();
   }
+  // the producer and MMA warps arrive for their CTA (they never wait)
+  if (p.split_s >= 2 && p.push && warp >= 4) cluster_arrive_relaxed();
 
   if (threadIdx.x == 0) tc_stamp(p, 4);
   tc_fence_before();
@@ -428,7 +536,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
-  if (p.split_s >= 2) {
+  if (p.split_s >= 2 && !p.push) {
     // Every CTA of the cluster has its partial in shared memory.  The sum
     // is scattered over the cluster: the tile's (32-row group, 16-column
     // chunk) items go round-robin to the S CTAs, and the warp of that row
@@ -662,6 +770,9 @@ static cudaError_t run_tc(const CUtensorMap& a, const CUtensorMap& a2, const CUt
   if (tiles < sm_count && fits && (S >= 2 || per_sm == 2) && S >= 1 &&
       tiles * S <= per_sm * sm_count) {
     p.split_s = S;
+    // the pushed reduction receives its items in the operand stages
+    // (token tiles of at most 32; wider tiles pull)
+    if (BN > 32 || C::push_bytes(S) > C::STAGES * C::STAGE_BYTES) p.push = 0;
     if (S == 1)
       return launch_pdl(gemm_tc_kernel<BN, DUAL>, dim3(tiles), dim3(192), C::SMEM, s, a, a2, b, p);
     return launch_pdl_cluster(gemm_tc_kernel<BN, DUAL>, dim3(tiles * S), dim3(192), C::SMEM, s, S,
@@ -736,6 +847,8 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
   p.split_s = 0;
   p.a_heads = 0;
   p.tl = ws.timeline;
+  p.push = ws.cluster_push;
+  p.pre_stages = ws.pre_stages;
   if (epi.kind == EPI_ROPE_KV) {
     // one token tile whose rotary table fits the staged [BN][64] floats
     if (dual || epi.dh <= 0 || 128 % epi.dh != 0 || N % 128 != 0 || M > bn || bn > 32 ||

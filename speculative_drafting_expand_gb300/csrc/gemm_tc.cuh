@@ -44,7 +44,18 @@ struct TcCfg {
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
-  static_assert((2 * STAGES + 5) * 8 + 12 <= RS_OFF, "barrier space");
+  static_assert((2 * STAGES + 6) * 8 + 12 <= RS_OFF, "barrier space");
+  // Pushed cluster reduction: items are (32-row group, 16-column chunk)
+  // pairs, four row groups a chunk; item i belongs to cluster rank i % S,
+  // which receives every rank's 32 x PW floats of it (PW: the chunk's
+  // columns, both halves of a dual pair) into the operand stages, slot
+  // [i / S][rank].  Rows are 16-byte chunks XOR-swizzled by the row so a
+  // quarter-warp's vector accesses of one chunk fall in distinct banks.
+  static constexpr int ITEMS = 4 * (BN / 16);
+  static constexpr int PW = 16 * NA;
+  static __host__ __device__ constexpr int push_bytes(int S) {
+    return ((ITEMS + S - 1) / S) * S * 32 * PW * 4;
+  }
 };
 
 struct TcParams {
@@ -57,12 +68,16 @@ struct TcParams {
   int* err;
   int split_s;  // 0: stream-K over all units; >= 1: S CTAs (one cluster) per tile
   int a_heads;  // 0: weights by a 2-D map; else a 4-D interleaved QKV map, heads per tile
+  int push;     // cluster split: 1 pushes each item's partials to its owner (st.async), 0 pulls them
+  int pre_stages;  // weight stages loaded before the wait for the previous kernel (-1: all)
   // diagnostic timeline, or null: [cta][16] %globaltimer stamps (ns): [0]
   // start, [1] the producer's wait for the previous kernel returned, [2]
   // the first stage landed (MMA issuer), [3] the last MMA issued, [4] the
   // epilogue's main loop done, [5] every partial of the cluster ready, [8]
   // the partials of the first item summed, [7] this CTA's share of the
-  // cluster reduction applied, [6] exit
+  // cluster reduction applied, [6] exit; pushed reduction: [5] every stage
+  // of the cluster free, [8] this CTA's items received, [9] the first
+  // item summed, [10] its epilogue done
   unsigned long long* tl;
 };
 __device__ __forceinline__ void tc_stamp(const TcParams& p, int slot) {

@@ -116,6 +116,8 @@ extern "C" pe_status pe_linear_static(const void* x, const void* w, float* y, in
   ws.max_tiles = kMaxTiles;
   ws.done_counter = nullptr;  // only the argmax epilogue uses it
   ws.timeline = nullptr;
+  ws.cluster_push = 1;
+  ws.pre_stages = -1;
   ws.sm_count = sms;
   EpiArgs ep = {};
   ep.kind = EPI_STORE;

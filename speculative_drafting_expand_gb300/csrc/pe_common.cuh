@@ -287,6 +287,28 @@ __device__ __forceinline__ void cluster_sync_relaxed() {
       "barrier.cluster.arrive.relaxed.aligned;\n\t"
       "barrier.cluster.wait.aligned;" ::: "memory");
 }
+// The two halves of the cluster barrier, for threads on different paths
+// (not .aligned).  Every thread of the cluster arrives exactly once per
+// phase; a thread that never waits may leave after arriving.
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+// 16 bytes from registers into the shared memory of a cluster peer (a
+// shared::cluster address); their arrival completes 16 bytes of the
+// transaction count of the peer's mbarrier `mbar` (also shared::cluster).
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d,
+                                            uint32_t mbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+      ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(mbar)
+      : "memory");
+}
 // Address of the same shared-memory offset in cluster CTA `rank`.
 __device__ __forceinline__ uint32_t cluster_map_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;

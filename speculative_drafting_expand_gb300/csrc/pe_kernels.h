@@ -257,6 +257,8 @@ struct TcGemmWorkspace {
   int* done_counter;        // zero on entry, left zero on exit
   int sm_count;
   unsigned long long* timeline;  // diagnostic per-CTA stamps of this launch, or null
+  int cluster_push;         // cluster split-K: 1 pushes partials to their owners, 0 pulls
+  int pre_stages;           // weight stages loaded before the dependency wait (-1: all)
 };
 cudaError_t launch_gemm_tc(const void* x, int ldx, const void* w, const void* w2, int M, int N,
                            int K, const EpiArgs& epi, const TcGemmWorkspace& ws, int* err,

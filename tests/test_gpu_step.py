@@ -212,3 +212,64 @@ def test_small_batch_stream_matches_the_per_projection_path(B, K, shape):
         fin = np.isfinite(b)
         assert np.array_equal(np.isfinite(a), fin)          # the same slots written
         assert np.abs(a[fin] - b[fin]).max() <= TOL_BF16 * np.abs(b[fin]).max()
+
+
+@pytest.mark.parametrize("mask", ["none", "rope_kv", "all"])
+@pytest.mark.parametrize("B,K,shape", [(4, 5, "small"), (1, 7, "dh128"), (1, 7, "gpt-oss")])
+def test_projection_fusions_match_the_oracle(mask, B, K, shape):
+    """Each fusion option of the per-projection path (none; RoPE + KV write
+    in the QKV epilogue; that plus RMSNorm folded into the projections as a
+    row scale) matches the oracle on its own.  The RoPE epilogue reads the
+    QKV weight as an interleaved copy the drafter makes when the option is
+    switched on."""
+    Bm = G.library()
+    m = {"none": 0, "rope_kv": Bm.PE_FUSE_ROPE_KV, "all": Bm.PE_FUSE_ALL}[mask]
+    if shape == "gpt-oss":
+        wl = W.gpt_oss_b1()
+    else:
+        sh = SMALL if shape == "small" else W.small_shape(
+            "small-dh128", d=512, n_layers=2, n_heads=4, n_kv_heads=1, head_dim=128, ffn=768,
+            vocab=2048)
+        rng = np.random.default_rng(900 + B * 10 + K)
+        wl = W.custom(f"fuse-{shape}-b{B}", 900 + B, sh, K, rng.integers(20, 500, size=B),
+                      np.full(B, K + 1), rng.integers(0, K + 1, size=B), gains="random")
+    G.full_parity(wl, TOL_BF16, configure=lambda dr: Bm.pe_set_fusions(dr, m))
+
+
+@pytest.mark.parametrize("B,K,shape", [(1, 7, "gpt-oss"), (4, 7, "small"), (2, 5, "dh128")])
+def test_pushed_and_pulled_split_reductions_are_bit_identical(B, K, shape):
+    """The cluster split-K projections add their partials in rank order
+    whether the partials are pushed to the owning CTA or pulled by it, so
+    the whole step's outputs agree bit for bit; the pushed default also
+    matches the oracle on its own."""
+    Bm = G.library()
+    if shape == "gpt-oss":
+        wl = W.gpt_oss_b1()
+    else:
+        sh = SMALL if shape == "small" else W.small_shape(
+            "small-dh128", d=512, n_layers=2, n_heads=4, n_kv_heads=1, head_dim=128, ffn=768,
+            vocab=2048)
+        rng = np.random.default_rng(950 + B * 10 + K)
+        wl = W.custom(f"reduce-{shape}-b{B}", 950 + B, sh, K, rng.integers(20, 500, size=B),
+                      np.full(B, K + 1), rng.integers(0, K + 1, size=B), gains="random")
+    G.full_parity(wl, TOL_BF16, configure=lambda dr: Bm.pe_set_split_reduce(dr, Bm.PE_REDUCE_PUSH))
+    sh = wl.shape
+    inp = W.make_step_inputs(wl)
+    w = W.make_weights(sh, wl.config_id, gains=wl.gains)
+    kc, vc = W.make_kv_cache(wl, inp)
+    outs = []
+    for mode in (Bm.PE_REDUCE_PUSH, Bm.PE_REDUCE_PULL):
+        dr = G.make_drafter(sh, w, max(wl.T_out, wl.B * wl.K), wl.B)
+        Bm.pe_set_split_reduce(dr, mode)
+        st = G.DeviceStep(wl, inp, kc, vc)
+        res = G.run_step(dr, st, want_logits=True)
+        assert res["err"] == 0
+        outs.append((Bm.to_host(res["out_hidden"]), Bm.to_host(res["logits"]),
+                     Bm.to_host(res["tokens"]), [Bm.to_host(k) for k in st.kc]))
+        dr.close()
+    (h1, l1, t1, k1), (h2, l2, t2, k2) = outs
+    assert h1.tobytes() == h2.tobytes()
+    assert l1.tobytes() == l2.tobytes()
+    assert np.array_equal(t1, t2)
+    for a, b in zip(k1, k2):
+        assert a.tobytes() == b.tobytes()
