@@ -62,7 +62,11 @@ struct pe_handle {
   float* rope_tab = nullptr;           // [max_tokens, dh] cos / sin of each row's angles
   int fusions = PE_FUSE_NORM;          // epilogue fusions of the per-projection path
   int cluster_push = PE_REDUCE_PUSH;   // cluster split-K reduction: push (1) or pull (0)
-  int gemm_pre_stages = -1;            // projection weight stages loaded before the dependency wait
+  // projection weight stages loaded before the dependency wait: three
+  // (measured on the GPT-OSS-20B-shaped batch-1 step: 498-505 us against
+  // 505-513 us with all five; fewer weight loads compete with the previous
+  // kernel's epilogue; no change at batch 64)
+  int gemm_pre_stages = 3;
   float* fc_hs = nullptr;              // [d] fc(h_shared), the projected hidden of every MASK row
   int32_t* fc_map = nullptr;           // [max_tokens] target row -> compact row
   uint8_t* masked_c = nullptr;         // [max_tokens] MASK flag of every compact row

@@ -674,40 +674,64 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
             asm volatile("cp.async.wait_all;" ::: "memory");
             named_bar_sync(1, C::SOFT);
             if (threadIdx.x == 64) attn_stamp(p, 10);
-            // thread -> (row slots rr, rr + 16, ..., group of DH / 16 columns)
-            constexpr int NCOL = DH / 16;
-            const int cg = t / 16;
-            for (int rr = t % 16; rr < per; rr += 16) {
-            const int q = q0 + rr;
-            const int mlr = q / p.G, mhl = q % p.G;
-            if (q < q1 && mlr < tile_rows) {
+            // Combine in parallel passes (row maxima; the weight of every
+            // (row, split); row sums; the columns).  Every sum runs over the
+            // splits in order, with the same operations as one thread per
+            // row would use.
+            const int nr = q1 - q0;                               // rows of the slice
+            float* mx = stage + nsplits * (DH + 2) * per;          // [per]
+            float* inv = mx + per;                                 // [per]
+            float* wgt = inv + per;                                // [per][nsplits]
+            auto st_m = [&](int sp, int rr) { return stage[(sp * (DH + 2) + DH) * per + rr]; };
+            auto st_l = [&](int sp, int rr) { return stage[(sp * (DH + 2) + DH + 1) * per + rr]; };
+            // (loops over the splits without branches, unrolled: their
+            // shared-memory loads are issued together, not one round trip
+            // per split)
+            for (int rr = t; rr < nr; rr += C::SOFT) {
               float Mx = -INFINITY;
+#pragma unroll 8
               for (int sp = 0; sp < nsplits; ++sp) {
-                const float ls = stage[(sp * (DH + 2) + DH + 1) * per + rr];
-                if (ls > 0.f) Mx = fmaxf(Mx, stage[(sp * (DH + 2) + DH) * per + rr]);
+                const float l = st_l(sp, rr), m = st_m(sp, rr);
+                Mx = l > 0.f ? fmaxf(Mx, m) : Mx;
               }
-              float acc[NCOL];
-#pragma unroll
-              for (int j = 0; j < NCOL; ++j) acc[j] = 0.f;
-              float Ls = 0.f;
-              for (int sp = 0; sp < nsplits; ++sp) {
-                const float ls = stage[(sp * (DH + 2) + DH + 1) * per + rr];
-                if (!(ls > 0.f)) continue;
-                const float w = exp2f(stage[(sp * (DH + 2) + DH) * per + rr] - Mx);
-                Ls += w * ls;
-#pragma unroll
-                for (int j = 0; j < NCOL; ++j)
-                  acc[j] += w * stage[(sp * (DH + 2) + cg * NCOL + j) * per + rr];
-              }
-              const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-              bf16* o2 = static_cast<bf16*>(a.out) +
-                         (static_cast<size_t>(row0 + tile_row0 + mlr) * a.Hq + g * p.G + mhl) * DH +
-                         cg * NCOL;
-#pragma unroll
-              for (int j = 0; j < NCOL; j += 2)
-                *reinterpret_cast<__nv_bfloat162*>(o2 + j) =
-                    __floats2bfloat162_rn(acc[j] * inv, acc[j + 1] * inv);
+              mx[rr] = Mx;
             }
+            named_bar_sync(1, C::SOFT);
+            for (int it = t; it < nr * nsplits; it += C::SOFT) {
+              const int rr = it / nsplits, sp = it % nsplits;
+              wgt[it] = st_l(sp, rr) > 0.f ? exp2f(st_m(sp, rr) - mx[rr]) : 0.f;
+            }
+            named_bar_sync(1, C::SOFT);
+            for (int rr = t; rr < nr; rr += C::SOFT) {
+              float Ls = 0.f;
+#pragma unroll 8
+              for (int sp = 0; sp < nsplits; ++sp) {
+                const float ls = st_l(sp, rr), w = wgt[rr * nsplits + sp];
+                Ls = ls > 0.f ? Ls + w * ls : Ls;
+              }
+              inv[rr] = Ls > 0.f ? 1.f / Ls : 0.f;
+            }
+            named_bar_sync(1, C::SOFT);
+            // thread -> (row, column pair), rows fastest
+            for (int it = t; it < nr * (DH / 2); it += C::SOFT) {
+              const int rr = it % nr, c = (it / nr) * 2;
+              const int q = q0 + rr, mlr = q / p.G, mhl = q % p.G;
+              float a0 = 0.f, a1 = 0.f;
+#pragma unroll 8
+              for (int sp = 0; sp < nsplits; ++sp) {
+                const bool in = st_l(sp, rr) > 0.f;
+                const float w = wgt[rr * nsplits + sp];
+                const float x0 = stage[(sp * (DH + 2) + c) * per + rr];
+                const float x1 = stage[(sp * (DH + 2) + c + 1) * per + rr];
+                a0 = in ? a0 + w * x0 : a0;
+                a1 = in ? a1 + w * x1 : a1;
+              }
+              if (mlr < tile_rows) {
+                bf16* o2 = static_cast<bf16*>(a.out) +
+                           (static_cast<size_t>(row0 + tile_row0 + mlr) * a.Hq + g * p.G + mhl) * DH + c;
+                *reinterpret_cast<__nv_bfloat162*>(o2) =
+                    __floats2bfloat162_rn(a0 * inv[rr], a1 * inv[rr]);
+              }
             }
           }
           // the last split to finish its slice leaves both counts zero

@@ -370,16 +370,29 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
 #pragma unroll
               for (int j = 0; j < 16; ++j) v[j] = v2[j] = 0.f;
               const float* base = recv + ((item / S) * S * 32 + lane) * C::PW;
-              for (int q = 0; q < S; ++q) {
-                const float* rowp = base + q * 32 * C::PW;
+              // ranks in order; two ranks' loads in flight together (one
+              // for a dual pair: registers)
+              constexpr int RB = DUAL ? 1 : 2;
+              for (int q = 0; q < S; q += RB) {
+                float4 t[RB][NQ];
 #pragma unroll
-                for (int c = 0; c < NQ; ++c) {
-                  const float4 t = *reinterpret_cast<const float4*>(rowp + swz(c) * 4);
-                  float* d = c < 4 ? v + 4 * c : v2 + 4 * (c - 4);
-                  d[0] += t.x;
-                  d[1] += t.y;
-                  d[2] += t.z;
-                  d[3] += t.w;
+                for (int h = 0; h < RB; ++h)
+#pragma unroll
+                  for (int c = 0; c < NQ; ++c)
+                    t[h][c] = q + h < S ? *reinterpret_cast<const float4*>(
+                                              base + (q + h) * 32 * C::PW + swz(c) * 4)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int h = 0; h < RB; ++h) {
+                  if (q + h >= S) break;
+#pragma unroll
+                  for (int c = 0; c < NQ; ++c) {
+                    float* d = c < 4 ? v + 4 * c : v2 + 4 * (c - 4);
+                    d[0] += t[h][c].x;
+                    d[1] += t[h][c].y;
+                    d[2] += t[h][c].z;
+                    d[3] += t[h][c].w;
+                  }
                 }
               }
               if (stamp && c0 == 0) tc_stamp(p, 9);
