@@ -376,7 +376,8 @@ def run_lmhead(args, local):
     z = np.zeros(64, np.uint16)
     g = torch.Generator().manual_seed(7)
     lm = (torch.randn(sh.vocab, sh.d, generator=g) * 0.02).to(torch.bfloat16)
-    w = {k: z for k in ("emb", "fc", "norm_final")}
+    w = {k: z for k in ("emb", "norm_final")}
+    w["fc"] = np.zeros(sh.d * sh.hidden3, np.uint16)   # read at pe_create (fc of h_shared)
     w["lm_head"] = lm.view(torch.int16).numpy().view(np.uint16)
     w["h_shared"] = np.zeros(sh.hidden3, np.uint16)
     w["layers"] = [dict(qkv=z, o=z, gate=z, up=z, down=z, norm_e=z, norm_h=z, norm_in=z,
@@ -714,7 +715,8 @@ def expand_only(wl, torch, B, hbm, n):
     launch, on a drafter whose only live weight is h_shared."""
     sh = wl.shape
     z = np.zeros(64, np.uint16)
-    w = {k: z for k in ("emb", "fc", "norm_final", "lm_head")}
+    w = {k: z for k in ("emb", "norm_final", "lm_head")}
+    w["fc"] = np.zeros(sh.d * sh.hidden3, np.uint16)   # read at pe_create (fc of h_shared)
     w["h_shared"] = W.normal(wl.config_id, "h_shared", (sh.hidden3,), 0.02, sh.dtype)
     w["layers"] = [dict(qkv=z, o=z, gate=z, up=z, down=z, norm_e=z, norm_h=z, norm_in=z,
                         norm_post=z) for _ in range(sh.n_layers)]

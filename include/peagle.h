@@ -157,7 +157,9 @@ typedef struct pe_handle pe_handle;
 /* Create a handle: validates the shape, copies the layer-pointer array,
  * builds the TMA descriptors of the weights and allocates the workspace for
  * up to max_tokens expanded rows and max_reqs requests.  Weights are
- * borrowed.  Returns PE_ERR_UNSUPPORTED for shapes the kernels do not cover
+ * borrowed; every weight buffer must hold its full shape.  fc and h_shared
+ * are read here (fc of h_shared, on the default stream, synchronised before
+ * returning).  Returns PE_ERR_UNSUPPORTED for shapes the kernels do not cover
  * (d, F, hidden3 and Hq*dh must be multiples of 64; dh in {64, 128};
  * page_size 16). */
 pe_status pe_create(const pe_model_desc* desc, const pe_weights* weights,
@@ -330,9 +332,16 @@ pe_status pe_set_split_reduce(pe_handle* h, int32_t mode);
  *                            (measured on the GPT-OSS-20B-shaped batch-1
  *                            step: about 500 us against 509 us with all
  *                            five stages of the narrow token tile).
+ *   PE_TUNE_ATTN_L2_AHEAD    how many 128-key chunks of K/V pages each
+ *                            attention CTA brings into L2 ahead of its
+ *                            shared-memory ring (cp.async.bulk.prefetch;
+ *                            the first ones before its wait for the
+ *                            previous kernel), 0..64; default 0 (2, 4
+ *                            and 8 measured slower: 2900 against 3230 us
+ *                            a GPT-OSS-shaped batch-64 step).
  * Returns PE_ERR_INVALID_ARGUMENT for an unknown key or a value out of
  * range.  The results do not depend on the setting. */
-enum { PE_TUNE_GEMM_PRE_STAGES = 1 };
+enum { PE_TUNE_GEMM_PRE_STAGES = 1, PE_TUNE_ATTN_L2_AHEAD = 2 };
 pe_status pe_set_tuning(pe_handle* h, int32_t key, int32_t value);
 
 /* Tuning of the small-batch streaming kernel.  tiles: how many 16 KB

@@ -27,7 +27,8 @@ size_t attention_tc_counters(const AttnArgs& a, int max_rows_per_req, int sm_cou
 cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                 const int32_t* seq_lens, int max_rows_per_req, int sm_count,
                                 float* part, size_t part_floats, int* counters,
-                                size_t n_counters, unsigned long long* timeline, cudaStream_t s);
+                                size_t n_counters, unsigned long long* timeline, int l2_ahead,
+                                cudaStream_t s);
 cudaError_t launch_bounded_wait_check(int* flag, int32_t* out, int* err, cudaStream_t s);
 }  // namespace pe
 
@@ -67,6 +68,10 @@ struct pe_handle {
   // 505-513 us with all five; fewer weight loads compete with the previous
   // kernel's epilogue; no change at batch 64)
   int gemm_pre_stages = 3;
+  // K/V chunks the attention brings into L2 ahead of its shared-memory ring:
+  // none (measured slower with 2, 4 or 8 at batch 1, batch 64 and the Qwen
+  // batch-16 step: 2900 -> 3230 us at batch 64)
+  int attn_l2_ahead = 0;
   float* fc_hs = nullptr;              // [d] fc(h_shared), the projected hidden of every MASK row
   int32_t* fc_map = nullptr;           // [max_tokens] target row -> compact row
   uint8_t* masked_c = nullptr;         // [max_tokens] MASK flag of every compact row
@@ -412,6 +417,10 @@ pe_status pe_set_tuning(pe_handle* h, int32_t key, int32_t value) {
       if (value < -1) return PE_ERR_INVALID_ARGUMENT;
       h->gemm_pre_stages = value;
       return PE_OK;
+    case PE_TUNE_ATTN_L2_AHEAD:
+      if (value < 0 || value > 64) return PE_ERR_INVALID_ARGUMENT;
+      h->attn_l2_ahead = value;
+      return PE_OK;
     default:
       return PE_ERR_INVALID_ARGUMENT;
   }
@@ -725,7 +734,8 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
       ++h->gemm_ordinal;
       e = counted(h, launch_attention_tc(at, *tk, *tv, ex->seq_lens, max_rows_per_req,
                                          h->sm_count, h->attn_partials, h->attn_partial_floats,
-                                         h->attn_counters, h->attn_n_counters, tl, s));
+                                         h->attn_counters, h->attn_n_counters, tl,
+                                         h->attn_l2_ahead, s));
       if (e) return PE_ERR_CUDA;
     }
     if ((e = mark(2 + 2 * l))) return PE_ERR_CUDA;

@@ -50,6 +50,11 @@ struct AttnTcParams {
   // unit's splits are written (the grid is one wave, so they are all
   // resident); 0: the last split to finish merges the whole unit
   int parallel_merge;
+  // K/V chunks brought into L2 ahead of the shared-memory ring: the first
+  // l2_ahead before the wait for the previous kernel (the context pages do
+  // not depend on it; L2 is where its new rows land, so nothing stale is
+  // read), then chunk c + l2_ahead when chunk c is loaded; 0: none
+  int l2_ahead;
   // diagnostic timeline, or null: [cta][16] %globaltimer stamps (ns): [0]
   // start, [1] set up (barriers, tensor memory, block ids), [2] the wait
   // for the previous kernel returned, [3] Q in shared memory, [4] the first
@@ -61,7 +66,21 @@ struct AttnTcParams {
 
 __device__ __forceinline__ void attn_stamp(const AttnTcParams& p, int slot) {
   const unsigned cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-  if (p.tl && cta < 512) p.tl[static_cast<size_t>(cta) * 16 + slot] = global_timer_ns();
+  if (p.tl && cta < 448) p.tl[static_cast<size_t>(cta) * 16 + slot] = global_timer_ns();
+}
+// Per-chunk stamps of the CTAs of split 0, kv head 0, query tile 0 of the
+// first two requests, chunks 0..31, after the 448 CTAs' stamps: [0] the
+// chunk's K/V copies issued, [1] landed (MMA issuer), [2] S issued, [3] S
+// seen by the softmax, [4] S in registers, [5] P stored, [6] P seen by the
+// MMA issuer, [7] P.V issued; then, for the first request's CTA, every
+// softmax warp's (S seen, P stored) per chunk.
+__device__ __forceinline__ void attn_chunk_stamp(const AttnTcParams& p, int c, int slot) {
+  if (p.tl && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z < 2 && c < 32)
+    p.tl[448 * 16 + (blockIdx.z * 32 + c) * 8 + slot] = global_timer_ns();
+}
+__device__ __forceinline__ void attn_warp_stamp(const AttnTcParams& p, int c, int w, int slot) {
+  if (p.tl && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && c < 32)
+    p.tl[448 * 16 + 512 + c * 16 + w * 2 + slot] = global_timer_ns();
 }
 
 // FP8: the pools hold e4m3 codes.  Their pages come by TMA into a two-stage
@@ -72,7 +91,15 @@ struct AttnCfg {
   static constexpr int NH = DH / 64;            // 64-wide halves of the head dim
   static constexpr int KEYS = 128;              // keys per chunk (two 64-key halves)
   static constexpr int TILE = 128 * 128;        // 128 rows x 128 B
-  static constexpr int KV_STAGES = DH == 64 ? 3 : 2;
+  // K/V ring depth: a stage is held from its copy until P.V has read it,
+  // so the ring covers the copy latency only while it has stages left.
+  // Two P buffers: with one, the softmax of chunk c + 1 stores P only
+  // after P.V of chunk c, which waits for the slowest softmax warp (five
+  // stages and one buffer measured no faster than three and two at batch
+  // 64).  Four stages at dh 64 (three with the fp8 staging ring), two at
+  // dh 128.
+  static constexpr int KV_STAGES = DH == 64 ? (FP8 ? 3 : 4) : 2;
+  static constexpr int P_BUFS = 2;
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + NH * TILE;                 // [stage][NH]
   static constexpr int V_OFF = K_OFF + KV_STAGES * NH * TILE;     // [stage][NH]
@@ -86,7 +113,8 @@ struct AttnCfg {
   // float[2 NQ][128] for combining the slices; used only after the last
   // P.V has finished reading P, so it shares P's space
   static constexpr int RED_OFF = P_OFF;
-  static constexpr int BAR_OFF = P_OFF + 4 * TILE;
+  static constexpr int BAR_OFF = P_OFF + 2 * P_BUFS * TILE;
+  __host__ __device__ static constexpr int pbuf(int c) { return P_BUFS == 1 ? 0 : (c & 1); }
   // block ids of the CTA's pages, read once: a split covers at most
   // BT_ENTRIES pages of 16 keys (32 chunks)
   static constexpr int BT_ENTRIES = 256;
@@ -237,6 +265,24 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
       __syncwarp();
     }
     if (lane == 0) attn_stamp(p, 1);
+    // the pages of chunk c into L2 (valid block ids only)
+    auto prefetch_chunk = [&](int c) {
+      const int t0 = key0 + c * C::KEYS;
+#pragma unroll
+      for (int pg = 0; pg < 8; ++pg) {
+        const int b = t0 + pg * 16 < key1 ? bt_s[c * 8 + pg] : -1;
+        if (b < 0) continue;
+        const int row = (b * a.Hkv + g) * 16;
+#pragma unroll
+        for (int h = 0; h < (FP8 ? 1 : C::NH); ++h) {
+          tma_prefetch_l2_2d(&tmK, h * 64, row);
+          tma_prefetch_l2_2d(&tmV, h * 64, row);
+        }
+      }
+    };
+    const int ahead = min(p.l2_ahead, nchunks);
+    if (lane == 0)
+      for (int c = 0; c < ahead; ++c) prefetch_chunk(c);
     grid_dep_wait();   // the previous kernel wrote this step's K/V
     if (lane == 0) attn_stamp(p, 2);
     if constexpr (!FP8) {
@@ -258,6 +304,8 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
             if (blks[pg] >= 0) bytes += 2u * C::NH * 2048u;
           }
           mbar_arrive_expect_tx(&kv_full[st], bytes);
+          attn_chunk_stamp(p, c, 0);
+          if (ahead > 0 && c + ahead < nchunks) prefetch_chunk(c + ahead);
   #pragma unroll
           for (int pg = 0; pg < 8; ++pg) {
             if (blks[pg] < 0) continue;
@@ -307,6 +355,7 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         for (int c = 0; c < min(nchunks, C::F8_STAGES); ++c) issue8(c);
+        for (int c = ahead; c < min(nchunks, ahead + C::F8_STAGES); ++c) prefetch_chunk(c);
       }
       int issued = min(nchunks, C::F8_STAGES), consumed = 0;
       for (int c = 0; c < nchunks; ++c) {
@@ -345,6 +394,8 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
         if (lane == 0) {
           mbar_arrive(&kv_full[st]);
           if (c + C::F8_STAGES < nchunks) issue8(c + C::F8_STAGES);
+          if (ahead > 0 && c + C::F8_STAGES + ahead < nchunks)
+            prefetch_chunk(c + C::F8_STAGES + ahead);
         }
         if (c + C::F8_STAGES < nchunks) issued = c + C::F8_STAGES + 1;
         __syncwarp();
@@ -359,11 +410,9 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t q_addr = smem_u32(smem + C::Q_OFF);
-      // S(c) = Q K(c)^T into TMEM columns 0..127
-      auto issue_s = [&](int c) -> bool {
+      // S(c) = Q K(c)^T into TMEM columns (c & 1) * 128 .. + 127
+      auto issue_s = [&](int c) {
         const int st = c % C::KV_STAGES;
-        if (!mbar_wait(&kv_full[st], (c / C::KV_STAGES) & 1, a.err)) return false;
-        if (c >= 2 && !mbar_wait(&s_free[c & 1], ((c - 2) >> 1) & 1, a.err)) return false;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(smem + C::K_OFF + st * C::NH * C::TILE);
 #pragma unroll
@@ -374,19 +423,15 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
                       sw128_kmajor_desc(k_addr + h * C::TILE + k4 * 32), C::IDESC_S,
                       (h | k4) != 0);
         umma_commit(&s_full[c & 1]);
-        return true;
+        attn_chunk_stamp(p, c, 2);
       };
-      bool ok = mbar_wait(q_ready, 0, a.err) && issue_s(0);
-      for (int c = 0; c < nchunks && ok; ++c) {
-        // the next chunk's scores are computed while this chunk's softmax runs
-        if (c + 1 < nchunks && !issue_s(c + 1)) break;
-        if (!mbar_wait(&p_full[c & 1], (c >> 1) & 1, a.err)) break;
+      // O_h += P(keys of slice h) V(keys of slice h), per 64-wide part of
+      // dh; P is stored as two 64-key half tiles
+      auto issue_pv = [&](int c) {
         tc_fence_after();
         const int st = c % C::KV_STAGES;
         const uint32_t v_addr = smem_u32(smem + C::V_OFF + st * C::NH * C::TILE);
-        const uint32_t p_addr = smem_u32(smem + C::P_OFF + (c & 1) * 2 * C::TILE);
-        // O_h += P(keys of slice h) V(keys of slice h), per 64-wide part of
-        // dh; P is stored as two 64-key half tiles
+        const uint32_t p_addr = smem_u32(smem + C::P_OFF + C::pbuf(c) * 2 * C::TILE);
 #pragma unroll
         for (int sl = 0; sl < C::NQ; ++sl)
 #pragma unroll
@@ -402,6 +447,45 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
           }
         umma_commit(&kv_empty[st]);
         umma_commit(&pv_done[c & 1]);
+        attn_chunk_stamp(p, c, 7);
+      };
+      // S(c) needs chunk c's copy and, from c = 2 on, the softmax's read of
+      // S(c - 2) (its buffer); P.V(c) needs P(c).  One thread polls both and
+      // issues whichever is ready -- S first, and S at most one chunk ahead
+      // of P.V (P.V is on the softmax's critical path) -- so that P.V(c)
+      // never waits for chunk c + 1's copy.  A bounded poll: no progress
+      // for kWaitTimeoutNs records PE_DEV_TIMEOUT and stops.
+      bool ok = mbar_wait(q_ready, 0, a.err);
+      int cs = 0, cp = 0;            // next S, next P.V
+      unsigned long long idle_since = 0;
+      while (ok && cp < nchunks) {
+        bool did = false;
+        if (cs < nchunks && cs <= cp + 1 &&
+            mbar_test_wait(&kv_full[cs % C::KV_STAGES], (cs / C::KV_STAGES) & 1) &&
+            (cs < 2 || mbar_test_wait(&s_free[cs & 1], ((cs - 2) >> 1) & 1))) {
+          attn_chunk_stamp(p, cs, 1);
+          issue_s(cs);
+          ++cs;
+          did = true;
+        }
+        if (cp < cs && mbar_test_wait(&p_full[cp & 1], (cp >> 1) & 1)) {
+          attn_chunk_stamp(p, cp, 6);
+          issue_pv(cp);
+          ++cp;
+          did = true;
+        }
+        if (did) {
+          idle_since = 0;
+        } else {
+          // idle: yield the scheduler to the softmax warps that share it
+          __nanosleep(64);
+          if (idle_since == 0) {
+            idle_since = global_timer_ns();
+          } else if (global_timer_ns() - idle_since > kWaitTimeoutNs) {
+            record_error(a.err, PE_DEV_TIMEOUT);
+            ok = false;
+          }
+        }
       }
       umma_commit(drain);
       mbar_wait(drain, 0, a.err);
@@ -450,81 +534,111 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     const uint32_t o_col = C::O_COL + h * DH;
+    // rows that read no key of this split (padding, rejected, or a position
+    // before the split): P rows of zeros, l = 0
+    const bool dead = P < key0;
+    const bool warp_dead = __all_sync(0xffffffffu, dead);
     for (int c = 0; c < nchunks; ++c) {
       if (!mbar_wait(&s_full[c & 1], (c >> 1) & 1, a.err)) { ok = false; break; }
       if (c == 0 && threadIdx.x == 64) attn_stamp(p, 4);
+      if (threadIdx.x == 64) attn_chunk_stamp(p, c, 3);
+      if (lane == 0) attn_warp_stamp(p, c, warp - 2, 0);
       tc_fence_after();
       constexpr int KPW = C::KPW;
-      float sv[KPW / 16][16];
-#pragma unroll
-      for (int q = 0; q < KPW / 16; ++q)
-        tmem_ld16(tmem + lane_off + (c & 1) * 128 + h * KPW + q * 16, sv[q]);
-      tmem_ld_wait();
-#pragma unroll
-      for (int q = 0; q < KPW / 16; ++q) reg_fence16(sv[q]);
-      const float* s = &sv[0][0];
-      tc_fence_before();
-      mbar_arrive(&s_free[c & 1]);                  // this S buffer may be reused
-      const int tb = key0 + c * C::KEYS + h * KPW;  // first key of this slice
-      const bool whole = tb + KPW - 1 <= P;         // no masking inside
-      // masked maximum (four independent chains)
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (whole) {
-        // two scores per instruction in each of the four chains
-#pragma unroll
-        for (int j = 0; j < KPW; j += 8) {
-          m4[0] = fmax3(m4[0], s[j], s[j + 1]);
-          m4[1] = fmax3(m4[1], s[j + 2], s[j + 3]);
-          m4[2] = fmax3(m4[2], s[j + 4], s[j + 5]);
-          m4[3] = fmax3(m4[3], s[j + 6], s[j + 7]);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < KPW; ++j)
-          if (tb + j <= P) m4[j & 3] = fmaxf(m4[j & 3], s[j]);
-      }
-      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sc;  // sc > 0
-      // lazy rescale: keep the old reference unless the max grew past 2^8
-      float m_new = m_used, factor = 1.f;
-      if (mx > -INFINITY) {
-        if (m_used == -INFINITY) m_new = mx;
-        else if (mx > m_used + 8.f) {
-          m_new = mx;
-          factor = fast_exp2(m_used - mx);
-        }
-      }
-      // probabilities: one FFMA and one MUFU.EX2 a score; the row sum is
-      // kept in fp32 (two chains), P goes to the MMA as bf16 pairs (f16
-      // with fp8 pools)
       uint32_t pk[KPW / 2];
-      float ps0 = 0.f, ps1 = 0.f;
-      const float nm = -m_new;
-      if (whole) {
+      float factor = 1.f;
+      if (warp_dead) {
+        // no row of this warp reads a key of this split: its P rows are
+        // zeros, nothing else to compute
+        tc_fence_before();
+        mbar_arrive(&s_free[c & 1]);
 #pragma unroll
-        for (int j = 0; j < KPW; j += 2) {
-          const float p0 = fast_exp2(fmaf(s[j], sc, nm));
-          const float p1 = fast_exp2(fmaf(s[j + 1], sc, nm));
-          ps0 += p0;
-          ps1 += p1;
-          pk[j / 2] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
-        }
+        for (int j = 0; j < KPW / 2; ++j) pk[j] = 0u;
       } else {
+        float sv[KPW / 16][16];
 #pragma unroll
-        for (int j = 0; j < KPW; j += 2) {
-          const float e0 = fast_exp2(fmaf(s[j], sc, nm));
-          const float e1 = fast_exp2(fmaf(s[j + 1], sc, nm));
-          const float p0 = (tb + j <= P) ? e0 : 0.f;
-          const float p1 = (tb + j + 1 <= P) ? e1 : 0.f;
-          ps0 += p0;
-          ps1 += p1;
-          pk[j / 2] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+        for (int q = 0; q < KPW / 16; ++q)
+          tmem_ld16(tmem + lane_off + (c & 1) * 128 + h * KPW + q * 16, sv[q]);
+        tmem_ld_wait();
+        if (threadIdx.x == 64) attn_chunk_stamp(p, c, 4);
+#pragma unroll
+        for (int q = 0; q < KPW / 16; ++q) reg_fence16(sv[q]);
+        const float* s = &sv[0][0];
+        tc_fence_before();
+        mbar_arrive(&s_free[c & 1]);                  // this S buffer may be reused
+        const int tb = key0 + c * C::KEYS + h * KPW;  // first key of this slice
+        // no masking inside the slice for any row of the warp (one path for
+        // the warp: a row with no key of the split counts as unmasked, its
+        // probabilities are replaced by zeros below)
+        const bool whole = __all_sync(0xffffffffu, dead || tb + KPW - 1 <= P);
+        // masked maximum (four independent chains)
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (whole) {
+          // two scores per instruction in each of the four chains
+#pragma unroll
+          for (int j = 0; j < KPW; j += 8) {
+            m4[0] = fmax3(m4[0], s[j], s[j + 1]);
+            m4[1] = fmax3(m4[1], s[j + 2], s[j + 3]);
+            m4[2] = fmax3(m4[2], s[j + 4], s[j + 5]);
+            m4[3] = fmax3(m4[3], s[j + 6], s[j + 7]);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < KPW; ++j)
+            if (tb + j <= P) m4[j & 3] = fmaxf(m4[j & 3], s[j]);
         }
+        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sc;  // sc > 0
+        // lazy rescale: keep the old reference unless the max grew past 2^8
+        float m_new = m_used;
+        if (mx > -INFINITY && !dead) {
+          if (m_used == -INFINITY) m_new = mx;
+          else if (mx > m_used + 8.f) {
+            m_new = mx;
+            factor = fast_exp2(m_used - mx);
+          }
+        }
+        // probabilities: one FFMA and one MUFU.EX2 a score; the row sum is
+        // kept in fp32 (two chains), P goes to the MMA as bf16 pairs (f16
+        // with fp8 pools)
+        float ps0 = 0.f, ps1 = 0.f;
+        const float nm = -m_new;
+        if (whole) {
+#pragma unroll
+          for (int j = 0; j < KPW; j += 2) {
+            const float p0 = fast_exp2(fmaf(s[j], sc, nm));
+            const float p1 = fast_exp2(fmaf(s[j + 1], sc, nm));
+            ps0 += p0;
+            ps1 += p1;
+            pk[j / 2] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+          }
+          if (dead) {
+#pragma unroll
+            for (int j = 0; j < KPW / 2; ++j) pk[j] = 0u;
+            ps0 = ps1 = 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < KPW; j += 2) {
+            const float e0 = fast_exp2(fmaf(s[j], sc, nm));
+            const float e1 = fast_exp2(fmaf(s[j + 1], sc, nm));
+            const float p0 = (tb + j <= P) ? e0 : 0.f;
+            const float p1 = (tb + j + 1 <= P) ? e1 : 0.f;
+            ps0 += p0;
+            ps1 += p1;
+            pk[j / 2] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+          }
+        }
+        const float psum = ps0 + ps1;
+        l = l * factor + psum;
+        m_used = m_new;
       }
-      const float psum = ps0 + ps1;
-      l = l * factor + psum;
-      m_used = m_new;
-      // the P buffer of this chunk was last read by P.V two chunks ago
-      if (c >= 2 && !mbar_wait(&pv_done[c & 1], ((c - 2) >> 1) & 1, a.err)) { ok = false; break; }
+      // the P buffer of this chunk was last read by an earlier P.V (one
+      // buffer: the previous chunk's; two: the one before it)
+      if (c >= C::P_BUFS &&
+          !mbar_wait(&pv_done[(c - C::P_BUFS) & 1], ((c - C::P_BUFS) >> 1) & 1, a.err)) {
+        ok = false;
+        break;
+      }
       // O must hold every earlier chunk before it is rescaled
       if (c >= 1 && __any_sync(0xffffffffu, factor != 1.f)) {
         if (!mbar_wait(&pv_done[(c - 1) & 1], ((c - 1) >> 1) & 1, a.err)) { ok = false; break; }
@@ -544,7 +658,7 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
       // P row of this slice -> its 16-byte chunks of the 64-key half tile
       // of the chunk's P buffer that holds it (128-byte swizzle)
       {
-        uint8_t* pt = smem + C::P_OFF + ((c & 1) * 2 + (h * KPW) / 64) * C::TILE + qrow * 128;
+        uint8_t* pt = smem + C::P_OFF + (C::pbuf(c) * 2 + (h * KPW) / 64) * C::TILE + qrow * 128;
         const int cb = ((h * KPW) % 64) / 8;
 #pragma unroll
         for (int cc = 0; cc < KPW / 8; ++cc)
@@ -567,6 +681,8 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full[c & 1]);
+      if (threadIdx.x == 64) attn_chunk_stamp(p, c, 5);
+      if (lane == 0) attn_warp_stamp(p, c, warp - 2, 1);
     }
     if (ok && !mbar_wait(&pv_done[(nchunks - 1) & 1], ((nchunks - 1) >> 1) & 1, a.err)) ok = false;
     if (threadIdx.x == 64) attn_stamp(p, 5);
@@ -907,7 +1023,8 @@ cudaError_t init_attention_tc() {
 cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                 const int32_t* seq_lens, int max_rows_per_req, int sm_count,
                                 float* part, size_t part_floats, int* counters,
-                                size_t n_counters, unsigned long long* timeline, cudaStream_t s) {
+                                size_t n_counters, unsigned long long* timeline, int l2_ahead,
+                                cudaStream_t s) {
   if (a.rows <= 0) return cudaSuccess;
   const AttnPlan pl = plan_attention(a, max_rows_per_req, sm_count);
   AttnTcParams p;
@@ -921,6 +1038,7 @@ cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const
   p.part = part;
   p.counters = counters;
   p.tl = timeline;
+  p.l2_ahead = l2_ahead < 0 ? 0 : l2_ahead;
   // every split CTA resident at once (one wave of one CTA per SM), at most
   // 32 splits: the splits merge their unit in parallel
   const long long ctas = static_cast<long long>(pl.max_splits) * a.Hkv * pl.qtiles * a.B;

@@ -23,7 +23,9 @@ def _lm_drafter(V, d, lm, max_tokens):
     sh = W.small_shape("tie", d=d, n_layers=1, n_heads=1, n_kv_heads=1, head_dim=64,
                        ffn=64, vocab=V)
     z = np.zeros(64, np.uint16)
-    w = {k: z for k in ("emb", "fc", "norm_final")}
+    w = {k: z for k in ("emb", "norm_final")}
+    # fc is read at pe_create (fc of h_shared): full size
+    w["fc"] = np.zeros(sh.d * sh.hidden3, np.uint16)
     w["lm_head"] = lm
     w["h_shared"] = np.zeros(sh.hidden3, np.uint16)
     w["layers"] = [dict(qkv=z, o=z, gate=z, up=z, down=z, norm_e=z, norm_h=z, norm_in=z,

@@ -16,10 +16,12 @@ pytestmark = pytest.mark.gpu
 
 
 def _expand_drafter(shape, max_tokens, max_reqs):
-    """A handle whose only real weight is h_shared (expansion needs no other)."""
+    """A handle whose only real weight is h_shared (expansion needs no
+    other); fc is read at pe_create (fc of h_shared), so it is full size."""
     dt = shape.dtype
     z = np.zeros(64, np.uint16 if dt == "bf16" else np.float32)
-    w = {k: z for k in ("emb", "fc", "norm_final", "lm_head")}
+    w = {k: z for k in ("emb", "norm_final", "lm_head")}
+    w["fc"] = np.zeros(shape.d * shape.hidden3, z.dtype)
     w["h_shared"] = W.normal(77, "h_shared", (shape.hidden3,), 0.02, dt)
     w["layers"] = [dict(qkv=z, o=z, gate=z, up=z, down=z, norm_e=z, norm_h=z, norm_in=z, norm_post=z)
                    for _ in range(shape.n_layers)]

@@ -39,8 +39,9 @@ def _handle(max_tokens, widest=8192):
     shape = W.small_shape("lin", d=64, n_layers=1, n_heads=1, n_kv_heads=1, head_dim=64,
                           ffn=64, vocab=max(8192, widest))
     z = np.zeros(64, np.uint16)
-    w = {k: z for k in ("emb", "fc", "norm_final", "lm_head", "h_shared")}
+    w = {k: z for k in ("emb", "norm_final", "lm_head")}
     w["h_shared"] = np.zeros(shape.hidden3, np.uint16)
+    w["fc"] = np.zeros(shape.d * shape.hidden3, np.uint16)   # read at pe_create
     w["layers"] = [dict(qkv=z, o=z, gate=z, up=z, down=z, norm_e=z, norm_h=z, norm_in=z, norm_post=z)]
     return G.make_drafter(shape, w, max_tokens, 1)
 
