@@ -309,6 +309,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
         tmem_walk<BN, DUAL>(taddr, [&](int c0, const float* v, const float* v2) {
           epi_chunk<DUAL>(p.epi, o, m * BN + c0, v, v2, lane, staged);
         });
+        if (threadIdx.x == 0) tc_stamp(p, 14);
         tc_fence_before();
         mbar_arrive(&acc_empty[acc]);
       } else if (BN <= 32 && p.split_s >= 2 && p.push) {
@@ -421,6 +422,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
         mbar_arrive(&acc_empty[acc]);
       } else {
         const int slot = (u == lo) ? 0 : 1;
+        if (threadIdx.x == 0) tc_stamp(p, 13);
         float* wsp = p.ws + (static_cast<size_t>(cta) * 2 + slot) * (128 * C::ACC_COLS);
         tmem_walk<BN, DUAL>(taddr, [&](int c0, const float* v, const float* v2) {
 #pragma unroll
@@ -438,6 +440,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
         if (threadIdx.x == 0) {
           const int old = atomicAdd(p.counters + tile, 1);
           *flag = (old == c_last - c_first) ? 1 : 0;
+          tc_stamp(p, 11);
         }
         named_bar_sync(1, 128);
         // contributors the pipelined path holds in registers: a tile spans at
@@ -495,7 +498,10 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
               finish(c0 + 16, xb);
             }
           }
-          if (threadIdx.x == 0) p.counters[tile] = 0;
+          if (threadIdx.x == 0) {
+            p.counters[tile] = 0;
+            tc_stamp(p, 12);
+          }
         } else if (*flag) {
           __threadfence();
           for (int c0 = 0; c0 < BN; c0 += 16) {
@@ -530,7 +536,10 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
             }
             epi_chunk<DUAL>(p.epi, o, m * BN + c0, v, v2, lane, staged);
           }
-          if (threadIdx.x == 0) p.counters[tile] = 0;
+          if (threadIdx.x == 0) {
+            p.counters[tile] = 0;
+            tc_stamp(p, 12);
+          }
         }
       }
       u += k_hi - k_lo;

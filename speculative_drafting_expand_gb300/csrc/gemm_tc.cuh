@@ -77,7 +77,9 @@ struct TcParams {
   // the partials of the first item summed, [7] this CTA's share of the
   // cluster reduction applied, [6] exit; pushed reduction: [5] every stage
   // of the cluster free, [8] this CTA's items received, [9] the first
-  // item summed, [10] its epilogue done
+  // item summed, [10] its epilogue done; stream-K: [13] the last partial
+  // store began, [11] its contributor count taken, [12] the last fix-up
+  // done, [14] the last whole tile's epilogue done
   unsigned long long* tl;
 };
 __device__ __forceinline__ void tc_stamp(const TcParams& p, int slot) {
