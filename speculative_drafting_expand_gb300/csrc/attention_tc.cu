@@ -91,19 +91,23 @@ struct AttnCfg {
   static constexpr int NH = DH / 64;            // 64-wide halves of the head dim
   static constexpr int KEYS = 128;              // keys per chunk (two 64-key halves)
   static constexpr int TILE = 128 * 128;        // 128 rows x 128 B
-  // K/V ring depth: a stage is held from its copy until P.V has read it,
-  // so the ring covers the copy latency only while it has stages left.
-  // Two P buffers: with one, the softmax of chunk c + 1 stores P only
-  // after P.V of chunk c, which waits for the slowest softmax warp (five
-  // stages and one buffer measured no faster than three and two at batch
-  // 64).  Four stages at dh 64 (three with the fp8 staging ring), two at
-  // dh 128.
-  static constexpr int KV_STAGES = DH == 64 ? (FP8 ? 3 : 4) : 2;
-  static constexpr int P_BUFS = 2;
+  // K/V rings.  At dh 128 K and V are separate rings: a K stage is free
+  // once S of its chunk is computed, a V stage only once P.V has read it,
+  // so V is the deeper ring (two K, three V stages: the Qwen-shaped batch
+  // 16 step 912 -> 857 us), with one P buffer to make room.  At dh 64 one
+  // ring carries K and V of a chunk together (four stages, three with the
+  // fp8 staging ring; split rings of 3 + 5 or 4 + 4 stages measured 6 %
+  // slower there) and two P buffers (with one, the softmax of chunk c + 1
+  // stores P only after P.V of chunk c, which waits for the slowest softmax
+  // warp).
+  static constexpr bool SPLIT = DH != 64;
+  static constexpr int K_STAGES = DH == 64 ? (FP8 ? 3 : 4) : 2;
+  static constexpr int V_STAGES = DH == 64 ? (FP8 ? 3 : 4) : 3;
+  static constexpr int P_BUFS = DH == 64 ? 2 : 1;
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + NH * TILE;                 // [stage][NH]
-  static constexpr int V_OFF = K_OFF + KV_STAGES * NH * TILE;     // [stage][NH]
-  static constexpr int P_OFF = V_OFF + KV_STAGES * NH * TILE;     // [buffer][key half]
+  static constexpr int V_OFF = K_OFF + K_STAGES * NH * TILE;      // [stage][NH]
+  static constexpr int P_OFF = V_OFF + V_STAGES * NH * TILE;      // [buffer][key half]
   // Key slices of a chunk: each query row is served by NQ softmax threads,
   // one per KPW-key slice, each with its own running max, sum and O.  Two
   // slices (8 softmax warps); four (16 warps) measured no faster at dh 64.
@@ -133,6 +137,8 @@ struct AttnCfg {
   static constexpr uint32_t IDESC_PV =
       FP8 ? idesc_f16_f32_bmn(128, 64) : idesc_bf16_f32_bmn(128, 64);
   static_assert(SMEM <= 232448, "shared memory");
+  static_assert((2 * K_STAGES + 2 * V_STAGES + 16) * 8 <= 256, "barrier space");
+  static_assert(SPLIT || K_STAGES == V_STAGES, "one ring");
   static_assert(!FP8 || DH == 64, "the fp8 pools are read at dh 64");
   static_assert(O_COL + NQ * DH <= TMEM_COLS && KPW % 16 == 0, "slices");
 };
@@ -146,9 +152,12 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-  uint64_t* kv_full = bars;                       // [KV_STAGES]
-  uint64_t* kv_empty = bars + C::KV_STAGES;       // [KV_STAGES]
-  uint64_t* q_ready = bars + 2 * C::KV_STAGES;
+  // one ring (dh 64): the V barriers are the K barriers
+  uint64_t* k_full = bars;                                              // [K_STAGES]
+  uint64_t* k_empty = k_full + C::K_STAGES;                             // [K_STAGES]
+  uint64_t* v_full = C::SPLIT ? k_empty + C::K_STAGES : k_full;         // [V_STAGES]
+  uint64_t* v_empty = C::SPLIT ? v_full + C::V_STAGES : k_empty;        // [V_STAGES]
+  uint64_t* q_ready = bars + 2 * C::K_STAGES + (C::SPLIT ? 2 * C::V_STAGES : 0);
   // [2] each: one per S buffer.  S(c + 2) reuses the buffer of S(c), so it
   // waits only until every softmax warp has read S(c): the next chunk's
   // scores are ready when the slowest warp gets to them.
@@ -204,9 +213,13 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
   const int nchunks = (key1 - key0 + C::KEYS - 1) / C::KEYS;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::KV_STAGES; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+    for (int i = 0; i < C::K_STAGES; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < (C::SPLIT ? C::V_STAGES : 0); ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
     }
     mbar_init(q_ready, 1);
     mbar_init(&s_full[0], 1);
@@ -291,9 +304,8 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
         tma_prefetch_desc(&tmV);
         const uint64_t pol = l2_policy_evict_first();
         for (int c = 0; c < nchunks; ++c) {
-          const int st = c % C::KV_STAGES;
-          const int round = c / C::KV_STAGES;
-          if (round > 0 && !mbar_wait(&kv_empty[st], (round - 1) & 1, a.err)) break;
+          const int ks = c % C::K_STAGES, kround = c / C::K_STAGES;
+          const int vs = c % C::V_STAGES, vround = c / C::V_STAGES;
           const int t0 = key0 + c * C::KEYS;
           int blks[8];
           uint32_t bytes = 0;
@@ -301,9 +313,12 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
           for (int pg = 0; pg < 8; ++pg) {
             const int t = t0 + pg * 16;
             blks[pg] = t < key1 ? bt_s[c * 8 + pg] : -1;
-            if (blks[pg] >= 0) bytes += 2u * C::NH * 2048u;
+            if (blks[pg] >= 0) bytes += C::NH * 2048u;
           }
-          mbar_arrive_expect_tx(&kv_full[st], bytes);
+          // K of the chunk once S of the chunk K_STAGES back is computed (one
+          // ring: K and V once P.V of that chunk has read the stage)
+          if (kround > 0 && !mbar_wait(&k_empty[ks], (kround - 1) & 1, a.err)) break;
+          mbar_arrive_expect_tx(&k_full[ks], C::SPLIT ? bytes : 2 * bytes);
           attn_chunk_stamp(p, c, 0);
           if (ahead > 0 && c + ahead < nchunks) prefetch_chunk(c + ahead);
   #pragma unroll
@@ -312,16 +327,33 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
             const int row = (blks[pg] * a.Hkv + g) * 16;
   #pragma unroll
             for (int h = 0; h < C::NH; ++h) {
-              uint8_t* kd = smem + C::K_OFF + (st * C::NH + h) * C::TILE + pg * 2048;
-              uint8_t* vd = smem + C::V_OFF + (st * C::NH + h) * C::TILE + pg * 2048;
-              tma_load_2d(kd, &tmK, &kv_full[st], h * 64, row, pol);
-              tma_load_2d(vd, &tmV, &kv_full[st], h * 64, row, pol);
+              tma_load_2d(smem + C::K_OFF + (ks * C::NH + h) * C::TILE + pg * 2048, &tmK,
+                          &k_full[ks], h * 64, row, pol);
+              if (!C::SPLIT)
+                tma_load_2d(smem + C::V_OFF + (ks * C::NH + h) * C::TILE + pg * 2048, &tmV,
+                            &k_full[ks], h * 64, row, pol);
             }
+          }
+          if (!C::SPLIT) continue;
+          // V of the chunk once P.V of the chunk V_STAGES back has read it
+          if (vround > 0 && !mbar_wait(&v_empty[vs], (vround - 1) & 1, a.err)) break;
+          mbar_arrive_expect_tx(&v_full[vs], bytes);
+  #pragma unroll
+          for (int pg = 0; pg < 8; ++pg) {
+            if (blks[pg] < 0) continue;
+            const int row = (blks[pg] * a.Hkv + g) * 16;
+  #pragma unroll
+            for (int h = 0; h < C::NH; ++h)
+              tma_load_2d(smem + C::V_OFF + (vs * C::NH + h) * C::TILE + pg * 2048, &tmV,
+                          &v_full[vs], h * 64, row, pol);
           }
         }
         // drain: the copies of the last stages have landed before exit
-        for (int c = max(0, nchunks - C::KV_STAGES); c < nchunks; ++c)
-          mbar_wait(&kv_full[c % C::KV_STAGES], (c / C::KV_STAGES) & 1, a.err);
+        for (int c = max(0, nchunks - C::K_STAGES); c < nchunks; ++c)
+          mbar_wait(&k_full[c % C::K_STAGES], (c / C::K_STAGES) & 1, a.err);
+        if (C::SPLIT)
+          for (int c = max(0, nchunks - C::V_STAGES); c < nchunks; ++c)
+            mbar_wait(&v_full[c % C::V_STAGES], (c / C::V_STAGES) & 1, a.err);
       }
     } else {
       // fp8 pages by TMA into the staging ring (lane 0), widened to f16 in
@@ -359,13 +391,18 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
       }
       int issued = min(nchunks, C::F8_STAGES), consumed = 0;
       for (int c = 0; c < nchunks; ++c) {
-        const int s8 = c & 1, st = c % C::KV_STAGES, round = c / C::KV_STAGES;
+        const int s8 = c & 1;
+        const int ks = c % C::K_STAGES, kround = c / C::K_STAGES;
+        const int vs = c % C::V_STAGES, vround = c / C::V_STAGES;
         // every lane waits (each needs the barrier's acquire); the outcome is
         // made warp-uniform so the lanes leave together
         if (!__all_sync(0xffffffffu, mbar_wait(&kv8_full[s8], (c >> 1) & 1, a.err))) break;
         consumed = c + 1;
-        if (round > 0 &&
-            !__all_sync(0xffffffffu, mbar_wait(&kv_empty[st], (round - 1) & 1, a.err)))
+        if (kround > 0 &&
+            !__all_sync(0xffffffffu, mbar_wait(&k_empty[ks], (kround - 1) & 1, a.err)))
+          break;
+        if (C::SPLIT && vround > 0 &&
+            !__all_sync(0xffffffffu, mbar_wait(&v_empty[vs], (vround - 1) & 1, a.err)))
           break;
         const int t0 = key0 + c * C::KEYS;
         const uint8_t* src = f8 + s8 * C::F8_STAGE;
@@ -385,14 +422,15 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
           }
           // row kk of the 128-byte-swizzled stage: dims q4*16 .. +15 are its
           // 16-byte chunks 2 q4 and 2 q4 + 1
-          uint8_t* dst = smem + (which ? C::V_OFF : C::K_OFF) + st * C::TILE + kk * 128;
+          uint8_t* dst = smem + (which ? C::V_OFF + vs * C::TILE : C::K_OFF + ks * C::TILE) + kk * 128;
           *reinterpret_cast<uint4*>(dst + (((2 * q4) ^ (kk & 7)) * 16)) = lo;
           *reinterpret_cast<uint4*>(dst + (((2 * q4 + 1) ^ (kk & 7)) * 16)) = hi;
         }
         fence_proxy_async_smem();   // the stage's f16 rows, for the MMA's reads
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&kv_full[st]);
+          mbar_arrive(&k_full[ks]);
+          if (C::SPLIT) mbar_arrive(&v_full[vs]);
           if (c + C::F8_STAGES < nchunks) issue8(c + C::F8_STAGES);
           if (ahead > 0 && c + C::F8_STAGES + ahead < nchunks)
             prefetch_chunk(c + C::F8_STAGES + ahead);
@@ -412,9 +450,9 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
       const uint32_t q_addr = smem_u32(smem + C::Q_OFF);
       // S(c) = Q K(c)^T into TMEM columns (c & 1) * 128 .. + 127
       auto issue_s = [&](int c) {
-        const int st = c % C::KV_STAGES;
+        const int ks = c % C::K_STAGES;
         tc_fence_after();
-        const uint32_t k_addr = smem_u32(smem + C::K_OFF + st * C::NH * C::TILE);
+        const uint32_t k_addr = smem_u32(smem + C::K_OFF + ks * C::NH * C::TILE);
 #pragma unroll
         for (int h = 0; h < C::NH; ++h)
 #pragma unroll
@@ -423,14 +461,15 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
                       sw128_kmajor_desc(k_addr + h * C::TILE + k4 * 32), C::IDESC_S,
                       (h | k4) != 0);
         umma_commit(&s_full[c & 1]);
+        if (C::SPLIT) umma_commit(&k_empty[ks]);  // K(c) is read once S(c) is done
         attn_chunk_stamp(p, c, 2);
       };
       // O_h += P(keys of slice h) V(keys of slice h), per 64-wide part of
       // dh; P is stored as two 64-key half tiles
       auto issue_pv = [&](int c) {
         tc_fence_after();
-        const int st = c % C::KV_STAGES;
-        const uint32_t v_addr = smem_u32(smem + C::V_OFF + st * C::NH * C::TILE);
+        const int vs = c % C::V_STAGES;
+        const uint32_t v_addr = smem_u32(smem + C::V_OFF + vs * C::NH * C::TILE);
         const uint32_t p_addr = smem_u32(smem + C::P_OFF + C::pbuf(c) * 2 * C::TILE);
 #pragma unroll
         for (int sl = 0; sl < C::NQ; ++sl)
@@ -445,12 +484,13 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
                         sw128_mnmajor_desc(v_addr + j * C::TILE + kk * 128), C::IDESC_PV,
                         (c > 0 || k > 0) ? 1u : 0u);
           }
-        umma_commit(&kv_empty[st]);
+        umma_commit(&v_empty[vs]);
         umma_commit(&pv_done[c & 1]);
         attn_chunk_stamp(p, c, 7);
       };
-      // S(c) needs chunk c's copy and, from c = 2 on, the softmax's read of
-      // S(c - 2) (its buffer); P.V(c) needs P(c).  One thread polls both and
+      // S(c) needs chunk c's K and, from c = 2 on, the softmax's read of
+      // S(c - 2) (its buffer); P.V(c) needs P(c) and chunk c's V.  One
+      // thread polls both and
       // issues whichever is ready -- S first, and S at most one chunk ahead
       // of P.V (P.V is on the softmax's critical path) -- so that P.V(c)
       // never waits for chunk c + 1's copy.  A bounded poll: no progress
@@ -461,14 +501,15 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
       while (ok && cp < nchunks) {
         bool did = false;
         if (cs < nchunks && cs <= cp + 1 &&
-            mbar_test_wait(&kv_full[cs % C::KV_STAGES], (cs / C::KV_STAGES) & 1) &&
+            mbar_test_wait(&k_full[cs % C::K_STAGES], (cs / C::K_STAGES) & 1) &&
             (cs < 2 || mbar_test_wait(&s_free[cs & 1], ((cs - 2) >> 1) & 1))) {
           attn_chunk_stamp(p, cs, 1);
           issue_s(cs);
           ++cs;
           did = true;
         }
-        if (cp < cs && mbar_test_wait(&p_full[cp & 1], (cp >> 1) & 1)) {
+        if (cp < cs && mbar_test_wait(&p_full[cp & 1], (cp >> 1) & 1) &&
+            mbar_test_wait(&v_full[cp % C::V_STAGES], (cp / C::V_STAGES) & 1)) {
           attn_chunk_stamp(p, cp, 6);
           issue_pv(cp);
           ++cp;
@@ -669,10 +710,12 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
       // reach O (the pool may hold anything there)
       const int t0 = key0 + c * C::KEYS;
       if (h == 0 && t0 + C::KEYS > key1 && t0 + qrow >= key1) {
-        const int st = c % C::KV_STAGES;
+        // (after the chunk's V copies have landed, so none lands on top)
+        const int vs = c % C::V_STAGES;
+        if (!mbar_wait(&v_full[vs], (c / C::V_STAGES) & 1, a.err)) ok = false;
 #pragma unroll
         for (int j = 0; j < C::NH; ++j) {
-          uint4* vr = reinterpret_cast<uint4*>(smem + C::V_OFF + (st * C::NH + j) * C::TILE +
+          uint4* vr = reinterpret_cast<uint4*>(smem + C::V_OFF + (vs * C::NH + j) * C::TILE +
                                                qrow * 128);
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) vr[cc] = make_uint4(0, 0, 0, 0);
