@@ -339,9 +339,14 @@ pe_status pe_set_split_reduce(pe_handle* h, int32_t mode);
  *                            previous kernel), 0..64; default 0 (2, 4
  *                            and 8 measured slower: 2900 against 3230 us
  *                            a GPT-OSS-shaped batch-64 step).
+ *   PE_TUNE_GEMM_MAX_SPLIT   the largest number of CTAs (a thread-block
+ *                            cluster) that split one projection tile's k
+ *                            range when there are fewer tiles than SMs,
+ *                            1..8; default 8 (4, 3 and 2 measured slower
+ *                            at batch 1 and on the Qwen-shaped batch 16).
  * Returns PE_ERR_INVALID_ARGUMENT for an unknown key or a value out of
  * range.  The results do not depend on the setting. */
-enum { PE_TUNE_GEMM_PRE_STAGES = 1, PE_TUNE_ATTN_L2_AHEAD = 2 };
+enum { PE_TUNE_GEMM_PRE_STAGES = 1, PE_TUNE_ATTN_L2_AHEAD = 2, PE_TUNE_GEMM_MAX_SPLIT = 3 };
 pe_status pe_set_tuning(pe_handle* h, int32_t key, int32_t value);
 
 /* Tuning of the small-batch streaming kernel.  tiles: how many 16 KB

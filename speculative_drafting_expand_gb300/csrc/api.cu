@@ -72,6 +72,7 @@ struct pe_handle {
   // none (measured slower with 2, 4 or 8 at batch 1, batch 64 and the Qwen
   // batch-16 step: 2900 -> 3230 us at batch 64)
   int attn_l2_ahead = 0;
+  int gemm_max_split = 8;              // the largest cluster split-K of a projection
   float* fc_hs = nullptr;              // [d] fc(h_shared), the projected hidden of every MASK row
   int32_t* fc_map = nullptr;           // [max_tokens] target row -> compact row
   uint8_t* masked_c = nullptr;         // [max_tokens] MASK flag of every compact row
@@ -214,6 +215,7 @@ TcGemmWorkspace tc_ws(pe_handle* h) {
   ws.sm_count = h->sm_count;
   ws.cluster_push = h->cluster_push;
   ws.pre_stages = h->gemm_pre_stages;
+  ws.max_split = h->gemm_max_split;
   return ws;
 }
 
@@ -416,6 +418,10 @@ pe_status pe_set_tuning(pe_handle* h, int32_t key, int32_t value) {
     case PE_TUNE_GEMM_PRE_STAGES:
       if (value < -1) return PE_ERR_INVALID_ARGUMENT;
       h->gemm_pre_stages = value;
+      return PE_OK;
+    case PE_TUNE_GEMM_MAX_SPLIT:
+      if (value < 1 || value > 8) return PE_ERR_INVALID_ARGUMENT;
+      h->gemm_max_split = value;
       return PE_OK;
     case PE_TUNE_ATTN_L2_AHEAD:
       if (value < 0 || value > 64) return PE_ERR_INVALID_ARGUMENT;

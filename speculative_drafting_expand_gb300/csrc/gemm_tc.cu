@@ -782,7 +782,7 @@ static cudaError_t run_tc(const CUtensorMap& a, const CUtensorMap& a2, const CUt
     while (S2 < S) S2 *= 2;
     if (tiles * S2 <= per_sm * sm_count) S = S2;
   }
-  S = std::min(S, std::min(8, p.kb));
+  S = std::min(S, std::min(std::max(1, std::min(8, p.max_split)), p.kb));
   // One CTA an SM: clusters are placed whole within a GPC, so no more than
   // the resident-cluster count the runtime reports (a cluster left for a
   // second wave doubles the time; measured on 256-row projections).  With
@@ -871,6 +871,7 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
   p.tl = ws.timeline;
   p.push = ws.cluster_push;
   p.pre_stages = ws.pre_stages;
+  p.max_split = ws.max_split > 0 ? ws.max_split : 8;
   if (epi.kind == EPI_ROPE_KV) {
     // one token tile whose rotary table fits the staged [BN][64] floats
     if (dual || epi.dh <= 0 || 128 % epi.dh != 0 || N % 128 != 0 || M > bn || bn > 32 ||

@@ -70,6 +70,7 @@ struct TcParams {
   int a_heads;  // 0: weights by a 2-D map; else a 4-D interleaved QKV map, heads per tile
   int push;     // cluster split: 1 pushes each item's partials to its owner (st.async), 0 pulls them
   int pre_stages;  // weight stages loaded before the wait for the previous kernel (-1: all)
+  int max_split;   // host side: the largest cluster split (2..8)
   // diagnostic timeline, or null: [cta][16] %globaltimer stamps (ns): [0]
   // start, [1] the producer's wait for the previous kernel returned, [2]
   // the first stage landed (MMA issuer), [3] the last MMA issued, [4] the

@@ -118,6 +118,7 @@ extern "C" pe_status pe_linear_static(const void* x, const void* w, float* y, in
   ws.timeline = nullptr;
   ws.cluster_push = 1;
   ws.pre_stages = -1;
+  ws.max_split = 8;
   ws.sm_count = sms;
   EpiArgs ep = {};
   ep.kind = EPI_STORE;

@@ -259,6 +259,7 @@ struct TcGemmWorkspace {
   unsigned long long* timeline;  // diagnostic per-CTA stamps of this launch, or null
   int cluster_push;         // cluster split-K: 1 pushes partials to their owners, 0 pulls
   int pre_stages;           // weight stages loaded before the dependency wait (-1: all)
+  int max_split;            // the largest cluster split-K (2..8; 0: 8)
 };
 cudaError_t launch_gemm_tc(const void* x, int ldx, const void* w, const void* w2, int M, int N,
                            int K, const EpiArgs& epi, const TcGemmWorkspace& ws, int* err,
