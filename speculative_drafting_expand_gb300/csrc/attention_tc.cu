@@ -91,23 +91,20 @@ struct AttnCfg {
   static constexpr int NH = DH / 64;            // 64-wide halves of the head dim
   static constexpr int KEYS = 128;              // keys per chunk (two 64-key halves)
   static constexpr int TILE = 128 * 128;        // 128 rows x 128 B
-  // K/V rings.  At dh 128 K and V are separate rings: a K stage is free
-  // once S of its chunk is computed, a V stage only once P.V has read it,
-  // so V is the deeper ring (two K, three V stages: the Qwen-shaped batch
-  // 16 step 912 -> 857 us), with one P buffer to make room.  At dh 64 one
-  // ring carries K and V of a chunk together (four stages, three with the
-  // fp8 staging ring; split rings of 3 + 5 or 4 + 4 stages measured 6 %
-  // slower there) and two P buffers (with one, the softmax of chunk c + 1
-  // stores P only after P.V of chunk c, which waits for the slowest softmax
-  // warp).
+  // K/V rings.  P lives in tensor memory (over the S columns it was
+  // computed from), so shared memory holds Q and the rings only.  At dh
+  // 128 K and V are separate rings: a K stage is free once S of its chunk
+  // is computed, a V stage only once P.V has read it, so V is the deeper
+  // ring (two K, four V stages).  At dh 64 one ring carries K and V of a
+  // chunk together (six stages, four with the fp8 staging ring; split
+  // rings measured 6 % slower there).
   static constexpr bool SPLIT = DH != 64;
-  static constexpr int K_STAGES = DH == 64 ? (FP8 ? 3 : 4) : 2;
-  static constexpr int V_STAGES = DH == 64 ? (FP8 ? 3 : 4) : 3;
-  static constexpr int P_BUFS = DH == 64 ? 2 : 1;
+  static constexpr int K_STAGES = DH == 64 ? (FP8 ? 4 : 6) : 2;
+  static constexpr int V_STAGES = DH == 64 ? K_STAGES : 4;
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + NH * TILE;                 // [stage][NH]
   static constexpr int V_OFF = K_OFF + K_STAGES * NH * TILE;      // [stage][NH]
-  static constexpr int P_OFF = V_OFF + V_STAGES * NH * TILE;      // [buffer][key half]
+  static constexpr int RING_END = V_OFF + V_STAGES * NH * TILE;
   // Key slices of a chunk: each query row is served by NQ softmax threads,
   // one per KPW-key slice, each with its own running max, sum and O.  Two
   // slices (8 softmax warps); four (16 warps) measured no faster at dh 64.
@@ -115,10 +112,10 @@ struct AttnCfg {
   static constexpr int KPW = KEYS / NQ;
   static constexpr int SOFT = 128 * NQ;          // softmax threads
   // float[2 NQ][128] for combining the slices; used only after the last
-  // P.V has finished reading P, so it shares P's space
-  static constexpr int RED_OFF = P_OFF;
-  static constexpr int BAR_OFF = P_OFF + 2 * P_BUFS * TILE;
-  __host__ __device__ static constexpr int pbuf(int c) { return P_BUFS == 1 ? 0 : (c & 1); }
+  // P.V has finished (every S, and so every read of Q, is done), so it
+  // shares Q's space
+  static constexpr int RED_OFF = Q_OFF;
+  static constexpr int BAR_OFF = RING_END;
   // block ids of the CTA's pages, read once: a split covers at most
   // BT_ENTRIES pages of 16 keys (32 chunks)
   static constexpr int BT_ENTRIES = 256;
@@ -137,7 +134,7 @@ struct AttnCfg {
   static constexpr uint32_t IDESC_PV =
       FP8 ? idesc_f16_f32_bmn(128, 64) : idesc_bf16_f32_bmn(128, 64);
   static_assert(SMEM <= 232448, "shared memory");
-  static_assert((2 * K_STAGES + 2 * V_STAGES + 16) * 8 <= 256, "barrier space");
+  static_assert((2 * K_STAGES + (SPLIT ? 2 * V_STAGES : 0) + 16) * 8 <= 256, "barrier space");
   static_assert(SPLIT || K_STAGES == V_STAGES, "one ring");
   static_assert(!FP8 || DH == 64, "the fp8 pools are read at dh 64");
   static_assert(O_COL + NQ * DH <= TMEM_COLS && KPW % 16 == 0, "slices");
@@ -465,24 +462,24 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
         attn_chunk_stamp(p, c, 2);
       };
       // O_h += P(keys of slice h) V(keys of slice h), per 64-wide part of
-      // dh; P is stored as two 64-key half tiles
+      // dh; P comes from tensor memory: slice h's probabilities, packed two
+      // to a column, over the first half of its own S columns (the A
+      // operand of a 16-key step is 8 columns)
       auto issue_pv = [&](int c) {
         tc_fence_after();
         const int vs = c % C::V_STAGES;
         const uint32_t v_addr = smem_u32(smem + C::V_OFF + vs * C::NH * C::TILE);
-        const uint32_t p_addr = smem_u32(smem + C::P_OFF + C::pbuf(c) * 2 * C::TILE);
 #pragma unroll
         for (int sl = 0; sl < C::NQ; ++sl)
 #pragma unroll
           for (int k = 0; k < C::KPW / 16; ++k) {
             const int kk = sl * C::KPW + k * 16;     // first key of this step
-            const uint64_t adesc =
-                sw128_kmajor_desc(p_addr + (kk / 64) * C::TILE + ((kk % 64) / 16) * 32);
+            const uint32_t a_tmem = tmem + (c & 1) * 128 + sl * C::KPW + k * 8;
 #pragma unroll
             for (int j = 0; j < C::NH; ++j)
-              umma_bf16(tmem + C::O_COL + sl * DH + j * 64, adesc,
-                        sw128_mnmajor_desc(v_addr + j * C::TILE + kk * 128), C::IDESC_PV,
-                        (c > 0 || k > 0) ? 1u : 0u);
+              umma_f16_ts(tmem + C::O_COL + sl * DH + j * 64, a_tmem,
+                          sw128_mnmajor_desc(v_addr + j * C::TILE + kk * 128), C::IDESC_PV,
+                          (c > 0 || k > 0) ? 1u : 0u);
           }
         umma_commit(&v_empty[vs]);
         umma_commit(&pv_done[c & 1]);
@@ -673,13 +670,6 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
         l = l * factor + psum;
         m_used = m_new;
       }
-      // the P buffer of this chunk was last read by an earlier P.V (one
-      // buffer: the previous chunk's; two: the one before it)
-      if (c >= C::P_BUFS &&
-          !mbar_wait(&pv_done[(c - C::P_BUFS) & 1], ((c - C::P_BUFS) >> 1) & 1, a.err)) {
-        ok = false;
-        break;
-      }
       // O must hold every earlier chunk before it is rescaled
       if (c >= 1 && __any_sync(0xffffffffu, factor != 1.f)) {
         if (!mbar_wait(&pv_done[(c - 1) & 1], ((c - 1) >> 1) & 1, a.err)) { ok = false; break; }
@@ -696,15 +686,15 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
         }
         tmem_st_wait();
       }
-      // P row of this slice -> its 16-byte chunks of the 64-key half tile
-      // of the chunk's P buffer that holds it (128-byte swizzle)
+      // P row of this slice -> tensor memory, over the first half of the
+      // slice's own S columns (this thread has read them; the next S into
+      // this buffer, of chunk c + 2, is issued after P.V of chunk c, and
+      // the tensor pipe runs them in order)
       {
-        uint8_t* pt = smem + C::P_OFF + (C::pbuf(c) * 2 + (h * KPW) / 64) * C::TILE + qrow * 128;
-        const int cb = ((h * KPW) % 64) / 8;
+        const uint32_t pcol = tmem + lane_off + (c & 1) * 128 + h * KPW;
 #pragma unroll
-        for (int cc = 0; cc < KPW / 8; ++cc)
-          *reinterpret_cast<uint4*>(pt + (((cb + cc) ^ (qrow & 7)) * 16)) =
-              make_uint4(pk[cc * 4], pk[cc * 4 + 1], pk[cc * 4 + 2], pk[cc * 4 + 3]);
+        for (int q = 0; q < KPW / 32; ++q) tmem_st16u(pcol + q * 16, pk + q * 16);
+        tmem_st_wait();
       }
       // keys past the sequence end: zero their V rows so 0 * garbage cannot
       // reach O (the pool may hold anything there)
