@@ -296,60 +296,70 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
     grid_dep_wait();   // the previous kernel wrote this step's K/V
     if (lane == 0) attn_stamp(p, 2);
     if constexpr (!FP8) {
+      // The page copies of a chunk go out from eight lanes at once (lane pg
+      // takes page pg): one copy instruction for the warp instead of eight
+      // issued one after another by one thread.  Lane 0 waits for the
+      // stage and posts the byte count first.
       if (lane == 0) {
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
-        const uint64_t pol = l2_policy_evict_first();
-        for (int c = 0; c < nchunks; ++c) {
-          const int ks = c % C::K_STAGES, kround = c / C::K_STAGES;
-          const int vs = c % C::V_STAGES, vround = c / C::V_STAGES;
-          const int t0 = key0 + c * C::KEYS;
-          int blks[8];
-          uint32_t bytes = 0;
-  #pragma unroll
-          for (int pg = 0; pg < 8; ++pg) {
-            const int t = t0 + pg * 16;
-            blks[pg] = t < key1 ? bt_s[c * 8 + pg] : -1;
-            if (blks[pg] >= 0) bytes += C::NH * 2048u;
+      }
+      const uint64_t pol = l2_policy_evict_first();
+      int k_issued = 0, v_issued = 0;   // chunks whose copies went out
+      for (int c = 0; c < nchunks; ++c) {
+        const int ks = c % C::K_STAGES, kround = c / C::K_STAGES;
+        const int vs = c % C::V_STAGES, vround = c / C::V_STAGES;
+        const int t0 = key0 + c * C::KEYS;
+        const int blk = (lane < 8 && t0 + lane * 16 < key1) ? bt_s[c * 8 + lane] : -1;
+        const uint32_t bytes = __popc(__ballot_sync(0xffffffffu, blk >= 0)) * C::NH * 2048u;
+        const int row = (blk * a.Hkv + g) * 16;
+        // K of the chunk once S of the chunk K_STAGES back is computed (one
+        // ring: K and V once P.V of that chunk has read the stage)
+        int ok0 = 1;
+        if (lane == 0) {
+          if (kround > 0 && !mbar_wait(&k_empty[ks], (kround - 1) & 1, a.err)) {
+            ok0 = 0;
+          } else {
+            mbar_arrive_expect_tx(&k_full[ks], C::SPLIT ? bytes : 2 * bytes);
+            attn_chunk_stamp(p, c, 0);
+            if (ahead > 0 && c + ahead < nchunks) prefetch_chunk(c + ahead);
           }
-          // K of the chunk once S of the chunk K_STAGES back is computed (one
-          // ring: K and V once P.V of that chunk has read the stage)
-          if (kround > 0 && !mbar_wait(&k_empty[ks], (kround - 1) & 1, a.err)) break;
-          mbar_arrive_expect_tx(&k_full[ks], C::SPLIT ? bytes : 2 * bytes);
-          attn_chunk_stamp(p, c, 0);
-          if (ahead > 0 && c + ahead < nchunks) prefetch_chunk(c + ahead);
-  #pragma unroll
-          for (int pg = 0; pg < 8; ++pg) {
-            if (blks[pg] < 0) continue;
-            const int row = (blks[pg] * a.Hkv + g) * 16;
-  #pragma unroll
-            for (int h = 0; h < C::NH; ++h) {
-              tma_load_2d(smem + C::K_OFF + (ks * C::NH + h) * C::TILE + pg * 2048, &tmK,
+        }
+        if (!__shfl_sync(0xffffffffu, ok0, 0)) break;
+        k_issued = c + 1;
+        if (!C::SPLIT) v_issued = c + 1;
+        if (blk >= 0) {
+#pragma unroll
+          for (int h = 0; h < C::NH; ++h) {
+            tma_load_2d(smem + C::K_OFF + (ks * C::NH + h) * C::TILE + lane * 2048, &tmK,
+                        &k_full[ks], h * 64, row, pol);
+            if (!C::SPLIT)
+              tma_load_2d(smem + C::V_OFF + (ks * C::NH + h) * C::TILE + lane * 2048, &tmV,
                           &k_full[ks], h * 64, row, pol);
-              if (!C::SPLIT)
-                tma_load_2d(smem + C::V_OFF + (ks * C::NH + h) * C::TILE + pg * 2048, &tmV,
-                            &k_full[ks], h * 64, row, pol);
-            }
           }
-          if (!C::SPLIT) continue;
+        }
+        if (C::SPLIT) {
           // V of the chunk once P.V of the chunk V_STAGES back has read it
-          if (vround > 0 && !mbar_wait(&v_empty[vs], (vround - 1) & 1, a.err)) break;
-          mbar_arrive_expect_tx(&v_full[vs], bytes);
-  #pragma unroll
-          for (int pg = 0; pg < 8; ++pg) {
-            if (blks[pg] < 0) continue;
-            const int row = (blks[pg] * a.Hkv + g) * 16;
-  #pragma unroll
+          if (lane == 0) {
+            if (vround > 0 && !mbar_wait(&v_empty[vs], (vround - 1) & 1, a.err)) ok0 = 0;
+            else mbar_arrive_expect_tx(&v_full[vs], bytes);
+          }
+          if (!__shfl_sync(0xffffffffu, ok0, 0)) break;
+          v_issued = c + 1;
+          if (blk >= 0) {
+#pragma unroll
             for (int h = 0; h < C::NH; ++h)
-              tma_load_2d(smem + C::V_OFF + (vs * C::NH + h) * C::TILE + pg * 2048, &tmV,
+              tma_load_2d(smem + C::V_OFF + (vs * C::NH + h) * C::TILE + lane * 2048, &tmV,
                           &v_full[vs], h * 64, row, pol);
           }
         }
-        // drain: the copies of the last stages have landed before exit
-        for (int c = max(0, nchunks - C::K_STAGES); c < nchunks; ++c)
+      }
+      // drain: the copies of the last stages have landed before exit
+      if (lane == 0) {
+        for (int c = max(0, k_issued - C::K_STAGES); c < k_issued; ++c)
           mbar_wait(&k_full[c % C::K_STAGES], (c / C::K_STAGES) & 1, a.err);
         if (C::SPLIT)
-          for (int c = max(0, nchunks - C::V_STAGES); c < nchunks; ++c)
+          for (int c = max(0, v_issued - C::V_STAGES); c < v_issued; ++c)
             mbar_wait(&v_full[c % C::V_STAGES], (c / C::V_STAGES) & 1, a.err);
       }
     } else {
