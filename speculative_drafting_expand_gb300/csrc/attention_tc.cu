@@ -363,29 +363,24 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
             mbar_wait(&v_full[c % C::V_STAGES], (c / C::V_STAGES) & 1, a.err);
       }
     } else {
-      // fp8 pages by TMA into the staging ring (lane 0), widened to f16 in
+      // fp8 pages by TMA into the staging ring (eight lanes), widened to f16 in
       // the chunk's K/V stage by the whole warp: per chunk 2 x 8 pages x 16
       // keys x 4 groups of 16 codes, 32 groups a lane.  Keys past the split
       // (and pages whose block id was bad) become zeros, so no stale value
       // reaches S or O.
       uint8_t* f8 = smem + C::F8_OFF;
       const uint64_t pol = l2_policy_evict_first();
+      // (the whole warp: lane pg < 8 copies page pg; lane 0 posts the bytes)
       auto issue8 = [&](int c) {
         const int s8 = c & 1;
         const int t0 = key0 + c * C::KEYS;
-        int blks[8];
-        uint32_t bytes = 0;
-#pragma unroll
-        for (int pg = 0; pg < 8; ++pg) {
-          blks[pg] = t0 + pg * 16 < key1 ? bt_s[c * 8 + pg] : -1;
-          if (blks[pg] >= 0) bytes += 2u * 16u * DH;
-        }
-        mbar_arrive_expect_tx(&kv8_full[s8], bytes);
-#pragma unroll
-        for (int pg = 0; pg < 8; ++pg) {
-          if (blks[pg] < 0) continue;
-          const int row = (blks[pg] * a.Hkv + g) * 16;
-          uint8_t* base = f8 + s8 * C::F8_STAGE + pg * 16 * DH;
+        const int blk = (lane < 8 && t0 + lane * 16 < key1) ? bt_s[c * 8 + lane] : -1;
+        const uint32_t bytes = __popc(__ballot_sync(0xffffffffu, blk >= 0)) * 2u * 16u * DH;
+        if (lane == 0) mbar_arrive_expect_tx(&kv8_full[s8], bytes);
+        __syncwarp();
+        if (blk >= 0) {
+          const int row = (blk * a.Hkv + g) * 16;
+          uint8_t* base = f8 + s8 * C::F8_STAGE + lane * 16 * DH;
           tma_load_2d(base, &tmK, &kv8_full[s8], 0, row, pol);
           tma_load_2d(base + 8 * 16 * DH, &tmV, &kv8_full[s8], 0, row, pol);
         }
@@ -393,9 +388,10 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
       if (lane == 0) {
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
-        for (int c = 0; c < min(nchunks, C::F8_STAGES); ++c) issue8(c);
-        for (int c = ahead; c < min(nchunks, ahead + C::F8_STAGES); ++c) prefetch_chunk(c);
       }
+      for (int c = 0; c < min(nchunks, C::F8_STAGES); ++c) issue8(c);
+      if (lane == 0)
+        for (int c = ahead; c < min(nchunks, ahead + C::F8_STAGES); ++c) prefetch_chunk(c);
       int issued = min(nchunks, C::F8_STAGES), consumed = 0;
       for (int c = 0; c < nchunks; ++c) {
         const int s8 = c & 1;
@@ -438,10 +434,10 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
         if (lane == 0) {
           mbar_arrive(&k_full[ks]);
           if (C::SPLIT) mbar_arrive(&v_full[vs]);
-          if (c + C::F8_STAGES < nchunks) issue8(c + C::F8_STAGES);
-          if (ahead > 0 && c + C::F8_STAGES + ahead < nchunks)
-            prefetch_chunk(c + C::F8_STAGES + ahead);
         }
+        if (c + C::F8_STAGES < nchunks) issue8(c + C::F8_STAGES);
+        if (lane == 0 && ahead > 0 && c + C::F8_STAGES + ahead < nchunks)
+          prefetch_chunk(c + C::F8_STAGES + ahead);
         if (c + C::F8_STAGES < nchunks) issued = c + C::F8_STAGES + 1;
         __syncwarp();
       }
