@@ -129,12 +129,14 @@ struct AttnCfg {
   // O of key slice h at 256 + h * DH
   static constexpr int O_COL = 256;
   static constexpr int TMEM_COLS = 512;
-  static constexpr int THREADS = 64 + SOFT;     // producer, MMA, softmax warps
+  // fp8 pools: four warps widen the staged codes (one per scheduler)
+  static constexpr int WIDEN_WARPS = FP8 ? 4 : 0;
+  static constexpr int THREADS = 64 + SOFT + 32 * WIDEN_WARPS;  // producer, MMA, softmax, widening
   static constexpr uint32_t IDESC_S = FP8 ? idesc_f16_f32(128, 128) : idesc_bf16_f32(128, 128);
   static constexpr uint32_t IDESC_PV =
       FP8 ? idesc_f16_f32_bmn(128, 64) : idesc_bf16_f32_bmn(128, 64);
   static_assert(SMEM <= 232448, "shared memory");
-  static_assert((2 * K_STAGES + (SPLIT ? 2 * V_STAGES : 0) + 16) * 8 <= 256, "barrier space");
+  static_assert((2 * K_STAGES + (SPLIT ? 2 * V_STAGES : 0) + 18) * 8 <= 256, "barrier space");
   static_assert(SPLIT || K_STAGES == V_STAGES, "one ring");
   static_assert(!FP8 || DH == 64, "the fp8 pools are read at dh 64");
   static_assert(O_COL + NQ * DH <= TMEM_COLS && KPW % 16 == 0, "slices");
@@ -171,6 +173,7 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
   uint64_t* drain = q_ready + 7;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 12);
   uint64_t* kv8_full = q_ready + 14;               // [2]: fp8 staging stages landed
+  uint64_t* kv8_empty = q_ready + 16;              // [2]: fp8 staging stages widened
   volatile int* flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
   float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
@@ -211,7 +214,7 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::K_STAGES; ++i) {
-      mbar_init(&k_full[i], 1);
+      mbar_init(&k_full[i], FP8 ? C::WIDEN_WARPS : 1);   // fp8: one arrival a widening warp
       mbar_init(&k_empty[i], 1);
     }
     for (int i = 0; i < (C::SPLIT ? C::V_STAGES : 0); ++i) {
@@ -231,6 +234,8 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
     if (FP8) {
       mbar_init(&kv8_full[0], 1);
       mbar_init(&kv8_full[1], 1);
+      mbar_init(&kv8_empty[0], C::WIDEN_WARPS);
+      mbar_init(&kv8_empty[1], C::WIDEN_WARPS);
     }
     *abort_flag = 0;
     mbar_fence_init();
@@ -363,11 +368,10 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
             mbar_wait(&v_full[c % C::V_STAGES], (c / C::V_STAGES) & 1, a.err);
       }
     } else {
-      // fp8 pages by TMA into the staging ring (eight lanes), widened to f16 in
-      // the chunk's K/V stage by the whole warp: per chunk 2 x 8 pages x 16
-      // keys x 4 groups of 16 codes, 32 groups a lane.  Keys past the split
-      // (and pages whose block id was bad) become zeros, so no stale value
-      // reaches S or O.
+      // fp8 pages by TMA into a two-stage staging ring (eight lanes at once);
+      // the widening warps turn each staged chunk into f16 rows of its K/V
+      // stage (per chunk 2 x 8 pages x 16 keys x 4 groups of 16 codes) and
+      // release the staging stage.
       uint8_t* f8 = smem + C::F8_OFF;
       const uint64_t pol = l2_policy_evict_first();
       // (the whole warp: lane pg < 8 copies page pg; lane 0 posts the bytes)
@@ -389,62 +393,23 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
       }
-      for (int c = 0; c < min(nchunks, C::F8_STAGES); ++c) issue8(c);
-      if (lane == 0)
-        for (int c = ahead; c < min(nchunks, ahead + C::F8_STAGES); ++c) prefetch_chunk(c);
-      int issued = min(nchunks, C::F8_STAGES), consumed = 0;
+      int issued = 0;
       for (int c = 0; c < nchunks; ++c) {
-        const int s8 = c & 1;
-        const int ks = c % C::K_STAGES, kround = c / C::K_STAGES;
-        const int vs = c % C::V_STAGES, vround = c / C::V_STAGES;
-        // every lane waits (each needs the barrier's acquire); the outcome is
-        // made warp-uniform so the lanes leave together
-        if (!__all_sync(0xffffffffu, mbar_wait(&kv8_full[s8], (c >> 1) & 1, a.err))) break;
-        consumed = c + 1;
-        if (kround > 0 &&
-            !__all_sync(0xffffffffu, mbar_wait(&k_empty[ks], (kround - 1) & 1, a.err)))
-          break;
-        if (C::SPLIT && vround > 0 &&
-            !__all_sync(0xffffffffu, mbar_wait(&v_empty[vs], (vround - 1) & 1, a.err)))
-          break;
-        const int t0 = key0 + c * C::KEYS;
-        const uint8_t* src = f8 + s8 * C::F8_STAGE;
-#pragma unroll 4
-        for (int k = 0; k < 32; ++k) {
-          const int item = lane + 32 * k;
-          const int which = item >> 9, pg = (item >> 6) & 7, kr = (item >> 2) & 15, q4 = item & 3;
-          const int kk = pg * 16 + kr;                 // key within the chunk
-          uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-          if (t0 + kk < key1 && bt_s[c * 8 + pg] >= 0) {
-            const uint4 x = *reinterpret_cast<const uint4*>(src + which * 8 * 16 * DH +
-                                                            pg * 16 * DH + kr * DH + q4 * 16);
-            lo = make_uint4(e4m3x2_to_f16x2(x.x), e4m3x2_to_f16x2(x.x >> 16),
-                            e4m3x2_to_f16x2(x.y), e4m3x2_to_f16x2(x.y >> 16));
-            hi = make_uint4(e4m3x2_to_f16x2(x.z), e4m3x2_to_f16x2(x.z >> 16),
-                            e4m3x2_to_f16x2(x.w), e4m3x2_to_f16x2(x.w >> 16));
-          }
-          // row kk of the 128-byte-swizzled stage: dims q4*16 .. +15 are its
-          // 16-byte chunks 2 q4 and 2 q4 + 1
-          uint8_t* dst = smem + (which ? C::V_OFF + vs * C::TILE : C::K_OFF + ks * C::TILE) + kk * 128;
-          *reinterpret_cast<uint4*>(dst + (((2 * q4) ^ (kk & 7)) * 16)) = lo;
-          *reinterpret_cast<uint4*>(dst + (((2 * q4 + 1) ^ (kk & 7)) * 16)) = hi;
+        if (c >= C::F8_STAGES) {
+          // the staging stage is free once every widening warp has read it
+          int ok0 = 1;
+          if (lane == 0 &&
+              !mbar_wait(&kv8_empty[c & 1], ((c - C::F8_STAGES) >> 1) & 1, a.err))
+            ok0 = 0;
+          if (!__shfl_sync(0xffffffffu, ok0, 0)) break;
         }
-        fence_proxy_async_smem();   // the stage's f16 rows, for the MMA's reads
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&k_full[ks]);
-          if (C::SPLIT) mbar_arrive(&v_full[vs]);
-        }
-        if (c + C::F8_STAGES < nchunks) issue8(c + C::F8_STAGES);
-        if (lane == 0 && ahead > 0 && c + C::F8_STAGES + ahead < nchunks)
-          prefetch_chunk(c + C::F8_STAGES + ahead);
-        if (c + C::F8_STAGES < nchunks) issued = c + C::F8_STAGES + 1;
-        __syncwarp();
+        issue8(c);
+        issued = c + 1;
+        if (lane == 0 && ahead > 0 && c + ahead < nchunks) prefetch_chunk(c + ahead);
       }
-      // drain: staging copies issued but not waited for (after a stop) land
-      // before the CTA exits
+      // drain: the last staging copies have landed before the CTA exits
       if (lane == 0)
-        for (int c = consumed; c < issued; ++c)
+        for (int c = max(0, issued - C::F8_STAGES); c < issued; ++c)
           mbar_wait(&kv8_full[c & 1], (c >> 1) & 1, a.err);
     }
   } else if (warp == 1) {
@@ -533,6 +498,60 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
       }
       umma_commit(drain);
       mbar_wait(drain, 0, a.err);
+    }
+  } else if (warp >= 2 + C::SOFT / 32) {
+    // ------------------------------------------------------------ widening
+    // (fp8 pools) The staged e4m3 codes of a chunk become f16 rows of its
+    // K/V stage, a quarter of the 16-byte groups a warp (warps 0-1 of the
+    // four: K, 2-3: V); each warp releases the staging stage and arrives on
+    // the chunk's K/V barrier (one arrival a warp).  Keys past the split
+    // (and pages whose block id was bad) become zeros, so no stale value
+    // reaches S or O.
+    if constexpr (FP8) {
+      const int wi = warp - (2 + C::SOFT / 32);
+      uint8_t* f8 = smem + C::F8_OFF;
+      // the split's block ids (written by the producer warp before its
+      // first copy; the staging barrier's phase orders them before here)
+      const int* bt_s = reinterpret_cast<const int*>(smem + C::BT_OFF);
+      for (int c = 0; c < nchunks; ++c) {
+        const int s8 = c & 1;
+        const int ks = c % C::K_STAGES, kround = c / C::K_STAGES;
+        const int vs = ks;   // one ring at dh 64
+        // every lane waits (each needs the barrier's acquire); the outcome is
+        // made warp-uniform so the lanes leave together
+        if (!__all_sync(0xffffffffu, mbar_wait(&kv8_full[s8], (c >> 1) & 1, a.err))) break;
+        if (kround > 0 &&
+            !__all_sync(0xffffffffu, mbar_wait(&k_empty[ks], (kround - 1) & 1, a.err)))
+          break;
+        const int t0 = key0 + c * C::KEYS;
+        const uint8_t* src = f8 + s8 * C::F8_STAGE;
+#pragma unroll 4
+        for (int k = wi * 8; k < wi * 8 + 8; ++k) {
+          const int item = lane + 32 * k;
+          const int which = item >> 9, pg = (item >> 6) & 7, kr = (item >> 2) & 15, q4 = item & 3;
+          const int kk = pg * 16 + kr;                 // key within the chunk
+          uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+          if (t0 + kk < key1 && bt_s[c * 8 + pg] >= 0) {
+            const uint4 x = *reinterpret_cast<const uint4*>(src + which * 8 * 16 * DH +
+                                                            pg * 16 * DH + kr * DH + q4 * 16);
+            lo = make_uint4(e4m3x2_to_f16x2(x.x), e4m3x2_to_f16x2(x.x >> 16),
+                            e4m3x2_to_f16x2(x.y), e4m3x2_to_f16x2(x.y >> 16));
+            hi = make_uint4(e4m3x2_to_f16x2(x.z), e4m3x2_to_f16x2(x.z >> 16),
+                            e4m3x2_to_f16x2(x.w), e4m3x2_to_f16x2(x.w >> 16));
+          }
+          // row kk of the 128-byte-swizzled stage: dims q4*16 .. +15 are its
+          // 16-byte chunks 2 q4 and 2 q4 + 1
+          uint8_t* dst = smem + (which ? C::V_OFF + vs * C::TILE : C::K_OFF + ks * C::TILE) + kk * 128;
+          *reinterpret_cast<uint4*>(dst + (((2 * q4) ^ (kk & 7)) * 16)) = lo;
+          *reinterpret_cast<uint4*>(dst + (((2 * q4 + 1) ^ (kk & 7)) * 16)) = hi;
+        }
+        fence_proxy_async_smem();   // the stage's f16 rows, for the MMA's reads
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&kv8_empty[s8]);
+          mbar_arrive(&k_full[ks]);
+        }
+      }
     }
   } else {
     // ------------------------------------------------------------ softmax
