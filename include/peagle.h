@@ -344,9 +344,17 @@ pe_status pe_set_split_reduce(pe_handle* h, int32_t mode);
  *                            range when there are fewer tiles than SMs,
  *                            1..8; default 8 (4, 3 and 2 measured slower
  *                            at batch 1 and on the Qwen-shaped batch 16).
+ *   PE_TUNE_ATTN_MIN_CHUNKS  the fewest 128-key chunks one attention CTA
+ *                            (key split) takes, 2..32; default 2 (splits
+ *                            are otherwise sized to fill the SMs).
  * Returns PE_ERR_INVALID_ARGUMENT for an unknown key or a value out of
  * range.  The results do not depend on the setting. */
-enum { PE_TUNE_GEMM_PRE_STAGES = 1, PE_TUNE_ATTN_L2_AHEAD = 2, PE_TUNE_GEMM_MAX_SPLIT = 3 };
+enum {
+  PE_TUNE_GEMM_PRE_STAGES = 1,
+  PE_TUNE_ATTN_L2_AHEAD = 2,
+  PE_TUNE_GEMM_MAX_SPLIT = 3,
+  PE_TUNE_ATTN_MIN_CHUNKS = 4
+};
 pe_status pe_set_tuning(pe_handle* h, int32_t key, int32_t value);
 
 /* Tuning of the small-batch streaming kernel.  tiles: how many 16 KB

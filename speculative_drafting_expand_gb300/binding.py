@@ -324,6 +324,7 @@ def pe_set_split_reduce(dr: Drafter, mode: int) -> None:
 PE_TUNE_GEMM_PRE_STAGES = 1
 PE_TUNE_ATTN_L2_AHEAD = 2
 PE_TUNE_GEMM_MAX_SPLIT = 3
+PE_TUNE_ATTN_MIN_CHUNKS = 4
 
 
 def pe_set_tuning(dr: Drafter, key: int, value: int) -> None:

@@ -28,7 +28,7 @@ cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const
                                 const int32_t* seq_lens, int max_rows_per_req, int sm_count,
                                 float* part, size_t part_floats, int* counters,
                                 size_t n_counters, unsigned long long* timeline, int l2_ahead,
-                                cudaStream_t s);
+                                int min_cps, cudaStream_t s);
 cudaError_t launch_bounded_wait_check(int* flag, int32_t* out, int* err, cudaStream_t s);
 }  // namespace pe
 
@@ -73,6 +73,7 @@ struct pe_handle {
   // batch-16 step: 2900 -> 3230 us at batch 64)
   int attn_l2_ahead = 0;
   int gemm_max_split = 8;              // the largest cluster split-K of a projection
+  int attn_min_chunks = 2;             // the fewest 128-key chunks an attention split takes
   float* fc_hs = nullptr;              // [d] fc(h_shared), the projected hidden of every MASK row
   int32_t* fc_map = nullptr;           // [max_tokens] target row -> compact row
   uint8_t* masked_c = nullptr;         // [max_tokens] MASK flag of every compact row
@@ -423,6 +424,10 @@ pe_status pe_set_tuning(pe_handle* h, int32_t key, int32_t value) {
       if (value < 1 || value > 8) return PE_ERR_INVALID_ARGUMENT;
       h->gemm_max_split = value;
       return PE_OK;
+    case PE_TUNE_ATTN_MIN_CHUNKS:
+      if (value < 2 || value > 32) return PE_ERR_INVALID_ARGUMENT;
+      h->attn_min_chunks = value;
+      return PE_OK;
     case PE_TUNE_ATTN_L2_AHEAD:
       if (value < 0 || value > 64) return PE_ERR_INVALID_ARGUMENT;
       h->attn_l2_ahead = value;
@@ -741,7 +746,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
       e = counted(h, launch_attention_tc(at, *tk, *tv, ex->seq_lens, max_rows_per_req,
                                          h->sm_count, h->attn_partials, h->attn_partial_floats,
                                          h->attn_counters, h->attn_n_counters, tl,
-                                         h->attn_l2_ahead, s));
+                                         h->attn_l2_ahead, h->attn_min_chunks, s));
       if (e) return PE_ERR_CUDA;
     }
     if ((e = mark(2 + 2 * l))) return PE_ERR_CUDA;

@@ -998,7 +998,10 @@ struct AttnPlan {
   int G, rows_per_qt, qtiles, split_keys, max_splits;
 };
 
-static AttnPlan plan_attention(const AttnArgs& a, int max_rows_per_req, int sm_count) {
+// min_cps: the fewest chunks a split takes (2 by default; the workspace is
+// sized for that, so a larger value only needs less of it)
+static AttnPlan plan_attention(const AttnArgs& a, int max_rows_per_req, int sm_count,
+                               int min_cps = 2) {
   AttnPlan pl;
   pl.G = a.Hq / a.Hkv;
   pl.rows_per_qt = 128 / pl.G;
@@ -1023,7 +1026,7 @@ static AttnPlan plan_attention(const AttnArgs& a, int max_rows_per_req, int sm_c
   int cps = pairs * 16 <= sm_count ? (chunks_max * static_cast<int>(pairs) + sm_count - 1) / sm_count
             : pairs < sm_count     ? (chunks_max + 7) / 8
                                    : (chunks_max + want - 1) / want;
-  cps = std::max(2, std::min(kMaxCps, cps));
+  cps = std::max(std::max(2, min_cps), std::min(kMaxCps, cps));
   pl.split_keys = cps * 128;
   pl.max_splits = (max_seq + pl.split_keys - 1) / pl.split_keys;
   return pl;
@@ -1082,9 +1085,9 @@ cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const
                                 const int32_t* seq_lens, int max_rows_per_req, int sm_count,
                                 float* part, size_t part_floats, int* counters,
                                 size_t n_counters, unsigned long long* timeline, int l2_ahead,
-                                cudaStream_t s) {
+                                int min_cps, cudaStream_t s) {
   if (a.rows <= 0) return cudaSuccess;
-  const AttnPlan pl = plan_attention(a, max_rows_per_req, sm_count);
+  const AttnPlan pl = plan_attention(a, max_rows_per_req, sm_count, min_cps);
   AttnTcParams p;
   p.a = a;
   p.seq_lens = seq_lens;
