@@ -347,13 +347,20 @@ pe_status pe_set_split_reduce(pe_handle* h, int32_t mode);
  *   PE_TUNE_ATTN_MIN_CHUNKS  the fewest 128-key chunks one attention CTA
  *                            (key split) takes, 2..32; default 2 (splits
  *                            are otherwise sized to fill the SMs).
+ *   PE_TUNE_ATTN_MAX_CHUNKS  the most chunks one attention split takes,
+ *                            2..64 (at most 32 at dh 128); default 64.
+ *                            More splits need a larger
+ *                            split workspace, which the next
+ *                            pe_draft_forward outside a graph capture
+ *                            allocates.
  * Returns PE_ERR_INVALID_ARGUMENT for an unknown key or a value out of
  * range.  The results do not depend on the setting. */
 enum {
   PE_TUNE_GEMM_PRE_STAGES = 1,
   PE_TUNE_ATTN_L2_AHEAD = 2,
   PE_TUNE_GEMM_MAX_SPLIT = 3,
-  PE_TUNE_ATTN_MIN_CHUNKS = 4
+  PE_TUNE_ATTN_MIN_CHUNKS = 4,
+  PE_TUNE_ATTN_MAX_CHUNKS = 5
 };
 pe_status pe_set_tuning(pe_handle* h, int32_t key, int32_t value);
 

@@ -22,13 +22,15 @@ size_t tc_partial_floats(int grid, int bn, bool dual);
 cudaError_t init_attention_tc();
 bool tensor_map_2d_u8(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
                       uint32_t box_rows);
-size_t attention_tc_partial_floats(const AttnArgs& a, int max_rows_per_req, int sm_count);
-size_t attention_tc_counters(const AttnArgs& a, int max_rows_per_req, int sm_count);
+size_t attention_tc_partial_floats(const AttnArgs& a, int max_rows_per_req, int sm_count,
+                                   int min_cps, int max_cps);
+size_t attention_tc_counters(const AttnArgs& a, int max_rows_per_req, int sm_count, int min_cps,
+                             int max_cps);
 cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                 const int32_t* seq_lens, int max_rows_per_req, int sm_count,
                                 float* part, size_t part_floats, int* counters,
                                 size_t n_counters, unsigned long long* timeline, int l2_ahead,
-                                int min_cps, cudaStream_t s);
+                                int min_cps, int max_cps, cudaStream_t s);
 cudaError_t launch_bounded_wait_check(int* flag, int32_t* out, int* err, cudaStream_t s);
 }  // namespace pe
 
@@ -74,6 +76,10 @@ struct pe_handle {
   int attn_l2_ahead = 0;
   int gemm_max_split = 8;              // the largest cluster split-K of a projection
   int attn_min_chunks = 2;             // the fewest 128-key chunks an attention split takes
+  // the most (a split's block ids: at most 64 chunks at dh 64, 32 at dh
+  // 128); longer splits measured better at batch 64 (16: 2757, 32: 2576, 64:
+  // 2544-2561 us a step), fewer CTAs each paying its setup and merge
+  int attn_max_chunks = 64;
   float* fc_hs = nullptr;              // [d] fc(h_shared), the projected hidden of every MASK row
   int32_t* fc_map = nullptr;           // [max_tokens] target row -> compact row
   uint8_t* masked_c = nullptr;         // [max_tokens] MASK flag of every compact row
@@ -428,6 +434,10 @@ pe_status pe_set_tuning(pe_handle* h, int32_t key, int32_t value) {
       if (value < 2 || value > 32) return PE_ERR_INVALID_ARGUMENT;
       h->attn_min_chunks = value;
       return PE_OK;
+    case PE_TUNE_ATTN_MAX_CHUNKS:
+      if (value < 2 || value > 64) return PE_ERR_INVALID_ARGUMENT;
+      h->attn_max_chunks = value;
+      return PE_OK;
     case PE_TUNE_ATTN_L2_AHEAD:
       if (value < 0 || value > 64) return PE_ERR_INVALID_ARGUMENT;
       h->attn_l2_ahead = value;
@@ -609,8 +619,10 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     probe.Hkv = d.n_kv_heads;
     probe.dh = d.head_dim;
     probe.bt_stride = bt_stride;
-    const size_t need = attention_tc_partial_floats(probe, max_rows_per_req, h->sm_count);
-    const size_t need_c = attention_tc_counters(probe, max_rows_per_req, h->sm_count);
+    const size_t need = attention_tc_partial_floats(probe, max_rows_per_req, h->sm_count,
+                                                    h->attn_min_chunks, h->attn_max_chunks);
+    const size_t need_c = attention_tc_counters(probe, max_rows_per_req, h->sm_count,
+                                                h->attn_min_chunks, h->attn_max_chunks);
     if (need > h->attn_partial_floats) {
       if ((e = dev_alloc(h, &h->attn_partials, need))) return PE_ERR_OUT_OF_MEMORY;
       h->attn_partial_floats = need;
@@ -746,7 +758,8 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
       e = counted(h, launch_attention_tc(at, *tk, *tv, ex->seq_lens, max_rows_per_req,
                                          h->sm_count, h->attn_partials, h->attn_partial_floats,
                                          h->attn_counters, h->attn_n_counters, tl,
-                                         h->attn_l2_ahead, h->attn_min_chunks, s));
+                                         h->attn_l2_ahead, h->attn_min_chunks,
+                                         h->attn_max_chunks, s));
       if (e) return PE_ERR_CUDA;
     }
     if ((e = mark(2 + 2 * l))) return PE_ERR_CUDA;

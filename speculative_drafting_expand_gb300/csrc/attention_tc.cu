@@ -117,8 +117,9 @@ struct AttnCfg {
   static constexpr int RED_OFF = Q_OFF;
   static constexpr int BAR_OFF = RING_END;
   // block ids of the CTA's pages, read once: a split covers at most
-  // BT_ENTRIES pages of 16 keys (32 chunks)
-  static constexpr int BT_ENTRIES = 256;
+  // BT_ENTRIES pages of 16 keys (64 chunks at dh 64, 32 at dh 128, where
+  // shared memory is full)
+  static constexpr int BT_ENTRIES = DH == 64 ? 512 : 256;
   static constexpr int BT_OFF = BAR_OFF + 256;
   // fp8 staging: [stage][K pages 8 x 1 KB | V pages 8 x 1 KB]
   static constexpr int F8_STAGES = 2;
@@ -1001,7 +1002,7 @@ struct AttnPlan {
 // min_cps: the fewest chunks a split takes (2 by default; the workspace is
 // sized for that, so a larger value only needs less of it)
 static AttnPlan plan_attention(const AttnArgs& a, int max_rows_per_req, int sm_count,
-                               int min_cps = 2) {
+                               int min_cps = 2, int max_cps = 32) {
   AttnPlan pl;
   pl.G = a.Hq / a.Hkv;
   pl.rows_per_qt = 128 / pl.G;
@@ -1010,7 +1011,8 @@ static AttnPlan plan_attention(const AttnArgs& a, int max_rows_per_req, int sm_c
   const int chunks_max = (max_seq + 127) / 128;
   const long long pairs = static_cast<long long>(a.B) * a.Hkv * pl.qtiles;
   const int want = static_cast<int>(std::max<long long>(1, (sm_count + pairs - 1) / pairs));
-  // A split is at most 32 chunks (its block ids fit the CTA's table).
+  // A split is at most 64 chunks at dh 64 and 32 at dh 128 (its block ids
+  // fit the CTA's table).
   // Fewer units than SMs: about 8 splits per unit, 16 where 8 would leave
   // more than half of the SMs idle (batch 1: 1.5 % faster step; at 16
   // requests 16 splits lost 5 %); otherwise enough splits to give every SM
@@ -1022,7 +1024,7 @@ static AttnPlan plan_attention(const AttnArgs& a, int max_rows_per_req, int sm_c
   // A few units (batch 1): as many splits as keep the grid one wave, two
   // chunks or more each; their merge is then parallel (every split merges
   // a slice of the rows, parallel_merge below).
-  constexpr int kMaxCps = 32;
+  const int kMaxCps = std::max(2, std::min(a.dh == 64 ? 64 : 32, max_cps));
   int cps = pairs * 16 <= sm_count ? (chunks_max * static_cast<int>(pairs) + sm_count - 1) / sm_count
             : pairs < sm_count     ? (chunks_max + 7) / 8
                                    : (chunks_max + want - 1) / want;
@@ -1032,13 +1034,15 @@ static AttnPlan plan_attention(const AttnArgs& a, int max_rows_per_req, int sm_c
   return pl;
 }
 
-size_t attention_tc_partial_floats(const AttnArgs& a, int max_rows_per_req, int sm_count) {
-  const AttnPlan pl = plan_attention(a, max_rows_per_req, sm_count);
+size_t attention_tc_partial_floats(const AttnArgs& a, int max_rows_per_req, int sm_count,
+                                   int min_cps, int max_cps) {
+  const AttnPlan pl = plan_attention(a, max_rows_per_req, sm_count, min_cps, max_cps);
   return static_cast<size_t>(a.B) * a.Hkv * pl.qtiles * pl.max_splits * 128 * (a.dh + 2);
 }
 
-size_t attention_tc_counters(const AttnArgs& a, int max_rows_per_req, int sm_count) {
-  const AttnPlan pl = plan_attention(a, max_rows_per_req, sm_count);
+size_t attention_tc_counters(const AttnArgs& a, int max_rows_per_req, int sm_count,
+                             int min_cps, int max_cps) {
+  const AttnPlan pl = plan_attention(a, max_rows_per_req, sm_count, min_cps, max_cps);
   return 2 * static_cast<size_t>(a.B) * a.Hkv * pl.qtiles;   // splits written, merged
 }
 
@@ -1085,9 +1089,9 @@ cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const
                                 const int32_t* seq_lens, int max_rows_per_req, int sm_count,
                                 float* part, size_t part_floats, int* counters,
                                 size_t n_counters, unsigned long long* timeline, int l2_ahead,
-                                int min_cps, cudaStream_t s) {
+                                int min_cps, int max_cps, cudaStream_t s) {
   if (a.rows <= 0) return cudaSuccess;
-  const AttnPlan pl = plan_attention(a, max_rows_per_req, sm_count, min_cps);
+  const AttnPlan pl = plan_attention(a, max_rows_per_req, sm_count, min_cps, max_cps);
   AttnTcParams p;
   p.a = a;
   p.seq_lens = seq_lens;
@@ -1104,7 +1108,7 @@ cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const
   // 32 splits: the splits merge their unit in parallel
   const long long ctas = static_cast<long long>(pl.max_splits) * a.Hkv * pl.qtiles * a.B;
   p.parallel_merge = (ctas <= sm_count && pl.max_splits <= 32) ? 1 : 0;
-  if (pl.split_keys / 16 > AttnCfg<64>::BT_ENTRIES || pl.split_keys / 16 > AttnCfg<128>::BT_ENTRIES)
+  if (pl.split_keys / 16 > (a.dh == 64 ? AttnCfg<64>::BT_ENTRIES : AttnCfg<128>::BT_ENTRIES))
     return cudaErrorInvalidValue;
   const size_t need = static_cast<size_t>(a.B) * a.Hkv * pl.qtiles * pl.max_splits * 128 * (a.dh + 2);
   if (need > part_floats || 2 * static_cast<size_t>(a.B) * a.Hkv * pl.qtiles > n_counters)
