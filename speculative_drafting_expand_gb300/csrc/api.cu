@@ -30,7 +30,13 @@ cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const
                                 const int32_t* seq_lens, int max_rows_per_req, int sm_count,
                                 float* part, size_t part_floats, int* counters,
                                 size_t n_counters, unsigned long long* timeline, int l2_ahead,
-                                int min_cps, int max_cps, cudaStream_t s);
+                                int min_cps, int max_cps, const int32_t* order,
+                                cudaStream_t s);
+int attention_tc_order_entries(const AttnArgs& a, int max_rows_per_req, int sm_count, int min_cps,
+                               int max_cps);
+cudaError_t launch_attention_order(const AttnArgs& a, const int32_t* seq_lens,
+                                   int max_rows_per_req, int sm_count, int min_cps, int max_cps,
+                                   int32_t* order, cudaStream_t s);
 cudaError_t launch_bounded_wait_check(int* flag, int32_t* out, int* err, cudaStream_t s);
 }  // namespace pe
 
@@ -93,6 +99,8 @@ struct pe_handle {
   float* attn_partials = nullptr;
   size_t attn_partial_floats = 0;
   int* attn_counters = nullptr;
+  int32_t* attn_order = nullptr;       // attention work items, longest first
+  size_t attn_order_cap = 0;
   size_t attn_n_counters = 0;
   // live-row compaction of the expanded batch (compact.cu)
   int32_t* row_map = nullptr;      // [max_tokens]
@@ -606,6 +614,13 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
   // what the batch leaves it) plus the K - 1 MASK rows
   const int max_rows_per_req = std::min(ex->T - B + 1, K + 1) + K - 1;
   cudaError_t e;
+  AttnArgs probe = {};                 // the attention's shape, for its plan
+  probe.B = B;
+  probe.Hq = d.n_heads;
+  probe.Hkv = d.n_kv_heads;
+  probe.dh = d.head_dim;
+  probe.bt_stride = bt_stride;
+  int order_entries = 0;               // > 0: the attention takes its work longest first
   if (dt == PE_DTYPE_BF16) {
     if (d.head_dim % 64 || (d.n_heads / d.n_kv_heads) > 128) return PE_ERR_UNSUPPORTED;
     for (int l = 0; l < d.n_layers; ++l)
@@ -613,12 +628,6 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     // the split-KV workspace depends on the batch and the block table; the
     // first call that needs more grows it (make that call before capturing
     // the step into a CUDA graph)
-    AttnArgs probe = {};
-    probe.B = B;
-    probe.Hq = d.n_heads;
-    probe.Hkv = d.n_kv_heads;
-    probe.dh = d.head_dim;
-    probe.bt_stride = bt_stride;
     const size_t need = attention_tc_partial_floats(probe, max_rows_per_req, h->sm_count,
                                                     h->attn_min_chunks, h->attn_max_chunks);
     const size_t need_c = attention_tc_counters(probe, max_rows_per_req, h->sm_count,
@@ -630,6 +639,13 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     if (need_c > h->attn_n_counters) {
       if ((e = dev_alloc(h, &h->attn_counters, need_c))) return PE_ERR_OUT_OF_MEMORY;
       h->attn_n_counters = need_c;
+    }
+    order_entries = attention_tc_order_entries(probe, max_rows_per_req, h->sm_count,
+                                               h->attn_min_chunks, h->attn_max_chunks);
+    if (static_cast<size_t>(order_entries) > h->attn_order_cap) {
+      if ((e = dev_alloc(h, &h->attn_order, static_cast<size_t>(order_entries))))
+        return PE_ERR_OUT_OF_MEMORY;
+      h->attn_order_cap = static_cast<size_t>(order_entries);
     }
   }
 
@@ -759,7 +775,8 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
                                          h->sm_count, h->attn_partials, h->attn_partial_floats,
                                          h->attn_counters, h->attn_n_counters, tl,
                                          h->attn_l2_ahead, h->attn_min_chunks,
-                                         h->attn_max_chunks, s));
+                                         h->attn_max_chunks,
+                                         order_entries > 0 ? h->attn_order : nullptr, s));
       if (e) return PE_ERR_CUDA;
     }
     if ((e = mark(2 + 2 * l))) return PE_ERR_CUDA;
@@ -984,6 +1001,14 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     ec.dh = d.head_dim;
   }
   if ((e = counted(h, launch_embed_concat(dt, ec, s)))) return PE_ERR_CUDA;
+  // More attention CTAs than one wave: the step's attention work items
+  // sorted longest first, once for all layers (same sequences); written
+  // well before the first attention reads it (two launches back at least)
+  if (order_entries > 0 &&
+      (e = counted(h, launch_attention_order(probe, ex->seq_lens, max_rows_per_req, h->sm_count,
+                                             h->attn_min_chunks, h->attn_max_chunks,
+                                             h->attn_order, s))))
+    return PE_ERR_CUDA;
   // RMSNorm folded into the projections (bf16, one token tile of at most 32
   // rows): O and down write x g_next and per-group sums of squares, the
   // next projection scales its rows by r

@@ -55,6 +55,10 @@ struct AttnTcParams {
   // not depend on it; L2 is where its new rows land, so nothing stale is
   // read), then chunk c + l2_ahead when chunk c is loaded; 0: none
   int l2_ahead;
+  // longest work first, or null: the grid is (kv heads x query tiles,
+  // B x max_splits) and CTA row y takes work item order[y] = request << 8 |
+  // split (-1: none), the items sorted by their chunk count, most first
+  const int32_t* order;
   // diagnostic timeline, or null: [cta][16] %globaltimer stamps (ns): [0]
   // start, [1] set up (barriers, tensor memory, block ids), [2] the wait
   // for the previous kernel returned, [3] Q in shared memory, [4] the first
@@ -180,10 +184,19 @@ __global__ void __launch_bounds__(AttnCfg<DH, FP8>::THREADS, 1)
   float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
 
   const AttnArgs& a = p.a;
-  const int split = blockIdx.x;
-  const int g = blockIdx.y % a.Hkv;
-  const int qt = blockIdx.y / a.Hkv;
-  const int r = blockIdx.z;
+  int split, g, qt, r;
+  if (p.order) {
+    g = blockIdx.x % a.Hkv;
+    qt = blockIdx.x / a.Hkv;
+    const int item = __ldg(p.order + blockIdx.y);   // written two or more launches back
+    r = item >= 0 ? (item >> 8) : 0;
+    split = item >= 0 ? (item & 255) : p.max_splits;  // past every sequence: no work
+  } else {
+    split = blockIdx.x;
+    g = blockIdx.y % a.Hkv;
+    qt = blockIdx.y / a.Hkv;
+    r = blockIdx.z;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- which rows and keys this CTA covers (uniform across the CTA) ------
@@ -1085,11 +1098,66 @@ cudaError_t init_attention_tc() {
   return e;
 }
 
+// Work items of an attention launch, longest first: item (request r, split
+// s) has min(split chunks, chunks left in r's sequence past s's first key)
+// chunks; a counting sort by that count, most first, items without keys
+// last as -1.  One CTA; the order among items of equal length is whatever
+// the atomics give (each item's result does not depend on it).
+__global__ void attention_order_kernel(const int32_t* seq_lens, int B, int split_keys,
+                                       int max_splits, int32_t* order) {
+  constexpr int kBuckets = 65;              // 0..64 chunks
+  __shared__ int count[kBuckets], start[kBuckets];
+  const int n = B * max_splits;
+  const int cps = split_keys / 128;
+  for (int i = threadIdx.x; i < kBuckets; i += blockDim.x) count[i] = 0;
+  __syncthreads();
+  auto chunks_of = [&](int it) {
+    const int r = it / max_splits, s = it % max_splits;
+    const int left = seq_lens[r] - s * split_keys;
+    return left <= 0 ? 0 : min(cps, (left + 127) / 128);
+  };
+  for (int it = threadIdx.x; it < n; it += blockDim.x) atomicAdd(&count[chunks_of(it)], 1);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int c = kBuckets - 1; c >= 0; --c) {   // most chunks first, empty items last
+      start[c] = acc;
+      acc += count[c];
+    }
+  }
+  __syncthreads();
+  for (int it = threadIdx.x; it < n; it += blockDim.x) {
+    const int c = chunks_of(it);
+    const int at = atomicAdd(&start[c], 1);
+    order[at] = c > 0 ? ((it / max_splits) << 8) | (it % max_splits) : -1;
+  }
+}
+
+// Whether a launch of this shape takes its work in a sorted order (many CTAs:
+// more than one wave), and then the order buffer entries it needs.
+int attention_tc_order_entries(const AttnArgs& a, int max_rows_per_req, int sm_count, int min_cps,
+                               int max_cps) {
+  const AttnPlan pl = plan_attention(a, max_rows_per_req, sm_count, min_cps, max_cps);
+  const long long ctas = static_cast<long long>(pl.max_splits) * a.Hkv * pl.qtiles * a.B;
+  if (ctas <= sm_count || pl.max_splits > 255 || a.B >= (1 << 22)) return 0;
+  return a.B * pl.max_splits;
+}
+
+cudaError_t launch_attention_order(const AttnArgs& a, const int32_t* seq_lens,
+                                   int max_rows_per_req, int sm_count, int min_cps, int max_cps,
+                                   int32_t* order, cudaStream_t s) {
+  const AttnPlan pl = plan_attention(a, max_rows_per_req, sm_count, min_cps, max_cps);
+  if (pl.split_keys / 128 > 64) return cudaErrorInvalidValue;
+  attention_order_kernel<<<1, 1024, 0, s>>>(seq_lens, a.B, pl.split_keys, pl.max_splits, order);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                 const int32_t* seq_lens, int max_rows_per_req, int sm_count,
                                 float* part, size_t part_floats, int* counters,
                                 size_t n_counters, unsigned long long* timeline, int l2_ahead,
-                                int min_cps, int max_cps, cudaStream_t s) {
+                                int min_cps, int max_cps, const int32_t* order,
+                                cudaStream_t s) {
   if (a.rows <= 0) return cudaSuccess;
   const AttnPlan pl = plan_attention(a, max_rows_per_req, sm_count, min_cps, max_cps);
   AttnTcParams p;
@@ -1104,6 +1172,7 @@ cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const
   p.counters = counters;
   p.tl = timeline;
   p.l2_ahead = l2_ahead < 0 ? 0 : l2_ahead;
+  p.order = nullptr;
   // every split CTA resident at once (one wave of one CTA per SM), at most
   // 32 splits: the splits merge their unit in parallel
   const long long ctas = static_cast<long long>(pl.max_splits) * a.Hkv * pl.qtiles * a.B;
@@ -1114,6 +1183,10 @@ cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const
   if (need > part_floats || 2 * static_cast<size_t>(a.B) * a.Hkv * pl.qtiles > n_counters)
     return cudaErrorInvalidValue;
   dim3 grid(pl.max_splits, a.Hkv * pl.qtiles, a.B);
+  if (order && !p.parallel_merge) {
+    p.order = order;
+    grid = dim3(a.Hkv * pl.qtiles, a.B * pl.max_splits, 1);
+  }
   if (a.kv_fp8) {
     if (a.dh != 64 || !(a.k_scale > 0.f) || !(a.v_scale > 0.f)) return cudaErrorInvalidValue;
     return launch_pdl(attention_tc_kernel<64, true>, grid, dim3(AttnCfg<64, true>::THREADS),
