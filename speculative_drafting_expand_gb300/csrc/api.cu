@@ -60,6 +60,7 @@ struct pe_handle {
   int* err = nullptr;
   int* diag_flag = nullptr;  // the flag the bounded-wait self-check waits on
   float* resid = nullptr;   // [max_tokens, d] fp32 residual stream
+  float* o_delta = nullptr; // [max_tokens, d] fp32 O-projection output, added by the next norm
   void* x_in = nullptr;     // [max_tokens, 2d] QKV input
   void* qkv = nullptr;      // [max_tokens, (Hq + 2Hkv) dh]
   void* q = nullptr;        // [max_tokens, Hq dh] rotated queries
@@ -335,6 +336,7 @@ pe_status pe_create(const pe_model_desc* desc, const pe_weights* weights, int32_
   if (e == cudaSuccess) e = dev_alloc(h, &h->err, 1);
   if (e == cudaSuccess) e = dev_alloc(h, &h->diag_flag, 1);
   if (e == cudaSuccess) e = dev_alloc(h, &h->resid, T * d.d);
+  if (e == cudaSuccess) e = dev_alloc(h, &h->o_delta, T * d.d);
   if (e == cudaSuccess) e = alloc_bytes(&h->x_in, T * 2 * d.d * es);
   if (e == cudaSuccess) e = alloc_bytes(&h->qkv, T * qkv_rows * es);
   if (e == cudaSuccess) e = alloc_bytes(&h->q, T * qd * es);
@@ -1030,6 +1032,7 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     ep2.rs_eps = d.rms_eps;
   };
 
+  bool down_deferred = false;   // the last down-projection left its residual add to the next norm
   for (int l = 0; l < d.n_layers; ++l) {
     const pe_layer_weights& L = h->layers[l];
     const int d_in = l == 0 ? 2 * d.d : d.d;
@@ -1044,6 +1047,10 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
       rn.y = h->x_in;
       rn.err = h->err;
       rn.live = live;
+      if (down_deferred) {         // the previous layer's down-projection output
+        rn.add = h->o_delta;
+        rn.x_w = h->resid;
+      }
       if ((e = counted(h, launch_rmsnorm(dt, rn, s)))) return PE_ERR_CUDA;
     }
     if (fuse_rope) {
@@ -1119,13 +1126,24 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     }
     // paged causal attention
     if (const pe_status st = attention(l); st != PE_OK) return st;
-    // O projection + residual
+    // O projection + residual.  Where the norm after it is a kernel of its
+    // own (bf16, more than 32 rows), the projection stores its fp32 output
+    // and that norm does the residual add (the same fp32 addition): the
+    // projection's epilogue then has no residual reads, each a dependent
+    // round trip per 16-token chunk of a wide tile.
+    const bool defer_add = !fuse_norm && dt == PE_DTYPE_BF16 && d.d % 4 == 0;
     ep = epi_none();
-    ep.kind = EPI_ADD;
+    ep.kind = defer_add ? EPI_STORE : EPI_ADD;
     ep.M = rows;
     ep.N = d.d;
-    ep.resid = h->resid;
-    ep.ldr = d.d;
+    if (defer_add) {
+      ep.out = h->o_delta;
+      ep.ldo = d.d;
+      ep.out_f32 = 1;
+    } else {
+      ep.resid = h->resid;
+      ep.ldr = d.d;
+    }
     ep.m_live = live;
     if (fuse_norm) fold_out(ep, L.norm_post, h->xn, h->ssq_post);
     if ((e = linear(h, h->attn, qd, L.o, nullptr, rows, d.d, qd, ep, s))) return PE_ERR_CUDA;
@@ -1141,6 +1159,10 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
       rn.y = h->xn;
       rn.err = h->err;
       rn.live = live;
+      if (defer_add) {
+        rn.add = h->o_delta;
+        rn.x_w = h->resid;
+      }
       if ((e = counted(h, launch_rmsnorm(dt, rn, s)))) return PE_ERR_CUDA;
     }
     ep = epi_none();
@@ -1153,12 +1175,22 @@ pe_status pe_draft_forward(pe_handle* h, const pe_expanded* ex, int32_t B, int32
     ep.m_live = live;
     if (fuse_norm) fold_in(ep, h->ssq_post);
     if ((e = linear(h, h->xn, d.d, L.gate, L.up, rows, d.ffn, d.d, ep, s))) return PE_ERR_CUDA;
+    // down-projection + residual; deferred into the next layer's input norm
+    // like the O projection's (not after the last layer, whose final norm
+    // gathers rows, nor when the per-layer residual is traced)
+    down_deferred = defer_add && l + 1 < d.n_layers && !h->trace;
     ep = epi_none();
-    ep.kind = EPI_ADD;
+    ep.kind = down_deferred ? EPI_STORE : EPI_ADD;
     ep.M = rows;
     ep.N = d.d;
-    ep.resid = h->resid;
-    ep.ldr = d.d;
+    if (down_deferred) {
+      ep.out = h->o_delta;
+      ep.ldo = d.d;
+      ep.out_f32 = 1;
+    } else {
+      ep.resid = h->resid;
+      ep.ldr = d.d;
+    }
     ep.m_live = live;
     if (fuse_norm && l + 1 < d.n_layers)
       fold_out(ep, h->layers[l + 1].norm_in, h->x_in, h->ssq_in);

@@ -153,6 +153,11 @@ struct RmsNormArgs {
   float eps;
   void* y;              // [rows, d] activations
   int* err;
+  // optional: a projection's output [rows, d] fp32 added to x first (x <-
+  // x + add, written back to x_w, the same storage as x), the residual add
+  // of that projection done here instead of in its epilogue (no row_index)
+  const float* add;
+  float* x_w;
 };
 cudaError_t launch_rmsnorm(int dtype, const RmsNormArgs& a, cudaStream_t s);
 

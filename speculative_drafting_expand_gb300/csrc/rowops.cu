@@ -233,6 +233,26 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_vec_kernel(const RmsNormA
       v[j][0] = v[j][1] = v[j][2] = v[j][3] = 0.f;
     }
   }
+  if (a.add && !bad) {
+    // the deferred residual add: x + add, written back (all loads first)
+    const float* __restrict__ ad = a.add + static_cast<size_t>(src) * a.d;
+    float t[NV][4];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int c4 = threadIdx.x + j * kRowThreads;
+      if (c4 < n4) ld4(ad + 4 * c4, t[j]);
+    }
+    float* __restrict__ xw = a.x_w + static_cast<size_t>(src) * a.d;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int c4 = threadIdx.x + j * kRowThreads;
+      if (c4 < n4) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[j][q] = v[j][q] + t[j][q];
+        *reinterpret_cast<float4*>(xw + 4 * c4) = make_float4(v[j][0], v[j][1], v[j][2], v[j][3]);
+      }
+    }
+  }
 #pragma unroll
   for (int j = 0; j < NV; ++j)
     ss += v[j][0] * v[j][0] + v[j][1] * v[j][1] + v[j][2] * v[j][2] + v[j][3] * v[j][3];
@@ -482,6 +502,9 @@ cudaError_t rms_vec(const RmsNormArgs& a, cudaStream_t s) {
 template <typename T>
 cudaError_t rms_launch(const RmsNormArgs& a, cudaStream_t s) {
   const int nv = al16(a.x) && al16(a.y) && al16(a.g) ? row_nv(a.d) : 0;
+  // the deferred residual add runs in the vector kernel only
+  if (a.add && (nv == 0 || a.row_index || !al16(a.add) || a.x_w != a.x))
+    return cudaErrorInvalidValue;
   switch (nv) {
     case 1: return rms_vec<T, 1>(a, s);
     case 2: return rms_vec<T, 2>(a, s);
