@@ -443,6 +443,57 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
           tc_stamp(p, 11);
         }
         named_bar_sync(1, 128);
+        // Two contributors and this CTA's last segment (its stages are free,
+        // its accumulator stays in TMEM): the other contributor's partial
+        // comes into the stages in bulk copies, one round trip, and is added
+        // to the accumulator read from TMEM, in contributor order.
+        const bool last_seg = u + (k_hi - k_lo) >= hi;
+        const size_t part_bytes = static_cast<size_t>(128) * C::ACC_COLS * 4;
+        if (*flag && c_last - c_first == 1 && last_seg &&
+            part_bytes <= static_cast<size_t>(C::STAGES) * C::STAGE_BYTES) {
+          const int other = cta == c_first ? c_last : c_first;
+          const int cs = unit_lo(other, U, G) >= static_cast<long long>(tile) * kb ? 0 : 1;
+          const float* osrc = p.ws + (static_cast<size_t>(other) * 2 + cs) * (128 * C::ACC_COLS);
+          float* ostage = reinterpret_cast<float*>(smem);
+          if (threadIdx.x == 0) {
+            __threadfence();
+            fence_proxy_async_global();
+            mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(part_bytes));
+            for (size_t off = 0; off < part_bytes; off += 16384)
+              bulk_copy_g2s(reinterpret_cast<uint8_t*>(ostage) + off,
+                            reinterpret_cast<const uint8_t*>(osrc) + off,
+                            static_cast<uint32_t>(part_bytes - off < 16384 ? part_bytes - off : 16384),
+                            recv_bar);
+          }
+          // warp-uniform outcome (the epilogue below shuffles across lanes)
+          const bool got = __all_sync(0xffffffffu, mbar_wait(recv_bar, 0, p.err));
+          if (got) {
+            const bool own_first = cta == c_first;
+            tc_fence_after();
+            tmem_walk<BN, DUAL>(taddr, [&](int c0, const float* v, const float* v2) {
+              float w[16], w2[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float ot = ostage[(c0 + j) * 128 + row];
+                w[j] = own_first ? (0.f + v[j]) + ot : (0.f + ot) + v[j];
+                if (DUAL) {
+                  const float ot2 = ostage[(BN + c0 + j) * 128 + row];
+                  w2[j] = own_first ? (0.f + v2[j]) + ot2 : (0.f + ot2) + v2[j];
+                } else {
+                  w2[j] = 0.f;
+                }
+              }
+              epi_chunk<DUAL>(p.epi, o, m * BN + c0, w, w2, lane, staged);
+            });
+          }
+          if (threadIdx.x == 0) {
+            p.counters[tile] = 0;
+            tc_stamp(p, 12);
+          }
+          u += k_hi - k_lo;
+          ++seg;
+          continue;
+        }
         // contributors the pipelined path holds in registers: a tile spans at
         // most three CTAs at the wide-tile shapes of the drafter (k-blocks
         // per tile below twice the k-blocks per CTA), two at the others

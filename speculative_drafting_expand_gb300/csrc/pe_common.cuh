@@ -271,6 +271,20 @@ __device__ __forceinline__ void tmem_st_wait() {
 }
 // Make this thread's generic-proxy shared-memory writes visible to the
 // async proxy (TMA, tensor cores).
+// Order this thread's view of global memory (including data other threads
+// published to it) before its later async-proxy (bulk copy) reads.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// A contiguous global -> shared copy (16-byte aligned, size a multiple of
+// 16) whose bytes complete on `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
