@@ -354,7 +354,10 @@ pe_status pe_set_split_reduce(pe_handle* h, int32_t mode);
  *                            pe_draft_forward outside a graph capture
  *                            allocates.
  * Returns PE_ERR_INVALID_ARGUMENT for an unknown key or a value out of
- * range.  The results do not depend on the setting. */
+ * range.  PE_TUNE_GEMM_PRE_STAGES and PE_TUNE_ATTN_L2_AHEAD leave the
+ * results bit-identical; the other keys move the points where a k range or
+ * a key range is split, so fp32 partial sums may round differently (each
+ * setting computes the same exact sums in another order). */
 enum {
   PE_TUNE_GEMM_PRE_STAGES = 1,
   PE_TUNE_ATTN_L2_AHEAD = 2,
