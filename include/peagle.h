@@ -353,6 +353,18 @@ pe_status pe_set_split_reduce(pe_handle* h, int32_t mode);
  *                            split workspace, which the next
  *                            pe_draft_forward outside a graph capture
  *                            allocates.
+ *   PE_TUNE_GEMM_TILE_ORDER  a stream-K projection with several token
+ *                            tiles and weights larger than L2 (the LM
+ *                            head at batch 64): 1 token-tile major, the
+ *                            grid cut to a multiple of the token tiles so
+ *                            that the CTAs of every token tile take the
+ *                            same k ranges of the same weight tiles at the
+ *                            same time (each weight k-block from memory
+ *                            once, then from L2); 0 weight-tile major (the
+ *                            token tiles of a weight tile one after
+ *                            another in one CTA's range, as the layer
+ *                            projections always are: token-tile major
+ *                            measured slower for them).  Default 1.
  * Returns PE_ERR_INVALID_ARGUMENT for an unknown key or a value out of
  * range.  PE_TUNE_GEMM_PRE_STAGES and PE_TUNE_ATTN_L2_AHEAD leave the
  * results bit-identical; the other keys move the points where a k range or
@@ -363,7 +375,8 @@ enum {
   PE_TUNE_ATTN_L2_AHEAD = 2,
   PE_TUNE_GEMM_MAX_SPLIT = 3,
   PE_TUNE_ATTN_MIN_CHUNKS = 4,
-  PE_TUNE_ATTN_MAX_CHUNKS = 5
+  PE_TUNE_ATTN_MAX_CHUNKS = 5,
+  PE_TUNE_GEMM_TILE_ORDER = 6
 };
 pe_status pe_set_tuning(pe_handle* h, int32_t key, int32_t value);
 

@@ -326,6 +326,7 @@ PE_TUNE_ATTN_L2_AHEAD = 2
 PE_TUNE_GEMM_MAX_SPLIT = 3
 PE_TUNE_ATTN_MIN_CHUNKS = 4
 PE_TUNE_ATTN_MAX_CHUNKS = 5
+PE_TUNE_GEMM_TILE_ORDER = 6
 
 
 def pe_set_tuning(dr: Drafter, key: int, value: int) -> None:

@@ -82,6 +82,9 @@ struct pe_handle {
   // batch-16 step: 2900 -> 3230 us at batch 64)
   int attn_l2_ahead = 0;
   int gemm_max_split = 8;              // the largest cluster split-K of a projection
+  // stream-K over several token tiles, weights larger than L2: token-tile-major
+  int gemm_tile_order = 1;
+  int l2_bytes = 0;                    // the device's L2 size
   int attn_min_chunks = 2;             // the fewest 128-key chunks an attention split takes
   // the most (a split's block ids: at most 64 chunks at dh 64, 32 at dh
   // 128); longer splits measured better at batch 64 (16: 2757, 32: 2576, 64:
@@ -232,6 +235,8 @@ TcGemmWorkspace tc_ws(pe_handle* h) {
   ws.cluster_push = h->cluster_push;
   ws.pre_stages = h->gemm_pre_stages;
   ws.max_split = h->gemm_max_split;
+  ws.tile_order = h->gemm_tile_order;
+  ws.l2_bytes = h->l2_bytes;
   return ws;
 }
 
@@ -324,6 +329,7 @@ pe_status pe_create(const pe_model_desc* desc, const pe_weights* weights, int32_
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->l2_bytes, cudaDevAttrL2CacheSize, h->device);
   const size_t T = max_tokens;
   const int qkv_rows = (d.n_heads + 2 * d.n_kv_heads) * d.head_dim;
   const int qd = d.n_heads * d.head_dim;
@@ -451,6 +457,10 @@ pe_status pe_set_tuning(pe_handle* h, int32_t key, int32_t value) {
     case PE_TUNE_ATTN_L2_AHEAD:
       if (value < 0 || value > 64) return PE_ERR_INVALID_ARGUMENT;
       h->attn_l2_ahead = value;
+      return PE_OK;
+    case PE_TUNE_GEMM_TILE_ORDER:
+      if (value < 0 || value > 1) return PE_ERR_INVALID_ARGUMENT;
+      h->gemm_tile_order = value;
       return PE_OK;
     default:
       return PE_ERR_INVALID_ARGUMENT;

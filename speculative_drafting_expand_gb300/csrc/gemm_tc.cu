@@ -99,12 +99,17 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
   // keeps its next-token row), so some CTA still waits before the grid lets
   // its dependents start.
   int tiles_m = p.tiles_m;
+  const int tiles_n = p.tiles_n;
+  const bool m_major = p.m_major != 0;
+  // weight tile and token tile of tile t
+  auto tile_f = [&](int t) { return m_major ? t % tiles_n : t / tiles_m; };
+  auto tile_m = [&](int t) { return m_major ? t / tiles_n : t % tiles_m; };
   long long U = p.units;
   int G = gridDim.x;
   const int cta = blockIdx.x, kb = p.kb;
+  bool dead = false;
   if (p.epi.m_live) {
     const int tm = (max(0, min(p.M, m_live)) + BN - 1) / BN;
-    bool dead;
     if (p.split_s >= 1) {
       dead = (cta / p.split_s) % p.tiles_m >= tm;  // the same for the whole cluster
     } else {
@@ -116,13 +121,22 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
                            : 0;
       dead = cta >= G;
     }
-    if (dead) {
-      if (warp == 5) {
-        tc_fence_after();
-        tmem_dealloc(tmem_base, C::TMEM_COLS);
-      }
-      return;
+  }
+  if (m_major) {
+    // Token-tile-major stream-K: the same number of CTAs for every live
+    // token tile, so that CTA j of each token tile's group covers the same
+    // k-blocks of the same weight tiles in the same order, all at once:
+    // one read of a weight k-block from memory, the others from L2.
+    const int g = G / tiles_m;
+    G = g * tiles_m;
+    dead = dead || cta >= G;
+  }
+  if (dead) {
+    if (warp == 5) {
+      tc_fence_after();
+      tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
+    return;
   }
 
   long long lo, hi;
@@ -154,7 +168,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
       for (int i = 0; i < npre; ++i) {
         const long long u = lo + i;
         const int tile = static_cast<int>(u / kb), kk = static_cast<int>(u % kb);
-        const int f = tile / tiles_m;
+        const int f = tile_f(tile);
         uint8_t* st = smem + i * C::STAGE_BYTES;
         mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
         load_a(st, &tmA, &full[i], kk, f);
@@ -169,7 +183,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
       for (int i = 0; i < npre; ++i) {
         const long long u = lo + i;
         const int tile = static_cast<int>(u / kb), kk = static_cast<int>(u % kb);
-        const int m = tile % tiles_m;
+        const int m = tile_m(tile);
         tma_load_2d(smem + i * C::STAGE_BYTES + C::NA * C::A_BYTES, &tmB, &full[i], kk * 64,
                     m * BN, pol_b);
       }
@@ -180,7 +194,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
         if (!mbar_wait(&empty[stage], (round - 1) & 1, p.err)) break;
         const long long u = lo + i;
         const int tile = static_cast<int>(u / kb), kk = static_cast<int>(u % kb);
-        const int f = tile / tiles_m, m = tile % tiles_m;
+        const int f = tile_f(tile), m = tile_m(tile);
         uint8_t* st = smem + stage * C::STAGE_BYTES;
         mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
         load_a(st, &tmA, &full[stage], kk, f);
@@ -280,7 +294,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
       pre = warp % p.split_s == static_cast<int>(cluster_ctarank());
       if (pre) {
         const int tile = static_cast<int>(lo / kb);
-        const int o = (tile / tiles_m) * 128 + row, t0 = (tile % tiles_m) * BN;
+        const int o = tile_f(tile) * 128 + row, t0 = tile_m(tile) * BN;
         const float* r = p.epi.resid + static_cast<size_t>(t0) * p.epi.ldr + o;
 #pragma unroll
         for (int j = 0; j < 16; ++j)
@@ -302,7 +316,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
       named_bar_sync(1, 128);
       if (!*epi_ok) break;
       tc_fence_after();
-      const int f = tile / tiles_m, m = tile % tiles_m;
+      const int f = tile_f(tile), m = tile_m(tile);
       const int o = f * 128 + row;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * C::ACC_COLS;
       if (k_lo == 0 && k_hi == kb) {
@@ -620,7 +634,7 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
     // by this kernel) is loaded before the cluster barrier, for one chunk.
     const int S = p.split_s, tile = cta / S;
     const int rk = static_cast<int>(cluster_ctarank());
-    const int f = tile / tiles_m, m = tile % tiles_m;
+    const int f = tile_f(tile), m = tile_m(tile);
     const int row = warp * 32 + lane;
     float old_pre[17];
     const bool pre = p.epi.kind == EPI_ADD && BN == 16 && warp < 4 && warp % S == rk;
@@ -843,6 +857,7 @@ static cudaError_t run_tc(const CUtensorMap& a, const CUtensorMap& a2, const CUt
   if (tiles < sm_count && fits && (S >= 2 || per_sm == 2) && S >= 1 &&
       tiles * S <= per_sm * sm_count) {
     p.split_s = S;
+    p.m_major = 0;   // one tile a cluster
     // the pushed reduction receives its items in the operand stages
     // (token tiles of at most 32; wider tiles pull)
     if (BN > 32 || C::push_bytes(S) > C::STAGES * C::STAGE_BYTES) p.push = 0;
@@ -917,6 +932,16 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
   p.done = ws.done_counter;
   p.err = err;
   const int tiles = tiles_n * p.tiles_m;
+  p.tiles_n = tiles_n;
+  // Token-tile-major where the weights cannot stay in L2 from one token
+  // tile of a weight tile to the next (the LM head at a few hundred rows):
+  // measured faster there, and slower for the layer projections, whose
+  // weights (24-90 MB) L2 partly keeps between token tiles.  Stream-K only
+  // (run_tc).
+  p.m_major = ws.tile_order == 1 && p.tiles_m > 1 && ws.l2_bytes > 0 &&
+                      static_cast<long long>(N) * K * 2 > ws.l2_bytes
+                  ? 1
+                  : 0;
   p.split_s = 0;
   p.a_heads = 0;
   p.tl = ws.timeline;

@@ -66,6 +66,11 @@ struct TcParams {
   int* counters;
   int* done;
   int* err;
+  int tiles_n;  // weight tiles (128 output features each)
+  // Tile t's weight tile and token tile: t / tiles_m and t % tiles_m, or
+  // with m_major (stream-K over several token tiles) t % tiles_n and
+  // t / tiles_n, the grid cut to a multiple of the live token tiles
+  int m_major;
   int split_s;  // 0: stream-K over all units; >= 1: S CTAs (one cluster) per tile
   int a_heads;  // 0: weights by a 2-D map; else a 4-D interleaved QKV map, heads per tile
   int push;     // cluster split: 1 pushes each item's partials to its owner (st.async), 0 pulls them

@@ -119,6 +119,8 @@ extern "C" pe_status pe_linear_static(const void* x, const void* w, float* y, in
   ws.cluster_push = 1;
   ws.pre_stages = -1;
   ws.max_split = 8;
+  ws.tile_order = 0;   // one weight-tile-major order for these launches
+  ws.l2_bytes = 0;
   ws.sm_count = sms;
   EpiArgs ep = {};
   ep.kind = EPI_STORE;

@@ -265,6 +265,10 @@ struct TcGemmWorkspace {
   int cluster_push;         // cluster split-K: 1 pushes partials to their owners, 0 pulls
   int pre_stages;           // weight stages loaded before the dependency wait (-1: all)
   int max_split;            // the largest cluster split-K (2..8; 0: 8)
+  // stream-K over several token tiles with weights larger than L2
+  // (l2_bytes, 0: unknown): 1 token-tile-major, 0 weight-tile-major
+  int tile_order;
+  long long l2_bytes;
 };
 cudaError_t launch_gemm_tc(const void* x, int ldx, const void* w, const void* w2, int M, int N,
                            int K, const EpiArgs& epi, const TcGemmWorkspace& ws, int* err,

@@ -75,3 +75,33 @@ def test_linear_is_deterministic():
     B.pe_linear(dr, x, w, y2)
     torch.cuda.synchronize()
     assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("order", [0, 1])
+@pytest.mark.parametrize("M,N,K", [(448, 80000, 2880), (700, 70000, 1024), (300, 80000, 1024)])
+def test_linear_tile_orders_match_fp64(M, N, K, order):
+    # several token tiles under stream-K, weights larger than L2:
+    # weight-tile-major, and token-tile-major with the grid cut to a
+    # multiple of the token tiles (three of 256 at 700 rows: 150 CTAs);
+    # the same sums split at other k-blocks
+    B = G.library()
+    torch = G.torch_mod()
+    dr = _handle(max(M, 16), N)
+    B.pe_set_tuning(dr, B.PE_TUNE_GEMM_TILE_ORDER, order)
+    x = W.normal(9, "x", (M, K), 1.0, "bf16", M, N)
+    w = W.normal(9, "w", (N, K), 0.05, "bf16", M, N)
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    B.pe_linear(dr, B.to_device(x, "bf16"), B.to_device(w, "bf16"), y)
+    torch.cuda.synchronize()
+    got = y.cpu().numpy().astype(np.float64)
+    want = O.to_f64(x, "bf16") @ O.to_f64(w, "bf16").T
+    assert np.isfinite(got).all()
+    assert np.abs(got - want).max() <= 2e-5 * np.sqrt(K) * max(1.0, np.abs(want).max())
+
+
+def test_tile_order_rejects_other_values():
+    B = G.library()
+    dr = _handle(16)
+    for bad in (-1, 2):
+        with pytest.raises(B.PeError):
+            B.pe_set_tuning(dr, B.PE_TUNE_GEMM_TILE_ORDER, bad)
