@@ -429,7 +429,22 @@ __device__ __forceinline__ bf16 from_f<bf16>(float x) {
   return __float2bfloat16_rn(x);
 }
 
-__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
+// SiLU x sigma(x) = x / (1 + e^-x).  The quotient by Markstein's method
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990): q0 = x r from an
+// approximate reciprocal r of y, the residual x - y q0 exact by one FMA, and
+// q = q0 + residual r, which is the correctly rounded x / y except in rare
+// cases next to a rounding midpoint.  Branch-free, so the 16 columns of an
+// epilogue chunk proceed in parallel instead of one division subroutine
+// after another in a warp's dependent chain.  e^-x is capped at e^80 so that
+// y and r stay finite and normal (the exact SiLU there is below 1e-33).
+__device__ __forceinline__ float silu_f(float x) {
+  const float y = 1.0f + __expf(fminf(-x, 80.0f));
+  const float r = __fdividef(1.0f, y);
+  const float q0 = x * r;
+  const float e = fmaf(-y, q0, x);
+  return fmaf(e, r, q0);
+}
 
 // 2^x with the hardware approximation (one MUFU op; relative error ~2^-22,
 // subnormal results flushed to zero): used for softmax weights that are
