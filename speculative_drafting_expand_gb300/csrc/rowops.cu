@@ -403,8 +403,12 @@ __global__ void __launch_bounds__(kRowThreads) rope_kv_vec_kernel(const RopeKvAr
   using R = RopeVec<T>;
   constexpr int E = R::EPV;
   __shared__ float cs[64], sn[64];
-  grid_dep_wait();
-  grid_dep_launch();
+  // The positions, slots and live count come from the expansion and the
+  // compaction, several launches back (each kernel waits for its
+  // predecessor before its dependents may start), so the rotary angles and
+  // the cache slot are worked out before the wait for the QKV projection,
+  // the one input that kernel writes.  Row 0 is always live: its CTA waits,
+  // so this grid never completes before the projection does.
   const int i = blockIdx.x;
   if (a.live && i >= __ldcg(a.live)) return;  // past the live rows
   const int half = a.dh / 2;
@@ -430,6 +434,8 @@ __global__ void __launch_bounds__(kRowThreads) rope_kv_vec_kernel(const RopeKvAr
       blk = -1;
     }
   }
+  grid_dep_wait();
+  grid_dep_launch();
   const int gpr = half / E;                        // vectors per half head
   const int n_rope = (a.Hq + a.Hkv) * gpr;
   const int n_v = blk >= 0 ? a.Hkv * a.dh / E : 0;
