@@ -510,10 +510,11 @@ __global__ void __launch_bounds__(192, BN <= 32 ? 2 : 1)
         }
         // contributors the pipelined path holds in registers: a tile spans at
         // most three CTAs at the wide-tile shapes of the drafter (k-blocks
-        // per tile below twice the k-blocks per CTA), two at the others
-        // (none for the gate/up pair at 32 tokens or fewer: its registers
-        // are capped by two CTAs an SM, and it splits by clusters there)
-        constexpr int NCM = (DUAL && BN <= 32) ? 0 : (DUAL || BN <= 64) ? 2 : 3;
+        // per tile below twice the k-blocks per CTA), two at the others;
+        // none for the gate/up pair, whose two accumulators' partials would
+        // spill registers across the whole kernel (its usual fix-up, a
+        // finisher at the end of its range, takes the bulk-copy path)
+        constexpr int NCM = DUAL ? 0 : (BN <= 64) ? 2 : 3;
         if (NCM > 0 && *flag && c_last - c_first < NCM) {
           // up to NCM contributors (the usual split): the loads of the next
           // chunk's partials are in flight while this chunk is summed (in
