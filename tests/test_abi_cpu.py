@@ -127,3 +127,22 @@ def test_training_entry_points_validate_on_the_host(B):
     assert lib.pe_train_partition(16, 4, 0.5, buf, 2, b, *args, 8 + 64 - 1, None) == 1
     assert lib.pe_train_partition(16, 4, 0.5, buf, 65, b, *args, 1000, None) == 1
     assert lib.pe_train_partition(16, 4, 0.5, None, 2, b, *args, 100, None) == 1
+
+
+def test_enum_constants_match_the_binding(B):
+    # every PE_* enumerator of the headers that the binding names has the
+    # binding's value (read from the compiled header, not parsed)
+    text = "".join(open(h).read() for h in HEADERS)
+    names = sorted(set(re.findall(r"\b(PE_[A-Z0-9_]+)\s*=", text)))
+    names = [n for n in names if hasattr(B, n)]
+    assert "PE_TUNE_GEMM_TILE_ORDER" in names and "PE_FUSE_NORM" in names
+    src = "#include <stdio.h>\n#include \"peagle.h\"\n#include \"peagle_train.h\"\nint main(void) {\n"
+    src += "".join(f'  printf("%lld\\n", (long long){n});\n' for n in names) + "  return 0;\n}\n"
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "e.c")
+        exe = os.path.join(d, "e")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
+        got = [int(v) for v in subprocess.run([exe], capture_output=True, text=True,
+                                              check=True).stdout.split()]
+    assert got == [int(getattr(B, n)) for n in names], list(zip(names, got))
