@@ -221,7 +221,7 @@ cudaError_t make_interleaved_qkv(pe_handle* h) {
 }
 
 TcGemmWorkspace tc_ws(pe_handle* h) {
-  TcGemmWorkspace ws;
+  TcGemmWorkspace ws = {};
   ws.timeline = nullptr;
   if (h->gemm_timeline && h->gemm_ordinal < h->gemm_timeline_launches)
     ws.timeline = h->gemm_timeline + static_cast<size_t>(h->gemm_ordinal) * 512 * 16;

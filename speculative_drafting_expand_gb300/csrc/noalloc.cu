@@ -109,7 +109,7 @@ extern "C" pe_status pe_linear_static(const void* x, const void* w, float* y, in
   if (!tensor_map_2d_bf16(&wa, w, N, K, K, 64, 128) ||
       !tensor_map_2d_bf16(&xb, x, M, K, K, 64, tc_b_box_rows(M, N, sms, false, false)))
     return PE_ERR_INVALID_ARGUMENT;
-  TcGemmWorkspace ws;
+  TcGemmWorkspace ws = {};
   ws.partials = partials;
   ws.partial_floats = kPartialFloats;
   ws.tile_counters = counters;
