@@ -939,8 +939,10 @@ cudaError_t launch_gemm_tc_maps(const CUtensorMap& wa, const CUtensorMap& wa2,
   // measured faster there, and slower for the layer projections, whose
   // weights (24-90 MB) L2 partly keeps between token tiles.  Stream-K only
   // (run_tc).
-  p.m_major = ws.tile_order == 1 && p.tiles_m > 1 && ws.l2_bytes > 0 &&
-                      static_cast<long long>(N) * K * 2 > ws.l2_bytes
+  // (At most one token tile an SM: the grid, at least the SM count here,
+  // then holds one CTA a token tile or more.)
+  p.m_major = ws.tile_order == 1 && p.tiles_m > 1 && p.tiles_m <= ws.sm_count &&
+                      ws.l2_bytes > 0 && static_cast<long long>(N) * K * 2 > ws.l2_bytes
                   ? 1
                   : 0;
   p.split_s = 0;
